@@ -1,0 +1,164 @@
+"""fp64 CPU oracle for paged GQA decode attention.
+
+TEST INFRASTRUCTURE ONLY: the tests, the smoke check and the benchmark's CPU
+baseline may import this package; the product package never does. It shares
+no code with the CUDA path. The arithmetic lives in ``ref_decode.c`` (plain C,
+fp64, OpenMP over query rows); this module only compiles it with gcc and
+marshals numpy arrays into it.
+
+bf16 tensors are passed as their raw bit patterns (numpy ``uint16``); the C
+code widens them exactly to fp64.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "ref_decode.c")
+_LIB_PATH = os.path.join(_HERE, "libref_decode.so")
+_lock = threading.Lock()
+_lib = None
+
+_STATUS = {
+    0: "ok",
+    -1: "invalid argument",
+    -2: "block table names a page outside the pool",
+    -3: "sequence length outside [0, max_pages * page_size]",
+    -4: "out of host memory",
+}
+
+
+class OracleError(RuntimeError):
+    pass
+
+
+def build(force: bool = False) -> str:
+    """Compile ref_decode.c into libref_decode.so next to it (gcc, -fopenmp)."""
+    if not force and os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fopenmp",
+           "-shared", "-fPIC", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB_PATH)
+            p = ctypes.c_void_p
+            i = ctypes.c_int
+            d = ctypes.c_double
+            lib.ref_decode_rows.argtypes = [i, i, i, i, i, i, i, p, p, p, p, p, i, d, p, i, p, p, i]
+            lib.ref_decode_rows.restype = i
+            lib.ref_decode_split.argtypes = [i, i, i, i, i, i, i, p, p, p, p, p, i, d, i, i, p, p, i]
+            lib.ref_decode_split.restype = i
+            lib.ref_merge.argtypes = [i, i, i, p, p, p]
+            lib.ref_merge.restype = i
+            lib.ref_max_threads.argtypes = []
+            lib.ref_max_threads.restype = i
+            _lib = lib
+    return _lib
+
+
+def _u16(a) -> np.ndarray:
+    a = np.ascontiguousarray(a)
+    if a.dtype != np.uint16:
+        raise TypeError(f"bf16 operands must be passed as uint16 bit patterns, got {a.dtype}")
+    return a
+
+
+def _i32(a) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=np.int32)
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _check(status: int):
+    if status != 0:
+        raise OracleError(_STATUS.get(status, f"status {status}"))
+
+
+def _shapes(q, k_pool, block_tables):
+    B, Hq, d = q.shape
+    num_pages, Hkv, P, d2 = k_pool.shape
+    if d2 != d:
+        raise ValueError("q and pool head_dim differ")
+    max_pages = block_tables.shape[1] if block_tables.ndim == 2 else 0
+    return B, Hq, Hkv, d, P, num_pages, max_pages
+
+
+def max_threads() -> int:
+    return int(_load().ref_max_threads())
+
+
+def decode(q, k_pool, v_pool, block_tables, seq_lens, scale: float, window: int = 0,
+           rows=None, nthreads: int = 0, return_lse: bool = False):
+    """Decode attention in fp64.
+
+    q: uint16 [B, Hq, d]; k_pool / v_pool: uint16 [num_pages, Hkv, P, d]
+    (v_pool None = K=V layer); block_tables: int32 [B, max_pages];
+    seq_lens: int32 [B]; window 0 = global layer.
+    rows: optional list of b * Hq + h to compute (others stay zero).
+    Returns float64 [B, Hq, d] (and [B, Hq] log-sum-exp if return_lse).
+    """
+    lib = _load()
+    q, k_pool = _u16(q), _u16(k_pool)
+    v_pool = None if v_pool is None else _u16(v_pool)
+    block_tables, seq_lens = _i32(block_tables), _i32(seq_lens)
+    B, Hq, Hkv, d, P, num_pages, max_pages = _shapes(q, k_pool, block_tables)
+    if v_pool is not None and v_pool.shape != k_pool.shape:
+        raise ValueError("k_pool and v_pool shapes differ")
+    out = np.zeros((B, Hq, d), dtype=np.float64)
+    lse = np.full((B, Hq), -np.inf, dtype=np.float64)
+    rows_arr = None if rows is None else _i32(rows)
+    n_rows = 0 if rows_arr is None else int(rows_arr.size)
+    st = lib.ref_decode_rows(B, Hq, Hkv, d, P, num_pages, max_pages, _ptr(q), _ptr(k_pool),
+                             _ptr(v_pool), _ptr(block_tables), _ptr(seq_lens), int(window),
+                             float(scale), _ptr(rows_arr), n_rows, _ptr(out), _ptr(lse), int(nthreads))
+    _check(st)
+    return (out, lse) if return_lse else out
+
+
+def decode_split(q, k_pool, v_pool, block_tables, seq_lens, scale: float, window: int,
+                 num_splits: int, chunk: int, nthreads: int = 0):
+    """Split-KV stage 1 in fp64: returns (o_part [B, Hq, S, d], lse_part [B, Hq, S])."""
+    lib = _load()
+    q, k_pool = _u16(q), _u16(k_pool)
+    v_pool = None if v_pool is None else _u16(v_pool)
+    block_tables, seq_lens = _i32(block_tables), _i32(seq_lens)
+    B, Hq, Hkv, d, P, num_pages, max_pages = _shapes(q, k_pool, block_tables)
+    o_part = np.zeros((B, Hq, num_splits, d), dtype=np.float64)
+    lse_part = np.full((B, Hq, num_splits), -np.inf, dtype=np.float64)
+    st = lib.ref_decode_split(B, Hq, Hkv, d, P, num_pages, max_pages, _ptr(q), _ptr(k_pool),
+                              _ptr(v_pool), _ptr(block_tables), _ptr(seq_lens), int(window),
+                              float(scale), int(num_splits), int(chunk), _ptr(o_part), _ptr(lse_part),
+                              int(nthreads))
+    _check(st)
+    return o_part, lse_part
+
+
+def merge(o_part, lse_part):
+    """Split-KV stage 2 in fp64: o_part [..., S, d], lse_part [..., S] -> [..., d]."""
+    lib = _load()
+    o_part = np.ascontiguousarray(o_part, dtype=np.float64)
+    lse_part = np.ascontiguousarray(lse_part, dtype=np.float64)
+    lead = o_part.shape[:-2]
+    S, d = o_part.shape[-2:]
+    if lse_part.shape != lead + (S,):
+        raise ValueError("lse_part shape does not match o_part")
+    rows = int(np.prod(lead)) if lead else 1
+    out = np.zeros(lead + (d,), dtype=np.float64)
+    _check(lib.ref_merge(rows, S, d, _ptr(o_part), _ptr(lse_part), _ptr(out)))
+    return out

@@ -1,0 +1,300 @@
+/*
+ * Paged GQA decode attention: plain fp64 CPU oracle.
+ *
+ * TEST INFRASTRUCTURE ONLY. Nothing in the product path may call, link or
+ * load this file; only the tests, the smoke check and the CPU-baseline leg of
+ * the benchmark use it. It shares no code, header or table with the CUDA path.
+ *
+ * What it computes (the plain definition of single-token decode attention):
+ *   for request b, query head h, KV head g = h / (Hq / Hkv):
+ *     A_b   = attended token positions: [0, L_b)            (global layer)
+ *                                        [max(0, L_b - W), L_b) (window W > 0)
+ *     K_b[t] = k_pool[block_table[b][t / P], g, t % P, :]   (V alike; V = K when
+ *                                                            the layer shares K=V)
+ *     s_t   = scale * sum_d q[b,h,d] * K_b[t,d]
+ *     p_t   = exp(s_t - max s) / sum_{A_b} exp(s - max s)
+ *     o     = sum_{t in A_b} p_t * V_b[t,:]
+ *   and o = 0 when A_b is empty.
+ *
+ * Sources (page title, section):
+ *   - decode = attention of one new token over the cached keys/values:
+ *     "模型库与算子层 — 概念" (vLLM model library & operator layer, concepts),
+ *     section "注意力层 / 核心操作" (attention layer, core operations);
+ *   - the paged KV cache, logical layout [L, B, H, N, C] and block sizes that are
+ *     multiples of 16: same page, "KV-Cache 布局统一" (KV-cache layout) and the
+ *     block-size paragraph of "核心操作";
+ *   - several query heads share one KV head (GQA), sliding-window layers and
+ *     global layers with their own head_dim / KV-head count, and K=V storage:
+ *     Sparse-vLLM PR #27 "feat: support Gemma 4 and native multimodal
+ *     inference", sections "Gemma 4 文本推理" (text inference) and
+ *     "专用算子与性能优化" (dedicated operators);
+ *   - the split-KV partial results with a log-sum-exp slot, merged afterwards:
+ *     vLLM concepts page, section "MLA 与 Sparse MLA（DSA）" (MLA decode).
+ *
+ * Readings where the pages are silent: the window keeps exactly the last W
+ * positions including the current token; query head h uses KV head h / G; the
+ * pool layout is [num_pages, Hkv, P, d] (the [B, H, N, C] slice of one layer).
+ *
+ * All arithmetic is IEEE fp64 from the exact bf16 input values. Build with
+ * -ffp-contract=off so x86 and Arm hosts produce identical bits.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* Status codes returned by every entry point. */
+#define REF_OK 0
+#define REF_BAD_ARG -1
+#define REF_BAD_PAGE -2
+#define REF_BAD_LEN -3
+#define REF_NO_MEM -4
+
+/* bf16 -> fp64: a bf16 value is the top 16 bits of an IEEE binary32. */
+static double bf16_to_f64(uint16_t bits) {
+  uint32_t u = ((uint32_t)bits) << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return (double)f;
+}
+
+typedef struct {
+  int B, Hq, Hkv, d, P, num_pages, max_pages;
+  const uint16_t *q, *k_pool, *v_pool; /* v_pool == NULL: V is K (K=V layer) */
+  const int32_t *block_tables, *seq_lens;
+  int window; /* 0 = global layer */
+  double scale;
+} ref_layer;
+
+static int check_layer(const ref_layer *ly) {
+  if (ly->B < 0 || ly->Hq <= 0 || ly->Hkv <= 0 || ly->d <= 0 || ly->P <= 0) return REF_BAD_ARG;
+  if (ly->Hq % ly->Hkv != 0) return REF_BAD_ARG;
+  if (ly->window < 0 || ly->num_pages < 0 || ly->max_pages < 0) return REF_BAD_ARG;
+  if (ly->B > 0 && (!ly->q || !ly->k_pool || !ly->block_tables || !ly->seq_lens)) return REF_BAD_ARG;
+  for (int b = 0; b < ly->B; ++b) {
+    int L = ly->seq_lens[b];
+    if (L < 0 || (long long)L > (long long)ly->max_pages * ly->P) return REF_BAD_LEN;
+  }
+  return REF_OK;
+}
+
+/* Attended range [lo, hi) of request b. */
+static void attended_range(const ref_layer *ly, int b, int *lo, int *hi) {
+  int L = ly->seq_lens[b];
+  *hi = L;
+  *lo = (ly->window > 0 && L > ly->window) ? L - ly->window : 0;
+}
+
+/* Pointer to the d values of token t of request b, KV head g, in `pool`.
+ * Returns NULL if the block table names a page outside the pool. */
+static const uint16_t *token_row(const ref_layer *ly, const uint16_t *pool, int b, int g, int t) {
+  int32_t page = ly->block_tables[(size_t)b * ly->max_pages + t / ly->P];
+  if (page < 0 || page >= ly->num_pages) return NULL;
+  size_t row = ((size_t)page * ly->Hkv + g) * ly->P + (size_t)(t % ly->P);
+  return pool + row * ly->d;
+}
+
+/*
+ * Attention of query head h of request b over the token positions [lo, hi):
+ * writes o[0..d) (normalised by the softmax denominator) and returns the
+ * natural-log log-sum-exp of the scaled scores through *lse (-inf, o = 0 when
+ * the range is empty).
+ */
+static int attend_range(const ref_layer *ly, int b, int h, int lo, int hi, double *o, double *lse,
+                        double *s /* scratch, >= hi - lo */) {
+  const int G = ly->Hq / ly->Hkv;
+  const int g = h / G;
+  const int d = ly->d;
+  const uint16_t *qrow = ly->q + ((size_t)b * ly->Hq + h) * d;
+  const uint16_t *vpool = ly->v_pool ? ly->v_pool : ly->k_pool;
+
+  for (int i = 0; i < d; ++i) o[i] = 0.0;
+  if (hi <= lo) {
+    *lse = -INFINITY;
+    return REF_OK;
+  }
+  /* scores s_t = scale * <q, K_t> */
+  double m = -INFINITY;
+  for (int t = lo; t < hi; ++t) {
+    const uint16_t *krow = token_row(ly, ly->k_pool, b, g, t);
+    if (!krow) return REF_BAD_PAGE;
+    double acc = 0.0;
+    for (int i = 0; i < d; ++i) acc += bf16_to_f64(qrow[i]) * bf16_to_f64(krow[i]);
+    s[t - lo] = ly->scale * acc;
+    if (s[t - lo] > m) m = s[t - lo];
+  }
+  /* softmax weights exp(s - max) and their sum */
+  double l = 0.0;
+  for (int t = lo; t < hi; ++t) {
+    s[t - lo] = exp(s[t - lo] - m);
+    l += s[t - lo];
+  }
+  /* weighted sum of the value rows */
+  for (int t = lo; t < hi; ++t) {
+    const uint16_t *vrow = token_row(ly, vpool, b, g, t);
+    if (!vrow) return REF_BAD_PAGE;
+    const double p = s[t - lo];
+    for (int i = 0; i < d; ++i) o[i] += p * bf16_to_f64(vrow[i]);
+  }
+  for (int i = 0; i < d; ++i) o[i] /= l;
+  *lse = m + log(l);
+  return REF_OK;
+}
+
+static void set_threads(int nthreads) {
+#ifdef _OPENMP
+  if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+  (void)nthreads;
+#endif
+}
+
+/*
+ * Full decode: out[b, h, :] for every request and query head (fp64), and the
+ * log-sum-exp of each row into lse_out[b, h] when lse_out is not NULL.
+ * Rows are listed by (b, h); `rows`/`n_rows` restrict the work to a subset
+ * (each entry b * Hq + h); pass rows = NULL for all B * Hq rows. Output rows
+ * not in the subset are left untouched.
+ */
+int ref_decode_rows(int B, int Hq, int Hkv, int d, int P, int num_pages, int max_pages,
+                    const uint16_t *q, const uint16_t *k_pool, const uint16_t *v_pool,
+                    const int32_t *block_tables, const int32_t *seq_lens, int window, double scale,
+                    const int32_t *rows, int n_rows, double *out, double *lse_out, int nthreads) {
+  ref_layer ly = {B, Hq, Hkv, d, P, num_pages, max_pages, q, k_pool, v_pool,
+                  block_tables, seq_lens, window, scale};
+  int st = check_layer(&ly);
+  if (st != REF_OK) return st;
+  if (!out) return REF_BAD_ARG;
+  const int total = rows ? n_rows : B * Hq;
+  int max_len = 0;
+  for (int b = 0; b < B; ++b) max_len = seq_lens[b] > max_len ? seq_lens[b] : max_len;
+
+  int status = REF_OK;
+  set_threads(nthreads);
+#pragma omp parallel
+  {
+    double *s = (double *)malloc(sizeof(double) * (size_t)(max_len > 0 ? max_len : 1));
+    if (!s) {
+#pragma omp critical
+      status = REF_NO_MEM;
+    }
+#pragma omp for schedule(dynamic, 1)
+    for (int r = 0; r < total; ++r) {
+      if (!s) continue;
+      const int row = rows ? rows[r] : r;
+      if (row < 0 || row >= B * Hq) {
+#pragma omp critical
+        status = REF_BAD_ARG;
+        continue;
+      }
+      const int b = row / Hq, h = row % Hq;
+      int lo, hi;
+      attended_range(&ly, b, &lo, &hi);
+      double lse;
+      int rs = attend_range(&ly, b, h, lo, hi, out + (size_t)row * d, &lse, s);
+      if (lse_out) lse_out[row] = lse;
+      if (rs != REF_OK) {
+#pragma omp critical
+        status = rs;
+      }
+    }
+    free(s);
+  }
+  return status;
+}
+
+/*
+ * Split-KV first stage (vLLM concepts page, "MLA 与 Sparse MLA（DSA）"): the
+ * attended range [lo, hi) of each request is cut into pieces of `chunk`
+ * consecutive positions starting at lo; piece k covers
+ * [lo + k * chunk, lo + (k + 1) * chunk) intersected with [lo, hi). Each piece
+ * yields its normalised partial output o_part[b, h, k, :] and the log-sum-exp
+ * lse_part[b, h, k] (-inf and zeros for an empty piece). num_splits pieces are
+ * produced per row; pieces past the range are empty.
+ */
+int ref_decode_split(int B, int Hq, int Hkv, int d, int P, int num_pages, int max_pages,
+                     const uint16_t *q, const uint16_t *k_pool, const uint16_t *v_pool,
+                     const int32_t *block_tables, const int32_t *seq_lens, int window, double scale,
+                     int num_splits, int chunk, double *o_part, double *lse_part, int nthreads) {
+  ref_layer ly = {B, Hq, Hkv, d, P, num_pages, max_pages, q, k_pool, v_pool,
+                  block_tables, seq_lens, window, scale};
+  int st = check_layer(&ly);
+  if (st != REF_OK) return st;
+  if (num_splits <= 0 || chunk <= 0 || !o_part || !lse_part) return REF_BAD_ARG;
+  int max_len = 0;
+  for (int b = 0; b < B; ++b) max_len = seq_lens[b] > max_len ? seq_lens[b] : max_len;
+
+  int status = REF_OK;
+  set_threads(nthreads);
+#pragma omp parallel
+  {
+    double *s = (double *)malloc(sizeof(double) * (size_t)(max_len > 0 ? max_len : 1));
+#pragma omp for schedule(dynamic, 1)
+    for (int row = 0; row < B * Hq; ++row) {
+      if (!s) continue;
+      const int b = row / Hq, h = row % Hq;
+      int lo, hi;
+      attended_range(&ly, b, &lo, &hi);
+      for (int k = 0; k < num_splits; ++k) {
+        long long plo = (long long)lo + (long long)k * chunk;
+        long long phi = plo + chunk;
+        if (plo > hi) plo = hi;
+        if (phi > hi) phi = hi;
+        const size_t idx = (size_t)row * num_splits + k;
+        int rs = attend_range(&ly, b, h, (int)plo, (int)phi, o_part + idx * d, lse_part + idx, s);
+        if (rs != REF_OK) {
+#pragma omp critical
+          status = rs;
+        }
+      }
+    }
+    if (!s) {
+#pragma omp critical
+      status = REF_NO_MEM;
+    }
+    free(s);
+  }
+  return status;
+}
+
+/*
+ * Split-KV second stage: merges the partial outputs of the pieces of each row
+ * by their log-sum-exp weights,
+ *   M = max_k lse_k,  w_k = exp(lse_k - M),  out = sum_k w_k o_k / sum_k w_k,
+ * with out = 0 when every piece is empty (M = -inf).
+ */
+int ref_merge(int rows, int num_splits, int d, const double *o_part, const double *lse_part,
+              double *out) {
+  if (rows < 0 || num_splits <= 0 || d <= 0 || !o_part || !lse_part || !out) return REF_BAD_ARG;
+  for (int r = 0; r < rows; ++r) {
+    const double *lse = lse_part + (size_t)r * num_splits;
+    double M = -INFINITY;
+    for (int k = 0; k < num_splits; ++k)
+      if (lse[k] > M) M = lse[k];
+    double *o = out + (size_t)r * d;
+    for (int i = 0; i < d; ++i) o[i] = 0.0;
+    if (M == -INFINITY) continue;
+    double wsum = 0.0;
+    for (int k = 0; k < num_splits; ++k) {
+      const double w = exp(lse[k] - M);
+      wsum += w;
+      const double *ok = o_part + ((size_t)r * num_splits + k) * d;
+      for (int i = 0; i < d; ++i) o[i] += w * ok[i];
+    }
+    for (int i = 0; i < d; ++i) o[i] /= wsum;
+  }
+  return REF_OK;
+}
+
+/* Number of OpenMP threads a parallel region would use (1 without OpenMP). */
+int ref_max_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
