@@ -1,0 +1,456 @@
+#!/usr/bin/env python
+"""Benchmark of one decode layer-step (stage 1 + stage 2) of paged GQA decode.
+
+Default workload: global-layer decode, batch 8, 16 query / 4 KV heads,
+head_dim 512, 1024 cached tokens per request, 16-token pages shuffled across a
+4096-page pool, K and V in separate pools (bf16).
+
+A "step" is one layer-step: the stage-1 launch and the merge launch over one
+batch. Timing: W warm-up steps, then exactly K steps replayed from CUDA graphs
+on one stream, bracketed by CUDA events with a synchronize (and, for N > 1, a
+barrier) on both sides. Each step reads a different replica of the K/V pools,
+and the replicas together are larger than 4x L2, so every step streams its KV
+from HBM. Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 1..5] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs an independent replica of the step
+(decode attention needs no exchange); the reported time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from paged_gqa_decode_global_gb300 import binding as pdb  # noqa: E402
+from paged_gqa_decode_global_gb300 import build as pd_build  # noqa: E402
+from paged_gqa_decode_global_gb300 import inputs as synth  # noqa: E402
+
+METRIC = "decode-attn µs/layer-step and KV HBM GB/s (% of GB300 peak), 1 GPU"
+UNIT = "us/layer-step"
+L2_BYTES = 129 * 1000 * 1000
+FALLBACK_HBM_GBS = 6800.0
+
+# DRAM bytes (read + write) per stage-1 launch from an ncu capture, keyed by the
+# hash of the kernel sources it was taken on; stale entries are ignored.
+NCU_TRAFFIC = {}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_gqa_decode_global_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            data = json.load(f)
+        for key in ("hbm_gbs", "hbm_GBs", "hbm_copy_gbs"):
+            if key in data:
+                return float(data[key]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.25)  # first sample lands before the region starts
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+        return False
+
+    def summary(self):
+        rows = []
+        for line in (self.out or "").strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[1]), max=float(parts[2]), power=float(parts[3]),
+                                 hw=parts[5], hw_thermal=parts[6], sw_thermal=parts[7], sw_power=parts[8]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        reasons = set()
+        for r in rows:
+            for key, name in (("hw", "hw_slowdown"), ("hw_thermal", "hw_thermal_slowdown"),
+                              ("sw_thermal", "sw_thermal_slowdown"), ("sw_power", "sw_power_cap")):
+                if r[key].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in rows), "sm_max_mhz": max(r["max"] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows),
+                "power_w": statistics.median(r["power"] for r in rows)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def workload_layer(cid: int, part, device):
+    layers = synth.workload(cid, device=device, part=part)
+    if len(layers) != 1:
+        raise SystemExit("pick one layer with --part (workload 4: a|b|c, workload 5: global|sliding)")
+    return layers[0]
+
+
+def config_of(li, cid, part, replicas, plan):
+    return {
+        "workload": synth.WORKLOADS[cid] + (f" [{li.name}]" if part else ""),
+        "batch": li.batch, "num_q_heads": li.num_q_heads, "num_kv_heads": li.num_kv_heads,
+        "head_dim": li.head_dim, "page_size": li.page_size, "pool_pages": li.num_pages,
+        "seq_lens": li.seq_lens_list() if li.batch <= 8 else f"{li.batch} requests",
+        "window": li.window, "kv_shared": li.kv_shared,
+        "kv_bytes_per_step": li.kv_bytes(),
+        "l2": f"{replicas} rotating K/V pool replicas, {replicas * li.kv_bytes() / 1e6:.0f} MB touched per cycle (> 4x L2)",
+        "num_splits": int(plan.num_splits), "chunk_tokens": int(plan.chunk_tokens),
+        "launch": "CUDA graph replay, one stream",
+        "parallelism": "replicas (no exchange)",
+    }
+
+
+# ----------------------------------------------------------------------------
+# our arm
+# ----------------------------------------------------------------------------
+
+def run_ours(args, world, rank, local):
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (the library has no CPU path)")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    pd_build.build()
+    pdb.load_library()
+
+    li = workload_layer(args.workload, args.part, dev)
+    step = pdb.LayerStep.for_inputs(li)
+    plan = step.plan
+    S = int(plan.num_splits)
+    launches_per_step = 1 + (1 if S > 1 else 0)
+
+    touched = max(1, li.kv_bytes())
+    replicas = max(1, min(16, math.ceil(4 * L2_BYTES / touched)))
+    pools = [(li.k_pool, li.v_pool)]
+    for _ in range(replicas - 1):
+        pools.append((li.k_pool.clone(), None if li.v_pool is None else li.v_pool.clone()))
+    out = torch.empty_like(li.q)
+    stream = torch.cuda.Stream(device=dev)
+
+    def one_step(i, stage1_only=False):
+        k, v = pools[i % replicas]
+        if li.window > 0:
+            pdb.paged_decode_window(plan, li.q, k, v, li.block_tables, li.seq_lens, li.window, li.scale,
+                                    step.workspace, out, stream)
+        else:
+            pdb.paged_decode_global(plan, li.q, k, v, li.block_tables, li.seq_lens, li.scale, step.workspace,
+                                    out, stream)
+        if not stage1_only:
+            pdb.paged_decode_merge(plan, step.workspace, out, stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(max(3, args.warmup)):
+            one_step(i)
+    torch.cuda.synchronize()
+    step.check(stream)
+
+    def capture(n, stage1_only=False):
+        graphs = []
+        per = min(n, 500)
+        left = n
+        i0 = 0
+        while left > 0:
+            m = min(per, left)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(m):
+                    one_step(i0 + i, stage1_only)
+            graphs.append(g)
+            left -= m
+            i0 += m
+        return graphs
+
+    def timed(graphs, sample_clocks=False):
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        for g in graphs[:1]:  # warm the graph exec once
+            g.replay()
+        torch.cuda.synchronize()
+        barrier(world)
+        sampler = ClockSampler(local) if sample_clocks else None
+        if sampler:
+            sampler.__enter__()
+        torch.cuda.synchronize()
+        start.record(stream)
+        for g in graphs:
+            g.replay()
+        end.record(stream)
+        torch.cuda.synchronize()
+        if sampler:
+            sampler.__exit__(None, None, None)
+        barrier(world)
+        return start.elapsed_time(end), (sampler.summary() if sampler else None)
+
+    K = args.steps
+    step_graphs = capture(K)
+    elapsed_ms, clocks = timed(step_graphs, sample_clocks=True)
+    elapsed_ms = max_over_ranks(elapsed_ms, world)
+    del step_graphs
+    s1_graphs = capture(K, stage1_only=True)
+    s1_ms, _ = timed(s1_graphs)
+    s1_ms = max_over_ranks(s1_ms, world)
+    del s1_graphs
+    step.check(stream)
+
+    us_per_step = elapsed_ms * 1e3 / K
+    s1_us = s1_ms * 1e3 / K
+    alg_bytes = li.algorithmic_bytes()
+    peak, peak_kind = measured_peaks()
+    achieved = alg_bytes / (s1_us * 1e-6) / 1e9
+    kv_gbs = li.kv_bytes() / (us_per_step * 1e-6) / 1e9
+    src_hash = kernel_source_hash()
+    traffic = NCU_TRAFFIC.get(src_hash, {}).get(f"w{args.workload}{args.part or ''}")
+
+    # end to end: host inputs -> device -> decode -> host output, eager launches
+    e2e = None
+    if not args.no_e2e:
+        q_h = li.q.cpu().pin_memory()
+        bt_h = li.block_tables.cpu().pin_memory()
+        sl_h = li.seq_lens.cpu().pin_memory()
+        out_h = torch.empty(li.q.shape, dtype=li.q.dtype, pin_memory=True)
+        q_d, bt_d, sl_d = torch.empty_like(li.q), torch.empty_like(li.block_tables), torch.empty_like(li.seq_lens)
+        n_e2e = K
+
+        def e2e_step(i):
+            k, v = pools[i % replicas]
+            q_d.copy_(q_h, non_blocking=True)
+            bt_d.copy_(bt_h, non_blocking=True)
+            sl_d.copy_(sl_h, non_blocking=True)
+            step(q_d, k, v, bt_d, sl_d, li.scale, out, stream)
+            out_h.copy_(out, non_blocking=True)
+
+        with torch.cuda.stream(stream):
+            for i in range(3):
+                e2e_step(i)
+            torch.cuda.synchronize()
+            barrier(world)
+            a = torch.cuda.Event(enable_timing=True)
+            z = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for i in range(n_e2e):
+                e2e_step(i)
+            z.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        e2e_ms = max_over_ranks(a.elapsed_time(z), world)
+        assert torch.equal(out_h, out.cpu())
+        e2e = {"value": round(e2e_ms * 1e3 / n_e2e, 3), "unit": UNIT,
+               "h2d_bytes_per_step": q_h.numel() * 2 + bt_h.numel() * 4 + sl_h.numel() * 4,
+               "d2h_bytes_per_step": out_h.numel() * 2, "steps": n_e2e,
+               "launch": "eager C-ABI calls with pinned host buffers"}
+        step.check(stream)
+
+    cpu_baseline = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu_baseline = oracle_baseline(li.to("cpu"), budget_s=args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(us_per_step, 3), "unit": UNIT, "n_gpus": world, "steps": K,
+            "warmup": max(3, args.warmup), "ms_per_step": round(us_per_step / 1e3, 6),
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "io_dtype": "bf16", "data": "synthetic",
+            "config": config_of(li, args.workload, args.part, replicas, plan),
+            "kv_gbs": round(kv_gbs, 1), "kv_hbm_frac": round(kv_gbs / peak, 4),
+            "roofline": {"bound": "hbm", "kernel": "stage1", "achieved": round(achieved, 1), "peak": peak,
+                         "peak_source": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                         "traffic": traffic, "algorithmic_bytes": alg_bytes, "kernel_us": round(s1_us, 3),
+                         "kernel_source": src_hash},
+            "cpu_baseline": cpu_baseline,
+            "e2e": e2e,
+            "gpu_launches": K * launches_per_step,
+            "clocks": clocks,
+            "device": torch.cuda.get_device_name(dev),
+        }
+        print(json.dumps(line), flush=True)
+
+
+def oracle_baseline(li_cpu, budget_s=10.0):
+    """The fp64 oracle, as it stands, on all host cores: full layer-steps
+    repeated for about `budget_s` seconds."""
+    import oracle
+    q = synth.bits_u16(li_cpu.q)
+    k = synth.bits_u16(li_cpu.k_pool)
+    v = None if li_cpu.v_pool is None else synth.bits_u16(li_cpu.v_pool)
+    bt = li_cpu.block_tables.numpy()
+    sl = li_cpu.seq_lens.numpy()
+    threads = oracle.max_threads()
+    times = []
+    t_end = time.perf_counter() + budget_s
+    while True:
+        t0 = time.perf_counter()
+        oracle.decode(q, k, v, bt, sl, li_cpu.scale, li_cpu.window)
+        times.append(time.perf_counter() - t0)
+        if time.perf_counter() > t_end and len(times) >= 3:
+            break
+    t = statistics.median(times)
+    return {"value": round(t * 1e6, 1), "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"full layer-step ({li_cpu.batch}x{li_cpu.num_q_heads} rows, {sum(li_cpu.attended())} "
+                      f"attended tokens), median of {len(times)} runs, fp64 C + OpenMP"}
+
+
+# ----------------------------------------------------------------------------
+# reference arm: the oracle on the host cores
+# ----------------------------------------------------------------------------
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    import numpy as np
+    import oracle
+    li = workload_layer(args.workload, args.part, "cpu")
+    q = synth.bits_u16(li.q)
+    k = synth.bits_u16(li.k_pool)
+    v = None if li.v_pool is None else synth.bits_u16(li.v_pool)
+    bt = li.block_tables.numpy()
+    full_lens = li.seq_lens.numpy().astype(np.int32)
+    threads = oracle.max_threads()
+    rows_all = li.batch * li.num_q_heads
+    rows = list(range(min(rows_all, threads)))
+    full_tokens = sum(li.attended()) * li.num_q_heads  # (row, token) pairs of a layer-step
+
+    def sample_step(frac):
+        lens = np.maximum(1, (full_lens * frac).astype(np.int64)).astype(np.int32)
+        if li.window > 0:
+            lens = full_lens  # the window bounds the work already
+        t0 = time.perf_counter()
+        oracle.decode(q, k, v, bt, lens, li.scale, li.window, rows=rows)
+        dt = time.perf_counter() - t0
+        att = [min(int(L), li.window) if li.window else int(L) for L in lens]
+        done = sum(att[r // li.num_q_heads] for r in rows)
+        return dt, done
+
+    # size the sample so warmup + steps fit the time budget
+    dt, done = sample_step(1.0)
+    per_step_budget = args.ref_seconds / max(1, args.steps + args.warmup)
+    frac = min(1.0, max(1e-4, per_step_budget / max(dt, 1e-9)))
+    for _ in range(args.warmup):
+        sample_step(frac)
+    t_total, work = 0.0, 0
+    for _ in range(args.steps):
+        dt, done = sample_step(frac)
+        t_total += dt
+        work += done
+    us_per_step = t_total / work * full_tokens * 1e6  # scaled to a full layer-step
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(us_per_step, 3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(us_per_step / 1e3, 6),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": synth.WORKLOADS[args.workload], "batch": li.batch, "head_dim": li.head_dim},
+        "cpu_baseline": {"value": round(us_per_step, 3), "unit": UNIT, "cores": len(rows), "kind": "oracle",
+                         "sample": f"{len(rows)} query rows over {frac:.4f} of each attended range per step, "
+                                   "time scaled linearly to a full layer-step"},
+        "e2e": {"value": round(us_per_step, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--part", default=None, help="workload 4: a|b|c; workload 5: global|sliding")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-seconds", type=float, default=60.0)
+    args = ap.parse_args()
+    if args.workload == 4 and args.part is None:
+        args.part = "a"
+    if args.workload == 5 and args.part is None:
+        args.part = "global"
+    world, rank, local = dist_setup()
+    if args.gpus != world and world > 1 and rank == 0:
+        print(f"warning: --gpus {args.gpus} but WORLD_SIZE {world}", file=sys.stderr)
+    try:
+        if args.impl == "reference":
+            run_reference(args, world, rank)
+        else:
+            run_ours(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

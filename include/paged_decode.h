@@ -1,0 +1,197 @@
+/*
+ * paged_decode.h — C ABI of the GB300 (sm_103a) paged GQA decode-attention library.
+ *
+ * One new query token per request attends over that request's cached keys and
+ * values, which live in fixed-size pages of a per-layer pool and are found
+ * through a block table. Both kinds of attention layer of a Gemma-4-style
+ * model are served:
+ *   - global layers (every cached token is attended; head_dim 512 in Gemma 4),
+ *     optionally with one tensor used as both K and V ("K=V" storage);
+ *   - sliding-window layers (only the last `window` tokens; head_dim 256),
+ * each with its own query/KV head counts, query heads grouped on KV heads (GQA).
+ *
+ * Sources (page title, section):
+ *   [PR27-text] Sparse-vLLM PR #27 "feat: support Gemma 4 and native multimodal
+ *               inference", section "Gemma 4 文本推理" (text inference):
+ *               heterogeneous sliding/global layers with their own head_dim and
+ *               KV-head count, K=V or K!=V storage, per-layer KV storage.
+ *   [PR27-ops]  same page, section "专用算子与性能优化" (dedicated operators and
+ *               performance): a stage-1 decode pass for head_dim 512 that serves
+ *               several GQA query heads of one KV head per program; grouped
+ *               sliding-window and global decode; window starts that are not
+ *               32-token aligned.
+ *   [vLLM-attn] "模型库与算子层 — 概念" (vLLM model library & operator layer,
+ *               concepts), section "注意力层" (attention layer): decode is the
+ *               single-token incremental attention; paged KV cache with logical
+ *               layout [L, B, H, N, C]; block sizes are multiples of 16.
+ *   [vLLM-MLA]  same page, section "MLA 与 Sparse MLA（DSA）": split-KV decode —
+ *               the KV sequence is cut into num_kv_splits pieces whose partial
+ *               results carry a log-sum-exp and are merged afterwards; the partial
+ *               buffer is reserved once for the worst case so no call allocates
+ *               and CUDA-graph capture works.
+ *
+ * Data layout (all device pointers, row-major, contiguous, 16-byte aligned):
+ *   q            bf16  [batch, num_q_heads, head_dim]
+ *   k_pool       bf16  [num_pages, num_kv_heads, page_size, head_dim]
+ *   v_pool       bf16  same shape as k_pool; NULL or == k_pool iff kv_shared
+ *   block_tables int32 [batch, max_pages_per_seq]; entry i of request b is the
+ *                      pool page holding its tokens [i*page_size, (i+1)*page_size)
+ *   seq_lens     int32 [batch]; cached tokens of each request, INCLUDING the new
+ *                      token (whose K/V the caller has already written)
+ *   out          bf16  [batch, num_q_heads, head_dim]
+ * Query head h reads KV head h / (num_q_heads / num_kv_heads).
+ * The attended positions of request b are [0, L) on a global layer and
+ * [max(0, L - window), L) on a window layer (exactly the last `window` tokens,
+ * the current one included); an empty range gives a zero output row.
+ *
+ * Ownership: the caller allocates and owns every buffer (inputs, the workspace
+ * and out). The library allocates and frees nothing, keeps no state between
+ * calls, and never synchronises except in paged_decode_check_device_error.
+ * Every launch is ordered on the given stream (a cudaStream_t passed as void*;
+ * NULL = the legacy default stream).
+ *
+ * Errors: no exception or trap crosses this boundary. Host-side argument checks
+ * return a status without launching anything. Conditions only the GPU can see
+ * (a block-table entry outside the pool, a device seq_len outside
+ * [0, max_pages_per_seq * page_size], a pipeline wait that timed out) set bits in
+ * an error word at the start of the workspace: the offending page is skipped
+ * (its tokens are masked out), the length clamped; paged_decode_check_device_error
+ * reports PD_ERR_DEVICE_FAULT. The error word must be zero before the first call:
+ * zero the workspace once after allocating it.
+ */
+#ifndef PAGED_DECODE_H
+#define PAGED_DECODE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  PD_OK = 0,
+  PD_ERR_INVALID_ARG = 1,          /* bad pointer, shape, length or scale */
+  PD_ERR_UNSUPPORTED = 2,          /* valid but not built: head_dim / group size */
+  PD_ERR_WORKSPACE_TOO_SMALL = 3,  /* workspace_bytes < plan->workspace_bytes */
+  PD_ERR_CUDA = 4,                 /* a CUDA runtime call failed */
+  PD_ERR_DEVICE_FAULT = 5          /* the device error word is non-zero */
+} pd_status;
+
+/* Bits of the device error word (paged_decode_check_device_error, *flags). */
+#define PD_DEVFLAG_BAD_PAGE 0x1u     /* a block-table entry outside [0, num_pages) */
+#define PD_DEVFLAG_BAD_SEQLEN 0x2u   /* a device seq_len outside the block table */
+#define PD_DEVFLAG_WAIT_TIMEOUT 0x4u /* a pipeline wait gave up after ~1 s */
+
+/* One attention layer's shape. */
+typedef struct {
+  int32_t num_q_heads;        /* Hq, a multiple of num_kv_heads */
+  int32_t num_kv_heads;       /* Hkv */
+  int32_t head_dim;           /* d: 256 or 512 */
+  int32_t page_size;          /* P: tokens per page, a multiple of 16 */
+  int32_t num_pages;          /* pages in the pool */
+  int32_t max_pages_per_seq;  /* block-table row length */
+  int32_t window;             /* 0 = global layer; > 0 = sliding window of this many tokens */
+  int32_t kv_shared;          /* 1 = one pool is both K and V (K=V storage) */
+} pd_layer_desc;
+
+/* Launch plan: a plain value filled by paged_decode_plan, copyable, reusable for
+ * any call with the same layer, batch and no longer sequences than it was made
+ * for. Callers read workspace_bytes and num_splits; the other fields are the
+ * library's. */
+typedef struct {
+  pd_layer_desc layer;
+  int32_t batch;
+  int32_t num_splits;       /* S: KV pieces per (request, KV head); 1 = no merge needed */
+  int32_t chunk_tokens;     /* tokens per piece */
+  int32_t block_tokens;     /* tokens per pipeline stage */
+  int32_t variant;          /* kernel instance */
+  int32_t grid_x, grid_y, grid_z;
+  int32_t threads_per_cta;
+  int32_t smem_bytes;
+  int32_t sm_count;
+  int32_t max_seq_len;      /* longest sequence the plan was made for */
+  int32_t reserved[4];
+  uint64_t workspace_bytes; /* bytes the caller must provide */
+  uint64_t lse_offset;      /* byte offset of the fp32 [batch, Hq, S] log-sum-exp part */
+  uint64_t opart_offset;    /* byte offset of the fp32 [batch, Hq, S, d] partial outputs */
+  uint32_t magic;
+  uint32_t version;
+} pd_plan;
+
+/*
+ * Choose the split count and launch shape for one decode step of one layer
+ * ([vLLM-MLA]: split-KV with a worst-case-sized partial buffer; [PR27-ops]: the
+ * stage-1 pass). Pure host function: no CUDA call.
+ *   layer         the layer shape; window and kv_shared included
+ *   batch         number of requests (>= 0)
+ *   seq_lens_host host array [batch] of sequence lengths, each in
+ *                 [0, max_pages_per_seq * page_size] — the plan stays valid for any
+ *                 later call whose lengths do not exceed max(seq_lens_host)
+ *   sm_count      streaming multiprocessors of the target GPU (> 0)
+ *   plan          output
+ * Returns PD_ERR_INVALID_ARG for a malformed shape or length, PD_ERR_UNSUPPORTED
+ * for a head_dim or group size (Hq / Hkv) this build has no kernel for.
+ */
+pd_status paged_decode_plan(const pd_layer_desc* layer, int32_t batch, const int32_t* seq_lens_host,
+                            int32_t sm_count, pd_plan* plan);
+
+/*
+ * Stage 1 on a global layer (plan->layer.window == 0): for every (request,
+ * KV head, KV piece) one CTA streams the piece's pages once and serves all
+ * query heads of that KV head ([PR27-ops] grouped decode, [vLLM-attn] decode).
+ * With plan->num_splits == 1 it writes `out` directly; otherwise it writes the
+ * partial outputs and log-sum-exps into the workspace and paged_decode_merge
+ * must follow on the same stream.
+ *   scale     softmax scale applied to q.k (finite, usually 1/sqrt(head_dim))
+ *   workspace device buffer of at least plan->workspace_bytes, 256-byte aligned
+ * Returns PD_ERR_INVALID_ARG (NULL/misaligned pointer, v_pool inconsistent with
+ * kv_shared, non-finite scale, window layer), PD_ERR_WORKSPACE_TOO_SMALL,
+ * PD_ERR_CUDA (launch failure).
+ */
+pd_status paged_decode_global(const pd_plan* plan, const void* q, const void* k_pool,
+                              const void* v_pool, const int32_t* block_tables,
+                              const int32_t* seq_lens, float scale, void* workspace,
+                              size_t workspace_bytes, void* out, void* stream);
+
+/*
+ * Stage 1 on a sliding-window layer: as paged_decode_global, attending only
+ * the last `window` positions of each request; pages wholly before the window
+ * are never read, and the window may start at any token offset ([PR27-ops]:
+ * window starts need no 32-token alignment). `window` must equal
+ * plan->layer.window (> 0).
+ */
+pd_status paged_decode_window(const pd_plan* plan, const void* q, const void* k_pool,
+                              const void* v_pool, const int32_t* block_tables,
+                              const int32_t* seq_lens, int32_t window, float scale,
+                              void* workspace, size_t workspace_bytes, void* out, void* stream);
+
+/*
+ * Stage 2 ([vLLM-MLA]: the pieces' partial results are merged): for each
+ * (request, query head), out = sum_s w_s o_s / sum_s w_s with
+ * w_s = exp(lse_s - max lse); pieces with no attended token are skipped; a row
+ * with none at all is zero. A no-op (PD_OK, nothing launched) when
+ * plan->num_splits == 1, so it is always safe to call after stage 1.
+ */
+pd_status paged_decode_merge(const pd_plan* plan, const void* workspace, size_t workspace_bytes,
+                             void* out, void* stream);
+
+/*
+ * Synchronise `stream`, read the device error word of `workspace`, store it in
+ * *flags (may be NULL) and reset it to zero. Returns PD_ERR_DEVICE_FAULT if it
+ * was non-zero, PD_ERR_CUDA if the synchronisation or copy failed.
+ */
+pd_status paged_decode_check_device_error(const pd_plan* plan, void* workspace,
+                                          size_t workspace_bytes, void* stream, uint32_t* flags);
+
+/* Static, human-readable name of a status. */
+const char* paged_decode_status_string(pd_status status);
+
+/* ABI version of this library (bumped when pd_plan or a signature changes). */
+int32_t paged_decode_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGED_DECODE_H */

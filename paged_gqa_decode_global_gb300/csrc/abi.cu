@@ -1,0 +1,149 @@
+// C ABI entry points: argument checks, kernel launch on the caller's stream,
+// device error-word readback. Declarations and contracts: include/paged_decode.h.
+#include <atomic>
+#include <cmath>
+#include <cstring>
+
+#include <cuda_runtime.h>
+
+#include "paged_decode.h"
+#include "pd_kernels.h"
+
+namespace pd {
+bool plan_is_valid(const pd_plan* plan);
+}
+
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kMaxDevices = 64;
+
+// Per device, one bit per variant whose dynamic shared-memory limit is raised.
+std::atomic<uint64_t> g_smem_ready[kMaxDevices];
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+pd_status ensure_smem_attr(int variant, const void* fn, int smem_bytes) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PD_ERR_CUDA;
+  const uint64_t bit = 1ull << variant;
+  if (dev >= 0 && dev < kMaxDevices && (g_smem_ready[dev].load(std::memory_order_acquire) & bit)) return PD_OK;
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes) != cudaSuccess)
+    return PD_ERR_CUDA;
+  if (dev >= 0 && dev < kMaxDevices) g_smem_ready[dev].fetch_or(bit, std::memory_order_acq_rel);
+  return PD_OK;
+}
+
+pd_status stage1(const pd_plan* plan, const void* q, const void* k_pool, const void* v_pool,
+                 const int32_t* block_tables, const int32_t* seq_lens, int32_t window, float scale,
+                 void* workspace, size_t workspace_bytes, void* out, void* stream) {
+  if (!pd::plan_is_valid(plan)) return PD_ERR_INVALID_ARG;
+  const pd_layer_desc& ly = plan->layer;
+  if (window != ly.window) return PD_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return PD_ERR_INVALID_ARG;
+  if (!workspace || !aligned(workspace, 256)) return PD_ERR_INVALID_ARG;
+  if (workspace_bytes < plan->workspace_bytes) return PD_ERR_WORKSPACE_TOO_SMALL;
+  if (plan->batch == 0) return PD_OK;
+  if (!q || !k_pool || !block_tables || !seq_lens || !out) return PD_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k_pool, 16) || !aligned(out, 16) || !aligned(block_tables, 4) ||
+      !aligned(seq_lens, 4))
+    return PD_ERR_INVALID_ARG;
+  if (ly.kv_shared) {
+    if (v_pool && v_pool != k_pool) return PD_ERR_INVALID_ARG;
+    v_pool = k_pool;
+  } else {
+    if (!v_pool || v_pool == k_pool || !aligned(v_pool, 16)) return PD_ERR_INVALID_ARG;
+  }
+
+  const void* fn = pd::stage1_kernel_ptr(plan->variant);
+  if (!fn) return PD_ERR_INVALID_ARG;
+  pd_status st = ensure_smem_attr(plan->variant, fn, plan->smem_bytes);
+  if (st != PD_OK) return st;
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  pd::Stage1Params p;
+  p.q = static_cast<const uint16_t*>(q);
+  p.k_pool = static_cast<const uint16_t*>(k_pool);
+  p.v_pool = static_cast<const uint16_t*>(v_pool);
+  p.block_tables = block_tables;
+  p.seq_lens = seq_lens;
+  p.out = out;
+  p.lse_part = reinterpret_cast<float*>(ws + plan->lse_offset);
+  p.o_part = reinterpret_cast<float*>(ws + plan->opart_offset);
+  p.err = reinterpret_cast<uint32_t*>(ws);
+  p.scale_log2 = scale * kLog2e;
+  p.window = ly.window;
+  p.num_pages = ly.num_pages;
+  p.max_pages = ly.max_pages_per_seq;
+  p.page_size = ly.page_size;
+  p.num_q_heads = ly.num_q_heads;
+  p.num_kv_heads = ly.num_kv_heads;
+  p.num_splits = plan->num_splits;
+  p.chunk_tokens = plan->chunk_tokens;
+
+  void* args[] = {&p};
+  const dim3 grid(plan->grid_x, plan->grid_y, plan->grid_z);
+  const dim3 block(plan->threads_per_cta);
+  cudaError_t e = cudaLaunchKernel(fn, grid, block, args, plan->smem_bytes, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    return PD_ERR_CUDA;
+  }
+  return PD_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+pd_status paged_decode_global(const pd_plan* plan, const void* q, const void* k_pool, const void* v_pool,
+                              const int32_t* block_tables, const int32_t* seq_lens, float scale,
+                              void* workspace, size_t workspace_bytes, void* out, void* stream) {
+  if (!plan || plan->layer.window != 0) return PD_ERR_INVALID_ARG;
+  return stage1(plan, q, k_pool, v_pool, block_tables, seq_lens, 0, scale, workspace, workspace_bytes, out,
+                stream);
+}
+
+pd_status paged_decode_window(const pd_plan* plan, const void* q, const void* k_pool, const void* v_pool,
+                              const int32_t* block_tables, const int32_t* seq_lens, int32_t window,
+                              float scale, void* workspace, size_t workspace_bytes, void* out, void* stream) {
+  if (!plan || window <= 0 || plan->layer.window != window) return PD_ERR_INVALID_ARG;
+  return stage1(plan, q, k_pool, v_pool, block_tables, seq_lens, window, scale, workspace, workspace_bytes,
+                out, stream);
+}
+
+pd_status paged_decode_merge(const pd_plan* plan, const void* workspace, size_t workspace_bytes, void* out,
+                             void* stream) {
+  if (!pd::plan_is_valid(plan)) return PD_ERR_INVALID_ARG;
+  if (plan->num_splits == 1 || plan->batch == 0) return PD_OK;
+  if (!workspace || !aligned(workspace, 256) || !out || !aligned(out, 16)) return PD_ERR_INVALID_ARG;
+  if (workspace_bytes < plan->workspace_bytes) return PD_ERR_WORKSPACE_TOO_SMALL;
+  const uint8_t* ws = static_cast<const uint8_t*>(workspace);
+  pd::MergeParams p;
+  p.lse_part = reinterpret_cast<const float*>(ws + plan->lse_offset);
+  p.o_part = reinterpret_cast<const float*>(ws + plan->opart_offset);
+  p.out = out;
+  p.num_splits = plan->num_splits;
+  p.head_dim = plan->layer.head_dim;
+  const int rows = plan->batch * plan->layer.num_q_heads;
+  if (pd::launch_merge(p, rows, stream) != 0) return PD_ERR_CUDA;
+  return PD_OK;
+}
+
+pd_status paged_decode_check_device_error(const pd_plan* plan, void* workspace, size_t workspace_bytes,
+                                          void* stream, uint32_t* flags) {
+  (void)plan;
+  if (!workspace || workspace_bytes < sizeof(uint32_t)) return PD_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return PD_ERR_CUDA;
+  uint32_t word = 0;
+  if (cudaMemcpy(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return PD_ERR_CUDA;
+  if (flags) *flags = word;
+  if (word != 0) {
+    if (cudaMemset(workspace, 0, sizeof(word)) != cudaSuccess) return PD_ERR_CUDA;
+    return PD_ERR_DEVICE_FAULT;
+  }
+  return PD_OK;
+}
+
+}  // extern "C"

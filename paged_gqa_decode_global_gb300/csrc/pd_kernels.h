@@ -1,0 +1,41 @@
+// Kernel parameter blocks and launch entry points shared by the C ABI layer.
+#pragma once
+
+#include <cstdint>
+
+#include "pd_variants.h"
+
+namespace pd {
+
+struct Stage1Params {
+  const uint16_t* q;            // bf16 [B, Hq, D]
+  const uint16_t* k_pool;       // bf16 [num_pages, Hkv, P, D]
+  const uint16_t* v_pool;       // bf16, == k_pool for a K=V layer
+  const int32_t* block_tables;  // [B, max_pages]
+  const int32_t* seq_lens;      // [B]
+  void* out;                    // bf16 [B, Hq, D] (written when num_splits == 1)
+  float* lse_part;              // [B, Hq, S] natural-log log-sum-exp of each piece
+  float* o_part;                // [B, Hq, S, D] normalised partial outputs
+  uint32_t* err;                // device error word
+  float scale_log2;             // softmax scale * log2(e)
+  int32_t window;               // 0 = global layer
+  int32_t num_pages, max_pages, page_size;
+  int32_t num_q_heads, num_kv_heads;
+  int32_t num_splits, chunk_tokens;
+};
+
+struct MergeParams {
+  const float* lse_part;  // [B, Hq, S]
+  const float* o_part;    // [B, Hq, S, D]
+  void* out;              // bf16 [B, Hq, D]
+  int32_t num_splits;
+  int32_t head_dim;
+};
+
+// Address of the stage-1 kernel of a variant (nullptr if unknown).
+const void* stage1_kernel_ptr(int variant);
+
+// Launch the merge for rows = B * Hq; returns the CUDA error code.
+int launch_merge(const MergeParams& p, int rows, void* stream);
+
+}  // namespace pd

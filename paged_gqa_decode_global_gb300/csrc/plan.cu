@@ -1,0 +1,230 @@
+// Host-side planner of the paged decode library: argument validation, the
+// choice of kernel instance, the KV split count and the workspace size.
+// Pure host code: no CUDA call.
+//
+// Split-KV with a worst-case-sized partial buffer follows the vLLM concepts page
+// "模型库与算子层 — 概念", section "MLA 与 Sparse MLA（DSA）" (num_kv_splits pieces,
+// partial results plus log-sum-exp, the buffer reserved up front). The split
+// count itself is this library's own choice: the pages give no rule for it.
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <functional>
+#include <queue>
+#include <vector>
+
+#include "paged_decode.h"
+#include "pd_kernels.h"
+
+namespace pd {
+
+#define PD_VARIANT_ROW(ID, D, G, KVS, NW, SPW)                                                       \
+  VariantInfo{ID, D, G, KVS ? 1 : 0, NW, SPW, Stage1Cfg<D, G, KVS, NW, SPW>::TB,                     \
+              Stage1Cfg<D, G, KVS, NW, SPW>::THREADS, Stage1Cfg<D, G, KVS, NW, SPW>::SMEM_BYTES},
+const VariantInfo kVariants[] = {PD_FOR_EACH_VARIANT(PD_VARIANT_ROW)};
+#undef PD_VARIANT_ROW
+const int kNumVariants = sizeof(kVariants) / sizeof(kVariants[0]);
+
+}  // namespace pd
+
+namespace {
+
+constexpr uint32_t kPlanMagic = 0x50444543u;  // "PDEC"
+constexpr int32_t kAbiVersion = 1;
+
+const pd::VariantInfo* find_variant(int head_dim, int group, int kv_shared) {
+  for (int i = 0; i < pd::kNumVariants; ++i) {
+    const pd::VariantInfo& v = pd::kVariants[i];
+    if (v.head_dim == head_dim && v.group == group && v.kv_shared == kv_shared) return &v;
+  }
+  return nullptr;
+}
+
+uint64_t align_up(uint64_t x, uint64_t a) { return (x + a - 1) / a * a; }
+
+// Cost model of one launch, in microseconds: every CTA takes a fixed start-up
+// cost plus its tokens' bytes at one SM's share of HBM bandwidth; CTAs are
+// handed to `slots` resident positions in launch order (split index fastest),
+// each to the position that frees first. Pieces past a request's range exit
+// almost at once. A split count above one adds the merge launch and its traffic.
+struct CostModel {
+  double us_per_token;   // one KV head's token bytes / per-SM bandwidth
+  double cta_fixed_us;   // launch, pipeline fill, epilogue
+  double empty_cta_us;
+  double merge_fixed_us;
+  double merge_us_per_byte;
+  int slots;
+};
+
+double simulate(const std::vector<int>& n_tok, int hkv, int chunk, int splits, const CostModel& cm,
+                uint64_t merge_bytes) {
+  std::priority_queue<double, std::vector<double>, std::greater<double>> free_at;
+  for (int i = 0; i < cm.slots; ++i) free_at.push(0.0);
+  double makespan = 0.0;
+  for (size_t b = 0; b < n_tok.size(); ++b) {
+    for (int g = 0; g < hkv; ++g) {
+      for (int s = 0; s < splits; ++s) {
+        const long long lo = (long long)s * chunk;
+        long long len = (s == splits - 1) ? n_tok[b] - lo : std::min<long long>(chunk, n_tok[b] - lo);
+        const double dur = len > 0 ? cm.cta_fixed_us + len * cm.us_per_token : cm.empty_cta_us;
+        const double start = free_at.top();
+        free_at.pop();
+        const double end = start + dur;
+        free_at.push(end);
+        makespan = std::max(makespan, end);
+      }
+    }
+  }
+  if (splits > 1) makespan += cm.merge_fixed_us + merge_bytes * cm.merge_us_per_byte;
+  return makespan;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t paged_decode_abi_version(void) { return kAbiVersion; }
+
+const char* paged_decode_status_string(pd_status status) {
+  switch (status) {
+    case PD_OK:
+      return "ok";
+    case PD_ERR_INVALID_ARG:
+      return "invalid argument";
+    case PD_ERR_UNSUPPORTED:
+      return "unsupported head_dim / group size";
+    case PD_ERR_WORKSPACE_TOO_SMALL:
+      return "workspace too small";
+    case PD_ERR_CUDA:
+      return "CUDA runtime error";
+    case PD_ERR_DEVICE_FAULT:
+      return "device reported a bad page, a bad length or a timed-out wait";
+  }
+  return "unknown status";
+}
+
+pd_status paged_decode_plan(const pd_layer_desc* layer, int32_t batch, const int32_t* seq_lens_host,
+                            int32_t sm_count, pd_plan* plan) {
+  if (!layer || !plan) return PD_ERR_INVALID_ARG;
+  const pd_layer_desc& ly = *layer;
+  if (ly.num_q_heads <= 0 || ly.num_kv_heads <= 0 || ly.num_q_heads % ly.num_kv_heads != 0)
+    return PD_ERR_INVALID_ARG;
+  if (ly.head_dim <= 0 || ly.page_size <= 0 || ly.page_size % 16 != 0) return PD_ERR_INVALID_ARG;
+  if (ly.num_pages <= 0 || ly.max_pages_per_seq <= 0 || ly.window < 0) return PD_ERR_INVALID_ARG;
+  if (ly.kv_shared != 0 && ly.kv_shared != 1) return PD_ERR_INVALID_ARG;
+  if (batch < 0 || batch > 65535 || ly.num_kv_heads > 65535 || sm_count <= 0) return PD_ERR_INVALID_ARG;
+  if (batch > 0 && !seq_lens_host) return PD_ERR_INVALID_ARG;
+  const long long cap = (long long)ly.max_pages_per_seq * ly.page_size;
+  if (cap > 0x7fffffffLL) return PD_ERR_INVALID_ARG;
+  int32_t max_len = 0;
+  for (int b = 0; b < batch; ++b) {
+    if (seq_lens_host[b] < 0 || seq_lens_host[b] > cap) return PD_ERR_INVALID_ARG;
+    max_len = std::max(max_len, seq_lens_host[b]);
+  }
+  const int group = ly.num_q_heads / ly.num_kv_heads;
+  const pd::VariantInfo* v = find_variant(ly.head_dim, group, ly.kv_shared);
+  if (!v) return PD_ERR_UNSUPPORTED;
+  const int TB = v->block_tokens;
+
+  // block-aligned attended span of each request
+  std::vector<int> n_tok(batch);
+  int max_n = 0;
+  long long total = 0;
+  for (int b = 0; b < batch; ++b) {
+    const int L = seq_lens_host[b];
+    const int lo = (ly.window > 0 && L > ly.window) ? L - ly.window : 0;
+    n_tok[b] = L > 0 ? L - (lo / TB) * TB : 0;
+    max_n = std::max(max_n, n_tok[b]);
+    total += n_tok[b];
+  }
+
+  CostModel cm;
+  const double kv_bytes_per_token = (double)ly.head_dim * 2.0 * (ly.kv_shared ? 1.0 : 2.0);
+  const double sm_bw_bytes_per_us = 7.0e12 / 1e6 / sm_count;  // ~7 TB/s shared by the SMs
+  cm.us_per_token = kv_bytes_per_token / sm_bw_bytes_per_us;
+  cm.cta_fixed_us = 2.0;
+  cm.empty_cta_us = 0.2;
+  cm.merge_fixed_us = 2.0;
+  cm.merge_us_per_byte = 1.0 / 7.0e6;
+  cm.slots = sm_count;  // one resident CTA per SM (shared memory bound)
+
+  int best_chunk = std::max(16, (int)align_up((uint64_t)std::max(max_n, 1), 16));
+  int best_splits = 1;
+  if (max_n > 0) {
+    // candidates: multiples of 16 on a geometric grid, from the point where the
+    // launch would need more than ~8 waves up to one piece per request
+    const long long work = total * ly.num_kv_heads;
+    const int c_min = (int)std::max<long long>(64, align_up((uint64_t)(work / (8LL * cm.slots) + 1), 16));
+    const int c_max = (int)align_up((uint64_t)max_n, 16);
+    std::vector<int> cands;
+    for (double c = c_min; c < c_max; c *= 1.08) cands.push_back((int)align_up((uint64_t)c, 16));
+    for (int w = 1; w <= 8; ++w) {
+      // pieces sized so B * Hkv * S lands on exactly w waves for the longest request
+      const long long per_wave = (long long)w * cm.slots;
+      const long long pairs = (long long)batch * ly.num_kv_heads;
+      const long long s = std::max<long long>(1, per_wave / std::max<long long>(1, pairs));
+      cands.push_back((int)align_up((uint64_t)((max_n + s - 1) / s), 16));
+    }
+    cands.push_back(c_max);
+    std::sort(cands.begin(), cands.end());
+    cands.erase(std::unique(cands.begin(), cands.end()), cands.end());
+    double best = 1e300;
+    for (int c : cands) {
+      if (c < 16) continue;
+      const int s = (max_n + c - 1) / c;
+      const uint64_t merge_bytes = (uint64_t)batch * ly.num_q_heads * s * (ly.head_dim + 1) * 4ull * 2ull;
+      const double cost = simulate(n_tok, ly.num_kv_heads, c, s, cm, merge_bytes);
+      if (cost < best * (1.0 - 1e-9) || (cost <= best && s < best_splits)) {
+        best = cost;
+        best_chunk = c;
+        best_splits = s;
+      }
+    }
+  }
+
+  std::memset(plan, 0, sizeof(*plan));
+  plan->layer = ly;
+  plan->batch = batch;
+  plan->num_splits = best_splits;
+  plan->chunk_tokens = best_chunk;
+  plan->block_tokens = TB;
+  plan->variant = v->id;
+  plan->grid_x = best_splits;
+  plan->grid_y = ly.num_kv_heads;
+  plan->grid_z = batch;
+  plan->threads_per_cta = v->threads;
+  plan->smem_bytes = v->smem_bytes;
+  plan->sm_count = sm_count;
+  plan->max_seq_len = max_len;
+  const uint64_t rows = (uint64_t)batch * ly.num_q_heads;
+  plan->lse_offset = pd::kWorkspaceHeader;
+  if (best_splits > 1) {
+    plan->opart_offset = align_up(plan->lse_offset + rows * best_splits * 4ull, 256);
+    plan->workspace_bytes = plan->opart_offset + rows * best_splits * (uint64_t)ly.head_dim * 4ull;
+  } else {
+    plan->opart_offset = pd::kWorkspaceHeader;
+    plan->workspace_bytes = pd::kWorkspaceHeader;
+  }
+  plan->magic = kPlanMagic;
+  plan->version = kAbiVersion;
+  return PD_OK;
+}
+
+}  // extern "C"
+
+namespace pd {
+
+bool plan_is_valid(const pd_plan* plan) {
+  if (!plan || plan->magic != kPlanMagic || plan->version != (uint32_t)kAbiVersion) return false;
+  if (plan->variant < 0 || plan->variant >= kNumVariants) return false;
+  const VariantInfo& v = kVariants[plan->variant];
+  const pd_layer_desc& ly = plan->layer;
+  if (ly.num_kv_heads <= 0 || ly.num_q_heads != ly.num_kv_heads * v.group) return false;
+  if (ly.head_dim != v.head_dim || ly.kv_shared != v.kv_shared) return false;
+  if (plan->num_splits < 1 || plan->chunk_tokens < 16 || plan->chunk_tokens % 16 != 0) return false;
+  if (plan->batch < 0 || plan->grid_x != plan->num_splits) return false;
+  if (plan->threads_per_cta != v.threads || plan->smem_bytes != v.smem_bytes) return false;
+  return true;
+}
+
+}  // namespace pd

@@ -1,0 +1,123 @@
+"""Host-side checks of the C ABI (no GPU): the library builds, loads and exports
+every function declared in include/*.h; the planner validates its arguments
+and its plans cover every attended token."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+from paged_gqa_decode_global_gb300 import binding as b
+from paged_gqa_decode_global_gb300 import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return b.load_library()
+
+
+def _declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^\s*[A-Za-z_][\w\s\*]*?\b([a-z_][a-z0-9_]*)\s*\(", text, flags=re.M):
+            if not m.group(1).startswith(("if", "sizeof")):
+                names.add(m.group(1))
+    return sorted(names)
+
+
+def test_header_declares_the_entry_points():
+    names = _declared_functions()
+    for n in b.EXPORTED:
+        assert n in names, n
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), f"{name} declared but not exported"
+
+
+def test_build_targets_sm103a_only():
+    assert build.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def test_status_strings_and_version(lib):
+    assert b.status_string(b.PD_OK) == "ok"
+    assert "workspace" in b.status_string(b.PD_ERR_WORKSPACE_TOO_SMALL)
+    assert b.abi_version() == 1
+
+
+def _plan(lens, Hq=16, Hkv=4, d=512, P=16, pages=4096, maxp=None, window=0, kv_shared=False, sms=152):
+    if maxp is None:
+        maxp = max(1, max([(L + P - 1) // P for L in lens] or [1]))
+    return b.paged_decode_plan(b.layer_desc(Hq, Hkv, d, P, pages, maxp, window, kv_shared), lens, sms)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(Hq=15), b.PD_ERR_INVALID_ARG),          # Hq not a multiple of Hkv
+    (dict(P=24), b.PD_ERR_INVALID_ARG),           # page size not a multiple of 16
+    (dict(window=-1), b.PD_ERR_INVALID_ARG),
+    (dict(sms=0), b.PD_ERR_INVALID_ARG),
+    (dict(d=384), b.PD_ERR_UNSUPPORTED),
+    (dict(d=128), b.PD_ERR_UNSUPPORTED),
+    (dict(Hq=64, Hkv=4), b.PD_ERR_UNSUPPORTED),   # group of 16
+    (dict(Hq=32, Hkv=4, d=512), b.PD_ERR_UNSUPPORTED),  # group of 8 at d = 512
+])
+def test_plan_rejects(lib, kw, status):
+    with pytest.raises(b.PagedDecodeError) as e:
+        _plan([100, 200], **kw)
+    assert e.value.status == status
+
+
+def test_plan_rejects_length_beyond_table(lib):
+    with pytest.raises(b.PagedDecodeError) as e:
+        _plan([100, 200], maxp=5)
+    assert e.value.status == b.PD_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("lens,window,d,Hkv", [
+    ([1024] * 8, 0, 512, 4),
+    ([32768] * 4, 0, 512, 4),
+    ([131072], 0, 512, 4),
+    ([4000, 4100, 4200, 4033], 1024, 256, 8),
+    ([1, 0, 17, 300000], 0, 512, 4),
+    ([1024, 131072, 5000, 77777, 1500], 0, 512, 4),
+    ([0, 0], 0, 256, 8),
+])
+def test_plan_covers_every_token(lib, lens, window, d, Hkv):
+    for sms in (1, 8, 152, 1000):
+        pl = _plan(lens, Hkv=Hkv, Hq=Hkv * 2, d=d, window=window, pages=10 ** 6, sms=sms)
+        TB = pl.block_tokens
+        assert pl.chunk_tokens % 16 == 0 and pl.num_splits >= 1
+        for L in lens:
+            lo = max(0, L - window) if window else 0
+            span = L - (lo // TB) * TB if L else 0
+            assert pl.num_splits * pl.chunk_tokens >= span
+        if pl.num_splits > 1:
+            rows = len(lens) * Hkv * 2
+            assert pl.workspace_bytes >= pl.opart_offset + rows * pl.num_splits * d * 4
+            assert pl.opart_offset >= pl.lse_offset + rows * pl.num_splits * 4
+        assert pl.workspace_bytes >= 256
+        assert (pl.grid_x, pl.grid_y, pl.grid_z) == (pl.num_splits, Hkv, len(lens))
+
+
+def test_plan_fills_the_machine_on_long_contexts(lib):
+    pl = _plan([131072], sms=152)
+    assert pl.grid_x * pl.grid_y >= 152
+    pl = _plan([1024] * 8, sms=152)
+    assert pl.grid_x * pl.grid_y * pl.grid_z >= 100
+
+
+def test_no_gpu_calls_fail_cleanly_without_a_device(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a device is present")
+    pl = _plan([64])
+    # a host-side argument error is reported before anything touches CUDA
+    st = lib.paged_decode_global(ctypes.byref(pl), None, None, None, None, None, 1.0, None, 0, None, None)
+    assert st == b.PD_ERR_INVALID_ARG

@@ -1,0 +1,217 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Bar (bf16 output, fp32 accumulation): max |gpu - oracle| <= 2e-2 and cosine
+similarity > 0.9995 over each output tensor; rows with nothing attended must be
+exactly zero; a one-token sequence must return its value row bit for bit.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_gqa_decode_global_gb300 import binding as b
+from paged_gqa_decode_global_gb300 import inputs as synth
+
+pytestmark = pytest.mark.gpu
+
+MAX_ABS = 2e-2
+MIN_COS = 0.9995
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from paged_gqa_decode_global_gb300 import build
+    build.build()
+    b.load_library()
+
+
+def run_gpu(li, sm_count=None, out_fill=float("nan")):
+    step = b.LayerStep.for_inputs(li, sm_count)
+    out = torch.full_like(li.q, out_fill)
+    step.run(li, out)
+    flags = step.check()
+    assert flags == 0
+    return out, step
+
+
+def run_oracle(li):
+    return oracle.decode(synth.bits_u16(li.q), synth.bits_u16(li.k_pool),
+                         None if li.v_pool is None else synth.bits_u16(li.v_pool),
+                         li.block_tables.cpu().numpy(), li.seq_lens.cpu().numpy(), li.scale, li.window)
+
+
+def compare(gpu_out, ref, li, tag=""):
+    got = gpu_out.float().cpu().numpy().astype(np.float64)
+    assert np.isfinite(got).all(), f"{tag}: non-finite output"
+    err = np.abs(got - ref).max()
+    empty = np.array([n == 0 for n in li.attended()])
+    if empty.any():
+        assert (got[empty] == 0).all(), f"{tag}: empty rows not zero"
+    g, r = got[~empty].ravel(), ref[~empty].ravel()
+    cos = float(g @ r / (np.linalg.norm(g) * np.linalg.norm(r))) if g.size else 1.0
+    assert err <= MAX_ABS, f"{tag}: max abs {err:.3e}"
+    assert cos > MIN_COS, f"{tag}: cosine {cos:.7f}"
+    return err, cos
+
+
+# ---- the five named workloads at full size -------------------------------------
+
+@pytest.mark.parametrize("cid,part", [(1, None), (2, None), (3, None), (4, "a"), (4, "b"), (4, "c"),
+                                      (5, "global"), (5, "sliding")])
+def test_workload_matches_oracle(cid, part):
+    for li in synth.workload(cid, device="cuda", part=part):
+        out, step = run_gpu(li)
+        err, cos = compare(out, run_oracle(li), li, f"{li.name} S={step.plan.num_splits}")
+        print(f"{li.name}: splits {step.plan.num_splits} chunk {step.plan.chunk_tokens} max_abs {err:.2e} cos {cos:.7f}")
+
+
+# ---- every kernel instance on ragged batches ----------------------------------
+
+VARIANTS = [(512, G, kvs) for G in (1, 2, 4) for kvs in (False, True)] + \
+           [(256, G, kvs) for G in (1, 2, 4, 8) for kvs in (False, True)]
+
+
+@pytest.mark.parametrize("d,G,kvs", VARIANTS)
+@pytest.mark.parametrize("window", [0, 37, 1000])
+def test_variants_ragged(d, G, kvs, window):
+    Hkv = 2
+    lens = [1, 17, 300, 0, 1000, 33]
+    li = synth.make_layer("v", lens, Hkv * G, Hkv, d, window=window, kv_shared=kvs,
+                          pool_pages=sum((L + 15) // 16 for L in lens) + 5, seed=d + G + 100 * kvs + window,
+                          device="cuda")
+    ref = run_oracle(li)
+    for sms in (3, 152):  # different split counts
+        out, step = run_gpu(li, sm_count=sms)
+        compare(out, ref, li, f"d{d} G{G} kvs{kvs} W{window} sms{sms} S{step.plan.num_splits}")
+
+
+def test_page_size_32():
+    lens = [100, 64, 5]
+    li = synth.make_layer("p32", lens, 8, 2, 512, page_size=32, pool_pages=12, seed=5, device="cuda")
+    compare(run_gpu(li)[0], run_oracle(li), li, "P32")
+
+
+# ---- closed forms and invariants on the GPU ------------------------------------
+
+@pytest.mark.parametrize("d,G,kvs", [(512, 4, False), (512, 4, True), (256, 2, False)])
+def test_single_token_is_bit_exact(d, G, kvs):
+    li = synth.make_layer("one", [1, 1, 1], 2 * G, 2, d, kv_shared=kvs, pool_pages=7, seed=3, device="cuda")
+    for sms in (1, 152):
+        out, _ = run_gpu(li, sm_count=sms)
+        pool = li.k_pool if kvs else li.v_pool
+        for bi in range(3):
+            page = int(li.block_tables[bi, 0])
+            want = pool[page, :, 0, :].repeat_interleave(G, dim=0)
+            assert torch.equal(out[bi], want)
+
+
+def test_empty_sequences_give_zero():
+    li = synth.make_layer("empty", [0, 0, 40], 8, 2, 512, pool_pages=8, seed=4, device="cuda")
+    out, _ = run_gpu(li)
+    assert (out[:2] == 0).all()
+    compare(out, run_oracle(li), li, "empty")
+
+
+def test_deterministic_and_split_consistent():
+    li = synth.workload(2, device="cuda")[0]
+    a, _ = run_gpu(li)
+    a2, _ = run_gpu(li)
+    assert torch.equal(a, a2), "repeated runs differ"
+    c, step_c = run_gpu(li, sm_count=1)
+    assert step_c.plan.num_splits == 1
+    diff = (a.float() - c.float()).abs().max().item()
+    assert diff <= 2 * MAX_ABS
+
+
+def test_page_permutation_is_bitwise_invariant():
+    li = synth.make_layer("perm", [300, 1000, 77], 16, 4, 512, pool_pages=120, seed=6, device="cuda")
+    a, step = run_gpu(li)
+    g = torch.Generator().manual_seed(1)
+    perm = torch.randperm(li.num_pages, generator=g)
+    inv = torch.empty_like(perm)
+    inv[perm] = torch.arange(li.num_pages)
+    inv = inv.cuda()
+    t2 = li.block_tables.clone()
+    valid = t2 >= 0
+    t2[valid] = perm.cuda()[t2[valid].long()].to(torch.int32)
+    out2 = torch.empty_like(li.q)
+    step(li.q, li.k_pool[inv].contiguous(), li.v_pool[inv].contiguous(), t2, li.seq_lens, li.scale, out2)
+    assert step.check() == 0
+    assert torch.equal(a, out2)
+
+
+def test_window_ignores_rows_before_the_window():
+    W = 100
+    li = synth.make_layer("win", [1000, 517, 250], 16, 8, 256, window=W, pool_pages=120, seed=8, device="cuda")
+    a, step = run_gpu(li)
+    k2, v2 = li.k_pool.clone(), li.v_pool.clone()
+    for bi, L in enumerate(li.seq_lens_list()):
+        for t in range(0, L - W):
+            page = int(li.block_tables[bi, t // 16])
+            k2[page, :, t % 16] = 50.0
+            v2[page, :, t % 16] = -50.0
+    out2 = torch.empty_like(li.q)
+    step(li.q, k2, v2, li.block_tables, li.seq_lens, li.scale, out2)
+    assert torch.equal(a, out2)
+
+
+# ---- device-side error reporting (the kernel's own checks; nothing faults) -------
+
+def test_bad_page_id_sets_flag_and_skips_the_page():
+    li = synth.make_layer("bad", [64, 64], 8, 2, 512, pool_pages=10, seed=9, device="cuda")
+    bt = li.block_tables.clone()
+    bt[1, 2] = 10 ** 6  # far outside the pool
+    step = b.LayerStep.for_inputs(li)
+    out = torch.empty_like(li.q)
+    step(li.q, li.k_pool, li.v_pool, bt, li.seq_lens, li.scale, out)
+    with pytest.raises(b.PagedDecodeError) as e:
+        step.check()
+    assert e.value.status == b.PD_ERR_DEVICE_FAULT and e.value.flags & b.PD_DEVFLAG_BAD_PAGE
+    assert step.check() == 0  # cleared
+    ref = run_oracle(li)
+    compare(out[:1], ref[:1], synth.make_layer("x", [64], 8, 2, 512, pool_pages=10, seed=9), "untouched row")
+    assert torch.isfinite(out[1].float()).all()
+
+
+def test_bad_seq_len_sets_flag():
+    li = synth.make_layer("len", [64, 64], 8, 2, 512, pool_pages=10, seed=10, device="cuda")
+    step = b.LayerStep.for_inputs(li)
+    out = torch.empty_like(li.q)
+    sl = li.seq_lens.clone()
+    sl[0] = -5
+    step(li.q, li.k_pool, li.v_pool, li.block_tables, sl, li.scale, out)
+    with pytest.raises(b.PagedDecodeError) as e:
+        step.check()
+    assert e.value.flags & b.PD_DEVFLAG_BAD_SEQLEN
+    assert (out[0] == 0).all()
+
+
+def test_abi_rejects_bad_arguments_without_launching():
+    li = synth.make_layer("args", [64], 8, 2, 512, pool_pages=5, seed=11, device="cuda")
+    step = b.LayerStep.for_inputs(li)
+    out = torch.zeros_like(li.q)
+    cases = [
+        dict(v_pool=None),                       # K != V layer without V
+        dict(v_pool=li.k_pool),                  # V aliasing K on a K != V layer
+        dict(scale=float("inf")),
+        dict(q=li.q.view(-1)[1:]),               # misaligned q
+    ]
+    for kw in cases:
+        args = dict(q=li.q, v_pool=li.v_pool, scale=li.scale)
+        args.update(kw)
+        with pytest.raises(b.PagedDecodeError) as e:
+            b.paged_decode_global(step.plan, args["q"], li.k_pool, args["v_pool"], li.block_tables, li.seq_lens,
+                                  args["scale"], step.workspace, out)
+        assert e.value.status == b.PD_ERR_INVALID_ARG
+    with pytest.raises(b.PagedDecodeError) as e:
+        b.paged_decode_window(step.plan, li.q, li.k_pool, li.v_pool, li.block_tables, li.seq_lens, 16, li.scale,
+                              step.workspace, out)
+    assert e.value.status == b.PD_ERR_INVALID_ARG
+    if step.plan.num_splits > 1:
+        with pytest.raises(b.PagedDecodeError) as e:
+            b.paged_decode_global(step.plan, li.q, li.k_pool, li.v_pool, li.block_tables, li.seq_lens, li.scale,
+                                  step.workspace, out, workspace_bytes=16)
+        assert e.value.status == b.PD_ERR_WORKSPACE_TOO_SMALL
+    torch.cuda.synchronize()
+    assert (out == 0).all()  # nothing ran
+    assert step.check() == 0
