@@ -237,20 +237,24 @@ def run_ours(args, world, rank, local):
         return graphs
 
     def timed(graphs, sample_clocks=False):
+        # CUDAGraph.replay() launches on the current stream: make it `stream`,
+        # the stream the events are recorded on
         start = torch.cuda.Event(enable_timing=True)
         end = torch.cuda.Event(enable_timing=True)
-        for g in graphs[:1]:  # warm the graph exec once
-            g.replay()
+        with torch.cuda.stream(stream):
+            for g in graphs[:1]:  # warm the graph exec once
+                g.replay()
         torch.cuda.synchronize()
         barrier(world)
         sampler = ClockSampler(local) if sample_clocks else None
         if sampler:
             sampler.__enter__()
         torch.cuda.synchronize()
-        start.record(stream)
-        for g in graphs:
-            g.replay()
-        end.record(stream)
+        with torch.cuda.stream(stream):
+            start.record(stream)
+            for g in graphs:
+                g.replay()
+            end.record(stream)
         torch.cuda.synchronize()
         if sampler:
             sampler.__exit__(None, None, None)

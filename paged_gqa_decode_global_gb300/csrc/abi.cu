@@ -23,6 +23,77 @@ std::atomic<uint64_t> g_smem_ready[kMaxDevices];
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
+// ---- TMA descriptors ----------------------------------------------------------
+// cuTensorMapEncodeTiled is a driver entry point; it is looked up once through
+// the runtime so the library does not link the driver library directly.
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled_fn() {
+  static std::atomic<EncodeTiledFn> cached{nullptr};
+  EncodeTiledFn fn = cached.load(std::memory_order_acquire);
+  if (fn) return fn;
+  void* sym = nullptr;
+  cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &sym, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || !sym) {
+    (void)cudaGetLastError();
+    return nullptr;
+  }
+  fn = reinterpret_cast<EncodeTiledFn>(sym);
+  cached.store(fn, std::memory_order_release);
+  return fn;
+}
+
+// Rank the pools are viewed at: 3 ({64 dims, rows, slabs}, one copy per block)
+// when the driver accepts that view, else 2 ({D, rows}, one copy per slab).
+std::atomic<int> g_tma_rank{0};
+
+// Describe a pool [num_pages, Hkv, P, D] bf16 for 16-row boxes that land as
+// [slab][row][128 B] with the 128-byte swizzle.
+pd_status encode_pool_map(CUtensorMap* map, const void* pool, const pd_layer_desc& ly, int rank) {
+  EncodeTiledFn fn = encode_tiled_fn();
+  if (!fn) return PD_ERR_CUDA;
+  const cuuint64_t rows = (cuuint64_t)ly.num_pages * ly.num_kv_heads * ly.page_size;
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r;
+  if (rank == 3) {
+    const cuuint64_t dims[3] = {64, rows, (cuuint64_t)ly.head_dim / 64};
+    const cuuint64_t strides[2] = {(cuuint64_t)ly.head_dim * 2, 128};
+    const cuuint32_t box[3] = {64, 16, (cuuint32_t)ly.head_dim / 64};
+    r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(pool), dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else {
+    const cuuint64_t dims[2] = {(cuuint64_t)ly.head_dim, rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)ly.head_dim * 2};
+    const cuuint32_t box[2] = {64, 16};
+    r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(pool), dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  }
+  return r == CUDA_SUCCESS ? PD_OK : PD_ERR_CUDA;
+}
+
+pd_status encode_pool_maps(pd::Stage1Params& p, const void* k_pool, const void* v_pool, const pd_layer_desc& ly) {
+  int rank = g_tma_rank.load(std::memory_order_acquire);
+  if (rank == 0) {
+    rank = encode_pool_map(&p.kmap, k_pool, ly, 3) == PD_OK ? 3 : 2;
+    g_tma_rank.store(rank, std::memory_order_release);
+  }
+  pd_status st = encode_pool_map(&p.kmap, k_pool, ly, rank);
+  if (st != PD_OK) return st;
+  if (v_pool == k_pool) {
+    p.vmap = p.kmap;
+  } else {
+    st = encode_pool_map(&p.vmap, v_pool, ly, rank);
+    if (st != PD_OK) return st;
+  }
+  p.tma_rank = rank;
+  return PD_OK;
+}
+
 pd_status ensure_smem_attr(int variant, const void* fn, int smem_bytes) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PD_ERR_CUDA;
@@ -62,6 +133,9 @@ pd_status stage1(const pd_plan* plan, const void* q, const void* k_pool, const v
 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   pd::Stage1Params p;
+  std::memset(&p, 0, sizeof(p));
+  st = encode_pool_maps(p, k_pool, v_pool, ly);
+  if (st != PD_OK) return st;
   p.q = static_cast<const uint16_t*>(q);
   p.k_pool = static_cast<const uint16_t*>(k_pool);
   p.v_pool = static_cast<const uint16_t*>(v_pool);

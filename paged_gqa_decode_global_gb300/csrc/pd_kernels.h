@@ -3,11 +3,19 @@
 
 #include <cstdint>
 
+#include <cuda.h>  // CUtensorMap (the encoder itself is fetched from the driver at run time)
+
 #include "pd_variants.h"
 
 namespace pd {
 
 struct Stage1Params {
+  // TMA descriptors of the K and V pools (V's = K's for a K=V layer), viewed as
+  // rank 3 {64 dims, rows = pages*Hkv*P, D/64 slabs} (tma_rank 3) or as rank 2
+  // {D, rows} (tma_rank 2); a 16-row box lands as [slab][row][128 B], 128-byte swizzled.
+  CUtensorMap kmap;
+  CUtensorMap vmap;
+  int32_t tma_rank;
   const uint16_t* q;            // bf16 [B, Hq, D]
   const uint16_t* k_pool;       // bf16 [num_pages, Hkv, P, D]
   const uint16_t* v_pool;       // bf16, == k_pool for a K=V layer

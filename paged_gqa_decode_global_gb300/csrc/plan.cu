@@ -116,6 +116,8 @@ pd_status paged_decode_plan(const pd_layer_desc* layer, int32_t batch, const int
   if (batch > 0 && !seq_lens_host) return PD_ERR_INVALID_ARG;
   const long long cap = (long long)ly.max_pages_per_seq * ly.page_size;
   if (cap > 0x7fffffffLL) return PD_ERR_INVALID_ARG;
+  // pool rows are addressed with 32-bit TMA coordinates
+  if ((long long)ly.num_pages * ly.num_kv_heads * ly.page_size > 0x7fffffffLL) return PD_ERR_UNSUPPORTED;
   int32_t max_len = 0;
   for (int b = 0; b < batch; ++b) {
     if (seq_lens_host[b] < 0 || seq_lens_host[b] > cap) return PD_ERR_INVALID_ARG;

@@ -10,18 +10,22 @@
 // result plus its log-sum-exp).
 //
 // GB300 design:
-//   * warp NW (one elected lane) is the producer: per block of TB tokens it
-//     issues one 1-D bulk TMA copy of the contiguous (page, KV head) rows of K
-//     (and one of V) into a ring stage, completion counted on an mbarrier;
+//   * warp NW (one elected lane) is the producer: per block of 16 tokens it
+//     issues one tiled TMA copy of the block's K rows (and one of its V rows)
+//     into a ring stage laid out [64-dim slab][token row][128 B] with the
+//     128-byte swizzle, so the 8 rows an ldmatrix reads fall in 8 different
+//     bank groups; completion is counted in bytes on the stage's mbarrier;
 //   * consumer warp w owns ring stages w, w+NW, ... and processes blocks
 //     w, w+NW, ... of the piece with its own online-softmax state, so warps
 //     never wait on one another inside the loop;
-//   * lanes split head_dim (16-byte chunks, conflict-free shared loads); q of
-//     all G heads and the fp32 accumulators of all G heads stay in registers;
-//   * QK: each lane forms TB*G partial dot products, one recursive-halving
-//     reduce-scatter over the 32 lanes leaves one full dot product per lane;
-//   * softmax in base 2 with q pre-scaled by scale*log2(e); PV broadcasts each
-//     probability from the lane that owns it;
+//   * both contractions run on the tensor cores (mma.sync m16n8k16, bf16
+//     inputs, fp32 accumulation), with the GQA group as the 8-wide N side:
+//       QK: S[16 tok x 8 heads]  = K[16 x d] . q^T       (A = K rows, B = q)
+//       PV: O^T[d x 8 heads]    += V^T[d x 16 tok] . P^T (A = V rows via
+//           ldmatrix.trans, B = P transposed in registers with movmatrix);
+//   * the online softmax runs in base 2 on the S fragments (scale * log2 e
+//     applied in fp32); each lane owns two heads, so the rescale of its O^T
+//     fragments needs no communication;
 //   * at the end the NW warp states are merged in shared memory and the CTA
 //     writes bf16 output (one piece) or an fp32 partial + log-sum-exp.
 #include <cuda_bf16.h>
@@ -33,31 +37,46 @@ namespace pd {
 
 namespace {
 
-// Sum NV values per lane across the warp; afterwards lane l holds, in v[0], the
-// full sum of value index l / (32 / NV). Recursive halving: at each level a lane
-// keeps the half of its values selected by its lane bit and adds the partner's.
-template <int NV>
-__device__ __forceinline__ void reduce_scatter(float (&v)[NV], int lane) {
-#pragma unroll
-  for (int half = NV / 2, mask = 16; half >= 1; half >>= 1, mask >>= 1) {
-    const bool upper = (lane & mask) != 0;
-#pragma unroll
-    for (int i = 0; i < half; ++i) {
-      const float send = upper ? v[i] : v[i + half];
-      const float keep = upper ? v[i + half] : v[i];
-      v[i] = keep + __shfl_xor_sync(kFullMask, send, mask);
-    }
-  }
-  // remaining lane bits: plain butterfly so every replica holds the sum
-#pragma unroll
-  for (int mask = 16 / NV; mask >= 1; mask >>= 1) v[0] += __shfl_xor_sync(kFullMask, v[0], mask);
+__device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+// D = A . B + D, m16n8k16, bf16 x bf16 -> fp32.
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Transpose an 8x8 bf16 matrix held one row pair per lane (fragment layout).
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
 }
 
 }  // namespace
 
 template <class C>
-__global__ void __launch_bounds__(C::THREADS, 1) stage1_kernel(const Stage1Params p) {
-  extern __shared__ __align__(128) uint8_t smem[];
+__global__ void __launch_bounds__(C::THREADS, 1) stage1_kernel(const __grid_constant__ Stage1Params p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // the swizzle pattern repeats every 1024 bytes of shared address: start there
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + C::BAR_OFFSET);
   uint64_t* empty_bar = full_bar + C::NST;
   uint32_t* stage_valid = reinterpret_cast<uint32_t*>(smem + C::VALID_OFFSET);
@@ -114,6 +133,8 @@ __global__ void __launch_bounds__(C::THREADS, 1) stage1_kernel(const Stage1Param
   if (warp == C::NW) {
     if (lane == 0) {
       const uint64_t policy = l2_evict_first_policy();
+      prefetch_tensormap(&p.kmap);
+      if (!C::KVS) prefetch_tensormap(&p.vmap);
       const int32_t* table = p.block_tables + (size_t)b * p.max_pages;
       int issued = 0;
 #pragma unroll 1
@@ -129,11 +150,20 @@ __global__ void __launch_bounds__(C::THREADS, 1) stage1_kernel(const Stage1Param
         const bool ok = (unsigned)page < (unsigned)p.num_pages;
         stage_valid[st] = ok ? 1u : 0u;
         if (ok) {
-          const size_t row = ((size_t)page * p.num_kv_heads + g) * p.page_size + (t0 % p.page_size);
+          const int row0 = (page * p.num_kv_heads + g) * p.page_size + (t0 % p.page_size);
           uint8_t* dst = smem + (size_t)st * C::STAGE_BYTES;
-          mbar_arrive_expect_tx(&full_bar[st], C::STAGE_BYTES);
-          bulk_g2s(dst, p.k_pool + row * C::D, C::KV_BYTES, &full_bar[st], policy);
-          if (!C::KVS) bulk_g2s(dst + C::KV_BYTES, p.v_pool + row * C::D, C::KV_BYTES, &full_bar[st], policy);
+          mbar_arrive_expect_tx(&full_bar[st], C::TX_BYTES);
+          if (p.tma_rank == 3) {
+            tma_load_3d(dst, &p.kmap, 0, row0, 0, &full_bar[st], policy);
+            if (!C::KVS) tma_load_3d(dst + C::KV_BYTES, &p.vmap, 0, row0, 0, &full_bar[st], policy);
+          } else {
+#pragma unroll
+            for (int sl = 0; sl < C::SLABS; ++sl) {
+              tma_load_2d(dst + sl * C::SLAB_BYTES, &p.kmap, sl * 64, row0, &full_bar[st], policy);
+              if (!C::KVS)
+                tma_load_2d(dst + C::KV_BYTES + sl * C::SLAB_BYTES, &p.vmap, sl * 64, row0, &full_bar[st], policy);
+            }
+          }
         } else {
           atomicOr(p.err, kErrBadPage);
           mbar_arrive(&full_bar[st]);
@@ -151,31 +181,49 @@ __global__ void __launch_bounds__(C::THREADS, 1) stage1_kernel(const Stage1Param
   }
 
   // ---- consumers -----------------------------------------------------------------
-  // q of the G heads for this lane's dims, pre-scaled to base-2 logits
-  float qf[C::G][C::DPL];
+  // B fragments of q (heads on N, dims on K): lane holds head lane/4, dims
+  // 2*(lane%4) + {0,1} and + {8,9} of every 16-dim step; heads past G are zero.
+  const int qh = lane >> 2;
+  const int qk = (lane & 3) * 2;
+  uint32_t qb[C::KSTEPS][2];
 #pragma unroll
-  for (int h = 0; h < C::G; ++h) {
-#pragma unroll
-    for (int c = 0; c < C::NCH; ++c) {
-      const uint4 w = __ldg(reinterpret_cast<const uint4*>(p.q + (row_hq + h) * C::D) + c * 32 + lane);
-      float f[8];
-      unpack_bf16x8(w, f);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) qf[h][c * 8 + i] = f[i] * p.scale_log2;
+  for (int ks = 0; ks < C::KSTEPS; ++ks) {
+    if (qh < C::G) {
+      const uint16_t* qrow = p.q + (row_hq + qh) * C::D + ks * 16 + qk;
+      qb[ks][0] = __ldg(reinterpret_cast<const unsigned int*>(qrow));
+      qb[ks][1] = __ldg(reinterpret_cast<const unsigned int*>(qrow + 8));
+    } else {
+      qb[ks][0] = 0u;
+      qb[ks][1] = 0u;
     }
   }
 
-  float acc[C::G][C::DPL];
+  // O^T accumulators: m-tile mt holds dims mt*16 + lane/4 (+8) x heads 2*(lane%4) (+1)
+  float acc[C::MTILES][4];
 #pragma unroll
-  for (int h = 0; h < C::G; ++h)
+  for (int mt = 0; mt < C::MTILES; ++mt)
 #pragma unroll
-    for (int i = 0; i < C::DPL; ++i) acc[h][i] = 0.f;
+    for (int i = 0; i < 4; ++i) acc[mt][i] = 0.f;
 
-  // this lane's value after the reduce-scatter: token vi / G, head vi % G
-  const int vi = lane / C::R;
-  const int my_tb = vi / C::G;
-  float m_run = -INFINITY;  // running max (base-2 logits) of head vi % G
-  float l_run = 0.f;        // running sum of 2^(s - m_run)
+  // this lane's two heads and their running max / sum (base-2 logits)
+  float m_run[2] = {-INFINITY, -INFINITY};
+  float l_run[2] = {0.f, 0.f};
+
+  // Per-lane ldmatrix offsets inside a stage. Byte (row r, 16-byte chunk c) of
+  // a slab sits at r * 128 + ((c ^ (r % 8)) * 16): the 128-byte swizzle.
+  // K (non-trans): lane supplies row (lane%8) + 8*((lane/8)%2), chunk 2*j + lane/16
+  // V (trans):     lane supplies row (lane%8) + 8*(lane/16),    chunk 2*j + (lane/8)%2
+  // for the 16-dim step j (mod 4) of a 64-dim slab.
+  const int sw = lane & 7;
+  const int kr = (lane & 7) | (((lane >> 3) & 1) << 3), kc = lane >> 4;
+  const int vr = (lane & 7) | ((lane >> 4) << 3), vc = (lane >> 3) & 1;
+  uint32_t koff[4], voff[4];
+#pragma unroll
+  for (int jj = 0; jj < 4; ++jj) {
+    koff[jj] = (uint32_t)(kr * 128 + (((2 * jj + kc) ^ sw) << 4));
+    voff[jj] = (uint32_t)(vr * 128 + (((2 * jj + vc) ^ sw) << 4));
+  }
+  const uint32_t ring = smem_u32(smem);
 
 #pragma unroll 1
   for (int j = warp; j < nblk; j += C::NW) {
@@ -186,80 +234,92 @@ __global__ void __launch_bounds__(C::THREADS, 1) stage1_kernel(const Stage1Param
       if (lane == 0) atomicOr(p.err, kErrTimeout);
       break;
     }
-    const uint8_t* kst = smem + (size_t)st * C::STAGE_BYTES;
-    const uint8_t* vst = C::KVS ? kst : kst + C::KV_BYTES;
+    const uint32_t kst = ring + st * C::STAGE_BYTES;
+    const uint32_t vst = C::KVS ? kst : kst + C::KV_BYTES;
     const bool stage_ok = stage_valid[st] != 0;
     const int t0 = blk_lo + j * C::TB;
 
-    // QK: partial dot products over this lane's dims
-    float part[C::NV];
+    // QK on the tensor cores, four independent accumulation chains
+    float sacc[4][4];
 #pragma unroll
-    for (int tb = 0; tb < C::TB; ++tb) {
-      float kf[C::DPL];
+    for (int c = 0; c < 4; ++c)
 #pragma unroll
-      for (int c = 0; c < C::NCH; ++c) {
-        const uint4 w = lds128(kst + tb * C::ROW_BYTES + (c * 32 + lane) * 16);
-        float f[8];
-        unpack_bf16x8(w, f);
+      for (int i = 0; i < 4; ++i) sacc[c][i] = 0.f;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) kf[c * 8 + i] = f[i];
-      }
+    for (int ks = 0; ks < C::KSTEPS; ++ks) {
+      uint32_t a[4];
+      ldmatrix_x4(a, kst + (ks >> 2) * C::SLAB_BYTES + koff[ks & 3]);
+      mma_bf16(sacc[ks & 3], a, qb[ks][0], qb[ks][1]);
+    }
+    // lane holds tokens t0 + lane/4 (s[0], s[1]) and t0 + lane/4 + 8 (s[2], s[3]);
+    // heads 2*(lane%4) (s[0], s[2]) and 2*(lane%4) + 1 (s[1], s[3])
+    float s[4];
 #pragma unroll
-      for (int h = 0; h < C::G; ++h) {
-        float s0 = 0.f, s1 = 0.f;
+    for (int i = 0; i < 4; ++i) s[i] = ((sacc[0][i] + sacc[1][i]) + (sacc[2][i] + sacc[3][i])) * p.scale_log2;
+    const int ta = t0 + qh;
+    const bool va = stage_ok && ta >= tlo && ta < thi;
+    const bool vb = stage_ok && ta + 8 >= tlo && ta + 8 < thi;
+    if (!va) s[0] = s[1] = -INFINITY;
+    if (!vb) s[2] = s[3] = -INFINITY;
+
+    // online softmax: max and sum over the block's 16 tokens (lane/4 and the two rows)
+    float bm0 = fmaxf(s[0], s[2]), bm1 = fmaxf(s[1], s[3]);
 #pragma unroll
-        for (int i = 0; i < C::DPL; i += 2) {
-          s0 = fmaf(qf[h][i], kf[i], s0);
-          s1 = fmaf(qf[h][i + 1], kf[i + 1], s1);
-        }
-        part[tb * C::G + h] = s0 + s1;
+    for (int mask = 4; mask < 32; mask <<= 1) {
+      bm0 = fmaxf(bm0, __shfl_xor_sync(kFullMask, bm0, mask));
+      bm1 = fmaxf(bm1, __shfl_xor_sync(kFullMask, bm1, mask));
+    }
+    const float mn0 = fmaxf(m_run[0], bm0), mn1 = fmaxf(m_run[1], bm1);
+    const float alpha0 = (mn0 == -INFINITY) ? 1.f : ex2(m_run[0] - mn0);
+    const float alpha1 = (mn1 == -INFINITY) ? 1.f : ex2(m_run[1] - mn1);
+    const float ms0 = (mn0 == -INFINITY) ? 0.f : mn0, ms1 = (mn1 == -INFINITY) ? 0.f : mn1;
+    const float p0 = ex2(s[0] - ms0), p1 = ex2(s[1] - ms1), p2 = ex2(s[2] - ms0), p3 = ex2(s[3] - ms1);
+    float bs0 = p0 + p2, bs1 = p1 + p3;
+#pragma unroll
+    for (int mask = 4; mask < 32; mask <<= 1) {
+      bs0 += __shfl_xor_sync(kFullMask, bs0, mask);
+      bs1 += __shfl_xor_sync(kFullMask, bs1, mask);
+    }
+    l_run[0] = l_run[0] * alpha0 + bs0;
+    l_run[1] = l_run[1] * alpha1 + bs1;
+    m_run[0] = mn0;
+    m_run[1] = mn1;
+    if (__any_sync(kFullMask, alpha0 != 1.f || alpha1 != 1.f)) {
+#pragma unroll
+      for (int mt = 0; mt < C::MTILES; ++mt) {
+        acc[mt][0] *= alpha0;
+        acc[mt][1] *= alpha1;
+        acc[mt][2] *= alpha0;
+        acc[mt][3] *= alpha1;
       }
     }
-    reduce_scatter<C::NV>(part, lane);
 
-    // online softmax over the block, per head
-    const int t = t0 + my_tb;
-    const bool valid = stage_ok && t >= tlo && t < thi;
-    const float s = valid ? part[0] : -INFINITY;
-    float bmax = s;
-#pragma unroll
-    for (int mask = C::R * C::G; mask < 32; mask <<= 1) bmax = fmaxf(bmax, __shfl_xor_sync(kFullMask, bmax, mask));
-    const float m_new = fmaxf(m_run, bmax);
-    const float alpha = (m_new == -INFINITY) ? 1.f : ex2(m_run - m_new);
-    const float pr = valid ? ex2(s - m_new) : 0.f;
-    float bsum = pr;
-#pragma unroll
-    for (int mask = C::R * C::G; mask < 32; mask <<= 1) bsum += __shfl_xor_sync(kFullMask, bsum, mask);
-    l_run = l_run * alpha + bsum;
-    m_run = m_new;
-
-    if (__any_sync(kFullMask, alpha != 1.f)) {
-#pragma unroll
-      for (int h = 0; h < C::G; ++h) {
-        const float a = __shfl_sync(kFullMask, alpha, h * C::R);
-#pragma unroll
-        for (int i = 0; i < C::DPL; ++i) acc[h][i] *= a;
-      }
-    }
-
-    // PV (kept rolled: the block's rows are consumed one at a time)
+    // Edge block (window start, sequence end, skipped page): the masked rows
+    // carry p = 0, but 0 * NaN is NaN, and a page's unused rows may hold any
+    // bits. Zero those V rows before they enter the PV contraction.
+    const bool edge = __any_sync(kFullMask, !(va && vb));
+    if (edge) {
 #pragma unroll 1
-    for (int tb = 0; tb < C::TB; ++tb) {
-      float vf[C::DPL];
-#pragma unroll
-      for (int c = 0; c < C::NCH; ++c) {
-        const uint4 w = lds128(vst + tb * C::ROW_BYTES + (c * 32 + lane) * 16);
-        float f[8];
-        unpack_bf16x8(w, f);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) vf[c * 8 + i] = f[i];
+      for (int r = 0; r < C::TB; ++r) {
+        const int t = t0 + r;
+        if (stage_ok && t >= tlo && t < thi) continue;
+        for (int idx = lane; idx < C::SLABS * 8; idx += 32)
+          sts128_zero(vst + (idx >> 3) * C::SLAB_BYTES + r * 128 + (idx & 7) * 16);
       }
+      fence_proxy_async_smem();  // these generic writes precede the next TMA fill
+      __syncwarp();
+    }
+
+    // P^T as the B operand: transpose the (token x head) bf16 fragments
+    const uint32_t pb0 = movmatrix_trans(pack_bf16x2(p0, p1));  // tokens 0..7
+    const uint32_t pb1 = movmatrix_trans(pack_bf16x2(p2, p3));  // tokens 8..15
+
+    // PV on the tensor cores
 #pragma unroll
-      for (int h = 0; h < C::G; ++h) {
-        const float ph = __shfl_sync(kFullMask, pr, (tb * C::G + h) * C::R);
-#pragma unroll
-        for (int i = 0; i < C::DPL; ++i) acc[h][i] = fmaf(ph, vf[i], acc[h][i]);
-      }
+    for (int mt = 0; mt < C::MTILES; ++mt) {
+      uint32_t a[4];
+      ldmatrix_x4_trans(a, vst + (mt >> 2) * C::SLAB_BYTES + voff[mt & 3]);
+      mma_bf16(acc[mt], a, pb0, pb1);
     }
 
     __syncwarp();
@@ -269,16 +329,20 @@ __global__ void __launch_bounds__(C::THREADS, 1) stage1_kernel(const Stage1Param
   // ---- merge the NW warp states --------------------------------------------------
   named_bar_sync(1, C::NW * 32);  // every consumer is done with the ring
   float* comb = reinterpret_cast<float*>(smem);  // [NW][G][D]
+  const int h0 = (lane & 3) * 2;
 #pragma unroll
-  for (int h = 0; h < C::G; ++h) {
+  for (int hh = 0; hh < 2; ++hh) {
+    const int h = h0 + hh;
+    if (h < C::G) {
+      float* dst = comb + ((size_t)warp * C::G + h) * C::D + qh;
 #pragma unroll
-    for (int c = 0; c < C::NCH; ++c) {
-      float4* dst = reinterpret_cast<float4*>(comb + ((size_t)warp * C::G + h) * C::D + (c * 32 + lane) * 8);
-      dst[0] = make_float4(acc[h][c * 8 + 0], acc[h][c * 8 + 1], acc[h][c * 8 + 2], acc[h][c * 8 + 3]);
-      dst[1] = make_float4(acc[h][c * 8 + 4], acc[h][c * 8 + 5], acc[h][c * 8 + 6], acc[h][c * 8 + 7]);
+      for (int mt = 0; mt < C::MTILES; ++mt) {
+        dst[mt * 16] = acc[mt][hh];
+        dst[mt * 16 + 8] = acc[mt][2 + hh];
+      }
+      if (qh == 0) warp_ml[warp * C::G + h] = make_float2(m_run[hh], l_run[hh]);
     }
   }
-  if (my_tb == 0 && (lane % C::R) == 0) warp_ml[warp * C::G + vi] = make_float2(m_run, l_run);
   named_bar_sync(1, C::NW * 32);
 
   const int tid = threadIdx.x;
@@ -312,8 +376,8 @@ __global__ void __launch_bounds__(C::THREADS, 1) stage1_kernel(const Stage1Param
 
 // ---- instantiation and dispatch -------------------------------------------------
 
-#define PD_STAGE1_INSTANCE(ID, D, G, KVS, NW, SPW)                                                   \
-  template __global__ void stage1_kernel<Stage1Cfg<D, G, KVS, NW, SPW>>(const Stage1Params);
+#define PD_STAGE1_INSTANCE(ID, D, G, KVS, NW, SPW) \
+  template __global__ void stage1_kernel<Stage1Cfg<D, G, KVS, NW, SPW>>(const __grid_constant__ Stage1Params);
 PD_FOR_EACH_VARIANT(PD_STAGE1_INSTANCE)
 #undef PD_STAGE1_INSTANCE
 

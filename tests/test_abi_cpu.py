@@ -66,7 +66,7 @@ def _plan(lens, Hq=16, Hkv=4, d=512, P=16, pages=4096, maxp=None, window=0, kv_s
     (dict(d=384), b.PD_ERR_UNSUPPORTED),
     (dict(d=128), b.PD_ERR_UNSUPPORTED),
     (dict(Hq=64, Hkv=4), b.PD_ERR_UNSUPPORTED),   # group of 16
-    (dict(Hq=32, Hkv=4, d=512), b.PD_ERR_UNSUPPORTED),  # group of 8 at d = 512
+    (dict(Hq=48, Hkv=4), b.PD_ERR_UNSUPPORTED),   # group of 12
 ])
 def test_plan_rejects(lib, kw, status):
     with pytest.raises(b.PagedDecodeError) as e:

@@ -67,8 +67,7 @@ def test_workload_matches_oracle(cid, part):
 
 # ---- every kernel instance on ragged batches ----------------------------------
 
-VARIANTS = [(512, G, kvs) for G in (1, 2, 4) for kvs in (False, True)] + \
-           [(256, G, kvs) for G in (1, 2, 4, 8) for kvs in (False, True)]
+VARIANTS = [(d, G, kvs) for d in (512, 256) for G in (1, 2, 4, 8) for kvs in (False, True)]
 
 
 @pytest.mark.parametrize("d,G,kvs", VARIANTS)
@@ -215,3 +214,23 @@ def test_abi_rejects_bad_arguments_without_launching():
     torch.cuda.synchronize()
     assert (out == 0).all()  # nothing ran
     assert step.check() == 0
+
+
+@pytest.mark.parametrize("kvs,window,d", [(False, 0, 512), (True, 0, 512), (False, 45, 256)])
+def test_nan_in_unattended_rows_does_not_leak(kvs, window, d):
+    """Rows a page holds past the sequence end (and before a window) are never
+    attended; whatever bits they hold must not reach the output."""
+    lens = [37, 100, 250]
+    li = synth.make_layer("nan", lens, 8, 2, d, window=window, kv_shared=kvs, pool_pages=30, seed=12,
+                          device="cuda")
+    ref = run_oracle(li)
+    for bi, L in enumerate(lens):
+        lo = max(0, L - window) if window else 0
+        npages = (L + 15) // 16
+        for t in list(range((lo // 16) * 16, lo)) + list(range(L, npages * 16)):
+            page = int(li.block_tables[bi, t // 16])
+            li.k_pool[page, :, t % 16] = float("nan")
+            if li.v_pool is not None:
+                li.v_pool[page, :, t % 16] = float("nan")
+    out, _ = run_gpu(li)
+    compare(out, ref, li, "nan rows")
