@@ -56,8 +56,9 @@
  * [0, max_pages_per_seq * page_size], a pipeline wait that timed out) set bits in
  * an error word at the start of the workspace: the offending page is skipped
  * (its tokens are masked out), the length clamped; paged_decode_check_device_error
- * reports PD_ERR_DEVICE_FAULT. The error word must be zero before the first call:
- * zero the workspace once after allocating it.
+ * reports PD_ERR_DEVICE_FAULT. The error word must be zero before the first
+ * call: zero the workspace once after allocating it. Calls that share a
+ * workspace must not overlap on the GPU: order them on one stream.
  */
 #ifndef PAGED_DECODE_H
 #define PAGED_DECODE_H
@@ -111,7 +112,9 @@ typedef struct {
   int32_t smem_bytes;
   int32_t sm_count;
   int32_t max_seq_len;      /* longest sequence the plan was made for */
-  int32_t reserved[4];
+  int32_t merge_mode;       /* 0: S = 1, stage 1 writes out and there is nothing to merge;
+                               1: paged_decode_merge launches the merge */
+  int32_t reserved[3];
   uint64_t workspace_bytes; /* bytes the caller must provide */
   uint64_t lse_offset;      /* byte offset of the fp32 [batch, Hq, S] log-sum-exp part */
   uint64_t opart_offset;    /* byte offset of the fp32 [batch, Hq, S, d] partial outputs */
@@ -169,9 +172,11 @@ pd_status paged_decode_window(const pd_plan* plan, const void* q, const void* k_
 /*
  * Stage 2 ([vLLM-MLA]: the pieces' partial results are merged): for each
  * (request, query head), out = sum_s w_s o_s / sum_s w_s with
- * w_s = exp(lse_s - max lse); pieces with no attended token are skipped; a row
- * with none at all is zero. A no-op (PD_OK, nothing launched) when
- * plan->num_splits == 1, so it is always safe to call after stage 1.
+ * w_s = exp(lse_s - max lse); pieces with no attended token weigh nothing; a
+ * row with none at all is zero. The launch may start while stage 1 is still
+ * running (programmatic dependent launch) and waits for it before reading the
+ * partials. With plan->merge_mode 0 (one piece) there is nothing to merge: it
+ * returns PD_OK without launching, so it is always safe to call after stage 1.
  */
 pd_status paged_decode_merge(const pd_plan* plan, const void* workspace, size_t workspace_bytes,
                              void* out, void* stream);

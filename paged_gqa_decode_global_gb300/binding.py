@@ -66,7 +66,8 @@ class Plan(ctypes.Structure):
         ("smem_bytes", ctypes.c_int32),
         ("sm_count", ctypes.c_int32),
         ("max_seq_len", ctypes.c_int32),
-        ("reserved", ctypes.c_int32 * 4),
+        ("merge_mode", ctypes.c_int32),
+        ("reserved", ctypes.c_int32 * 3),
         ("workspace_bytes", ctypes.c_uint64),
         ("lse_offset", ctypes.c_uint64),
         ("opart_offset", ctypes.c_uint64),

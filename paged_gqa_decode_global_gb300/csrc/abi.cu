@@ -189,7 +189,7 @@ pd_status paged_decode_window(const pd_plan* plan, const void* q, const void* k_
 pd_status paged_decode_merge(const pd_plan* plan, const void* workspace, size_t workspace_bytes, void* out,
                              void* stream) {
   if (!pd::plan_is_valid(plan)) return PD_ERR_INVALID_ARG;
-  if (plan->num_splits == 1 || plan->batch == 0) return PD_OK;
+  if (plan->merge_mode != 1 || plan->batch == 0) return PD_OK;  // one piece: nothing to merge
   if (!workspace || !aligned(workspace, 256) || !out || !aligned(out, 16)) return PD_ERR_INVALID_ARG;
   if (workspace_bytes < plan->workspace_bytes) return PD_ERR_WORKSPACE_TOO_SMALL;
   const uint8_t* ws = static_cast<const uint8_t*>(workspace);

@@ -1,63 +1,94 @@
 // Stage 2 of paged GQA decode attention (sm_103a): merge the KV pieces of every
-// (request, query head) by their log-sum-exp weights.
+// (request, query head) by their log-sum-exp weights, as its own launch (used
+// when the pieces of one (request, KV head) are too many to merge in stage 1).
 //
 // Method: vLLM concepts page "模型库与算子层 — 概念", section "MLA 与 Sparse MLA
 // （DSA）" — split-KV decode whose pieces each produce partial results carrying a
 // log-sum-exp, combined afterwards:
-//   M = max_s lse_s,  w_s = exp(lse_s - M),  out = sum_s w_s o_s / sum_s w_s.
-// Pieces with no attended token (lse = -inf) are skipped, so their partial rows
-// are never read; a row with no piece at all is zero.
+//   M = max_s lse_s,  w_s = exp(lse_s - M) / sum_s' exp(lse_s' - M),  out = sum_s w_s o_s.
+// Empty pieces carry lse = -inf (weight 0) and zero partial rows; a row with no
+// piece at all is zero.
 //
-// One CTA per (request, query head) row; each thread owns 4 consecutive dims
-// (one 16-byte fp32 load per piece); the output row is written as bf16.
+// Grid (row, 128-dim slice of the row), one warp each, launched behind stage 1
+// as a programmatic dependent (it waits for stage 1 before reading). The warp stages the
+// row's S weights in shared memory, then every lane sums its 4 dims over the
+// pieces with independent 16-byte loads in flight.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include "pd_common.cuh"
 #include "pd_kernels.h"
 
 namespace pd {
 
 namespace {
 
-__global__ void __launch_bounds__(128) merge_kernel(const MergeParams p) {
+constexpr int kMergeMaxSplits = 1024;
+
+__global__ void __launch_bounds__(32) merge_kernel(const MergeParams p) {
+  __shared__ float w[kMergeMaxSplits];
+  grid_dependency_wait();  // stage 1 (launched before this grid) has finished
   const size_t row = blockIdx.x;
+  const int lane = threadIdx.x;
   const int S = p.num_splits;
-  const int D = p.head_dim;
   const float* lse = p.lse_part + row * S;
   float M = -INFINITY;
-  for (int s = 0; s < S; ++s) M = fmaxf(M, lse[s]);
-  __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out) + row * D;
-  for (int d4 = threadIdx.x * 4; d4 < D; d4 += blockDim.x * 4) {
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    float wsum = 0.f;
-    if (M != -INFINITY) {
-      for (int s = 0; s < S; ++s) {
-        const float l = lse[s];
-        if (l == -INFINITY) continue;
-        const float w = expf(l - M);
-        const float4 o = *reinterpret_cast<const float4*>(p.o_part + (row * S + s) * D + d4);
-        wsum += w;
-        acc.x = fmaf(w, o.x, acc.x);
-        acc.y = fmaf(w, o.y, acc.y);
-        acc.z = fmaf(w, o.z, acc.z);
-        acc.w = fmaf(w, o.w, acc.w);
-      }
-    }
-    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
-    __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
-    reinterpret_cast<__nv_bfloat162*>(out + d4)[0] = lo;
-    reinterpret_cast<__nv_bfloat162*>(out + d4)[1] = hi;
+  for (int s = lane; s < S; s += 32) {
+    const float l = lse[s];
+    w[s] = l;
+    M = fmaxf(M, l);
   }
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, m));
+  float sum = 0.f;
+  for (int s = lane; s < S; s += 32) {
+    const float e = (M == -INFINITY) ? 0.f : expf(w[s] - M);
+    w[s] = e;
+    sum += e;
+  }
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, m);
+  const float inv = sum > 0.f ? 1.f / sum : 0.f;
+  __syncwarp();
+  const int D4 = p.head_dim / 4;
+  const int d4 = blockIdx.y * 32 + lane;
+  if (d4 >= D4) return;
+  const float4* src = reinterpret_cast<const float4*>(p.o_part + row * S * p.head_dim) + d4;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+  for (int s = 0; s < S; ++s) {
+    const float ws = w[s] * inv;
+    const float4 o = src[(size_t)s * D4];
+    acc.x = fmaf(ws, o.x, acc.x);
+    acc.y = fmaf(ws, o.y, acc.y);
+    acc.z = fmaf(ws, o.z, acc.z);
+    acc.w = fmaf(ws, o.w, acc.w);
+  }
+  __nv_bfloat162* out = reinterpret_cast<__nv_bfloat162*>(reinterpret_cast<__nv_bfloat16*>(p.out) + row * p.head_dim) + d4 * 2;
+  out[0] = __floats2bfloat162_rn(acc.x, acc.y);
+  out[1] = __floats2bfloat162_rn(acc.z, acc.w);
 }
 
 }  // namespace
 
 int launch_merge(const MergeParams& p, int rows, void* stream) {
   if (rows <= 0) return 0;
-  const int threads = p.head_dim / 4 < 128 ? p.head_dim / 4 : 128;
-  merge_kernel<<<rows, threads, 0, static_cast<cudaStream_t>(stream)>>>(p);
-  return static_cast<int>(cudaGetLastError());
+  if (p.num_splits > kMergeMaxSplits || p.head_dim % 4 != 0) return static_cast<int>(cudaErrorInvalidValue);
+  // launched with programmatic stream serialisation: its CTAs may become
+  // resident while stage 1 drains and wait there for its completion
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(rows, (p.head_dim / 4 + 31) / 32);
+  cfg.blockDim = dim3(32);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, merge_kernel, p);
+  if (e != cudaSuccess) (void)cudaGetLastError();
+  return static_cast<int>(e);
 }
 
 }  // namespace pd

@@ -36,13 +36,15 @@ struct Stage1Cfg {
   static constexpr int STAGE_BYTES = KV_BYTES * (KVS ? 1 : 2);
   static constexpr int TX_BYTES = STAGE_BYTES;                  // bytes the copies deliver
   static constexpr int RING_BYTES = NST * STAGE_BYTES;
-  static constexpr int COMBINE_BYTES = NW * G * D * 4;         // per-warp outputs (aliases the ring)
+  static constexpr int COMB_STRIDE = D + 4;                    // floats per head row of the warp merge
+  static constexpr int COMBINE_BYTES = NW * G * COMB_STRIDE * 4; // per-warp outputs (aliases the ring)
   static constexpr int BODY_BYTES = RING_BYTES > COMBINE_BYTES ? RING_BYTES : COMBINE_BYTES;
   static constexpr int BAR_OFFSET = BODY_BYTES;                // full[NST], empty[NST]
   static constexpr int VALID_OFFSET = BAR_OFFSET + NST * 16;   // u32 valid[NST]
   static constexpr int ML_OFFSET = VALID_OFFSET + NST * 4;     // float2 ml[NW][G]
+  static constexpr int COEF_OFFSET = ML_OFFSET + NW * G * 8;   // float coef[NW][G], lse[G]
   // + 1 KiB so the ring can start on a 1024-byte boundary (the swizzle period)
-  static constexpr int SMEM_BYTES = ML_OFFSET + NW * G * 8 + 1024;
+  static constexpr int SMEM_BYTES = COEF_OFFSET + (NW * G + G) * 4 + 1024;
   static constexpr int THREADS = 32 * (NW + 1);
   static_assert(D % 64 == 0, "head_dim must be a multiple of 64 (one swizzle span)");
   static_assert(G >= 1 && G <= 8, "the GQA group is the MMA's 8-wide side");

@@ -30,7 +30,10 @@ const int kNumVariants = sizeof(kVariants) / sizeof(kVariants[0]);
 namespace {
 
 constexpr uint32_t kPlanMagic = 0x50444543u;  // "PDEC"
-constexpr int32_t kAbiVersion = 1;
+constexpr int32_t kAbiVersion = 2;
+// Pieces per (request, KV head) are capped (the merge stages their weights in
+// shared memory).
+constexpr int kMaxSplits = 1024;
 
 const pd::VariantInfo* find_variant(int head_dim, int group, int kv_shared) {
   for (int i = 0; i < pd::kNumVariants; ++i) {
@@ -174,6 +177,7 @@ pd_status paged_decode_plan(const pd_layer_desc* layer, int32_t batch, const int
     for (int c : cands) {
       if (c < 16) continue;
       const int s = (max_n + c - 1) / c;
+      if (s > kMaxSplits) continue;
       const uint64_t merge_bytes = (uint64_t)batch * ly.num_q_heads * s * (ly.head_dim + 1) * 4ull * 2ull;
       const double cost = simulate(n_tok, ly.num_kv_heads, c, s, cm, merge_bytes);
       if (cost < best * (1.0 - 1e-9) || (cost <= best && s < best_splits)) {
@@ -199,11 +203,14 @@ pd_status paged_decode_plan(const pd_layer_desc* layer, int32_t batch, const int
   plan->sm_count = sm_count;
   plan->max_seq_len = max_len;
   const uint64_t rows = (uint64_t)batch * ly.num_q_heads;
-  plan->lse_offset = pd::kWorkspaceHeader;
   if (best_splits > 1) {
+    plan->merge_mode = 1;
+    plan->lse_offset = pd::kWorkspaceHeader;
     plan->opart_offset = align_up(plan->lse_offset + rows * best_splits * 4ull, 256);
     plan->workspace_bytes = plan->opart_offset + rows * best_splits * (uint64_t)ly.head_dim * 4ull;
   } else {
+    plan->merge_mode = 0;
+    plan->lse_offset = pd::kWorkspaceHeader;
     plan->opart_offset = pd::kWorkspaceHeader;
     plan->workspace_bytes = pd::kWorkspaceHeader;
   }
@@ -226,6 +233,8 @@ bool plan_is_valid(const pd_plan* plan) {
   if (plan->num_splits < 1 || plan->chunk_tokens < 16 || plan->chunk_tokens % 16 != 0) return false;
   if (plan->batch < 0 || plan->grid_x != plan->num_splits) return false;
   if (plan->threads_per_cta != v.threads || plan->smem_bytes != v.smem_bytes) return false;
+  if (plan->merge_mode < 0 || plan->merge_mode > 1) return false;
+  if ((plan->num_splits == 1) != (plan->merge_mode == 0)) return false;
   return true;
 }
 

@@ -10,8 +10,8 @@
 // result plus its log-sum-exp).
 //
 // GB300 design:
-//   * warp NW (one elected lane) is the producer: per block of 16 tokens it
-//     issues one tiled TMA copy of the block's K rows (and one of its V rows)
+//   * warp NW is the producer: its lanes fetch the page ids of 32 blocks at a
+//     time and one lane issues, per block of 16 tokens, one tiled TMA copy of the block's K rows (and one of its V rows)
 //     into a ring stage laid out [64-dim slab][token row][128 B] with the
 //     128-byte swizzle, so the 8 rows an ldmatrix reads fall in 8 different
 //     bank groups; completion is counted in bytes on the stage's mbarrier;
@@ -90,6 +90,14 @@ __global__ void __launch_bounds__(C::THREADS, 1) stage1_kernel(const __grid_cons
 
   // ---- attended range of this request and this piece -------------------------
   const int cap = p.max_pages * p.page_size;
+  const int32_t* table = p.block_tables + (size_t)b * p.max_pages;
+  // On a global layer a piece starts at split * chunk whatever the length, so
+  // the producer fetches its first 32 page ids while the length is in flight.
+  int page_spec = -1;
+  if (warp == C::NW && p.window == 0) {
+    const long long t = (long long)split * p.chunk_tokens + (long long)lane * C::TB;
+    if (t < cap) page_spec = __ldg(table + t / p.page_size);
+  }
   int L = p.seq_lens[b];
   if (L < 0 || L > cap) {
     if (threadIdx.x == 0) atomicOr(p.err, kErrBadSeqLen);
@@ -113,10 +121,38 @@ __global__ void __launch_bounds__(C::THREADS, 1) stage1_kernel(const __grid_cons
     if (p.num_splits == 1) {
       __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out) + row_hq * C::D;
       for (int i = threadIdx.x; i < C::G * C::D; i += C::THREADS) o[i] = __float2bfloat16_rn(0.f);
-    } else if (threadIdx.x < C::G) {
-      p.lse_part[(row_hq + threadIdx.x) * p.num_splits + split] = -INFINITY;
+    } else {
+      // weight 0 and a zero partial row, so the merge needs no special case
+      for (int i = threadIdx.x; i < C::G * C::D; i += C::THREADS)
+        p.o_part[((row_hq + i / C::D) * p.num_splits + split) * C::D + i % C::D] = 0.f;
+      if (threadIdx.x < C::G) p.lse_part[(row_hq + threadIdx.x) * p.num_splits + split] = -INFINITY;
     }
     return;
+  }
+
+  // Start each role's first global loads before the barrier set-up so their
+  // latency overlaps it: the producer warp fetches the page ids of its first 32
+  // blocks (one per lane), the consumers their q fragments.
+  int page_next = -1;
+  // B fragments of q (heads on N, dims on K): lane holds head lane/4, dims
+  // 2*(lane%4) + {0,1} and + {8,9} of every 16-dim step; heads past G are zero.
+  const int qh = lane >> 2;
+  const int qk = (lane & 3) * 2;
+  uint32_t qb[C::KSTEPS][2];
+  if (warp == C::NW) {
+    if (lane < nblk) page_next = (p.window == 0) ? page_spec : __ldg(table + (blk_lo + lane * C::TB) / p.page_size);
+  } else {
+#pragma unroll
+    for (int ks = 0; ks < C::KSTEPS; ++ks) {
+      if (qh < C::G) {
+        const uint16_t* qrow = p.q + (row_hq + qh) * C::D + ks * 16 + qk;
+        qb[ks][0] = __ldg(reinterpret_cast<const unsigned int*>(qrow));
+        qb[ks][1] = __ldg(reinterpret_cast<const unsigned int*>(qrow + 8));
+      } else {
+        qb[ks][0] = 0u;
+        qb[ks][1] = 0u;
+      }
+    }
   }
 
   if (threadIdx.x == 0) {
@@ -128,49 +164,73 @@ __global__ void __launch_bounds__(C::THREADS, 1) stage1_kernel(const __grid_cons
     fence_barrier_init();
   }
   __syncthreads();
+  // a merge launched behind this kernel may start its (waiting) CTAs now
+  grid_launch_dependents();
 
   // ---- producer ------------------------------------------------------------------
   if (warp == C::NW) {
+    const uint64_t policy = l2_evict_first_policy();
     if (lane == 0) {
-      const uint64_t policy = l2_evict_first_policy();
       prefetch_tensormap(&p.kmap);
       if (!C::KVS) prefetch_tensormap(&p.vmap);
-      const int32_t* table = p.block_tables + (size_t)b * p.max_pages;
-      int issued = 0;
+    }
+    // The whole warp walks the blocks 32 at a time: each lane holds one block's
+    // page id (fetched a round ahead), lane 0 waits for the stage and issues
+    // the copies, so page-id loads never serialise the issue of copies.
+    int issued = 0;
+    bool stop = false;
 #pragma unroll 1
-      for (int j = 0; j < nblk; ++j) {
-        const int st = j % C::NST;
-        const int round = j / C::NST;
-        if (round > 0 && !mbar_wait(&empty_bar[st], (round - 1) & 1)) {
-          atomicOr(p.err, kErrTimeout);
-          break;
-        }
-        const int t0 = blk_lo + j * C::TB;
-        const int page = table[t0 / p.page_size];
-        const bool ok = (unsigned)page < (unsigned)p.num_pages;
-        stage_valid[st] = ok ? 1u : 0u;
-        if (ok) {
-          const int row0 = (page * p.num_kv_heads + g) * p.page_size + (t0 % p.page_size);
-          uint8_t* dst = smem + (size_t)st * C::STAGE_BYTES;
-          mbar_arrive_expect_tx(&full_bar[st], C::TX_BYTES);
-          if (p.tma_rank == 3) {
-            tma_load_3d(dst, &p.kmap, 0, row0, 0, &full_bar[st], policy);
-            if (!C::KVS) tma_load_3d(dst + C::KV_BYTES, &p.vmap, 0, row0, 0, &full_bar[st], policy);
+    for (int j0 = 0; j0 < nblk && !stop; j0 += 32) {
+      const int page_mine = page_next;
+      const int jn = j0 + 32 + lane;
+      page_next = (jn < nblk) ? __ldg(table + (blk_lo + jn * C::TB) / p.page_size) : -1;
+      const int cnt = min(32, nblk - j0);
+#pragma unroll 1
+      for (int k = 0; k < cnt; ++k) {
+        const int j = j0 + k;
+        const int page = __shfl_sync(kFullMask, page_mine, k);
+        int go = 1;
+        if (lane == 0) {
+          const int st = j % C::NST;
+          const int round = j / C::NST;
+          if (round > 0 && !mbar_wait(&empty_bar[st], (round - 1) & 1)) {
+            atomicOr(p.err, kErrTimeout);
+            go = 0;
           } else {
+            const int t0 = blk_lo + j * C::TB;
+            const bool ok = (unsigned)page < (unsigned)p.num_pages;
+            stage_valid[st] = ok ? 1u : 0u;
+            if (ok) {
+              const int row0 = (page * p.num_kv_heads + g) * p.page_size + (t0 % p.page_size);
+              uint8_t* dst = smem + (size_t)st * C::STAGE_BYTES;
+              mbar_arrive_expect_tx(&full_bar[st], C::TX_BYTES);
+              if (p.tma_rank == 3) {
+                tma_load_3d(dst, &p.kmap, 0, row0, 0, &full_bar[st], policy);
+                if (!C::KVS) tma_load_3d(dst + C::KV_BYTES, &p.vmap, 0, row0, 0, &full_bar[st], policy);
+              } else {
 #pragma unroll
-            for (int sl = 0; sl < C::SLABS; ++sl) {
-              tma_load_2d(dst + sl * C::SLAB_BYTES, &p.kmap, sl * 64, row0, &full_bar[st], policy);
-              if (!C::KVS)
-                tma_load_2d(dst + C::KV_BYTES + sl * C::SLAB_BYTES, &p.vmap, sl * 64, row0, &full_bar[st], policy);
+                for (int sl = 0; sl < C::SLABS; ++sl) {
+                  tma_load_2d(dst + sl * C::SLAB_BYTES, &p.kmap, sl * 64, row0, &full_bar[st], policy);
+                  if (!C::KVS)
+                    tma_load_2d(dst + C::KV_BYTES + sl * C::SLAB_BYTES, &p.vmap, sl * 64, row0, &full_bar[st],
+                                policy);
+                }
+              }
+            } else {
+              atomicOr(p.err, kErrBadPage);
+              mbar_arrive(&full_bar[st]);
             }
           }
-        } else {
-          atomicOr(p.err, kErrBadPage);
-          mbar_arrive(&full_bar[st]);
+        }
+        if (__shfl_sync(kFullMask, go, 0) == 0) {
+          stop = true;
+          break;
         }
         issued = j + 1;
       }
-      // no copy may still be landing in shared memory when the CTA exits
+    }
+    // no copy may still be landing in shared memory when the CTA exits
+    if (lane == 0) {
 #pragma unroll 1
       for (int st = 0; st < C::NST && st < issued; ++st) {
         const int j_last = st + C::NST * ((issued - 1 - st) / C::NST);
@@ -181,23 +241,6 @@ __global__ void __launch_bounds__(C::THREADS, 1) stage1_kernel(const __grid_cons
   }
 
   // ---- consumers -----------------------------------------------------------------
-  // B fragments of q (heads on N, dims on K): lane holds head lane/4, dims
-  // 2*(lane%4) + {0,1} and + {8,9} of every 16-dim step; heads past G are zero.
-  const int qh = lane >> 2;
-  const int qk = (lane & 3) * 2;
-  uint32_t qb[C::KSTEPS][2];
-#pragma unroll
-  for (int ks = 0; ks < C::KSTEPS; ++ks) {
-    if (qh < C::G) {
-      const uint16_t* qrow = p.q + (row_hq + qh) * C::D + ks * 16 + qk;
-      qb[ks][0] = __ldg(reinterpret_cast<const unsigned int*>(qrow));
-      qb[ks][1] = __ldg(reinterpret_cast<const unsigned int*>(qrow + 8));
-    } else {
-      qb[ks][0] = 0u;
-      qb[ks][1] = 0u;
-    }
-  }
-
   // O^T accumulators: m-tile mt holds dims mt*16 + lane/4 (+8) x heads 2*(lane%4) (+1)
   float acc[C::MTILES][4];
 #pragma unroll
@@ -328,13 +371,16 @@ __global__ void __launch_bounds__(C::THREADS, 1) stage1_kernel(const __grid_cons
 
   // ---- merge the NW warp states --------------------------------------------------
   named_bar_sync(1, C::NW * 32);  // every consumer is done with the ring
-  float* comb = reinterpret_cast<float*>(smem);  // [NW][G][D]
+  // per-warp accumulators [NW][G][CS]: the 4-float pad of a head row puts the
+  // heads 2 apart that a warp stores at once in different banks
+  constexpr int CS = C::COMB_STRIDE;
+  float* comb = reinterpret_cast<float*>(smem);
   const int h0 = (lane & 3) * 2;
 #pragma unroll
   for (int hh = 0; hh < 2; ++hh) {
     const int h = h0 + hh;
     if (h < C::G) {
-      float* dst = comb + ((size_t)warp * C::G + h) * C::D + qh;
+      float* dst = comb + (warp * C::G + h) * CS + qh;
 #pragma unroll
       for (int mt = 0; mt < C::MTILES; ++mt) {
         dst[mt * 16] = acc[mt][hh];
@@ -345,31 +391,54 @@ __global__ void __launch_bounds__(C::THREADS, 1) stage1_kernel(const __grid_cons
   }
   named_bar_sync(1, C::NW * 32);
 
+  // merge coefficients, once per head: c_w = 2^(m_w - M) / sum_w' 2^(m_w' - M) l_w'
   const int tid = threadIdx.x;
-#pragma unroll 1
-  for (int e = tid; e < C::G * C::D; e += C::NW * 32) {
-    const int h = e / C::D;
-    const int dim = e % C::D;
+  float* coef = reinterpret_cast<float*>(smem + C::COEF_OFFSET);  // [NW][G], then lse[G]
+  if (tid < C::G) {
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < C::NW; ++w) M = fmaxf(M, warp_ml[w * C::G + h].x);
-    float Lsum = 0.f, O = 0.f;
-    if (M != -INFINITY) {
+    for (int w = 0; w < C::NW; ++w) M = fmaxf(M, warp_ml[w * C::G + tid].x);
+    float Lsum = 0.f;
+    float f[C::NW];
 #pragma unroll
-      for (int w = 0; w < C::NW; ++w) {
-        const float2 ml = warp_ml[w * C::G + h];
-        const float f = ex2(ml.x - M);  // 0 for a warp that saw no token
-        Lsum = fmaf(f, ml.y, Lsum);
-        O = fmaf(f, comb[((size_t)w * C::G + h) * C::D + dim], O);
-      }
+    for (int w = 0; w < C::NW; ++w) {
+      const float2 ml = warp_ml[w * C::G + tid];
+      f[w] = (M == -INFINITY) ? 0.f : ex2(ml.x - M);  // 0 for a warp that saw no token
+      Lsum = fmaf(f[w], ml.y, Lsum);
     }
-    const float o = (Lsum > 0.f) ? O / Lsum : 0.f;
+    const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+#pragma unroll
+    for (int w = 0; w < C::NW; ++w) coef[w * C::G + tid] = f[w] * inv;
+    coef[C::NW * C::G + tid] = (Lsum > 0.f) ? (M + log2f(Lsum)) * 0.69314718055994530942f : -INFINITY;
+  }
+  named_bar_sync(1, C::NW * 32);
+
+  constexpr int D4 = C::D / 4;
+#pragma unroll 2
+  for (int e = tid; e < C::G * D4; e += C::NW * 32) {
+    const int h = e / D4;
+    const int d4 = e % D4;
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int w = 0; w < C::NW; ++w) {
+      const float c = coef[w * C::G + h];
+      const float4 a = *reinterpret_cast<const float4*>(comb + (w * C::G + h) * CS + d4 * 4);
+      o.x = fmaf(c, a.x, o.x);
+      o.y = fmaf(c, a.y, o.y);
+      o.z = fmaf(c, a.z, o.z);
+      o.w = fmaf(c, a.w, o.w);
+    }
     if (p.num_splits == 1) {
-      reinterpret_cast<__nv_bfloat16*>(p.out)[(row_hq + h) * C::D + dim] = __float2bfloat16_rn(o);
+      __nv_bfloat162* dst =
+          reinterpret_cast<__nv_bfloat162*>(reinterpret_cast<__nv_bfloat16*>(p.out) + (row_hq + h) * C::D) + d4 * 2;
+      uint2 packed;
+      packed.x = pack_bf16x2(o.x, o.y);
+      packed.y = pack_bf16x2(o.z, o.w);
+      *reinterpret_cast<uint2*>(dst) = packed;
     } else {
       const size_t prow = (row_hq + h) * p.num_splits + split;
-      p.o_part[prow * C::D + dim] = o;
-      if (dim == 0) p.lse_part[prow] = (Lsum > 0.f) ? (M + log2f(Lsum)) * 0.69314718055994530942f : -INFINITY;
+      reinterpret_cast<float4*>(p.o_part + prow * C::D)[d4] = o;
+      if (d4 == 0) p.lse_part[prow] = coef[C::NW * C::G + h];
     }
   }
 }

@@ -49,7 +49,7 @@ def test_build_targets_sm103a_only():
 def test_status_strings_and_version(lib):
     assert b.status_string(b.PD_OK) == "ok"
     assert "workspace" in b.status_string(b.PD_ERR_WORKSPACE_TOO_SMALL)
-    assert b.abi_version() == 1
+    assert b.abi_version() == 2
 
 
 def _plan(lens, Hq=16, Hkv=4, d=512, P=16, pages=4096, maxp=None, window=0, kv_shared=False, sms=152):
@@ -100,8 +100,12 @@ def test_plan_covers_every_token(lib, lens, window, d, Hkv):
             assert pl.num_splits * pl.chunk_tokens >= span
         if pl.num_splits > 1:
             rows = len(lens) * Hkv * 2
+            assert pl.merge_mode == 1
             assert pl.workspace_bytes >= pl.opart_offset + rows * pl.num_splits * d * 4
             assert pl.opart_offset >= pl.lse_offset + rows * pl.num_splits * 4
+            assert pl.lse_offset >= 4
+        else:
+            assert pl.merge_mode == 0
         assert pl.workspace_bytes >= 256
         assert (pl.grid_x, pl.grid_y, pl.grid_z) == (pl.num_splits, Hkv, len(lens))
 

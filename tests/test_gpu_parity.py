@@ -234,3 +234,19 @@ def test_nan_in_unattended_rows_does_not_leak(kvs, window, d):
                 li.v_pool[page, :, t % 16] = float("nan")
     out, _ = run_gpu(li)
     compare(out, ref, li, "nan rows")
+
+
+@pytest.mark.parametrize("sms", [20, 152, 4000])
+def test_many_pieces_merge(sms):
+    """From a few pieces to one per 16-token page: the merge matches the oracle,
+    and a second call on the same workspace gives the same bits."""
+    lens = [1000, 977, 513, 64]
+    li = synth.make_layer("mm", lens, 16, 2, 512, pool_pages=200, seed=13, device="cuda")
+    ref = run_oracle(li)
+    out, step = run_gpu(li, sm_count=sms)
+    assert step.plan.num_splits > 1 and step.plan.merge_mode == 1
+    compare(out, ref, li, f"S={step.plan.num_splits}")
+    again = torch.empty_like(out)
+    step.run(li, again)
+    assert step.check() == 0
+    assert torch.equal(out, again)
