@@ -44,14 +44,21 @@ L2_BYTES = 129 * 1000 * 1000
 FALLBACK_HBM_GBS = 6800.0
 
 # DRAM bytes (read + write) per stage-1 launch from an ncu capture, keyed by the
-# hash of the kernel sources it was taken on; stale entries are ignored.
-NCU_TRAFFIC = {}
+# hash of the kernel sources it was taken on; stale entries are ignored (the
+# captures and their commands are summarised under profiles/).
+NCU_TRAFFIC = {
+    "d43a34abd8cc9f4e": {"w2": 67279360 + 747264, "w4a": 1073882000 + 3600640},
+}
+
+
+STAGE1_SOURCES = ("stage1.cu", "pd_common.cuh", "pd_variants.h", "pd_kernels.h")
 
 
 def kernel_source_hash() -> str:
+    """Hash of the stage-1 kernel's sources (what an ncu capture describes)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_gqa_decode_global_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in STAGE1_SOURCES:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
@@ -280,6 +287,8 @@ def run_ours(args, world, rank, local):
     kv_gbs = li.kv_bytes() / (us_per_step * 1e-6) / 1e9
     src_hash = kernel_source_hash()
     traffic = NCU_TRAFFIC.get(src_hash, {}).get(f"w{args.workload}{args.part or ''}")
+    if args.workload == 2 and traffic is None:
+        traffic = NCU_TRAFFIC.get(src_hash, {}).get("w2")
 
     # end to end: host inputs -> device -> decode -> host output, eager launches
     e2e = None
