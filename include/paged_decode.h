@@ -189,6 +189,32 @@ pd_status paged_decode_merge(const pd_plan* plan, const void* workspace, size_t 
 pd_status paged_decode_check_device_error(const pd_plan* plan, void* workspace,
                                           size_t workspace_bytes, void* stream, uint32_t* flags);
 
+/*
+ * One decode layer-step (stage 1, then the merge) for callers that cannot
+ * allocate device memory. The source pages have no counterpart to this entry
+ * point; it exists for callers such as a plugin inside an inference engine that
+ * owns all device memory, or a serving loop that must not call cudaMalloc (which
+ * can synchronise the device) mid-step. Instead of a caller-provided workspace
+ * it uses an 8 MiB scratch array compiled into the library, which every GPU that
+ * loads the library holds until the process exits.
+ *   plan, q, k_pool, v_pool, block_tables, seq_lens, scale, out: as for
+ *                 paged_decode_global / paged_decode_window
+ *   window        0 on a global layer, else plan->layer.window
+ *   device_flags  optional device pointer: receives the device error word
+ *                 (PD_DEVFLAG_*) of this call; NULL to ignore it
+ *   stream        cudaStream_t as void*
+ * Returns PD_ERR_WORKSPACE_TOO_SMALL, without launching, when the plan needs
+ * more than 8 MiB of scratch (plan->workspace_bytes > 8 MiB); otherwise the
+ * statuses of the calls it makes. The first call on a device looks up the
+ * scratch array's device address, so make it before any stream capture. All
+ * calls share the one array and each starts by clearing its error word: calls
+ * that overlap on the GPU race, so order them on one stream. It allocates
+ * nothing.
+ */
+pd_status paged_decode_noalloc(const pd_plan* plan, const void* q, const void* k_pool, const void* v_pool,
+                               const int32_t* block_tables, const int32_t* seq_lens, int32_t window, float scale,
+                               void* out, uint32_t* device_flags, void* stream);
+
 /* Static, human-readable name of a status. */
 const char* paged_decode_status_string(pd_status status);
 

@@ -35,6 +35,7 @@ EXPORTED = (
     "paged_decode_check_device_error",
     "paged_decode_status_string",
     "paged_decode_abi_version",
+    "paged_decode_noalloc",
 )
 
 
@@ -118,6 +119,8 @@ def load_library(path: Optional[str] = None):
         lib.paged_decode_status_string.restype = ctypes.c_char_p
         lib.paged_decode_abi_version.argtypes = []
         lib.paged_decode_abi_version.restype = i32
+        lib.paged_decode_noalloc.argtypes = [ctypes.POINTER(Plan), vp, vp, vp, vp, vp, i32, f32, vp, vp, vp]
+        lib.paged_decode_noalloc.restype = ctypes.c_int
         if path is None:
             _lib = lib
         return lib
@@ -206,6 +209,19 @@ def paged_decode_check_device_error(plan: Plan, workspace, stream=None) -> int:
     if st != PD_OK:
         raise PagedDecodeError(st, "paged_decode_check_device_error", flags.value)
     return flags.value
+
+
+def paged_decode_noalloc(plan: Plan, q, k_pool, v_pool, block_tables, seq_lens, window: int, scale: float, out,
+                         device_flags=None, stream=None) -> None:
+    """Stage 1 + merge using the library's own scratch array instead of a
+    workspace, for callers that cannot allocate device memory (see the C
+    header). `device_flags`: optional int32/uint32 device tensor receiving the
+    call's device error word."""
+    lib = load_library()
+    st = lib.paged_decode_noalloc(ctypes.byref(plan), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables),
+                                  _ptr(seq_lens), int(window), float(scale), _ptr(out), _ptr(device_flags),
+                                  _stream_ptr(stream))
+    _check(st, "paged_decode_noalloc")
 
 
 def abi_version() -> int:
