@@ -179,6 +179,8 @@ def config_of(li, cid, part, replicas, plan):
         "kv_bytes_per_step": li.kv_bytes(),
         "l2": f"{replicas} rotating K/V pool replicas, {replicas * li.kv_bytes() / 1e6:.0f} MB touched per cycle (> 4x L2)",
         "num_splits": int(plan.num_splits), "chunk_tokens": int(plan.chunk_tokens),
+        "merge": {0: "none (one piece)", 1: "merge kernel", 2: "in-cluster (distributed shared memory)"}[
+            int(plan.merge_mode)],
         "launch": "CUDA graph replay, one stream",
         "parallelism": "replicas (no exchange)",
     }
@@ -200,7 +202,7 @@ def run_ours(args, world, rank, local):
     step = pdb.LayerStep.for_inputs(li)
     plan = step.plan
     S = int(plan.num_splits)
-    launches_per_step = 1 + (1 if S > 1 else 0)
+    launches_per_step = 1 + (1 if int(plan.merge_mode) == 1 else 0)  # mode 2 merges inside stage 1
 
     touched = max(1, li.kv_bytes())
     replicas = max(1, min(16, math.ceil(4 * L2_BYTES / touched)))

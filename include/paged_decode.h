@@ -113,7 +113,9 @@ typedef struct {
   int32_t sm_count;
   int32_t max_seq_len;      /* longest sequence the plan was made for */
   int32_t merge_mode;       /* 0: S = 1, stage 1 writes out and there is nothing to merge;
-                               1: paged_decode_merge launches the merge */
+                               1: paged_decode_merge launches the merge;
+                               2: 2 <= S <= 8, stage 1 runs each (request, KV head)'s pieces as
+                                  one thread-block cluster that merges them and writes out */
   int32_t reserved[3];
   uint64_t workspace_bytes; /* bytes the caller must provide */
   uint64_t lse_offset;      /* byte offset of the fp32 [batch, Hq, S] log-sum-exp part */
@@ -175,8 +177,9 @@ pd_status paged_decode_window(const pd_plan* plan, const void* q, const void* k_
  * w_s = exp(lse_s - max lse); pieces with no attended token weigh nothing; a
  * row with none at all is zero. The launch may start while stage 1 is still
  * running (programmatic dependent launch) and waits for it before reading the
- * partials. With plan->merge_mode 0 (one piece) there is nothing to merge: it
- * returns PD_OK without launching, so it is always safe to call after stage 1.
+ * partials. With plan->merge_mode 0 (one piece) there is nothing to merge and
+ * with mode 2 stage 1 merged the pieces itself: it returns PD_OK without
+ * launching, so it is always safe to call after stage 1.
  */
 pd_status paged_decode_merge(const pd_plan* plan, const void* workspace, size_t workspace_bytes,
                              void* out, void* stream);

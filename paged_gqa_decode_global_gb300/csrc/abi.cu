@@ -145,6 +145,7 @@ pd_status stage1(const pd_plan* plan, const void* q, const void* k_pool, const v
   p.lse_part = reinterpret_cast<float*>(ws + plan->lse_offset);
   p.o_part = reinterpret_cast<float*>(ws + plan->opart_offset);
   p.err = reinterpret_cast<uint32_t*>(ws);
+  p.cluster_merge = plan->merge_mode == 2 ? 1 : 0;
   p.scale_log2 = scale * kLog2e;
   p.window = ly.window;
   p.num_pages = ly.num_pages;
@@ -156,9 +157,22 @@ pd_status stage1(const pd_plan* plan, const void* q, const void* k_pool, const v
   p.chunk_tokens = plan->chunk_tokens;
 
   void* args[] = {&p};
-  const dim3 grid(plan->grid_x, plan->grid_y, plan->grid_z);
-  const dim3 block(plan->threads_per_cta);
-  cudaError_t e = cudaLaunchKernel(fn, grid, block, args, plan->smem_bytes, static_cast<cudaStream_t>(stream));
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(plan->grid_x, plan->grid_y, plan->grid_z);
+  cfg.blockDim = dim3(plan->threads_per_cta);
+  cfg.dynamicSmemBytes = plan->smem_bytes;
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  if (p.cluster_merge) {
+    // the S pieces of one (request, KV head) are consecutive in x: one cluster
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = plan->num_splits;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
   if (e != cudaSuccess) {
     (void)cudaGetLastError();
     return PD_ERR_CUDA;
@@ -189,7 +203,8 @@ pd_status paged_decode_window(const pd_plan* plan, const void* q, const void* k_
 pd_status paged_decode_merge(const pd_plan* plan, const void* workspace, size_t workspace_bytes, void* out,
                              void* stream) {
   if (!pd::plan_is_valid(plan)) return PD_ERR_INVALID_ARG;
-  if (plan->merge_mode != 1 || plan->batch == 0) return PD_OK;  // one piece: nothing to merge
+  // mode 0: one piece, nothing to merge; mode 2: merged inside the stage-1 clusters
+  if (plan->merge_mode != 1 || plan->batch == 0) return PD_OK;
   if (!workspace || !aligned(workspace, 256) || !out || !aligned(out, 16)) return PD_ERR_INVALID_ARG;
   if (workspace_bytes < plan->workspace_bytes) return PD_ERR_WORKSPACE_TOO_SMALL;
   const uint8_t* ws = static_cast<const uint8_t*>(workspace);

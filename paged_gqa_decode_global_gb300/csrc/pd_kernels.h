@@ -25,6 +25,7 @@ struct Stage1Params {
   float* lse_part;              // [B, Hq, S] natural-log log-sum-exp of each piece
   float* o_part;                // [B, Hq, S, D] normalised partial outputs
   uint32_t* err;                // device error word
+  int32_t cluster_merge;        // the S pieces of a (request, KV head) are one cluster; rank 0 merges
   float scale_log2;             // softmax scale * log2(e)
   int32_t window;               // 0 = global layer
   int32_t num_pages, max_pages, page_size;

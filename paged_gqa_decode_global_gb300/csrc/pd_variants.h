@@ -39,6 +39,16 @@ struct Stage1Cfg {
   static constexpr int COMB_STRIDE = D + 4;                    // floats per head row of the warp merge
   static constexpr int COMBINE_BYTES = NW * G * COMB_STRIDE * 4; // per-warp outputs (aliases the ring)
   static constexpr int BODY_BYTES = RING_BYTES > COMBINE_BYTES ? RING_BYTES : COMBINE_BYTES;
+  // cluster merge (after the ring is drained): this CTA's result and lse, and
+  // rank 0's merge weights
+  static constexpr int MAX_CLUSTER = 8;
+  static constexpr int CTA_OUT_OFFSET = (COMBINE_BYTES + 15) / 16 * 16;  // float [G][D]
+  static constexpr int CTA_LSE_OFFSET = CTA_OUT_OFFSET + G * D * 4;      // float [G]
+  static constexpr int CTA_W_OFFSET = CTA_LSE_OFFSET + G * 4;            // float [MAX_CLUSTER][G]
+  // rank 0 only: results pushed by ranks 1..S-1, float [MAX_CLUSTER-1][G][D] + lse [MAX_CLUSTER-1][G]
+  static constexpr int PUSH_OFFSET = (CTA_W_OFFSET + MAX_CLUSTER * G * 4 + 15) / 16 * 16;
+  static constexpr int PUSH_LSE_OFFSET = PUSH_OFFSET + (MAX_CLUSTER - 1) * G * D * 4;
+  static_assert(PUSH_LSE_OFFSET + (MAX_CLUSTER - 1) * G * 4 <= BODY_BYTES, "cluster merge buffers fit in the ring");
   static constexpr int BAR_OFFSET = BODY_BYTES;                // full[NST], empty[NST]
   static constexpr int VALID_OFFSET = BAR_OFFSET + NST * 16;   // u32 valid[NST]
   static constexpr int ML_OFFSET = VALID_OFFSET + NST * 4;     // float2 ml[NW][G]

@@ -56,8 +56,13 @@ struct CostModel {
   double empty_cta_us;
   double merge_fixed_us;
   double merge_us_per_byte;
+  double cluster_merge_us;
   int slots;
 };
+
+// GPCs the SMs are grouped in (GB300: 8). Only the cost model uses it.
+constexpr int kAssumedGpcs = 8;
+constexpr int kMaxClusterSplits = 8;
 
 double simulate(const std::vector<int>& n_tok, int hkv, int chunk, int splits, const CostModel& cm,
                 uint64_t merge_bytes) {
@@ -79,6 +84,36 @@ double simulate(const std::vector<int>& n_tok, int hkv, int chunk, int splits, c
     }
   }
   if (splits > 1) makespan += cm.merge_fixed_us + merge_bytes * cm.merge_us_per_byte;
+  return makespan;
+}
+
+// The same launch with the S pieces of each (request, KV head) run as one
+// thread-block cluster (merged in the cluster, no merge launch): a cluster
+// needs S SMs of one GPC at once, so only floor(SMs per GPC / S) clusters fit
+// in a GPC; it lasts as long as its longest piece plus the in-cluster merge.
+double simulate_clusters(const std::vector<int>& n_tok, int hkv, int chunk, int splits, const CostModel& cm,
+                         int gpcs) {
+  const int per_gpc = cm.slots / gpcs;
+  const int cl_slots = gpcs * (per_gpc / splits);
+  if (cl_slots <= 0) return 1e300;
+  std::priority_queue<double, std::vector<double>, std::greater<double>> free_at;
+  for (int i = 0; i < cl_slots; ++i) free_at.push(0.0);
+  double makespan = 0.0;
+  for (size_t b = 0; b < n_tok.size(); ++b) {
+    double dur = cm.empty_cta_us;
+    for (int s = 0; s < splits; ++s) {
+      const long long lo = (long long)s * chunk;
+      const long long len = (s == splits - 1) ? n_tok[b] - lo : std::min<long long>(chunk, n_tok[b] - lo);
+      if (len > 0) dur = std::max(dur, cm.cta_fixed_us + len * cm.us_per_token);
+    }
+    dur += cm.cluster_merge_us;
+    for (int g = 0; g < hkv; ++g) {
+      const double start = free_at.top();
+      free_at.pop();
+      free_at.push(start + dur);
+      makespan = std::max(makespan, start + dur);
+    }
+  }
   return makespan;
 }
 
@@ -151,10 +186,12 @@ pd_status paged_decode_plan(const pd_layer_desc* layer, int32_t batch, const int
   cm.empty_cta_us = 0.2;
   cm.merge_fixed_us = 2.0;
   cm.merge_us_per_byte = 1.0 / 7.0e6;
+  cm.cluster_merge_us = 0.5;
   cm.slots = sm_count;  // one resident CTA per SM (shared memory bound)
 
   int best_chunk = std::max(16, (int)align_up((uint64_t)std::max(max_n, 1), 16));
   int best_splits = 1;
+  bool best_cluster = false;
   if (max_n > 0) {
     // candidates: multiples of 16 on a geometric grid, from the point where the
     // launch would need more than ~8 waves up to one piece per request
@@ -179,11 +216,20 @@ pd_status paged_decode_plan(const pd_layer_desc* layer, int32_t batch, const int
       const int s = (max_n + c - 1) / c;
       if (s > kMaxSplits) continue;
       const uint64_t merge_bytes = (uint64_t)batch * ly.num_q_heads * s * (ly.head_dim + 1) * 4ull * 2ull;
-      const double cost = simulate(n_tok, ly.num_kv_heads, c, s, cm, merge_bytes);
+      double cost = simulate(n_tok, ly.num_kv_heads, c, s, cm, merge_bytes);
+      bool cluster = false;
+      if (s >= 2 && s <= kMaxClusterSplits) {
+        const double cc = simulate_clusters(n_tok, ly.num_kv_heads, c, s, cm, kAssumedGpcs);
+        if (cc < cost) {
+          cost = cc;
+          cluster = true;
+        }
+      }
       if (cost < best * (1.0 - 1e-9) || (cost <= best && s < best_splits)) {
         best = cost;
         best_chunk = c;
         best_splits = s;
+        best_cluster = cluster;
       }
     }
   }
@@ -203,7 +249,13 @@ pd_status paged_decode_plan(const pd_layer_desc* layer, int32_t batch, const int
   plan->sm_count = sm_count;
   plan->max_seq_len = max_len;
   const uint64_t rows = (uint64_t)batch * ly.num_q_heads;
-  if (best_splits > 1) {
+  if (best_splits > 1 && best_cluster) {
+    // merged inside each cluster: the workspace holds only the error word
+    plan->merge_mode = 2;
+    plan->lse_offset = pd::kWorkspaceHeader;
+    plan->opart_offset = pd::kWorkspaceHeader;
+    plan->workspace_bytes = pd::kWorkspaceHeader;
+  } else if (best_splits > 1) {
     plan->merge_mode = 1;
     plan->lse_offset = pd::kWorkspaceHeader;
     plan->opart_offset = align_up(plan->lse_offset + rows * best_splits * 4ull, 256);
@@ -233,8 +285,9 @@ bool plan_is_valid(const pd_plan* plan) {
   if (plan->num_splits < 1 || plan->chunk_tokens < 16 || plan->chunk_tokens % 16 != 0) return false;
   if (plan->batch < 0 || plan->grid_x != plan->num_splits) return false;
   if (plan->threads_per_cta != v.threads || plan->smem_bytes != v.smem_bytes) return false;
-  if (plan->merge_mode < 0 || plan->merge_mode > 1) return false;
+  if (plan->merge_mode < 0 || plan->merge_mode > 2) return false;
   if ((plan->num_splits == 1) != (plan->merge_mode == 0)) return false;
+  if (plan->merge_mode == 2 && plan->num_splits > kMaxClusterSplits) return false;
   return true;
 }
 

@@ -27,7 +27,10 @@
 //     applied in fp32); each lane owns two heads, so the rescale of its O^T
 //     fragments needs no communication;
 //   * at the end the NW warp states are merged in shared memory and the CTA
-//     writes bf16 output (one piece) or an fp32 partial + log-sum-exp.
+//     writes bf16 output (one piece), or keeps its normalised result and
+//     log-sum-exp for rank 0 of its thread-block cluster to merge over
+//     distributed shared memory (up to 8 pieces), or writes an fp32 partial +
+//     log-sum-exp for the merge kernel (more pieces).
 #include <cuda_bf16.h>
 
 #include "pd_common.cuh"
@@ -72,11 +75,12 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 
 }  // namespace
 
+// One CTA's piece: stream, attend, merge the warps, and leave the piece's result
+// in `out` (one piece), in the workspace (pieces merged by a later launch) or in
+// this CTA's shared memory (pieces merged across the cluster). Threads return
+// from here at different points; none leaves the kernel early.
 template <class C>
-__global__ void __launch_bounds__(C::THREADS, 1) stage1_kernel(const __grid_constant__ Stage1Params p) {
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
-  // the swizzle pattern repeats every 1024 bytes of shared address: start there
-  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+__device__ __forceinline__ void stage1_cta(const Stage1Params& p, uint8_t* smem) {
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + C::BAR_OFFSET);
   uint64_t* empty_bar = full_bar + C::NST;
   uint32_t* stage_valid = reinterpret_cast<uint32_t*>(smem + C::VALID_OFFSET);
@@ -118,7 +122,9 @@ __global__ void __launch_bounds__(C::THREADS, 1) stage1_kernel(const __grid_cons
 
   if (nblk == 0) {
     // nothing attended in this piece
-    if (p.num_splits == 1) {
+    if (p.cluster_merge) {
+      if (threadIdx.x < C::G) reinterpret_cast<float*>(smem + C::CTA_LSE_OFFSET)[threadIdx.x] = -INFINITY;
+    } else if (p.num_splits == 1) {
       __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out) + row_hq * C::D;
       for (int i = threadIdx.x; i < C::G * C::D; i += C::THREADS) o[i] = __float2bfloat16_rn(0.f);
     } else {
@@ -435,12 +441,101 @@ __global__ void __launch_bounds__(C::THREADS, 1) stage1_kernel(const __grid_cons
       packed.x = pack_bf16x2(o.x, o.y);
       packed.y = pack_bf16x2(o.z, o.w);
       *reinterpret_cast<uint2*>(dst) = packed;
+    } else if (p.cluster_merge) {
+      // kept in shared memory for rank 0 of the cluster
+      reinterpret_cast<float4*>(smem + C::CTA_OUT_OFFSET)[h * D4 + d4] = o;
+      if (d4 == 0) reinterpret_cast<float*>(smem + C::CTA_LSE_OFFSET)[h] = coef[C::NW * C::G + h];
     } else {
       const size_t prow = (row_hq + h) * p.num_splits + split;
       reinterpret_cast<float4*>(p.o_part + prow * C::D)[d4] = o;
       if (d4 == 0) p.lse_part[prow] = coef[C::NW * C::G + h];
     }
   }
+}
+
+// Stage 2 inside the cluster (vLLM concepts page, "MLA 与 Sparse MLA（DSA）":
+// the pieces' partial results, each with its log-sum-exp, are merged). The S
+// CTAs of one (request, KV head) form a cluster; each holds its normalised
+// result and log-sum-exp in shared memory. Once every CTA is done with its ring,
+// ranks 1..S-1 push theirs into rank 0's ring area with posted distributed-
+// shared-memory stores; after a second cluster barrier rank 0 merges locally:
+//   out = sum_r w_r o_r,  w_r = exp(lse_r - M) / sum_r' exp(lse_r' - M),  M = max_r lse_r
+// in piece order; pieces with no attended token (lse = -inf) weigh nothing.
+template <class C>
+__device__ __forceinline__ void cluster_merge(const Stage1Params& p, uint8_t* smem) {
+  const int S = p.num_splits;
+  const uint32_t rank = cluster_ctarank();
+  const int tid = threadIdx.x;
+  constexpr int D4 = C::D / 4;
+  const float* my_lse = reinterpret_cast<const float*>(smem + C::CTA_LSE_OFFSET);
+  const float4* my_out = reinterpret_cast<const float4*>(smem + C::CTA_OUT_OFFSET);
+  cluster_sync_all();  // every CTA of the cluster is done with its ring
+  if (rank != 0) {
+    const uint32_t slot = smem_u32(smem + C::PUSH_OFFSET) + (rank - 1) * (C::G * C::D * 4);
+    const uint32_t lse_slot = smem_u32(smem + C::PUSH_LSE_OFFSET) + (rank - 1) * (C::G * 4);
+    if (tid < C::G) st_dsmem_f32(map_smem_rank(lse_slot + tid * 4, 0), my_lse[tid]);
+    const uint32_t remote = map_smem_rank(slot, 0);
+    for (int e = tid; e < C::G * D4; e += C::THREADS) {
+      if (my_lse[e / D4] == -INFINITY) continue;  // nothing attended: only the lse is pushed
+      st_dsmem_f32x4(remote + e * 16, my_out[e]);
+    }
+  }
+  cluster_sync_all();  // the pushes are visible in rank 0
+  if (rank != 0) return;
+  const float* push_lse = reinterpret_cast<const float*>(smem + C::PUSH_LSE_OFFSET);
+  const float4* push_out = reinterpret_cast<const float4*>(smem + C::PUSH_OFFSET);
+  float* wts = reinterpret_cast<float*>(smem + C::CTA_W_OFFSET);  // [S][G]
+  if (tid < C::G) {
+    float l[C::MAX_CLUSTER];
+    float M = -INFINITY;
+#pragma unroll
+    for (int r = 0; r < C::MAX_CLUSTER; ++r) {
+      l[r] = r >= S ? -INFINITY : (r == 0 ? my_lse[tid] : push_lse[(r - 1) * C::G + tid]);
+      M = fmaxf(M, l[r]);
+    }
+    float sum = 0.f;
+#pragma unroll
+    for (int r = 0; r < C::MAX_CLUSTER; ++r) {
+      l[r] = (M == -INFINITY) ? 0.f : expf(l[r] - M);
+      sum += l[r];
+    }
+    const float inv = sum > 0.f ? 1.f / sum : 0.f;
+#pragma unroll
+    for (int r = 0; r < C::MAX_CLUSTER; ++r)
+      if (r < S) wts[r * C::G + tid] = l[r] * inv;
+  }
+  __syncthreads();
+  const size_t row_hq = (size_t)blockIdx.z * p.num_q_heads + (size_t)blockIdx.y * C::G;
+#pragma unroll 2
+  for (int e = tid; e < C::G * D4; e += C::THREADS) {
+    const int h = e / D4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int r = 0; r < C::MAX_CLUSTER; ++r) {
+      if (r >= S) break;
+      const float w = wts[r * C::G + h];
+      if (w == 0.f) continue;  // an empty piece pushed no result
+      const float4 v = r == 0 ? my_out[e] : push_out[(r - 1) * C::G * D4 + e];
+      acc.x = fmaf(w, v.x, acc.x);
+      acc.y = fmaf(w, v.y, acc.y);
+      acc.z = fmaf(w, v.z, acc.z);
+      acc.w = fmaf(w, v.w, acc.w);
+    }
+    uint2 packed;
+    packed.x = pack_bf16x2(acc.x, acc.y);
+    packed.y = pack_bf16x2(acc.z, acc.w);
+    *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.out) + (row_hq + h) * C::D + (e % D4) * 4) =
+        packed;
+  }
+}
+
+template <class C>
+__global__ void __launch_bounds__(C::THREADS, 1) stage1_kernel(const __grid_constant__ Stage1Params p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // the swizzle pattern repeats every 1024 bytes of shared address: start there
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  stage1_cta<C>(p, smem);
+  if (p.cluster_merge) cluster_merge<C>(p, smem);
 }
 
 // ---- instantiation and dispatch -------------------------------------------------

@@ -98,12 +98,13 @@ def test_plan_covers_every_token(lib, lens, window, d, Hkv):
             lo = max(0, L - window) if window else 0
             span = L - (lo // TB) * TB if L else 0
             assert pl.num_splits * pl.chunk_tokens >= span
-        if pl.num_splits > 1:
+        if pl.num_splits > 1 and pl.merge_mode == 1:
             rows = len(lens) * Hkv * 2
-            assert pl.merge_mode == 1
             assert pl.workspace_bytes >= pl.opart_offset + rows * pl.num_splits * d * 4
             assert pl.opart_offset >= pl.lse_offset + rows * pl.num_splits * 4
             assert pl.lse_offset >= 4
+        elif pl.num_splits > 1:
+            assert pl.merge_mode == 2 and 2 <= pl.num_splits <= 8
         else:
             assert pl.merge_mode == 0
         assert pl.workspace_bytes >= 256
