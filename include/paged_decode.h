@@ -116,7 +116,10 @@ typedef struct {
                                1: paged_decode_merge launches the merge;
                                2: 2 <= S <= 8, stage 1 runs each (request, KV head)'s pieces as
                                   one thread-block cluster that merges them and writes out */
-  int32_t reserved[3];
+  int32_t test_stall_bytes;  /* 0. Tests set it > 0 to make stage 1 expect more bytes per stage
+                                than its copies deliver, so its pipeline waits run out (~1 s) and
+                                report PD_DEVFLAG_WAIT_TIMEOUT without any fault */
+  int32_t reserved[2];
   uint64_t workspace_bytes; /* bytes the caller must provide */
   uint64_t lse_offset;      /* byte offset of the fp32 [batch, Hq, S] log-sum-exp part */
   uint64_t opart_offset;    /* byte offset of the fp32 [batch, Hq, S, d] partial outputs */

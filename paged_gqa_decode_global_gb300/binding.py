@@ -68,7 +68,8 @@ class Plan(ctypes.Structure):
         ("sm_count", ctypes.c_int32),
         ("max_seq_len", ctypes.c_int32),
         ("merge_mode", ctypes.c_int32),
-        ("reserved", ctypes.c_int32 * 3),
+        ("test_stall_bytes", ctypes.c_int32),
+        ("reserved", ctypes.c_int32 * 2),
         ("workspace_bytes", ctypes.c_uint64),
         ("lse_offset", ctypes.c_uint64),
         ("opart_offset", ctypes.c_uint64),

@@ -146,6 +146,7 @@ pd_status stage1(const pd_plan* plan, const void* q, const void* k_pool, const v
   p.o_part = reinterpret_cast<float*>(ws + plan->opart_offset);
   p.err = reinterpret_cast<uint32_t*>(ws);
   p.cluster_merge = plan->merge_mode == 2 ? 1 : 0;
+  p.stall_bytes = plan->test_stall_bytes;
   p.scale_log2 = scale * kLog2e;
   p.window = ly.window;
   p.num_pages = ly.num_pages;

@@ -66,6 +66,17 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   }
 }
 
+// Wait for the phase of `parity` to complete until the %globaltimer deadline;
+// false if it passes.
+__device__ __forceinline__ bool mbar_wait_until(uint64_t* bar, uint32_t parity, unsigned long long deadline) {
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (global_timer_ns() > deadline) return false;
+  }
+}
+
 // L2 policy for data read exactly once (the KV stream).
 __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   uint64_t pol;

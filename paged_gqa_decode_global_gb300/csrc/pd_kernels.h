@@ -26,6 +26,7 @@ struct Stage1Params {
   float* o_part;                // [B, Hq, S, D] normalised partial outputs
   uint32_t* err;                // device error word
   int32_t cluster_merge;        // the S pieces of a (request, KV head) are one cluster; rank 0 merges
+  int32_t stall_bytes;          // tests only: bytes expected per stage beyond what the copies deliver
   float scale_log2;             // softmax scale * log2(e)
   int32_t window;               // 0 = global layer
   int32_t num_pages, max_pages, page_size;

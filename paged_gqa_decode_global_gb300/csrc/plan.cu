@@ -286,6 +286,8 @@ bool plan_is_valid(const pd_plan* plan) {
   if (plan->batch < 0 || plan->grid_x != plan->num_splits) return false;
   if (plan->threads_per_cta != v.threads || plan->smem_bytes != v.smem_bytes) return false;
   if (plan->merge_mode < 0 || plan->merge_mode > 2) return false;
+  if (plan->test_stall_bytes < 0 || plan->test_stall_bytes > (1 << 16) || plan->test_stall_bytes % 16 != 0)
+    return false;
   if ((plan->num_splits == 1) != (plan->merge_mode == 0)) return false;
   if (plan->merge_mode == 2 && plan->num_splits > kMaxClusterSplits) return false;
   return true;

@@ -209,7 +209,7 @@ __device__ __forceinline__ void stage1_cta(const Stage1Params& p, uint8_t* smem)
             if (ok) {
               const int row0 = (page * p.num_kv_heads + g) * p.page_size + (t0 % p.page_size);
               uint8_t* dst = smem + (size_t)st * C::STAGE_BYTES;
-              mbar_arrive_expect_tx(&full_bar[st], C::TX_BYTES);
+              mbar_arrive_expect_tx(&full_bar[st], C::TX_BYTES + p.stall_bytes);
               if (p.tma_rank == 3) {
                 tma_load_3d(dst, &p.kmap, 0, row0, 0, &full_bar[st], policy);
                 if (!C::KVS) tma_load_3d(dst + C::KV_BYTES, &p.vmap, 0, row0, 0, &full_bar[st], policy);
@@ -235,12 +235,17 @@ __device__ __forceinline__ void stage1_cta(const Stage1Params& p, uint8_t* smem)
         issued = j + 1;
       }
     }
-    // no copy may still be landing in shared memory when the CTA exits
+    // no copy may still be landing in shared memory when the CTA exits (one
+    // deadline for all stages)
     if (lane == 0) {
+      const unsigned long long deadline = global_timer_ns() + kWaitTimeoutNs;
 #pragma unroll 1
       for (int st = 0; st < C::NST && st < issued; ++st) {
         const int j_last = st + C::NST * ((issued - 1 - st) / C::NST);
-        if (!mbar_wait(&full_bar[st], (j_last / C::NST) & 1)) atomicOr(p.err, kErrTimeout);
+        if (!mbar_wait_until(&full_bar[st], (j_last / C::NST) & 1, deadline)) {
+          atomicOr(p.err, kErrTimeout);
+          break;
+        }
       }
     }
     return;

@@ -251,3 +251,24 @@ def test_many_pieces_merge(sms):
     step.run(li, again)
     assert step.check() == 0
     assert torch.equal(out, again)
+
+
+@pytest.mark.parametrize("lens,sms,mode", [([32], 152, 0), ([1000, 900], 152, 1), ([1000, 900], 20, 2)])
+def test_pipeline_wait_timeout_is_reported_and_context_survives(lens, sms, mode):
+    """A stage that never completes (the copies deliver fewer bytes than the
+    stage expects): every wait gives up after ~1 s, the kernel returns, the
+    host reads PD_DEVFLAG_WAIT_TIMEOUT, and the next call on the same context
+    is correct."""
+    li = synth.make_layer("stall", lens, 4, 2, 256, pool_pages=sum((L + 15) // 16 for L in lens) + 2, seed=30,
+                          device="cuda")
+    step = b.LayerStep.for_inputs(li, sm_count=sms)
+    assert step.plan.merge_mode == mode
+    step.plan.test_stall_bytes = 16
+    out = torch.zeros_like(li.q)
+    step.run(li, out)
+    with pytest.raises(b.PagedDecodeError) as e:
+        step.check()
+    assert e.value.status == b.PD_ERR_DEVICE_FAULT and e.value.flags & b.PD_DEVFLAG_WAIT_TIMEOUT
+    step.plan.test_stall_bytes = 0
+    out2, _ = run_gpu(li, sm_count=sms)
+    compare(out2, run_oracle(li), li, "after a timed-out call")
