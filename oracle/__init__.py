@@ -66,6 +66,10 @@ def _load():
             lib.ref_merge.restype = i
             lib.ref_max_threads.argtypes = []
             lib.ref_max_threads.restype = i
+            lib.ref_decode_rows_fp8.argtypes = [i, i, i, i, i, i, i, p, p, p, p, p, p, p, i, d, p, i, p, p, i]
+            lib.ref_decode_rows_fp8.restype = i
+            lib.ref_e4m3_to_f64.argtypes = [i]
+            lib.ref_e4m3_to_f64.restype = d
             _lib = lib
     return _lib
 
@@ -129,6 +133,42 @@ def decode(q, k_pool, v_pool, block_tables, seq_lens, scale: float, window: int 
                              float(scale), _ptr(rows_arr), n_rows, _ptr(out), _ptr(lse), int(nthreads))
     _check(st)
     return (out, lse) if return_lse else out
+
+
+def decode_fp8(q, k8, v8, k_scale, v_scale, block_tables, seq_lens, scale: float, window: int = 0,
+               rows=None, nthreads: int = 0, return_lse: bool = False):
+    """Decode over an FP8 KV cache in fp64.
+
+    q: uint16 (bf16 bits) [B, Hq, d]; k8 / v8: uint8 e4m3 bytes
+    [num_pages, Hkv, P, d] (v8 None = K=V layer, K's scales);
+    k_scale / v_scale: float32 [num_pages, Hkv] (the cached value is the e4m3
+    value times its (page, KV head) scale). Otherwise as `decode`.
+    """
+    lib = _load()
+    q = _u16(q)
+    k8 = np.ascontiguousarray(k8, dtype=np.uint8)
+    v8 = None if v8 is None else np.ascontiguousarray(v8, dtype=np.uint8)
+    k_scale = np.ascontiguousarray(k_scale, dtype=np.float32)
+    v_scale = None if v_scale is None else np.ascontiguousarray(v_scale, dtype=np.float32)
+    block_tables, seq_lens = _i32(block_tables), _i32(seq_lens)
+    B, Hq, Hkv, d, P, num_pages, max_pages = _shapes(q, k8, block_tables)
+    if k_scale.shape != (num_pages, Hkv) or (v8 is not None and (v8.shape != k8.shape or v_scale is None
+                                                                  or v_scale.shape != k_scale.shape)):
+        raise ValueError("fp8 pool / scale shapes disagree")
+    out = np.zeros((B, Hq, d), dtype=np.float64)
+    lse = np.full((B, Hq), -np.inf, dtype=np.float64)
+    rows_arr = None if rows is None else _i32(rows)
+    n_rows = 0 if rows_arr is None else int(rows_arr.size)
+    st = lib.ref_decode_rows_fp8(B, Hq, Hkv, d, P, num_pages, max_pages, _ptr(q), _ptr(k8), _ptr(v8),
+                                 _ptr(k_scale), _ptr(v_scale), _ptr(block_tables), _ptr(seq_lens), int(window),
+                                 float(scale), _ptr(rows_arr), n_rows, _ptr(out), _ptr(lse), int(nthreads))
+    _check(st)
+    return (out, lse) if return_lse else out
+
+
+def e4m3_to_f64(code: int) -> float:
+    """The oracle's e4m3 decoder, for its pin."""
+    return float(_load().ref_e4m3_to_f64(int(code)))
 
 
 def decode_split(q, k_pool, v_pool, block_tables, seq_lens, scale: float, window: int,

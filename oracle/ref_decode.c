@@ -29,13 +29,20 @@
  *     inference", sections "Gemma 4 文本推理" (text inference) and
  *     "专用算子与性能优化" (dedicated operators);
  *   - the split-KV partial results with a log-sum-exp slot, merged afterwards:
- *     vLLM concepts page, section "MLA 与 Sparse MLA（DSA）" (MLA decode).
+ *     vLLM concepts page, section "MLA 与 Sparse MLA（DSA）" (MLA decode);
+ *   - an FP8 KV cache (the same decode over e4m3 values times per-(page, KV
+ *     head) scales): the vLLM concepts page records FP8 KV-cache support in its
+ *     Blackwell (SM100) FlashAttention-4 backend (section "JIT 预热基础设施") and a
+ *     Blackwell sparse-MLA backend that takes an FP8 KV cache (section "MLA 与
+ *     Sparse MLA（DSA）"); the e4m3 format and the scale granularity are this
+ *     library's reading.
  *
  * Readings where the pages are silent: the window keeps exactly the last W
  * positions including the current token; query head h uses KV head h / G; the
  * pool layout is [num_pages, Hkv, P, d] (the [B, H, N, C] slice of one layer).
  *
- * All arithmetic is IEEE fp64 from the exact bf16 input values. Build with
+ * All arithmetic is IEEE fp64 from the exact bf16 (or e4m3 x fp32 scale) input
+ * values. Build with
  * -ffp-contract=off so x86 and Arm hosts produce identical bits.
  */
 #include <math.h>
@@ -62,19 +69,38 @@ static double bf16_to_f64(uint16_t bits) {
   return (double)f;
 }
 
+/*
+ * OCP FP8 E4M3 ("fn" flavour: no infinities; S.1111.111 is the only NaN) ->
+ * fp64, from the format's definition: 1 sign bit, 4 exponent bits with bias 7,
+ * 3 mantissa bits; exponent field 0 encodes the subnormals m * 2^-9.
+ */
+static double e4m3_to_f64(uint8_t x) {
+  const int sign = x >> 7, e = (x >> 3) & 15, m = x & 7;
+  if (e == 15 && m == 7) return NAN;
+  const double v = (e == 0) ? ldexp((double)m, -9) : ldexp(1.0 + m / 8.0, e - 7);
+  return sign ? -v : v;
+}
+
 typedef struct {
   int B, Hq, Hkv, d, P, num_pages, max_pages;
   const uint16_t *q, *k_pool, *v_pool; /* v_pool == NULL: V is K (K=V layer) */
   const int32_t *block_tables, *seq_lens;
   int window; /* 0 = global layer */
   double scale;
+  /* FP8 KV cache: e4m3 pools with one scale per (page, KV head) for K and for V
+   * (k8/v8 replace k_pool/v_pool; v8 == NULL: V is K, with K's scales) */
+  int kv_fp8;
+  const uint8_t *k8, *v8;
+  const float *k_scale, *v_scale; /* [num_pages, Hkv] */
 } ref_layer;
 
 static int check_layer(const ref_layer *ly) {
   if (ly->B < 0 || ly->Hq <= 0 || ly->Hkv <= 0 || ly->d <= 0 || ly->P <= 0) return REF_BAD_ARG;
   if (ly->Hq % ly->Hkv != 0) return REF_BAD_ARG;
   if (ly->window < 0 || ly->num_pages < 0 || ly->max_pages < 0) return REF_BAD_ARG;
-  if (ly->B > 0 && (!ly->q || !ly->k_pool || !ly->block_tables || !ly->seq_lens)) return REF_BAD_ARG;
+  if (ly->B > 0 && (!ly->q || !ly->block_tables || !ly->seq_lens)) return REF_BAD_ARG;
+  if (ly->B > 0 && !ly->kv_fp8 && !ly->k_pool) return REF_BAD_ARG;
+  if (ly->B > 0 && ly->kv_fp8 && (!ly->k8 || !ly->k_scale || (ly->v8 && !ly->v_scale))) return REF_BAD_ARG;
   for (int b = 0; b < ly->B; ++b) {
     int L = ly->seq_lens[b];
     if (L < 0 || (long long)L > (long long)ly->max_pages * ly->P) return REF_BAD_LEN;
@@ -89,13 +115,25 @@ static void attended_range(const ref_layer *ly, int b, int *lo, int *hi) {
   *lo = (ly->window > 0 && L > ly->window) ? L - ly->window : 0;
 }
 
-/* Pointer to the d values of token t of request b, KV head g, in `pool`.
- * Returns NULL if the block table names a page outside the pool. */
-static const uint16_t *token_row(const ref_layer *ly, const uint16_t *pool, int b, int g, int t) {
+/* The d values of token t of request b, KV head g, from the K (which = 0) or
+ * V (which = 1) pool, widened to fp64 into row[0..d) (FP8 pools: the e4m3
+ * value times its (page, KV head) scale). REF_BAD_PAGE if the block table
+ * names a page outside the pool. */
+static int load_row(const ref_layer *ly, int which, int b, int g, int t, double *row) {
   int32_t page = ly->block_tables[(size_t)b * ly->max_pages + t / ly->P];
-  if (page < 0 || page >= ly->num_pages) return NULL;
-  size_t row = ((size_t)page * ly->Hkv + g) * ly->P + (size_t)(t % ly->P);
-  return pool + row * ly->d;
+  if (page < 0 || page >= ly->num_pages) return REF_BAD_PAGE;
+  const size_t r = ((size_t)page * ly->Hkv + g) * ly->P + (size_t)(t % ly->P);
+  const size_t base = r * ly->d;
+  if (!ly->kv_fp8) {
+    const uint16_t *pool = (which == 1 && ly->v_pool) ? ly->v_pool : ly->k_pool;
+    for (int i = 0; i < ly->d; ++i) row[i] = bf16_to_f64(pool[base + i]);
+  } else {
+    const int use_v = (which == 1 && ly->v8);
+    const uint8_t *pool8 = use_v ? ly->v8 : ly->k8;
+    const double s = (use_v ? ly->v_scale : ly->k_scale)[(size_t)page * ly->Hkv + g];
+    for (int i = 0; i < ly->d; ++i) row[i] = e4m3_to_f64(pool8[base + i]) * s;
+  }
+  return REF_OK;
 }
 
 /*
@@ -105,12 +143,11 @@ static const uint16_t *token_row(const ref_layer *ly, const uint16_t *pool, int 
  * the range is empty).
  */
 static int attend_range(const ref_layer *ly, int b, int h, int lo, int hi, double *o, double *lse,
-                        double *s /* scratch, >= hi - lo */) {
+                        double *s /* scratch, >= hi - lo */, double *row /* scratch, d */) {
   const int G = ly->Hq / ly->Hkv;
   const int g = h / G;
   const int d = ly->d;
   const uint16_t *qrow = ly->q + ((size_t)b * ly->Hq + h) * d;
-  const uint16_t *vpool = ly->v_pool ? ly->v_pool : ly->k_pool;
 
   for (int i = 0; i < d; ++i) o[i] = 0.0;
   if (hi <= lo) {
@@ -120,10 +157,9 @@ static int attend_range(const ref_layer *ly, int b, int h, int lo, int hi, doubl
   /* scores s_t = scale * <q, K_t> */
   double m = -INFINITY;
   for (int t = lo; t < hi; ++t) {
-    const uint16_t *krow = token_row(ly, ly->k_pool, b, g, t);
-    if (!krow) return REF_BAD_PAGE;
+    if (load_row(ly, 0, b, g, t, row) != REF_OK) return REF_BAD_PAGE;
     double acc = 0.0;
-    for (int i = 0; i < d; ++i) acc += bf16_to_f64(qrow[i]) * bf16_to_f64(krow[i]);
+    for (int i = 0; i < d; ++i) acc += bf16_to_f64(qrow[i]) * row[i];
     s[t - lo] = ly->scale * acc;
     if (s[t - lo] > m) m = s[t - lo];
   }
@@ -135,10 +171,9 @@ static int attend_range(const ref_layer *ly, int b, int h, int lo, int hi, doubl
   }
   /* weighted sum of the value rows */
   for (int t = lo; t < hi; ++t) {
-    const uint16_t *vrow = token_row(ly, vpool, b, g, t);
-    if (!vrow) return REF_BAD_PAGE;
+    if (load_row(ly, 1, b, g, t, row) != REF_OK) return REF_BAD_PAGE;
     const double p = s[t - lo];
-    for (int i = 0; i < d; ++i) o[i] += p * bf16_to_f64(vrow[i]);
+    for (int i = 0; i < d; ++i) o[i] += p * row[i];
   }
   for (int i = 0; i < d; ++i) o[i] /= l;
   *lse = m + log(l);
@@ -153,6 +188,58 @@ static void set_threads(int nthreads) {
 #endif
 }
 
+static int max_seq_len(const ref_layer *ly) {
+  int max_len = 0;
+  for (int b = 0; b < ly->B; ++b) max_len = ly->seq_lens[b] > max_len ? ly->seq_lens[b] : max_len;
+  return max_len;
+}
+
+/* Rows (b * Hq + h) of the decode, in parallel over rows. */
+static int decode_rows(const ref_layer *ly, const int32_t *rows, int n_rows, double *out, double *lse_out,
+                       int nthreads) {
+  int st = check_layer(ly);
+  if (st != REF_OK) return st;
+  if (!out) return REF_BAD_ARG;
+  const int B = ly->B, Hq = ly->Hq, d = ly->d;
+  const int total = rows ? n_rows : B * Hq;
+  const int max_len = max_seq_len(ly);
+
+  int status = REF_OK;
+  set_threads(nthreads);
+#pragma omp parallel
+  {
+    double *s = (double *)malloc(sizeof(double) * (size_t)(max_len > 0 ? max_len : 1));
+    double *row = (double *)malloc(sizeof(double) * (size_t)d);
+    if (!s || !row) {
+#pragma omp critical
+      status = REF_NO_MEM;
+    }
+#pragma omp for schedule(dynamic, 1)
+    for (int r = 0; r < total; ++r) {
+      if (!s || !row) continue;
+      const int rix = rows ? rows[r] : r;
+      if (rix < 0 || rix >= B * Hq) {
+#pragma omp critical
+        status = REF_BAD_ARG;
+        continue;
+      }
+      const int b = rix / Hq, h = rix % Hq;
+      int lo, hi;
+      attended_range(ly, b, &lo, &hi);
+      double lse;
+      int rs = attend_range(ly, b, h, lo, hi, out + (size_t)rix * d, &lse, s, row);
+      if (lse_out) lse_out[rix] = lse;
+      if (rs != REF_OK) {
+#pragma omp critical
+        status = rs;
+      }
+    }
+    free(s);
+    free(row);
+  }
+  return status;
+}
+
 /*
  * Full decode: out[b, h, :] for every request and query head (fp64), and the
  * log-sum-exp of each row into lse_out[b, h] when lse_out is not NULL.
@@ -165,47 +252,28 @@ int ref_decode_rows(int B, int Hq, int Hkv, int d, int P, int num_pages, int max
                     const int32_t *block_tables, const int32_t *seq_lens, int window, double scale,
                     const int32_t *rows, int n_rows, double *out, double *lse_out, int nthreads) {
   ref_layer ly = {B, Hq, Hkv, d, P, num_pages, max_pages, q, k_pool, v_pool,
-                  block_tables, seq_lens, window, scale};
-  int st = check_layer(&ly);
-  if (st != REF_OK) return st;
-  if (!out) return REF_BAD_ARG;
-  const int total = rows ? n_rows : B * Hq;
-  int max_len = 0;
-  for (int b = 0; b < B; ++b) max_len = seq_lens[b] > max_len ? seq_lens[b] : max_len;
-
-  int status = REF_OK;
-  set_threads(nthreads);
-#pragma omp parallel
-  {
-    double *s = (double *)malloc(sizeof(double) * (size_t)(max_len > 0 ? max_len : 1));
-    if (!s) {
-#pragma omp critical
-      status = REF_NO_MEM;
-    }
-#pragma omp for schedule(dynamic, 1)
-    for (int r = 0; r < total; ++r) {
-      if (!s) continue;
-      const int row = rows ? rows[r] : r;
-      if (row < 0 || row >= B * Hq) {
-#pragma omp critical
-        status = REF_BAD_ARG;
-        continue;
-      }
-      const int b = row / Hq, h = row % Hq;
-      int lo, hi;
-      attended_range(&ly, b, &lo, &hi);
-      double lse;
-      int rs = attend_range(&ly, b, h, lo, hi, out + (size_t)row * d, &lse, s);
-      if (lse_out) lse_out[row] = lse;
-      if (rs != REF_OK) {
-#pragma omp critical
-        status = rs;
-      }
-    }
-    free(s);
-  }
-  return status;
+                  block_tables, seq_lens, window, scale, 0, NULL, NULL, NULL, NULL};
+  return decode_rows(&ly, rows, n_rows, out, lse_out, nthreads);
 }
+
+/*
+ * The same decode over an FP8 KV cache: k8 / v8 hold e4m3 bytes in the pool
+ * layout [num_pages, Hkv, P, d], k_scale / v_scale one fp32 scale per
+ * (page, KV head); the cached value is the e4m3 value times its scale. v8 =
+ * NULL: V is K (K=V layer), with K's scales. q stays bf16.
+ */
+int ref_decode_rows_fp8(int B, int Hq, int Hkv, int d, int P, int num_pages, int max_pages,
+                        const uint16_t *q, const uint8_t *k8, const uint8_t *v8, const float *k_scale,
+                        const float *v_scale, const int32_t *block_tables, const int32_t *seq_lens, int window,
+                        double scale, const int32_t *rows, int n_rows, double *out, double *lse_out,
+                        int nthreads) {
+  ref_layer ly = {B, Hq, Hkv, d, P, num_pages, max_pages, q, NULL, NULL,
+                  block_tables, seq_lens, window, scale, 1, k8, v8, k_scale, v8 ? v_scale : NULL};
+  return decode_rows(&ly, rows, n_rows, out, lse_out, nthreads);
+}
+
+/* e4m3 byte -> fp64 (exposed for the tests that pin the decoder). */
+double ref_e4m3_to_f64(int x) { return e4m3_to_f64((uint8_t)x); }
 
 /*
  * Split-KV first stage (vLLM concepts page, "MLA 与 Sparse MLA（DSA）"): the
@@ -221,21 +289,21 @@ int ref_decode_split(int B, int Hq, int Hkv, int d, int P, int num_pages, int ma
                      const int32_t *block_tables, const int32_t *seq_lens, int window, double scale,
                      int num_splits, int chunk, double *o_part, double *lse_part, int nthreads) {
   ref_layer ly = {B, Hq, Hkv, d, P, num_pages, max_pages, q, k_pool, v_pool,
-                  block_tables, seq_lens, window, scale};
+                  block_tables, seq_lens, window, scale, 0, NULL, NULL, NULL, NULL};
   int st = check_layer(&ly);
   if (st != REF_OK) return st;
   if (num_splits <= 0 || chunk <= 0 || !o_part || !lse_part) return REF_BAD_ARG;
-  int max_len = 0;
-  for (int b = 0; b < B; ++b) max_len = seq_lens[b] > max_len ? seq_lens[b] : max_len;
+  const int max_len = max_seq_len(&ly);
 
   int status = REF_OK;
   set_threads(nthreads);
 #pragma omp parallel
   {
     double *s = (double *)malloc(sizeof(double) * (size_t)(max_len > 0 ? max_len : 1));
+    double *rowbuf = (double *)malloc(sizeof(double) * (size_t)d);
 #pragma omp for schedule(dynamic, 1)
     for (int row = 0; row < B * Hq; ++row) {
-      if (!s) continue;
+      if (!s || !rowbuf) continue;
       const int b = row / Hq, h = row % Hq;
       int lo, hi;
       attended_range(&ly, b, &lo, &hi);
@@ -245,18 +313,19 @@ int ref_decode_split(int B, int Hq, int Hkv, int d, int P, int num_pages, int ma
         if (plo > hi) plo = hi;
         if (phi > hi) phi = hi;
         const size_t idx = (size_t)row * num_splits + k;
-        int rs = attend_range(&ly, b, h, (int)plo, (int)phi, o_part + idx * d, lse_part + idx, s);
+        int rs = attend_range(&ly, b, h, (int)plo, (int)phi, o_part + idx * d, lse_part + idx, s, rowbuf);
         if (rs != REF_OK) {
 #pragma omp critical
           status = rs;
         }
       }
     }
-    if (!s) {
+    if (!s || !rowbuf) {
 #pragma omp critical
       status = REF_NO_MEM;
     }
     free(s);
+    free(rowbuf);
   }
   return status;
 }

@@ -223,3 +223,77 @@ def workload(cid: int, device="cpu", part: Optional[str] = None) -> List[LayerIn
                                      seed=seed + 1, device=device, block_tables=table))
         return layers
     raise ValueError(f"unknown workload {cid}")
+
+
+# --------------------------------------------------------------------------
+# FP8 KV cache inputs
+# --------------------------------------------------------------------------
+
+E4M3_MAX = 448.0
+
+
+@dataclass
+class Fp8LayerInputs:
+    """A layer whose KV cache holds e4m3 bytes with one fp32 scale per
+    (page, KV head) for K and for V; the cached value is byte * scale."""
+
+    name: str
+    q: torch.Tensor                  # bf16 [B, Hq, d]
+    k8: torch.Tensor                 # uint8 (e4m3 bits) [num_pages, Hkv, P, d]
+    v8: Optional[torch.Tensor]       # like k8; None for a K=V layer
+    k_scale: torch.Tensor            # float32 [num_pages, Hkv]
+    v_scale: Optional[torch.Tensor]  # float32 [num_pages, Hkv]; None for a K=V layer
+    block_tables: torch.Tensor
+    seq_lens: torch.Tensor
+    window: int
+    scale: float
+
+    batch = LayerInputs.batch
+    num_q_heads = LayerInputs.num_q_heads
+    head_dim = LayerInputs.head_dim
+    max_pages = LayerInputs.max_pages
+    seq_lens_list = LayerInputs.seq_lens_list
+    attended = LayerInputs.attended
+
+    @property
+    def num_pages(self) -> int:
+        return int(self.k8.shape[0])
+
+    @property
+    def num_kv_heads(self) -> int:
+        return int(self.k8.shape[1])
+
+    @property
+    def page_size(self) -> int:
+        return int(self.k8.shape[2])
+
+    @property
+    def kv_shared(self) -> bool:
+        return self.v8 is None
+
+    def kv_bytes(self) -> int:
+        per_token = self.num_kv_heads * self.head_dim * (1 if self.kv_shared else 2)
+        return sum(self.attended()) * per_token
+
+    def algorithmic_bytes(self) -> int:
+        """KV bytes, their scales (one per page and KV head touched), q read and out written."""
+        qo = 2 * self.batch * self.num_q_heads * self.head_dim * 2
+        pages = sum((n + self.page_size - 1) // self.page_size for n in self.attended())
+        return self.kv_bytes() + pages * self.num_kv_heads * 4 * (1 if self.kv_shared else 2) + qo
+
+
+def _quantize_pool(pool: torch.Tensor):
+    """Per (page, KV head): scale = max |x| / 448, bytes = e4m3(x / scale)."""
+    x = pool.float()
+    amax = x.abs().amax(dim=(2, 3))
+    scale = torch.where(amax > 0, amax / E4M3_MAX, torch.ones_like(amax))
+    q8 = (x / scale[:, :, None, None]).clamp_(-E4M3_MAX, E4M3_MAX).to(torch.float8_e4m3fn)
+    return q8.view(torch.uint8), scale.contiguous()
+
+
+def quantize_kv_fp8(li: LayerInputs) -> Fp8LayerInputs:
+    """The same layer with its KV cache stored as e4m3 with per-(page, KV head) scales."""
+    k8, ks = _quantize_pool(li.k_pool)
+    v8, vs = (None, None) if li.v_pool is None else _quantize_pool(li.v_pool)
+    return Fp8LayerInputs(li.name + "-fp8", li.q, k8, v8, ks, vs, li.block_tables, li.seq_lens, li.window,
+                          li.scale)

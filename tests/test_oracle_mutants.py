@@ -25,7 +25,11 @@ MUTANTS = {
     "page_row_swapped": ("(size_t)(t % ly->P);", "(size_t)(t / ly->P);"),
     "scale_dropped": ("s[t - lo] = ly->scale * acc;", "s[t - lo] = acc;"),
     "normalisation_dropped": ("for (int i = 0; i < d; ++i) o[i] /= l;", ""),
-    "k_used_as_v": ("token_row(ly, vpool, b, g, t)", "token_row(ly, ly->k_pool, b, g, t)"),
+    "k_used_as_v": ("load_row(ly, 1, b, g, t, row)", "load_row(ly, 0, b, g, t, row)"),
+    "fp8_scale_dropped": ("row[i] = e4m3_to_f64(pool8[base + i]) * s;", "row[i] = e4m3_to_f64(pool8[base + i]);"),
+    "fp8_exponent_bias": ("ldexp(1.0 + m / 8.0, e - 7)", "ldexp(1.0 + m / 8.0, e - 8)"),
+    "fp8_subnormal": ("ldexp((double)m, -9)", "ldexp((double)m, -10)"),
+    "fp8_v_scale_from_k": ("(use_v ? ly->v_scale : ly->k_scale)", "(ly->k_scale)"),
     "merge_weight_sign": ("exp(lse[k] - M)", "exp(M - lse[k])"),
     "lse_without_log": ("*lse = m + log(l);", "*lse = m;"),
     "split_ignores_range_start": ("long long plo = (long long)lo + (long long)k * chunk;",
@@ -47,6 +51,9 @@ def _battery():
         "split_merge_global": lambda: pins.test_split_merge_equals_unsplit(7, 5, 0),
         "lse": pins.test_lse_matches_scores,
         "window_invariant": pins.test_window_mask_invariant,
+        "e4m3_codes": pins.test_e4m3_decoder_matches_torch_for_every_code,
+        "fp8_sdpa": lambda: pins.test_fp8_decode_matches_sdpa_on_dequantized_kv(False, 0),
+        "fp8_sdpa_kvshared": lambda: pins.test_fp8_decode_matches_sdpa_on_dequantized_kv(True, 9),
     }
     for name, fn in checks.items():
         try:
@@ -65,7 +72,8 @@ def _load_variant(src_text, workdir, tag):
                     "-o", path_so, path_c, "-lm"], check=True)
     lib = ctypes.CDLL(path_so)
     ref = oracle._load()
-    for fn in ("ref_decode_rows", "ref_decode_split", "ref_merge", "ref_max_threads"):
+    for fn in ("ref_decode_rows", "ref_decode_split", "ref_merge", "ref_max_threads", "ref_decode_rows_fp8",
+               "ref_e4m3_to_f64"):
         getattr(lib, fn).argtypes = getattr(ref, fn).argtypes
         getattr(lib, fn).restype = getattr(ref, fn).restype
     return lib

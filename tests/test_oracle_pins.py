@@ -259,3 +259,82 @@ def test_row_subset_matches_full():
         b, h = divmod(r, 8)
         assert np.array_equal(part[b, h], full[b, h])
     assert (part[0, 0] == 0).all()
+
+
+# ---- FP8 KV cache ---------------------------------------------------------------
+
+def test_e4m3_decoder_matches_torch_for_every_code():
+    """The oracle's e4m3 decoder against torch's float8_e4m3fn for all 256 codes."""
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = np.array([oracle.e4m3_to_f64(c) for c in range(256)])
+    nan = np.isnan(ref)
+    assert (np.isnan(got) == nan).all() and nan.sum() == 2  # S.1111.111 for both signs
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert got[0x7E] == 448.0 and got[0x01] == 2.0 ** -9 and got[0x08] == 2.0 ** -6
+
+
+def _fp8_layer(lens, Hq, Hkv, d, window=0, kv_shared=False, seed=0):
+    ly = _layer(lens, Hq, Hkv, d, window=window, kv_shared=kv_shared, seed=seed)
+    return synth.quantize_kv_fp8(ly)
+
+
+def _dequant(pool8, scale):
+    return pool8.view(torch.float8_e4m3fn).to(torch.float64) * scale.to(torch.float64)[:, :, None, None]
+
+
+@pytest.mark.parametrize("kv_shared,window", [(False, 0), (True, 9), (False, 20)])
+def test_fp8_decode_matches_sdpa_on_dequantized_kv(kv_shared, window):
+    """FP8 decode equals library attention over the explicitly dequantized cache."""
+    f = _fp8_layer([37, 64, 5], 8, 2, 16, window=window, kv_shared=kv_shared, seed=40 + window)
+    got = oracle.decode_fp8(synth.bits_u16(f.q), f.k8.numpy(), None if f.v8 is None else f.v8.numpy(),
+                            f.k_scale.numpy(), None if f.v_scale is None else f.v_scale.numpy(),
+                            f.block_tables.numpy(), f.seq_lens.numpy(), f.scale, window)
+    K = _dequant(f.k8, f.k_scale)
+    V = K if f.v8 is None else _dequant(f.v8, f.v_scale)
+    dense = synth.make_layer("dq", [37, 64, 5], 8, 2, 16, window=window, pool_pages=f.num_pages, seed=0,
+                             block_tables=f.block_tables)
+    ref = _sdpa_reference_pools(dense, K, V, f.q)
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-12)
+
+
+def _sdpa_reference_pools(ly, K_pool, V_pool, q):
+    """Library attention over float64 pools (any values), explicit window mask."""
+    out = torch.zeros(ly.batch, q.shape[1], ly.head_dim, dtype=torch.float64)
+    G = q.shape[1] // ly.num_kv_heads
+    for b in range(ly.batch):
+        L = int(ly.seq_lens[b])
+        if L == 0:
+            continue
+        P = ly.page_size
+        pages = [int(ly.block_tables[b, t // P]) for t in range(L)]
+        K = torch.stack([K_pool[pages[t], :, t % P] for t in range(L)], dim=1).repeat_interleave(G, dim=0)
+        V = torch.stack([V_pool[pages[t], :, t % P] for t in range(L)], dim=1).repeat_interleave(G, dim=0)
+        qq = q[b].to(torch.float64).unsqueeze(1)
+        pos = torch.arange(L)
+        keep = pos >= (L - ly.window) if ly.window > 0 else torch.ones(L, dtype=torch.bool)
+        mask = keep.view(1, 1, L).expand(q.shape[1], 1, L)
+        out[b] = torch.nn.functional.scaled_dot_product_attention(qq, K, V, attn_mask=mask, scale=ly.scale)[:, 0]
+    return out.numpy()
+
+
+def test_fp8_single_token_is_its_scaled_value_row():
+    f = _fp8_layer([1, 1], 4, 2, 32, seed=41)
+    got = oracle.decode_fp8(synth.bits_u16(f.q), f.k8.numpy(), f.v8.numpy(), f.k_scale.numpy(), f.v_scale.numpy(),
+                            f.block_tables.numpy(), f.seq_lens.numpy(), f.scale)
+    for b in range(2):
+        page = int(f.block_tables[b, 0])
+        want = (f.v8[page, :, 0].view(torch.float8_e4m3fn).to(torch.float64)
+                * f.v_scale[page].to(torch.float64)[:, None]).repeat_interleave(2, dim=0).numpy()
+        assert np.array_equal(got[b], want)
+
+
+def test_fp8_key_scale_is_a_logit_scale():
+    """Doubling every K scale is the same as doubling the softmax scale."""
+    f = _fp8_layer([50, 23], 4, 2, 16, seed=42)
+    args = (f.k8.numpy(), f.v8.numpy())
+    a = oracle.decode_fp8(synth.bits_u16(f.q), *args, (f.k_scale * 2).numpy(), f.v_scale.numpy(),
+                          f.block_tables.numpy(), f.seq_lens.numpy(), f.scale)
+    b_ = oracle.decode_fp8(synth.bits_u16(f.q), *args, f.k_scale.numpy(), f.v_scale.numpy(),
+                           f.block_tables.numpy(), f.seq_lens.numpy(), 2 * f.scale)
+    np.testing.assert_allclose(a, b_, rtol=1e-13, atol=1e-15)
