@@ -171,7 +171,7 @@ def workload_layer(cid: int, part, device):
 
 def config_of(li, cid, part, replicas, plan):
     return {
-        "workload": synth.WORKLOADS[cid] + (f" [{li.name}]" if part else ""),
+        "workload": synth.WORKLOADS[cid] + (f" [{li.name}]" if part or hasattr(li, "k8") else ""),
         "batch": li.batch, "num_q_heads": li.num_q_heads, "num_kv_heads": li.num_kv_heads,
         "head_dim": li.head_dim, "page_size": li.page_size, "pool_pages": li.num_pages,
         "seq_lens": li.seq_lens_list() if li.batch <= 8 else f"{li.batch} requests",
@@ -199,6 +199,9 @@ def run_ours(args, world, rank, local):
     pdb.load_library()
 
     li = workload_layer(args.workload, args.part, dev)
+    fp8 = args.kv == "fp8"
+    if fp8:
+        li = synth.quantize_kv_fp8(li)
     step = pdb.LayerStep.for_inputs(li)
     plan = step.plan
     S = int(plan.num_splits)
@@ -206,15 +209,24 @@ def run_ours(args, world, rank, local):
 
     touched = max(1, li.kv_bytes())
     replicas = max(1, min(16, math.ceil(4 * L2_BYTES / touched)))
-    pools = [(li.k_pool, li.v_pool)]
+    kp, vp = (li.k8, li.v8) if fp8 else (li.k_pool, li.v_pool)
+    pools = [(kp, vp)]
     for _ in range(replicas - 1):
-        pools.append((li.k_pool.clone(), None if li.v_pool is None else li.v_pool.clone()))
+        pools.append((kp.clone(), None if vp is None else vp.clone()))
+    k_sc = li.k_scale if fp8 else None
+    v_sc = li.v_scale if fp8 else None
     out = torch.empty_like(li.q)
     stream = torch.cuda.Stream(device=dev)
 
     def one_step(i, stage1_only=False):
         k, v = pools[i % replicas]
-        if li.window > 0:
+        if fp8 and li.window > 0:
+            pdb.paged_decode_window_fp8(plan, li.q, k, v, k_sc, v_sc, li.block_tables, li.seq_lens, li.window,
+                                        li.scale, step.workspace, out, stream)
+        elif fp8:
+            pdb.paged_decode_global_fp8(plan, li.q, k, v, k_sc, v_sc, li.block_tables, li.seq_lens, li.scale,
+                                        step.workspace, out, stream)
+        elif li.window > 0:
             pdb.paged_decode_window(plan, li.q, k, v, li.block_tables, li.seq_lens, li.window, li.scale,
                                     step.workspace, out, stream)
         else:
@@ -288,9 +300,8 @@ def run_ours(args, world, rank, local):
     achieved = alg_bytes / (s1_us * 1e-6) / 1e9
     kv_gbs = li.kv_bytes() / (us_per_step * 1e-6) / 1e9
     src_hash = kernel_source_hash()
-    traffic = NCU_TRAFFIC.get(src_hash, {}).get(f"w{args.workload}{args.part or ''}")
-    if args.workload == 2 and traffic is None:
-        traffic = NCU_TRAFFIC.get(src_hash, {}).get("w2")
+    traffic = NCU_TRAFFIC.get(src_hash, {}).get(f"w{args.workload}{args.part or ''}{'-fp8' if fp8 else ''}")
+
 
     # end to end: every step copies its inputs (q, block table, seq_lens) from
     # pinned host memory, decodes, and copies out back to pinned host memory.
@@ -319,7 +330,7 @@ def run_ours(args, world, rank, local):
         def e2e_step(i):
             k, v = pools[i % replicas]
             stage_d.copy_(stage_h, non_blocking=True)
-            step(q_d, k, v, bt_d, sl_d, li.scale, out_d, stream)
+            step(q_d, k, v, bt_d, sl_d, li.scale, out_d, stream, k_scale=k_sc, v_scale=v_sc)
             out_h.copy_(out_d, non_blocking=True)
 
         with torch.cuda.stream(stream):
@@ -363,7 +374,7 @@ def run_ours(args, world, rank, local):
         step.check(stream)
 
     cpu_baseline = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not fp8:
         cpu_baseline = oracle_baseline(li.to("cpu"), budget_s=args.cpu_seconds)
 
     if rank == 0:
@@ -371,7 +382,7 @@ def run_ours(args, world, rank, local):
             "metric": METRIC, "value": round(us_per_step, 3), "unit": UNIT, "n_gpus": world, "steps": K,
             "warmup": max(3, args.warmup), "ms_per_step": round(us_per_step / 1e3, 6),
             "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
-            "dtype": "f32", "io_dtype": "bf16", "data": "synthetic",
+            "dtype": "f32", "io_dtype": "bf16" if not fp8 else "bf16 q/out, e4m3 KV", "data": "synthetic",
             "config": config_of(li, args.workload, args.part, replicas, plan),
             "kv_gbs": round(kv_gbs, 1), "kv_hbm_frac": round(kv_gbs / peak, 4),
             "roofline": {"bound": "hbm", "kernel": "stage1", "achieved": round(achieved, 1), "peak": peak,
@@ -475,6 +486,8 @@ def main():
     ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--part", default=None, help="workload 4: a|b|c; workload 5: global|sliding")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--kv", default="bf16", choices=["bf16", "fp8"],
+                    help="KV-cache element type (fp8: e4m3 with per-(page, KV head) scales)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)

@@ -33,6 +33,7 @@
  * Data layout (all device pointers, row-major, contiguous, 16-byte aligned):
  *   q            bf16  [batch, num_q_heads, head_dim]
  *   k_pool       bf16  [num_pages, num_kv_heads, page_size, head_dim]
+ *                      (FP8 layers: e4m3 bytes, plus fp32 scales [num_pages, num_kv_heads])
  *   v_pool       bf16  same shape as k_pool; NULL or == k_pool iff kv_shared
  *   block_tables int32 [batch, max_pages_per_seq]; entry i of request b is the
  *                      pool page holding its tokens [i*page_size, (i+1)*page_size)
@@ -84,6 +85,10 @@ typedef enum {
 #define PD_DEVFLAG_BAD_SEQLEN 0x2u   /* a device seq_len outside the block table */
 #define PD_DEVFLAG_WAIT_TIMEOUT 0x4u /* a pipeline wait gave up after ~1 s */
 
+/* Element type of the KV cache (pd_layer_desc.kv_dtype). */
+#define PD_KV_BF16 0      /* bf16 K/V rows */
+#define PD_KV_FP8_E4M3 1  /* OCP e4m3 bytes; the value is byte * scale[page, KV head] */
+
 /* One attention layer's shape. */
 typedef struct {
   int32_t num_q_heads;        /* Hq, a multiple of num_kv_heads */
@@ -94,6 +99,7 @@ typedef struct {
   int32_t max_pages_per_seq;  /* block-table row length */
   int32_t window;             /* 0 = global layer; > 0 = sliding window of this many tokens */
   int32_t kv_shared;          /* 1 = one pool is both K and V (K=V storage) */
+  int32_t kv_dtype;           /* PD_KV_BF16 or PD_KV_FP8_E4M3 */
 } pd_layer_desc;
 
 /* Launch plan: a plain value filled by paged_decode_plan, copyable, reusable for
@@ -173,6 +179,28 @@ pd_status paged_decode_window(const pd_plan* plan, const void* q, const void* k_
                               const void* v_pool, const int32_t* block_tables,
                               const int32_t* seq_lens, int32_t window, float scale,
                               void* workspace, size_t workspace_bytes, void* out, void* stream);
+
+/*
+ * Stage 1 over an FP8 KV cache (plan->layer.kv_dtype == PD_KV_FP8_E4M3): as
+ * paged_decode_global / paged_decode_window, with k_pool / v_pool holding OCP
+ * e4m3 bytes [num_pages, Hkv, P, head_dim] and k_scale / v_scale fp32
+ * [num_pages, Hkv]: the cached value of an element is its e4m3 value times the
+ * scale of its (page, KV head). For a K=V layer v_pool and v_scale are NULL or
+ * equal to k_pool and k_scale. q stays bf16 (it is rounded once to f16 for the
+ * tensor cores; |q| must stay below 65504). window = 0 on a global layer.
+ * FP8 KV caches halve the bytes of this bandwidth-bound pass; the vLLM
+ * concepts page records FP8 KV-cache support in Blackwell attention backends
+ * (sections "JIT 预热基础设施" and "MLA 与 Sparse MLA（DSA）"). Errors as for the
+ * bf16 calls; a bf16 plan is rejected with PD_ERR_INVALID_ARG.
+ */
+pd_status paged_decode_global_fp8(const pd_plan* plan, const void* q, const void* k_pool, const void* v_pool,
+                                  const float* k_scale, const float* v_scale, const int32_t* block_tables,
+                                  const int32_t* seq_lens, float scale, void* workspace, size_t workspace_bytes,
+                                  void* out, void* stream);
+pd_status paged_decode_window_fp8(const pd_plan* plan, const void* q, const void* k_pool, const void* v_pool,
+                                  const float* k_scale, const float* v_scale, const int32_t* block_tables,
+                                  const int32_t* seq_lens, int32_t window, float scale, void* workspace,
+                                  size_t workspace_bytes, void* out, void* stream);
 
 /*
  * Stage 2 ([vLLM-MLA]: the pieces' partial results are merged): for each

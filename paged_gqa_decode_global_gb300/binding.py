@@ -23,6 +23,9 @@ PD_ERR_WORKSPACE_TOO_SMALL = 3
 PD_ERR_CUDA = 4
 PD_ERR_DEVICE_FAULT = 5
 
+PD_KV_BF16 = 0
+PD_KV_FP8_E4M3 = 1
+
 PD_DEVFLAG_BAD_PAGE = 0x1
 PD_DEVFLAG_BAD_SEQLEN = 0x2
 PD_DEVFLAG_WAIT_TIMEOUT = 0x4
@@ -36,6 +39,8 @@ EXPORTED = (
     "paged_decode_status_string",
     "paged_decode_abi_version",
     "paged_decode_noalloc",
+    "paged_decode_global_fp8",
+    "paged_decode_window_fp8",
 )
 
 
@@ -49,6 +54,7 @@ class LayerDesc(ctypes.Structure):
         ("max_pages_per_seq", ctypes.c_int32),
         ("window", ctypes.c_int32),
         ("kv_shared", ctypes.c_int32),
+        ("kv_dtype", ctypes.c_int32),
     ]
 
 
@@ -122,6 +128,12 @@ def load_library(path: Optional[str] = None):
         lib.paged_decode_abi_version.restype = i32
         lib.paged_decode_noalloc.argtypes = [ctypes.POINTER(Plan), vp, vp, vp, vp, vp, i32, f32, vp, vp, vp]
         lib.paged_decode_noalloc.restype = ctypes.c_int
+        lib.paged_decode_global_fp8.argtypes = [ctypes.POINTER(Plan), vp, vp, vp, vp, vp, vp, vp, f32, vp, u64, vp,
+                                                vp]
+        lib.paged_decode_global_fp8.restype = ctypes.c_int
+        lib.paged_decode_window_fp8.argtypes = [ctypes.POINTER(Plan), vp, vp, vp, vp, vp, vp, vp, i32, f32, vp, u64,
+                                                vp, vp]
+        lib.paged_decode_window_fp8.restype = ctypes.c_int
         if path is None:
             _lib = lib
         return lib
@@ -157,9 +169,10 @@ def _check(status: int, where: str):
 
 
 def layer_desc(num_q_heads: int, num_kv_heads: int, head_dim: int, page_size: int, num_pages: int,
-               max_pages_per_seq: int, window: int = 0, kv_shared: bool = False) -> LayerDesc:
+               max_pages_per_seq: int, window: int = 0, kv_shared: bool = False,
+               kv_dtype: int = PD_KV_BF16) -> LayerDesc:
     return LayerDesc(num_q_heads, num_kv_heads, head_dim, page_size, num_pages, max_pages_per_seq,
-                     window, 1 if kv_shared else 0)
+                     window, 1 if kv_shared else 0, int(kv_dtype))
 
 
 def paged_decode_plan(desc: LayerDesc, seq_lens_host: Sequence[int], sm_count: int) -> Plan:
@@ -191,6 +204,26 @@ def paged_decode_window(plan: Plan, q, k_pool, v_pool, block_tables, seq_lens, w
                                  _ptr(seq_lens), int(window), float(scale), _ptr(workspace), int(wb), _ptr(out),
                                  _stream_ptr(stream))
     _check(st, "paged_decode_window")
+
+
+def paged_decode_global_fp8(plan: Plan, q, k_pool, v_pool, k_scale, v_scale, block_tables, seq_lens,
+                            scale: float, workspace, out, stream=None, workspace_bytes: Optional[int] = None) -> None:
+    lib = load_library()
+    wb = workspace.numel() * workspace.element_size() if workspace_bytes is None else workspace_bytes
+    st = lib.paged_decode_global_fp8(ctypes.byref(plan), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(k_scale),
+                                     _ptr(v_scale), _ptr(block_tables), _ptr(seq_lens), float(scale),
+                                     _ptr(workspace), int(wb), _ptr(out), _stream_ptr(stream))
+    _check(st, "paged_decode_global_fp8")
+
+
+def paged_decode_window_fp8(plan: Plan, q, k_pool, v_pool, k_scale, v_scale, block_tables, seq_lens, window: int,
+                            scale: float, workspace, out, stream=None, workspace_bytes: Optional[int] = None) -> None:
+    lib = load_library()
+    wb = workspace.numel() * workspace.element_size() if workspace_bytes is None else workspace_bytes
+    st = lib.paged_decode_window_fp8(ctypes.byref(plan), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(k_scale),
+                                     _ptr(v_scale), _ptr(block_tables), _ptr(seq_lens), int(window), float(scale),
+                                     _ptr(workspace), int(wb), _ptr(out), _stream_ptr(stream))
+    _check(st, "paged_decode_window_fp8")
 
 
 def paged_decode_merge(plan: Plan, workspace, out, stream=None, workspace_bytes: Optional[int] = None) -> None:
@@ -238,13 +271,14 @@ class LayerStep:
     are no longer than the planned ones."""
 
     def __init__(self, num_q_heads, num_kv_heads, head_dim, page_size, num_pages, max_pages_per_seq,
-                 seq_lens_host, *, window=0, kv_shared=False, sm_count=None, device=None):
+                 seq_lens_host, *, window=0, kv_shared=False, kv_dtype=PD_KV_BF16, sm_count=None, device=None):
         import torch
         device = torch.device("cuda") if device is None else torch.device(device)
         if sm_count is None:
             sm_count = torch.cuda.get_device_properties(device).multi_processor_count
         self.desc = layer_desc(num_q_heads, num_kv_heads, head_dim, page_size, num_pages, max_pages_per_seq,
-                               window, kv_shared)
+                               window, kv_shared, kv_dtype)
+        self.fp8 = kv_dtype == PD_KV_FP8_E4M3
         self.plan = paged_decode_plan(self.desc, list(seq_lens_host), sm_count)
         nbytes = int(self.plan.workspace_bytes)
         # zeroed once: the first word is the device error flag
@@ -253,12 +287,22 @@ class LayerStep:
 
     @classmethod
     def for_inputs(cls, li, sm_count=None):
+        """A step for a LayerInputs (bf16 cache) or Fp8LayerInputs (e4m3 cache)."""
+        fp8 = hasattr(li, "k8")
         return cls(li.num_q_heads, li.num_kv_heads, li.head_dim, li.page_size, li.num_pages, li.max_pages,
-                   li.seq_lens_list(), window=li.window, kv_shared=li.kv_shared, sm_count=sm_count,
-                   device=li.q.device)
+                   li.seq_lens_list(), window=li.window, kv_shared=li.kv_shared,
+                   kv_dtype=PD_KV_FP8_E4M3 if fp8 else PD_KV_BF16, sm_count=sm_count, device=li.q.device)
 
-    def __call__(self, q, k_pool, v_pool, block_tables, seq_lens, scale, out, stream=None):
-        if self.window > 0:
+    def __call__(self, q, k_pool, v_pool, block_tables, seq_lens, scale, out, stream=None, k_scale=None,
+                 v_scale=None):
+        if self.fp8:
+            if self.window > 0:
+                paged_decode_window_fp8(self.plan, q, k_pool, v_pool, k_scale, v_scale, block_tables, seq_lens,
+                                        self.window, scale, self.workspace, out, stream)
+            else:
+                paged_decode_global_fp8(self.plan, q, k_pool, v_pool, k_scale, v_scale, block_tables, seq_lens,
+                                        scale, self.workspace, out, stream)
+        elif self.window > 0:
             paged_decode_window(self.plan, q, k_pool, v_pool, block_tables, seq_lens, self.window, scale,
                                 self.workspace, out, stream)
         else:
@@ -271,6 +315,9 @@ class LayerStep:
         import torch
         if out is None:
             out = torch.empty_like(li.q)
+        if self.fp8:
+            return self(li.q, li.k8, li.v8, li.block_tables, li.seq_lens, li.scale, out, stream,
+                        k_scale=li.k_scale, v_scale=li.v_scale)
         return self(li.q, li.k_pool, li.v_pool, li.block_tables, li.seq_lens, li.scale, out, stream)
 
     def check(self, stream=None) -> int:

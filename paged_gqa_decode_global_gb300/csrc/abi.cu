@@ -55,23 +55,26 @@ std::atomic<int> g_tma_rank{0};
 pd_status encode_pool_map(CUtensorMap* map, const void* pool, const pd_layer_desc& ly, int rank) {
   EncodeTiledFn fn = encode_tiled_fn();
   if (!fn) return PD_ERR_CUDA;
+  // 128-byte rows of the swizzle: 64 bf16 or 128 e4m3 elements
+  const bool fp8 = ly.kv_dtype == PD_KV_FP8_E4M3;
+  const cuuint64_t elem = fp8 ? 1 : 2;
+  const cuuint64_t span = 128 / elem;
+  const CUtensorMapDataType type = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const cuuint64_t rows = (cuuint64_t)ly.num_pages * ly.num_kv_heads * ly.page_size;
   const cuuint32_t estr[3] = {1, 1, 1};
   CUresult r;
   if (rank == 3) {
-    const cuuint64_t dims[3] = {64, rows, (cuuint64_t)ly.head_dim / 64};
-    const cuuint64_t strides[2] = {(cuuint64_t)ly.head_dim * 2, 128};
-    const cuuint32_t box[3] = {64, 16, (cuuint32_t)ly.head_dim / 64};
-    r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(pool), dims, strides, box, estr,
-           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    const cuuint64_t dims[3] = {span, rows, (cuuint64_t)ly.head_dim / span};
+    const cuuint64_t strides[2] = {(cuuint64_t)ly.head_dim * elem, 128};
+    const cuuint32_t box[3] = {(cuuint32_t)span, 16, (cuuint32_t)(ly.head_dim / span)};
+    r = fn(map, type, 3, const_cast<void*>(pool), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   } else {
     const cuuint64_t dims[2] = {(cuuint64_t)ly.head_dim, rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)ly.head_dim * 2};
-    const cuuint32_t box[2] = {64, 16};
-    r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(pool), dims, strides, box, estr,
-           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    const cuuint64_t strides[1] = {(cuuint64_t)ly.head_dim * elem};
+    const cuuint32_t box[2] = {(cuuint32_t)span, 16};
+    r = fn(map, type, 2, const_cast<void*>(pool), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   }
   return r == CUDA_SUCCESS ? PD_OK : PD_ERR_CUDA;
 }
@@ -105,11 +108,21 @@ pd_status ensure_smem_attr(int variant, const void* fn, int smem_bytes) {
   return PD_OK;
 }
 
-pd_status stage1(const pd_plan* plan, const void* q, const void* k_pool, const void* v_pool,
-                 const int32_t* block_tables, const int32_t* seq_lens, int32_t window, float scale,
-                 void* workspace, size_t workspace_bytes, void* out, void* stream) {
+pd_status stage1(const pd_plan* plan, const void* q, const void* k_pool, const void* v_pool, const float* k_scale,
+                 const float* v_scale, const int32_t* block_tables, const int32_t* seq_lens, int32_t window,
+                 float scale, void* workspace, size_t workspace_bytes, void* out, void* stream) {
   if (!pd::plan_is_valid(plan)) return PD_ERR_INVALID_ARG;
   const pd_layer_desc& ly = plan->layer;
+  const bool fp8 = ly.kv_dtype == PD_KV_FP8_E4M3;
+  if (fp8) {
+    if (!k_scale || !aligned(k_scale, 4)) return PD_ERR_INVALID_ARG;
+    if (ly.kv_shared) {
+      if (v_scale && v_scale != k_scale) return PD_ERR_INVALID_ARG;
+      v_scale = k_scale;
+    } else if (!v_scale || !aligned(v_scale, 4)) {
+      return PD_ERR_INVALID_ARG;
+    }
+  }
   if (window != ly.window) return PD_ERR_INVALID_ARG;
   if (!std::isfinite(scale)) return PD_ERR_INVALID_ARG;
   if (!workspace || !aligned(workspace, 256)) return PD_ERR_INVALID_ARG;
@@ -139,6 +152,8 @@ pd_status stage1(const pd_plan* plan, const void* q, const void* k_pool, const v
   p.q = static_cast<const uint16_t*>(q);
   p.k_pool = static_cast<const uint16_t*>(k_pool);
   p.v_pool = static_cast<const uint16_t*>(v_pool);
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
   p.block_tables = block_tables;
   p.seq_lens = seq_lens;
   p.out = out;
@@ -188,17 +203,37 @@ extern "C" {
 pd_status paged_decode_global(const pd_plan* plan, const void* q, const void* k_pool, const void* v_pool,
                               const int32_t* block_tables, const int32_t* seq_lens, float scale,
                               void* workspace, size_t workspace_bytes, void* out, void* stream) {
-  if (!plan || plan->layer.window != 0) return PD_ERR_INVALID_ARG;
-  return stage1(plan, q, k_pool, v_pool, block_tables, seq_lens, 0, scale, workspace, workspace_bytes, out,
-                stream);
+  if (!plan || plan->layer.window != 0 || plan->layer.kv_dtype != PD_KV_BF16) return PD_ERR_INVALID_ARG;
+  return stage1(plan, q, k_pool, v_pool, nullptr, nullptr, block_tables, seq_lens, 0, scale, workspace,
+                workspace_bytes, out, stream);
 }
 
 pd_status paged_decode_window(const pd_plan* plan, const void* q, const void* k_pool, const void* v_pool,
                               const int32_t* block_tables, const int32_t* seq_lens, int32_t window,
                               float scale, void* workspace, size_t workspace_bytes, void* out, void* stream) {
-  if (!plan || window <= 0 || plan->layer.window != window) return PD_ERR_INVALID_ARG;
-  return stage1(plan, q, k_pool, v_pool, block_tables, seq_lens, window, scale, workspace, workspace_bytes,
-                out, stream);
+  if (!plan || window <= 0 || plan->layer.window != window || plan->layer.kv_dtype != PD_KV_BF16)
+    return PD_ERR_INVALID_ARG;
+  return stage1(plan, q, k_pool, v_pool, nullptr, nullptr, block_tables, seq_lens, window, scale, workspace,
+                workspace_bytes, out, stream);
+}
+
+pd_status paged_decode_global_fp8(const pd_plan* plan, const void* q, const void* k_pool, const void* v_pool,
+                                  const float* k_scale, const float* v_scale, const int32_t* block_tables,
+                                  const int32_t* seq_lens, float scale, void* workspace, size_t workspace_bytes,
+                                  void* out, void* stream) {
+  if (!plan || plan->layer.window != 0 || plan->layer.kv_dtype != PD_KV_FP8_E4M3) return PD_ERR_INVALID_ARG;
+  return stage1(plan, q, k_pool, v_pool, k_scale, v_scale, block_tables, seq_lens, 0, scale, workspace,
+                workspace_bytes, out, stream);
+}
+
+pd_status paged_decode_window_fp8(const pd_plan* plan, const void* q, const void* k_pool, const void* v_pool,
+                                  const float* k_scale, const float* v_scale, const int32_t* block_tables,
+                                  const int32_t* seq_lens, int32_t window, float scale, void* workspace,
+                                  size_t workspace_bytes, void* out, void* stream) {
+  if (!plan || window <= 0 || plan->layer.window != window || plan->layer.kv_dtype != PD_KV_FP8_E4M3)
+    return PD_ERR_INVALID_ARG;
+  return stage1(plan, q, k_pool, v_pool, k_scale, v_scale, block_tables, seq_lens, window, scale, workspace,
+                workspace_bytes, out, stream);
 }
 
 pd_status paged_decode_merge(const pd_plan* plan, const void* workspace, size_t workspace_bytes, void* out,

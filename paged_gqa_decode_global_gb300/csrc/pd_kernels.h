@@ -17,8 +17,10 @@ struct Stage1Params {
   CUtensorMap vmap;
   int32_t tma_rank;
   const uint16_t* q;            // bf16 [B, Hq, D]
-  const uint16_t* k_pool;       // bf16 [num_pages, Hkv, P, D]
+  const uint16_t* k_pool;       // bf16 [num_pages, Hkv, P, D] (FP8: e4m3 bytes, read only by TMA)
   const uint16_t* v_pool;       // bf16, == k_pool for a K=V layer
+  const float* k_scale;         // FP8: [num_pages, Hkv] scale of each (page, KV head) of K
+  const float* v_scale;         // FP8: same for V (== k_scale for a K=V layer)
   const int32_t* block_tables;  // [B, max_pages]
   const int32_t* seq_lens;      // [B]
   void* out;                    // bf16 [B, Hq, D] (written when num_splits == 1)

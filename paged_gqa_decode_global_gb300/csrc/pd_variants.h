@@ -17,76 +17,112 @@ constexpr uint64_t kWorkspaceHeader = 256;
 // Geometry of one stage-1 instance.
 //   D   head_dim          G    query heads per KV head (GQA group, <= 8: the
 //                              8-wide N side of the m16n8k16 MMAs)
-//   KVS K=V shared pool   NW   consumer warps (+1 producer warp)
+//   KVS K=V shared pool   KV8  the KV cache holds e4m3 bytes (+ per-(page, KV
+//                              head) scales) instead of bf16
+//   NW  consumer warps (+1 producer warp)
 //   SPW ring stages owned by each consumer warp
-template <int D_, int G_, bool KVS_, int NW_, int SPW_>
+template <int D_, int G_, bool KVS_, bool KV8_, int NW_, int SPW_>
 struct Stage1Cfg {
   static constexpr int D = D_;
   static constexpr int G = G_;
   static constexpr bool KVS = KVS_;
+  static constexpr bool KV8 = KV8_;
   static constexpr int NW = NW_;
   static constexpr int SPW = SPW_;
   static constexpr int TB = 16;                  // tokens per stage = the MMA's 16-row side
   static constexpr int KSTEPS = D / 16;          // QK k-steps
   static constexpr int MTILES = D / 16;          // PV m-tiles (head dims)
   static constexpr int NST = NW * SPW;
-  static constexpr int SLABS = D / 64;           // 128-byte swizzle spans per token row
-  static constexpr int SLAB_BYTES = TB * 128;    // one slab of a 16-token block
-  static constexpr int KV_BYTES = SLABS * SLAB_BYTES;           // = 16 rows of K (or V)
+  static constexpr int SLAB_BYTES = TB * 128;    // one 128-byte-wide slab of a 16-token block
+  // 16-bit tiles the MMAs read (bf16 stages, or the f16 tiles FP8 stages are
+  // converted into): [D/64 slabs][16 rows][128 B]
+  static constexpr int SLABS = D / 64;
+  static constexpr int TILE16_BYTES = SLABS * SLAB_BYTES;
+  // what TMA lands per K (or V) block: bf16 rows, or e4m3 rows ([D/128 slabs][16][128 B])
+  static constexpr int ELEM = KV8 ? 1 : 2;
+  static constexpr int TMA_SLABS = D * ELEM / 128;
+  static constexpr int KV_BYTES = TMA_SLABS * SLAB_BYTES;
   static constexpr int STAGE_BYTES = KV_BYTES * (KVS ? 1 : 2);
   static constexpr int TX_BYTES = STAGE_BYTES;                  // bytes the copies deliver
   static constexpr int RING_BYTES = NST * STAGE_BYTES;
+  // FP8: each consumer warp's f16 tile, after the ring (K, then V once QK is done)
+  static constexpr int SCRATCH_BYTES = KV8 ? TILE16_BYTES : 0;
+  static constexpr int SCRATCH_OFFSET = RING_BYTES;
+  static constexpr int WORK_BYTES = RING_BYTES + NW * SCRATCH_BYTES;
   static constexpr int COMB_STRIDE = D + 4;                    // floats per head row of the warp merge
   static constexpr int COMBINE_BYTES = NW * G * COMB_STRIDE * 4; // per-warp outputs (aliases the ring)
-  static constexpr int BODY_BYTES = RING_BYTES > COMBINE_BYTES ? RING_BYTES : COMBINE_BYTES;
+  static constexpr int BODY_BYTES = WORK_BYTES > COMBINE_BYTES ? WORK_BYTES : COMBINE_BYTES;
   // cluster merge (after the ring is drained): this CTA's result and lse, and
-  // rank 0's merge weights
-  static constexpr int MAX_CLUSTER = 8;
+  // rank 0's merge weights; rank 0 then receives the results of ranks
+  // 1..S-1, float [S-1][G][D] + lse [S-1][G], in what is left of the body
   static constexpr int CTA_OUT_OFFSET = (COMBINE_BYTES + 15) / 16 * 16;  // float [G][D]
   static constexpr int CTA_LSE_OFFSET = CTA_OUT_OFFSET + G * D * 4;      // float [G]
-  static constexpr int CTA_W_OFFSET = CTA_LSE_OFFSET + G * 4;            // float [MAX_CLUSTER][G]
-  // rank 0 only: results pushed by ranks 1..S-1, float [MAX_CLUSTER-1][G][D] + lse [MAX_CLUSTER-1][G]
-  static constexpr int PUSH_OFFSET = (CTA_W_OFFSET + MAX_CLUSTER * G * 4 + 15) / 16 * 16;
+  static constexpr int CTA_W_OFFSET = CTA_LSE_OFFSET + G * 4;            // float [8][G]
+  static constexpr int PUSH_OFFSET = (CTA_W_OFFSET + 8 * G * 4 + 15) / 16 * 16;
+  static constexpr int PUSH_ROOM = BODY_BYTES - PUSH_OFFSET;
+  static constexpr int MAX_CLUSTER_FIT = 1 + (PUSH_ROOM > 0 ? PUSH_ROOM / ((G * D + G) * 4) : 0);
+  static constexpr int MAX_CLUSTER = MAX_CLUSTER_FIT < 8 ? MAX_CLUSTER_FIT : 8;  // pieces one cluster merges
   static constexpr int PUSH_LSE_OFFSET = PUSH_OFFSET + (MAX_CLUSTER - 1) * G * D * 4;
-  static_assert(PUSH_LSE_OFFSET + (MAX_CLUSTER - 1) * G * 4 <= BODY_BYTES, "cluster merge buffers fit in the ring");
+  static_assert(PUSH_LSE_OFFSET + (MAX_CLUSTER - 1) * G * 4 <= BODY_BYTES, "cluster merge buffers fit in the body");
   static constexpr int BAR_OFFSET = BODY_BYTES;                // full[NST], empty[NST]
   static constexpr int VALID_OFFSET = BAR_OFFSET + NST * 16;   // u32 valid[NST]
-  static constexpr int ML_OFFSET = VALID_OFFSET + NST * 4;     // float2 ml[NW][G]
+  static constexpr int SCALE_OFFSET = (VALID_OFFSET + NST * 4 + 7) / 8 * 8;  // float2 (k, v) scale[NST] (FP8)
+  static constexpr int ML_OFFSET = SCALE_OFFSET + NST * 8;     // float2 ml[NW][G]
   static constexpr int COEF_OFFSET = ML_OFFSET + NW * G * 8;   // float coef[NW][G], lse[G]
   // + 1 KiB so the ring can start on a 1024-byte boundary (the swizzle period)
   static constexpr int SMEM_BYTES = COEF_OFFSET + (NW * G + G) * 4 + 1024;
   static constexpr int THREADS = 32 * (NW + 1);
-  static_assert(D % 64 == 0, "head_dim must be a multiple of 64 (one swizzle span)");
+  static_assert(D % 128 == 0, "head_dim must be a multiple of 128");
   static_assert(G >= 1 && G <= 8, "the GQA group is the MMA's 8-wide side");
   static_assert(16 % TB == 0, "a block must lie inside one 16-token page slice");
-  static_assert(STAGE_BYTES % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
+  static_assert(STAGE_BYTES % 1024 == 0 && TILE16_BYTES % 1024 == 0, "tiles keep the 1024-byte swizzle alignment");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+  static_assert(SCALE_OFFSET % 8 == 0 && ML_OFFSET % 8 == 0, "float2 arrays need 8-byte alignment");
 };
 
-// The instances this library is built with, by variant id. Three consumer
-// warps (the tensor cores leave the CUDA cores mostly idle) plus the producer;
-// the ring holds 192 KiB: 32 KiB stages x 6 (d512, K!=V), 16 KiB x 12
-// (d512 K=V, d256 K!=V), 8 KiB x 24 (d256 K=V).
-#define PD_FOR_EACH_VARIANT(X) \
-  X(0, 512, 1, false, 3, 2)    \
-  X(1, 512, 2, false, 3, 2)    \
-  X(2, 512, 4, false, 3, 2)    \
-  X(3, 512, 8, false, 3, 2)    \
-  X(4, 512, 1, true, 3, 4)     \
-  X(5, 512, 2, true, 3, 4)     \
-  X(6, 512, 4, true, 3, 4)     \
-  X(7, 512, 8, true, 3, 4)     \
-  X(8, 256, 1, false, 3, 4)    \
-  X(9, 256, 2, false, 3, 4)    \
-  X(10, 256, 4, false, 3, 4)   \
-  X(11, 256, 8, false, 3, 4)   \
-  X(12, 256, 1, true, 3, 8)    \
-  X(13, 256, 2, true, 3, 8)    \
-  X(14, 256, 4, true, 3, 8)    \
-  X(15, 256, 8, true, 3, 8)
+// The instances this library is built with, by variant id:
+// X(id, head_dim, group, K=V, FP8, consumer warps, stages per warp).
+// bf16: three consumer warps (the tensor cores leave the CUDA cores mostly
+// idle) plus the producer; rings of 192 KiB: 32 KiB stages x 6 (d512 K!=V),
+// 16 KiB x 12 (d512 K=V, d256 K!=V), 8 KiB x 24 (d256 K=V). FP8: seven
+// consumer warps (two per SM sub-partition hide the latency of widening e4m3
+// tiles to f16) with one 16-bit tile each beside rings of 56-112 KiB.
+#define PD_FOR_EACH_VARIANT(X)        \
+  X(0, 512, 1, false, false, 3, 2)    \
+  X(1, 512, 2, false, false, 3, 2)    \
+  X(2, 512, 4, false, false, 3, 2)    \
+  X(3, 512, 8, false, false, 3, 2)    \
+  X(4, 512, 1, true, false, 3, 4)     \
+  X(5, 512, 2, true, false, 3, 4)     \
+  X(6, 512, 4, true, false, 3, 4)     \
+  X(7, 512, 8, true, false, 3, 4)     \
+  X(8, 256, 1, false, false, 3, 4)    \
+  X(9, 256, 2, false, false, 3, 4)    \
+  X(10, 256, 4, false, false, 3, 4)   \
+  X(11, 256, 8, false, false, 3, 4)   \
+  X(12, 256, 1, true, false, 3, 8)    \
+  X(13, 256, 2, true, false, 3, 8)    \
+  X(14, 256, 4, true, false, 3, 8)    \
+  X(15, 256, 8, true, false, 3, 8)    \
+  X(16, 512, 1, false, true, 7, 1)  \
+  X(17, 512, 2, false, true, 7, 1)  \
+  X(18, 512, 4, false, true, 7, 1)  \
+  X(19, 512, 8, false, true, 7, 1)  \
+  X(20, 512, 1, true, true, 7, 2)   \
+  X(21, 512, 2, true, true, 7, 2)   \
+  X(22, 512, 4, true, true, 7, 2)   \
+  X(23, 512, 8, true, true, 7, 2)   \
+  X(24, 256, 1, false, true, 7, 2)  \
+  X(25, 256, 2, false, true, 7, 2)  \
+  X(26, 256, 4, false, true, 7, 2)  \
+  X(27, 256, 8, false, true, 7, 2)  \
+  X(28, 256, 1, true, true, 7, 4)   \
+  X(29, 256, 2, true, true, 7, 4)   \
+  X(30, 256, 4, true, true, 7, 4)   \
+  X(31, 256, 8, true, true, 7, 4)
 
 struct VariantInfo {
-  int id, head_dim, group, kv_shared, nw, spw, block_tokens, threads, smem_bytes;
+  int id, head_dim, group, kv_shared, kv_fp8, nw, spw, block_tokens, threads, smem_bytes, max_cluster;
 };
 
 // Host-visible table, defined in plan.cu.

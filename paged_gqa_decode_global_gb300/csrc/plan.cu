@@ -18,9 +18,10 @@
 
 namespace pd {
 
-#define PD_VARIANT_ROW(ID, D, G, KVS, NW, SPW)                                                       \
-  VariantInfo{ID, D, G, KVS ? 1 : 0, NW, SPW, Stage1Cfg<D, G, KVS, NW, SPW>::TB,                     \
-              Stage1Cfg<D, G, KVS, NW, SPW>::THREADS, Stage1Cfg<D, G, KVS, NW, SPW>::SMEM_BYTES},
+#define PD_VARIANT_ROW(ID, D, G, KVS, KV8, NW, SPW)                                                  \
+  VariantInfo{ID, D, G, KVS ? 1 : 0, KV8 ? 1 : 0, NW, SPW, Stage1Cfg<D, G, KVS, KV8, NW, SPW>::TB,      \
+              Stage1Cfg<D, G, KVS, KV8, NW, SPW>::THREADS, Stage1Cfg<D, G, KVS, KV8, NW, SPW>::SMEM_BYTES, \
+              Stage1Cfg<D, G, KVS, KV8, NW, SPW>::MAX_CLUSTER},
 const VariantInfo kVariants[] = {PD_FOR_EACH_VARIANT(PD_VARIANT_ROW)};
 #undef PD_VARIANT_ROW
 const int kNumVariants = sizeof(kVariants) / sizeof(kVariants[0]);
@@ -30,15 +31,15 @@ const int kNumVariants = sizeof(kVariants) / sizeof(kVariants[0]);
 namespace {
 
 constexpr uint32_t kPlanMagic = 0x50444543u;  // "PDEC"
-constexpr int32_t kAbiVersion = 2;
+constexpr int32_t kAbiVersion = 3;
 // Pieces per (request, KV head) are capped (the merge stages their weights in
 // shared memory).
 constexpr int kMaxSplits = 1024;
 
-const pd::VariantInfo* find_variant(int head_dim, int group, int kv_shared) {
+const pd::VariantInfo* find_variant(int head_dim, int group, int kv_shared, int kv_fp8) {
   for (int i = 0; i < pd::kNumVariants; ++i) {
     const pd::VariantInfo& v = pd::kVariants[i];
-    if (v.head_dim == head_dim && v.group == group && v.kv_shared == kv_shared) return &v;
+    if (v.head_dim == head_dim && v.group == group && v.kv_shared == kv_shared && v.kv_fp8 == kv_fp8) return &v;
   }
   return nullptr;
 }
@@ -150,6 +151,7 @@ pd_status paged_decode_plan(const pd_layer_desc* layer, int32_t batch, const int
   if (ly.head_dim <= 0 || ly.page_size <= 0 || ly.page_size % 16 != 0) return PD_ERR_INVALID_ARG;
   if (ly.num_pages <= 0 || ly.max_pages_per_seq <= 0 || ly.window < 0) return PD_ERR_INVALID_ARG;
   if (ly.kv_shared != 0 && ly.kv_shared != 1) return PD_ERR_INVALID_ARG;
+  if (ly.kv_dtype != PD_KV_BF16 && ly.kv_dtype != PD_KV_FP8_E4M3) return PD_ERR_INVALID_ARG;
   if (batch < 0 || batch > 65535 || ly.num_kv_heads > 65535 || sm_count <= 0) return PD_ERR_INVALID_ARG;
   if (batch > 0 && !seq_lens_host) return PD_ERR_INVALID_ARG;
   const long long cap = (long long)ly.max_pages_per_seq * ly.page_size;
@@ -162,7 +164,7 @@ pd_status paged_decode_plan(const pd_layer_desc* layer, int32_t batch, const int
     max_len = std::max(max_len, seq_lens_host[b]);
   }
   const int group = ly.num_q_heads / ly.num_kv_heads;
-  const pd::VariantInfo* v = find_variant(ly.head_dim, group, ly.kv_shared);
+  const pd::VariantInfo* v = find_variant(ly.head_dim, group, ly.kv_shared, ly.kv_dtype == PD_KV_FP8_E4M3);
   if (!v) return PD_ERR_UNSUPPORTED;
   const int TB = v->block_tokens;
 
@@ -179,7 +181,8 @@ pd_status paged_decode_plan(const pd_layer_desc* layer, int32_t batch, const int
   }
 
   CostModel cm;
-  const double kv_bytes_per_token = (double)ly.head_dim * 2.0 * (ly.kv_shared ? 1.0 : 2.0);
+  const double kv_bytes_per_token =
+      (double)ly.head_dim * (ly.kv_dtype == PD_KV_FP8_E4M3 ? 1.0 : 2.0) * (ly.kv_shared ? 1.0 : 2.0);
   const double sm_bw_bytes_per_us = 7.0e12 / 1e6 / sm_count;  // ~7 TB/s shared by the SMs
   cm.us_per_token = kv_bytes_per_token / sm_bw_bytes_per_us;
   cm.cta_fixed_us = 2.0;
@@ -218,7 +221,7 @@ pd_status paged_decode_plan(const pd_layer_desc* layer, int32_t batch, const int
       const uint64_t merge_bytes = (uint64_t)batch * ly.num_q_heads * s * (ly.head_dim + 1) * 4ull * 2ull;
       double cost = simulate(n_tok, ly.num_kv_heads, c, s, cm, merge_bytes);
       bool cluster = false;
-      if (s >= 2 && s <= kMaxClusterSplits) {
+      if (s >= 2 && s <= std::min(kMaxClusterSplits, v->max_cluster)) {
         const double cc = simulate_clusters(n_tok, ly.num_kv_heads, c, s, cm, kAssumedGpcs);
         if (cc < cost) {
           cost = cc;
@@ -282,6 +285,7 @@ bool plan_is_valid(const pd_plan* plan) {
   const pd_layer_desc& ly = plan->layer;
   if (ly.num_kv_heads <= 0 || ly.num_q_heads != ly.num_kv_heads * v.group) return false;
   if (ly.head_dim != v.head_dim || ly.kv_shared != v.kv_shared) return false;
+  if ((ly.kv_dtype == PD_KV_FP8_E4M3) != (v.kv_fp8 == 1)) return false;
   if (plan->num_splits < 1 || plan->chunk_tokens < 16 || plan->chunk_tokens % 16 != 0) return false;
   if (plan->batch < 0 || plan->grid_x != plan->num_splits) return false;
   if (plan->threads_per_cta != v.threads || plan->smem_bytes != v.smem_bytes) return false;
@@ -289,7 +293,7 @@ bool plan_is_valid(const pd_plan* plan) {
   if (plan->test_stall_bytes < 0 || plan->test_stall_bytes > (1 << 16) || plan->test_stall_bytes % 16 != 0)
     return false;
   if ((plan->num_splits == 1) != (plan->merge_mode == 0)) return false;
-  if (plan->merge_mode == 2 && plan->num_splits > kMaxClusterSplits) return false;
+  if (plan->merge_mode == 2 && plan->num_splits > std::min(kMaxClusterSplits, v.max_cluster)) return false;
   return true;
 }
 

@@ -32,6 +32,8 @@
 //     distributed shared memory (up to 8 pieces), or writes an fp32 partial +
 //     log-sum-exp for the merge kernel (more pieces).
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include "pd_common.cuh"
 #include "pd_kernels.h"
@@ -61,6 +63,62 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], 
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// D = A . B + D, m16n8k16, f16 x f16 -> fp32 (the FP8 path: e4m3 widens to f16 exactly).
+__device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+template <bool F16>
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  if constexpr (F16)
+    mma_f16(d, a, b0, b1);
+  else
+    mma_bf16(d, a, b0, b1);
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Four e4m3 bytes (little-endian in w) -> four f16 (exact), as two f16x2
+// words: the hardware conversion takes a 16-bit pair, lower byte to lower half.
+__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
+}
+
+// Widen one 16-token e4m3 tile ([D/128 slabs][16 rows][128 B], 128-byte
+// swizzle) into the f16 tile the MMAs read ([D/64 slabs][16 rows][128 B],
+// 128-byte swizzle). Lane-parallel: one 16-byte e4m3 chunk (16 dims) per step.
+// Plain shared-memory accesses, so the loads of later chunks overlap earlier
+// conversions; the caller orders them against the ring and the MMAs.
+template <int D>
+__device__ __forceinline__ void widen_e4m3_tile(const uint8_t* src, uint8_t* dst, int lane) {
+  constexpr int CHUNKS = D / 16;  // per row
+#pragma unroll 8
+  for (int idx = lane; idx < 16 * CHUNKS; idx += 32) {
+    const int r = idx / CHUNKS, cj = idx % CHUNKS;
+    const int sw = r & 7;
+    const uint4 raw = *reinterpret_cast<const uint4*>(src + (cj >> 3) * 2048 + r * 128 + (((cj & 7) ^ sw) << 4));
+    uint4 o0, o1;
+    e4m3x4_to_f16x4(raw.x, o0.x, o0.y);
+    e4m3x4_to_f16x4(raw.y, o0.z, o0.w);
+    e4m3x4_to_f16x4(raw.z, o1.x, o1.y);
+    e4m3x4_to_f16x4(raw.w, o1.z, o1.w);
+    uint8_t* row = dst + (cj >> 2) * 2048 + r * 128;
+    const int c0 = (cj & 3) * 2;
+    *reinterpret_cast<uint4*>(row + ((c0 ^ sw) << 4)) = o0;
+    *reinterpret_cast<uint4*>(row + (((c0 + 1) ^ sw) << 4)) = o1;
+  }
+}
+
 // Transpose an 8x8 bf16 matrix held one row pair per lane (fragment layout).
 __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
   uint32_t y;
@@ -84,6 +142,7 @@ __device__ __forceinline__ void stage1_cta(const Stage1Params& p, uint8_t* smem)
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + C::BAR_OFFSET);
   uint64_t* empty_bar = full_bar + C::NST;
   uint32_t* stage_valid = reinterpret_cast<uint32_t*>(smem + C::VALID_OFFSET);
+  float2* stage_scale = reinterpret_cast<float2*>(smem + C::SCALE_OFFSET);  // FP8: (K, V) scale per stage
   float2* warp_ml = reinterpret_cast<float2*>(smem + C::ML_OFFSET);
 
   const int split = blockIdx.x;
@@ -154,6 +213,14 @@ __device__ __forceinline__ void stage1_cta(const Stage1Params& p, uint8_t* smem)
         const uint16_t* qrow = p.q + (row_hq + qh) * C::D + ks * 16 + qk;
         qb[ks][0] = __ldg(reinterpret_cast<const unsigned int*>(qrow));
         qb[ks][1] = __ldg(reinterpret_cast<const unsigned int*>(qrow + 8));
+        if constexpr (C::KV8) {
+          // the FP8 path multiplies in f16: q rounds to f16 once here
+#pragma unroll
+          for (int w = 0; w < 2; ++w) {
+            const uint32_t x = qb[ks][w];
+            qb[ks][w] = pack_f16x2(__uint_as_float(x << 16), __uint_as_float(x & 0xffff0000u));
+          }
+        }
       } else {
         qb[ks][0] = 0u;
         qb[ks][1] = 0u;
@@ -188,6 +255,15 @@ __device__ __forceinline__ void stage1_cta(const Stage1Params& p, uint8_t* smem)
 #pragma unroll 1
     for (int j0 = 0; j0 < nblk && !stop; j0 += 32) {
       const int page_mine = page_next;
+      // FP8: each lane also fetches its block's (K, V) scales
+      float2 scale_mine = make_float2(1.f, 1.f);
+      if constexpr (C::KV8) {
+        if ((unsigned)page_mine < (unsigned)p.num_pages) {
+          const size_t si = (size_t)page_mine * p.num_kv_heads + g;
+          scale_mine.x = __ldg(p.k_scale + si);
+          scale_mine.y = C::KVS ? scale_mine.x : __ldg(p.v_scale + si);
+        }
+      }
       const int jn = j0 + 32 + lane;
       page_next = (jn < nblk) ? __ldg(table + (blk_lo + jn * C::TB) / p.page_size) : -1;
       const int cnt = min(32, nblk - j0);
@@ -195,6 +271,9 @@ __device__ __forceinline__ void stage1_cta(const Stage1Params& p, uint8_t* smem)
       for (int k = 0; k < cnt; ++k) {
         const int j = j0 + k;
         const int page = __shfl_sync(kFullMask, page_mine, k);
+        float2 scale_blk;
+        scale_blk.x = __shfl_sync(kFullMask, scale_mine.x, k);
+        scale_blk.y = __shfl_sync(kFullMask, scale_mine.y, k);
         int go = 1;
         if (lane == 0) {
           const int st = j % C::NST;
@@ -206,6 +285,7 @@ __device__ __forceinline__ void stage1_cta(const Stage1Params& p, uint8_t* smem)
             const int t0 = blk_lo + j * C::TB;
             const bool ok = (unsigned)page < (unsigned)p.num_pages;
             stage_valid[st] = ok ? 1u : 0u;
+            if constexpr (C::KV8) stage_scale[st] = scale_blk;
             if (ok) {
               const int row0 = (page * p.num_kv_heads + g) * p.page_size + (t0 % p.page_size);
               uint8_t* dst = smem + (size_t)st * C::STAGE_BYTES;
@@ -214,12 +294,13 @@ __device__ __forceinline__ void stage1_cta(const Stage1Params& p, uint8_t* smem)
                 tma_load_3d(dst, &p.kmap, 0, row0, 0, &full_bar[st], policy);
                 if (!C::KVS) tma_load_3d(dst + C::KV_BYTES, &p.vmap, 0, row0, 0, &full_bar[st], policy);
               } else {
+                constexpr int SLAB_ELEMS = 128 / C::ELEM;
 #pragma unroll
-                for (int sl = 0; sl < C::SLABS; ++sl) {
-                  tma_load_2d(dst + sl * C::SLAB_BYTES, &p.kmap, sl * 64, row0, &full_bar[st], policy);
+                for (int sl = 0; sl < C::TMA_SLABS; ++sl) {
+                  tma_load_2d(dst + sl * C::SLAB_BYTES, &p.kmap, sl * SLAB_ELEMS, row0, &full_bar[st], policy);
                   if (!C::KVS)
-                    tma_load_2d(dst + C::KV_BYTES + sl * C::SLAB_BYTES, &p.vmap, sl * 64, row0, &full_bar[st],
-                                policy);
+                    tma_load_2d(dst + C::KV_BYTES + sl * C::SLAB_BYTES, &p.vmap, sl * SLAB_ELEMS, row0,
+                                &full_bar[st], policy);
                 }
               }
             } else {
@@ -292,6 +373,26 @@ __device__ __forceinline__ void stage1_cta(const Stage1Params& p, uint8_t* smem)
     const uint32_t vst = C::KVS ? kst : kst + C::KV_BYTES;
     const bool stage_ok = stage_valid[st] != 0;
     const int t0 = blk_lo + j * C::TB;
+    // the 16-bit K and V tiles the MMAs read: the stage itself (bf16), or this
+    // warp's f16 tiles widened from the e4m3 stage, which is then released
+    // (FP8: one f16 tile per warp holds K for QK, then V for PV; the e4m3
+    // stage is released once its last tile is widened)
+    uint32_t kt = kst, vt = vst;
+    float k_sc = 1.f, v_sc = 1.f;
+    uint8_t* scr = smem + C::SCRATCH_OFFSET + warp * C::SCRATCH_BYTES;
+    const uint8_t* stg = smem + (size_t)st * C::STAGE_BYTES;
+    if constexpr (C::KV8) {
+      const float2 sc = stage_scale[st];
+      k_sc = sc.x;
+      v_sc = sc.y;
+      widen_e4m3_tile<C::D>(stg, scr, lane);
+      kt = vt = smem_u32(scr);
+      __syncwarp();
+      asm volatile("" ::: "memory");  // the widened tile is in place before any ldmatrix
+      if constexpr (C::KVS) {
+        if (lane == 0) mbar_arrive(&empty_bar[st]);
+      }
+    }
 
     // QK on the tensor cores, four independent accumulation chains
     float sacc[4][4];
@@ -302,14 +403,15 @@ __device__ __forceinline__ void stage1_cta(const Stage1Params& p, uint8_t* smem)
 #pragma unroll
     for (int ks = 0; ks < C::KSTEPS; ++ks) {
       uint32_t a[4];
-      ldmatrix_x4(a, kst + (ks >> 2) * C::SLAB_BYTES + koff[ks & 3]);
-      mma_bf16(sacc[ks & 3], a, qb[ks][0], qb[ks][1]);
+      ldmatrix_x4(a, kt + (ks >> 2) * C::SLAB_BYTES + koff[ks & 3]);
+      mma_16816<C::KV8>(sacc[ks & 3], a, qb[ks][0], qb[ks][1]);
     }
     // lane holds tokens t0 + lane/4 (s[0], s[1]) and t0 + lane/4 + 8 (s[2], s[3]);
     // heads 2*(lane%4) (s[0], s[2]) and 2*(lane%4) + 1 (s[1], s[3])
     float s[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) s[i] = ((sacc[0][i] + sacc[1][i]) + (sacc[2][i] + sacc[3][i])) * p.scale_log2;
+    for (int i = 0; i < 4; ++i)
+      s[i] = ((sacc[0][i] + sacc[1][i]) + (sacc[2][i] + sacc[3][i])) * (p.scale_log2 * k_sc);
     const int ta = t0 + qh;
     const bool va = stage_ok && ta >= tlo && ta < thi;
     const bool vb = stage_ok && ta + 8 >= tlo && ta + 8 < thi;
@@ -348,6 +450,15 @@ __device__ __forceinline__ void stage1_cta(const Stage1Params& p, uint8_t* smem)
       }
     }
 
+    if constexpr (C::KV8 && !C::KVS) {
+      __syncwarp();
+      asm volatile("" ::: "memory");  // QK's reads of the K tile are done
+      widen_e4m3_tile<C::D>(stg + C::KV_BYTES, scr, lane);
+      __syncwarp();
+      asm volatile("" ::: "memory");
+      if (lane == 0) mbar_arrive(&empty_bar[st]);
+    }
+
     // Edge block (window start, sequence end, skipped page): the masked rows
     // carry p = 0, but 0 * NaN is NaN, and a page's unused rows may hold any
     // bits. Zero those V rows before they enter the PV contraction.
@@ -358,26 +469,36 @@ __device__ __forceinline__ void stage1_cta(const Stage1Params& p, uint8_t* smem)
         const int t = t0 + r;
         if (stage_ok && t >= tlo && t < thi) continue;
         for (int idx = lane; idx < C::SLABS * 8; idx += 32)
-          sts128_zero(vst + (idx >> 3) * C::SLAB_BYTES + r * 128 + (idx & 7) * 16);
+          sts128_zero(vt + (idx >> 3) * C::SLAB_BYTES + r * 128 + (idx & 7) * 16);
       }
-      fence_proxy_async_smem();  // these generic writes precede the next TMA fill
+      if constexpr (!C::KV8) fence_proxy_async_smem();  // these writes precede the next TMA fill
       __syncwarp();
     }
 
-    // P^T as the B operand: transpose the (token x head) bf16 fragments
-    const uint32_t pb0 = movmatrix_trans(pack_bf16x2(p0, p1));  // tokens 0..7
-    const uint32_t pb1 = movmatrix_trans(pack_bf16x2(p2, p3));  // tokens 8..15
+    // P^T as the B operand: transpose the (token x head) 16-bit fragments; on
+    // the FP8 path the block's V scale rides on P (sum_t p_t (v_sc v8_t))
+    uint32_t pb0, pb1;
+    if constexpr (C::KV8) {
+      pb0 = movmatrix_trans(pack_f16x2(p0 * v_sc, p1 * v_sc));  // tokens 0..7
+      pb1 = movmatrix_trans(pack_f16x2(p2 * v_sc, p3 * v_sc));  // tokens 8..15
+    } else {
+      pb0 = movmatrix_trans(pack_bf16x2(p0, p1));
+      pb1 = movmatrix_trans(pack_bf16x2(p2, p3));
+    }
 
     // PV on the tensor cores
 #pragma unroll
     for (int mt = 0; mt < C::MTILES; ++mt) {
       uint32_t a[4];
-      ldmatrix_x4_trans(a, vst + (mt >> 2) * C::SLAB_BYTES + voff[mt & 3]);
-      mma_bf16(acc[mt], a, pb0, pb1);
+      ldmatrix_x4_trans(a, vt + (mt >> 2) * C::SLAB_BYTES + voff[mt & 3]);
+      mma_16816<C::KV8>(acc[mt], a, pb0, pb1);
     }
 
     __syncwarp();
-    if (lane == 0) mbar_arrive(&empty_bar[st]);
+    asm volatile("" ::: "memory");
+    if constexpr (!C::KV8) {
+      if (lane == 0) mbar_arrive(&empty_bar[st]);
+    }
   }
 
   // ---- merge the NW warp states --------------------------------------------------
@@ -545,16 +666,16 @@ __global__ void __launch_bounds__(C::THREADS, 1) stage1_kernel(const __grid_cons
 
 // ---- instantiation and dispatch -------------------------------------------------
 
-#define PD_STAGE1_INSTANCE(ID, D, G, KVS, NW, SPW) \
-  template __global__ void stage1_kernel<Stage1Cfg<D, G, KVS, NW, SPW>>(const __grid_constant__ Stage1Params);
+#define PD_STAGE1_INSTANCE(ID, D, G, KVS, KV8, NW, SPW) \
+  template __global__ void stage1_kernel<Stage1Cfg<D, G, KVS, KV8, NW, SPW>>(const __grid_constant__ Stage1Params);
 PD_FOR_EACH_VARIANT(PD_STAGE1_INSTANCE)
 #undef PD_STAGE1_INSTANCE
 
 const void* stage1_kernel_ptr(int variant) {
   switch (variant) {
-#define PD_STAGE1_CASE(ID, D, G, KVS, NW, SPW) \
-  case ID:                                     \
-    return reinterpret_cast<const void*>(&stage1_kernel<Stage1Cfg<D, G, KVS, NW, SPW>>);
+#define PD_STAGE1_CASE(ID, D, G, KVS, KV8, NW, SPW) \
+  case ID:                                          \
+    return reinterpret_cast<const void*>(&stage1_kernel<Stage1Cfg<D, G, KVS, KV8, NW, SPW>>);
     PD_FOR_EACH_VARIANT(PD_STAGE1_CASE)
 #undef PD_STAGE1_CASE
     default:

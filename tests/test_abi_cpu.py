@@ -49,7 +49,7 @@ def test_build_targets_sm103a_only():
 def test_status_strings_and_version(lib):
     assert b.status_string(b.PD_OK) == "ok"
     assert "workspace" in b.status_string(b.PD_ERR_WORKSPACE_TOO_SMALL)
-    assert b.abi_version() == 2
+    assert b.abi_version() == 3
 
 
 def _plan(lens, Hq=16, Hkv=4, d=512, P=16, pages=4096, maxp=None, window=0, kv_shared=False, sms=152):
@@ -72,6 +72,22 @@ def test_plan_rejects(lib, kw, status):
     with pytest.raises(b.PagedDecodeError) as e:
         _plan([100, 200], **kw)
     assert e.value.status == status
+
+
+def test_plan_kv_dtypes(lib):
+    for dt in (b.PD_KV_BF16, b.PD_KV_FP8_E4M3):
+        pl = b.paged_decode_plan(b.layer_desc(16, 4, 512, 16, 4096, 64, kv_dtype=dt), [1024] * 8, 152)
+        assert pl.layer.kv_dtype == dt
+    with pytest.raises(b.PagedDecodeError) as e:
+        b.paged_decode_plan(b.layer_desc(16, 4, 512, 16, 4096, 64, kv_dtype=7), [1024] * 8, 152)
+    assert e.value.status == b.PD_ERR_INVALID_ARG
+    # the bf16 and FP8 entry points refuse each other's plans before touching CUDA
+    bf = b.paged_decode_plan(b.layer_desc(16, 4, 512, 16, 4096, 64), [64], 152)
+    f8 = b.paged_decode_plan(b.layer_desc(16, 4, 512, 16, 4096, 64, kv_dtype=b.PD_KV_FP8_E4M3), [64], 152)
+    assert lib.paged_decode_global_fp8(ctypes.byref(bf), 16, 16, 32, 48, 48, 64, 64, 1.0, 256, 1 << 20, 512,
+                                       None) == b.PD_ERR_INVALID_ARG
+    assert lib.paged_decode_global(ctypes.byref(f8), 16, 16, 32, 64, 64, 1.0, 256, 1 << 20, 512,
+                                   None) == b.PD_ERR_INVALID_ARG
 
 
 def test_plan_rejects_length_beyond_table(lib):

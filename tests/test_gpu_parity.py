@@ -272,3 +272,74 @@ def test_pipeline_wait_timeout_is_reported_and_context_survives(lens, sms, mode)
     step.plan.test_stall_bytes = 0
     out2, _ = run_gpu(li, sm_count=sms)
     compare(out2, run_oracle(li), li, "after a timed-out call")
+
+
+# ---- FP8 (e4m3) KV cache -----------------------------------------------------------
+
+def run_oracle_fp8(f):
+    return oracle.decode_fp8(synth.bits_u16(f.q), f.k8.cpu().numpy(),
+                             None if f.v8 is None else f.v8.cpu().numpy(), f.k_scale.cpu().numpy(),
+                             None if f.v_scale is None else f.v_scale.cpu().numpy(), f.block_tables.cpu().numpy(),
+                             f.seq_lens.cpu().numpy(), f.scale, f.window)
+
+
+@pytest.mark.parametrize("d,G,kvs", VARIANTS)
+@pytest.mark.parametrize("window", [0, 37])
+def test_fp8_variants_ragged(d, G, kvs, window):
+    Hkv = 2
+    lens = [1, 17, 300, 0, 1000, 33]
+    li = synth.make_layer("f8", lens, Hkv * G, Hkv, d, window=window, kv_shared=kvs,
+                          pool_pages=sum((L + 15) // 16 for L in lens) + 5, seed=500 + d + G + 100 * kvs + window,
+                          device="cuda")
+    f = synth.quantize_kv_fp8(li)
+    ref = run_oracle_fp8(f)
+    for sms in (3, 152):
+        out, step = run_gpu(f, sm_count=sms)
+        compare(out, ref, f, f"fp8 d{d} G{G} kvs{kvs} W{window} sms{sms} S{step.plan.num_splits}")
+
+
+@pytest.mark.parametrize("cid,part", [(2, None), (3, None), (4, "c"), (5, "global"), (5, "sliding")])
+def test_fp8_workload_matches_oracle(cid, part):
+    for li in synth.workload(cid, device="cuda", part=part):
+        f = synth.quantize_kv_fp8(li)
+        out, step = run_gpu(f)
+        err, cos = compare(out, run_oracle_fp8(f), f, f"{f.name} S={step.plan.num_splits}")
+        print(f"{f.name}: splits {step.plan.num_splits} max_abs {err:.2e} cos {cos:.7f}")
+
+
+def test_fp8_nan_bytes_in_unattended_rows_do_not_leak():
+    lens = [37, 100, 250]
+    li = synth.make_layer("f8nan", lens, 8, 2, 512, pool_pages=30, seed=31, device="cuda")
+    f = synth.quantize_kv_fp8(li)
+    ref = run_oracle_fp8(f)
+    for bi, L in enumerate(lens):
+        for t in range(L, (L + 15) // 16 * 16):
+            page = int(f.block_tables[bi, t // 16])
+            f.k8[page, :, t % 16] = 0x7F  # e4m3 NaN
+            f.v8[page, :, t % 16] = 0xFF
+    out, _ = run_gpu(f)
+    compare(out, ref, f, "fp8 nan rows")
+
+
+def test_fp8_scales_reach_the_result():
+    """Doubling every V scale doubles the output; doubling every K scale equals
+    doubling the softmax scale."""
+    li = synth.make_layer("f8s", [500, 70], 8, 2, 512, pool_pages=40, seed=32, device="cuda")
+    f = synth.quantize_kv_fp8(li)
+    out, step = run_gpu(f)
+    f.v_scale.mul_(2)
+    out2 = torch.empty_like(out)
+    step.run(f, out2)
+    assert step.check() == 0
+    assert torch.allclose(out2.float(), 2 * out.float(), rtol=1e-2, atol=1e-3)
+    f.v_scale.div_(2)
+    import dataclasses
+    f.k_scale.mul_(2)
+    out3 = torch.empty_like(out)
+    step.run(f, out3)
+    f.k_scale.div_(2)
+    out4 = torch.empty_like(out)
+    step.run(dataclasses.replace(f, scale=2 * f.scale), out4)
+    assert step.check() == 0
+    assert torch.equal(out3, out4)  # products with 2 are exact in fp32
+    assert not torch.equal(out3, out)
