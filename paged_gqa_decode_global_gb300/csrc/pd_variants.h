@@ -34,21 +34,16 @@ struct Stage1Cfg {
   static constexpr int MTILES = D / 16;          // PV m-tiles (head dims)
   static constexpr int NST = NW * SPW;
   static constexpr int SLAB_BYTES = TB * 128;    // one 128-byte-wide slab of a 16-token block
-  // 16-bit tiles the MMAs read (bf16 stages, or the f16 tiles FP8 stages are
-  // converted into): [D/64 slabs][16 rows][128 B]
-  static constexpr int SLABS = D / 64;
-  static constexpr int TILE16_BYTES = SLABS * SLAB_BYTES;
-  // what TMA lands per K (or V) block: bf16 rows, or e4m3 rows ([D/128 slabs][16][128 B])
+  // what TMA lands per K (or V) block, [slab][16 rows][128 B] with the
+  // 128-byte swizzle: bf16 rows (64 dims a slab) or e4m3 rows (128 dims)
+  static constexpr int SLABS = D / 64;           // bf16 slabs
   static constexpr int ELEM = KV8 ? 1 : 2;
   static constexpr int TMA_SLABS = D * ELEM / 128;
   static constexpr int KV_BYTES = TMA_SLABS * SLAB_BYTES;
   static constexpr int STAGE_BYTES = KV_BYTES * (KVS ? 1 : 2);
   static constexpr int TX_BYTES = STAGE_BYTES;                  // bytes the copies deliver
   static constexpr int RING_BYTES = NST * STAGE_BYTES;
-  // FP8: each consumer warp's f16 tile, after the ring (K, then V once QK is done)
-  static constexpr int SCRATCH_BYTES = KV8 ? TILE16_BYTES : 0;
-  static constexpr int SCRATCH_OFFSET = RING_BYTES;
-  static constexpr int WORK_BYTES = RING_BYTES + NW * SCRATCH_BYTES;
+  static constexpr int WORK_BYTES = RING_BYTES;
   static constexpr int COMB_STRIDE = D + 4;                    // floats per head row of the warp merge
   static constexpr int COMBINE_BYTES = NW * G * COMB_STRIDE * 4; // per-warp outputs (aliases the ring)
   static constexpr int BODY_BYTES = WORK_BYTES > COMBINE_BYTES ? WORK_BYTES : COMBINE_BYTES;
@@ -75,7 +70,7 @@ struct Stage1Cfg {
   static_assert(D % 128 == 0, "head_dim must be a multiple of 128");
   static_assert(G >= 1 && G <= 8, "the GQA group is the MMA's 8-wide side");
   static_assert(16 % TB == 0, "a block must lie inside one 16-token page slice");
-  static_assert(STAGE_BYTES % 1024 == 0 && TILE16_BYTES % 1024 == 0, "tiles keep the 1024-byte swizzle alignment");
+  static_assert(STAGE_BYTES % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
   static_assert(SCALE_OFFSET % 8 == 0 && ML_OFFSET % 8 == 0, "float2 arrays need 8-byte alignment");
 };
@@ -86,7 +81,7 @@ struct Stage1Cfg {
 // idle) plus the producer; rings of 192 KiB: 32 KiB stages x 6 (d512 K!=V),
 // 16 KiB x 12 (d512 K=V, d256 K!=V), 8 KiB x 24 (d256 K=V). FP8: seven
 // consumer warps (two per SM sub-partition hide the latency of widening e4m3
-// tiles to f16) with one 16-bit tile each beside rings of 56-112 KiB.
+// fragments to f16) and rings of 196-224 KiB.
 #define PD_FOR_EACH_VARIANT(X)        \
   X(0, 512, 1, false, false, 3, 2)    \
   X(1, 512, 2, false, false, 3, 2)    \
@@ -104,22 +99,22 @@ struct Stage1Cfg {
   X(13, 256, 2, true, false, 3, 8)    \
   X(14, 256, 4, true, false, 3, 8)    \
   X(15, 256, 8, true, false, 3, 8)    \
-  X(16, 512, 1, false, true, 7, 1)  \
-  X(17, 512, 2, false, true, 7, 1)  \
-  X(18, 512, 4, false, true, 7, 1)  \
-  X(19, 512, 8, false, true, 7, 1)  \
-  X(20, 512, 1, true, true, 7, 2)   \
-  X(21, 512, 2, true, true, 7, 2)   \
-  X(22, 512, 4, true, true, 7, 2)   \
-  X(23, 512, 8, true, true, 7, 2)   \
-  X(24, 256, 1, false, true, 7, 2)  \
-  X(25, 256, 2, false, true, 7, 2)  \
-  X(26, 256, 4, false, true, 7, 2)  \
-  X(27, 256, 8, false, true, 7, 2)  \
-  X(28, 256, 1, true, true, 7, 4)   \
-  X(29, 256, 2, true, true, 7, 4)   \
-  X(30, 256, 4, true, true, 7, 4)   \
-  X(31, 256, 8, true, true, 7, 4)
+  X(16, 512, 1, false, true, 7, 2)  \
+  X(17, 512, 2, false, true, 7, 2)  \
+  X(18, 512, 4, false, true, 7, 2)  \
+  X(19, 512, 8, false, true, 7, 2)  \
+  X(20, 512, 1, true, true, 7, 4)   \
+  X(21, 512, 2, true, true, 7, 4)   \
+  X(22, 512, 4, true, true, 7, 4)   \
+  X(23, 512, 8, true, true, 7, 4)   \
+  X(24, 256, 1, false, true, 7, 4)  \
+  X(25, 256, 2, false, true, 7, 4)  \
+  X(26, 256, 4, false, true, 7, 4)  \
+  X(27, 256, 8, false, true, 7, 4)  \
+  X(28, 256, 1, true, true, 7, 7)   \
+  X(29, 256, 2, true, true, 7, 7)   \
+  X(30, 256, 4, true, true, 7, 7)   \
+  X(31, 256, 8, true, true, 7, 7)
 
 struct VariantInfo {
   int id, head_dim, group, kv_shared, kv_fp8, nw, spw, block_tokens, threads, smem_bytes, max_cluster;

@@ -23,6 +23,12 @@
 //       QK: S[16 tok x 8 heads]  = K[16 x d] . q^T       (A = K rows, B = q)
 //       PV: O^T[d x 8 heads]    += V^T[d x 16 tok] . P^T (A = V rows via
 //           ldmatrix.trans, B = P transposed in registers with movmatrix);
+//   * FP8 (e4m3) caches land in the ring as bytes; each lane loads its MMA
+//     fragments straight from them with 16-byte shared loads and widens them
+//     to f16 in registers (exact), taking the head dims in an order that
+//     makes every load feed four MMAs (q and the output follow that order);
+//     the products run in f16 with fp32 accumulation, the per-(page, KV head)
+//     K scale multiplies the scores and the V scale the probabilities;
 //   * the online softmax runs in base 2 on the S fragments (scale * log2 e
 //     applied in fp32); each lane owns two heads, so the rescale of its O^T
 //     fragments needs no communication;
@@ -72,14 +78,6 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], u
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-template <bool F16>
-__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  if constexpr (F16)
-    mma_f16(d, a, b0, b1);
-  else
-    mma_bf16(d, a, b0, b1);
-}
-
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   __half2 v = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
@@ -94,29 +92,13 @@ __device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t& lo, uint32
       : "r"(w));
 }
 
-// Widen one 16-token e4m3 tile ([D/128 slabs][16 rows][128 B], 128-byte
-// swizzle) into the f16 tile the MMAs read ([D/64 slabs][16 rows][128 B],
-// 128-byte swizzle). Lane-parallel: one 16-byte e4m3 chunk (16 dims) per step.
-// Plain shared-memory accesses, so the loads of later chunks overlap earlier
-// conversions; the caller orders them against the ring and the MMAs.
-template <int D>
-__device__ __forceinline__ void widen_e4m3_tile(const uint8_t* src, uint8_t* dst, int lane) {
-  constexpr int CHUNKS = D / 16;  // per row
-#pragma unroll 8
-  for (int idx = lane; idx < 16 * CHUNKS; idx += 32) {
-    const int r = idx / CHUNKS, cj = idx % CHUNKS;
-    const int sw = r & 7;
-    const uint4 raw = *reinterpret_cast<const uint4*>(src + (cj >> 3) * 2048 + r * 128 + (((cj & 7) ^ sw) << 4));
-    uint4 o0, o1;
-    e4m3x4_to_f16x4(raw.x, o0.x, o0.y);
-    e4m3x4_to_f16x4(raw.y, o0.z, o0.w);
-    e4m3x4_to_f16x4(raw.z, o1.x, o1.y);
-    e4m3x4_to_f16x4(raw.w, o1.z, o1.w);
-    uint8_t* row = dst + (cj >> 2) * 2048 + r * 128;
-    const int c0 = (cj & 3) * 2;
-    *reinterpret_cast<uint4*>(row + ((c0 ^ sw) << 4)) = o0;
-    *reinterpret_cast<uint4*>(row + (((c0 + 1) ^ sw) << 4)) = o1;
-  }
+// FP8 QK order of the head dims. In k-step ks = 8*sl + 4*hf + jj the MMA's
+// columns 2*(lane%4) + {0, 1} and + {8, 9} are the dims returned + {0, 1} and
+// + {2, 3}: four consecutive bytes of the 16-byte chunk 2*(lane%4) + hf of the
+// 128-dim slab sl, so one load of a token row feeds four k-steps. (A sum over
+// the dims may take them in any order, as long as q and K agree.)
+__device__ __forceinline__ int kv8_qk_dim(int ks, int lane) {
+  return (ks >> 3) * 128 + (2 * (lane & 3) + ((ks >> 2) & 1)) * 16 + 4 * (ks & 3);
 }
 
 // Transpose an 8x8 bf16 matrix held one row pair per lane (fragment layout).
@@ -210,16 +192,16 @@ __device__ __forceinline__ void stage1_cta(const Stage1Params& p, uint8_t* smem)
 #pragma unroll
     for (int ks = 0; ks < C::KSTEPS; ++ks) {
       if (qh < C::G) {
-        const uint16_t* qrow = p.q + (row_hq + qh) * C::D + ks * 16 + qk;
-        qb[ks][0] = __ldg(reinterpret_cast<const unsigned int*>(qrow));
-        qb[ks][1] = __ldg(reinterpret_cast<const unsigned int*>(qrow + 8));
         if constexpr (C::KV8) {
-          // the FP8 path multiplies in f16: q rounds to f16 once here
-#pragma unroll
-          for (int w = 0; w < 2; ++w) {
-            const uint32_t x = qb[ks][w];
-            qb[ks][w] = pack_f16x2(__uint_as_float(x << 16), __uint_as_float(x & 0xffff0000u));
-          }
+          // dims in the FP8 QK order (see the consumer loop); the products run
+          // in f16, so q rounds to f16 once here
+          const uint2 x = __ldg(reinterpret_cast<const uint2*>(p.q + (row_hq + qh) * C::D + kv8_qk_dim(ks, lane)));
+          qb[ks][0] = pack_f16x2(__uint_as_float(x.x << 16), __uint_as_float(x.x & 0xffff0000u));
+          qb[ks][1] = pack_f16x2(__uint_as_float(x.y << 16), __uint_as_float(x.y & 0xffff0000u));
+        } else {
+          const uint16_t* qrow = p.q + (row_hq + qh) * C::D + ks * 16 + qk;
+          qb[ks][0] = __ldg(reinterpret_cast<const unsigned int*>(qrow));
+          qb[ks][1] = __ldg(reinterpret_cast<const unsigned int*>(qrow + 8));
         }
       } else {
         qb[ks][0] = 0u;
@@ -373,25 +355,12 @@ __device__ __forceinline__ void stage1_cta(const Stage1Params& p, uint8_t* smem)
     const uint32_t vst = C::KVS ? kst : kst + C::KV_BYTES;
     const bool stage_ok = stage_valid[st] != 0;
     const int t0 = blk_lo + j * C::TB;
-    // the 16-bit K and V tiles the MMAs read: the stage itself (bf16), or this
-    // warp's f16 tiles widened from the e4m3 stage, which is then released
-    // (FP8: one f16 tile per warp holds K for QK, then V for PV; the e4m3
-    // stage is released once its last tile is widened)
-    uint32_t kt = kst, vt = vst;
-    float k_sc = 1.f, v_sc = 1.f;
-    uint8_t* scr = smem + C::SCRATCH_OFFSET + warp * C::SCRATCH_BYTES;
     const uint8_t* stg = smem + (size_t)st * C::STAGE_BYTES;
+    float k_sc = 1.f, v_sc = 1.f;
     if constexpr (C::KV8) {
       const float2 sc = stage_scale[st];
       k_sc = sc.x;
       v_sc = sc.y;
-      widen_e4m3_tile<C::D>(stg, scr, lane);
-      kt = vt = smem_u32(scr);
-      __syncwarp();
-      asm volatile("" ::: "memory");  // the widened tile is in place before any ldmatrix
-      if constexpr (C::KVS) {
-        if (lane == 0) mbar_arrive(&empty_bar[st]);
-      }
     }
 
     // QK on the tensor cores, four independent accumulation chains
@@ -400,11 +369,36 @@ __device__ __forceinline__ void stage1_cta(const Stage1Params& p, uint8_t* smem)
     for (int c = 0; c < 4; ++c)
 #pragma unroll
       for (int i = 0; i < 4; ++i) sacc[c][i] = 0.f;
+    if constexpr (C::KV8) {
+      // A fragments straight from the e4m3 rows: one 16-byte chunk of token
+      // rows lane/4 and lane/4 + 8 holds this lane's part of four k-steps
+      // (the dims are taken in the order kv8_qk_dim gives; q follows it)
 #pragma unroll
-    for (int ks = 0; ks < C::KSTEPS; ++ks) {
-      uint32_t a[4];
-      ldmatrix_x4(a, kt + (ks >> 2) * C::SLAB_BYTES + koff[ks & 3]);
-      mma_16816<C::KV8>(sacc[ks & 3], a, qb[ks][0], qb[ks][1]);
+      for (int sl = 0; sl < C::TMA_SLABS; ++sl) {
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          const uint8_t* sp = stg + sl * C::SLAB_BYTES + qh * 128 + (((2 * (lane & 3) + hf) ^ qh) << 4);
+          const uint4 ra = *reinterpret_cast<const uint4*>(sp);
+          const uint4 rb = *reinterpret_cast<const uint4*>(sp + 8 * 128);
+          const uint32_t wa[4] = {ra.x, ra.y, ra.z, ra.w};
+          const uint32_t wb[4] = {rb.x, rb.y, rb.z, rb.w};
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            uint32_t a[4];
+            e4m3x4_to_f16x4(wa[jj], a[0], a[2]);
+            e4m3x4_to_f16x4(wb[jj], a[1], a[3]);
+            const int ks = sl * 8 + hf * 4 + jj;
+            mma_f16(sacc[jj], a, qb[ks][0], qb[ks][1]);
+          }
+        }
+      }
+    } else {
+#pragma unroll
+      for (int ks = 0; ks < C::KSTEPS; ++ks) {
+        uint32_t a[4];
+        ldmatrix_x4(a, kst + (ks >> 2) * C::SLAB_BYTES + koff[ks & 3]);
+        mma_bf16(sacc[ks & 3], a, qb[ks][0], qb[ks][1]);
+      }
     }
     // lane holds tokens t0 + lane/4 (s[0], s[1]) and t0 + lane/4 + 8 (s[2], s[3]);
     // heads 2*(lane%4) (s[0], s[2]) and 2*(lane%4) + 1 (s[1], s[3])
@@ -450,29 +444,23 @@ __device__ __forceinline__ void stage1_cta(const Stage1Params& p, uint8_t* smem)
       }
     }
 
-    if constexpr (C::KV8 && !C::KVS) {
-      __syncwarp();
-      asm volatile("" ::: "memory");  // QK's reads of the K tile are done
-      widen_e4m3_tile<C::D>(stg + C::KV_BYTES, scr, lane);
-      __syncwarp();
-      asm volatile("" ::: "memory");
-      if (lane == 0) mbar_arrive(&empty_bar[st]);
-    }
-
     // Edge block (window start, sequence end, skipped page): the masked rows
     // carry p = 0, but 0 * NaN is NaN, and a page's unused rows may hold any
     // bits. Zero those V rows before they enter the PV contraction.
-    const bool edge = __any_sync(kFullMask, !(va && vb));
-    if (edge) {
+    // (The FP8 path zeroes them in registers, below.)
+    if constexpr (!C::KV8) {
+      const bool edge = __any_sync(kFullMask, !(va && vb));
+      if (edge) {
 #pragma unroll 1
-      for (int r = 0; r < C::TB; ++r) {
-        const int t = t0 + r;
-        if (stage_ok && t >= tlo && t < thi) continue;
-        for (int idx = lane; idx < C::SLABS * 8; idx += 32)
-          sts128_zero(vt + (idx >> 3) * C::SLAB_BYTES + r * 128 + (idx & 7) * 16);
+        for (int r = 0; r < C::TB; ++r) {
+          const int t = t0 + r;
+          if (stage_ok && t >= tlo && t < thi) continue;
+          for (int idx = lane; idx < C::SLABS * 8; idx += 32)
+            sts128_zero(vst + (idx >> 3) * C::SLAB_BYTES + r * 128 + (idx & 7) * 16);
+        }
+        fence_proxy_async_smem();  // these writes precede the next TMA fill
+        __syncwarp();
       }
-      if constexpr (!C::KV8) fence_proxy_async_smem();  // these writes precede the next TMA fill
-      __syncwarp();
     }
 
     // P^T as the B operand: transpose the (token x head) 16-bit fragments; on
@@ -487,18 +475,59 @@ __device__ __forceinline__ void stage1_cta(const Stage1Params& p, uint8_t* smem)
     }
 
     // PV on the tensor cores
+    if constexpr (C::KV8) {
+      // A fragments (dims x tokens) straight from the e4m3 rows: this lane
+      // reads the 16-byte chunk lane/4 of tokens 2*(lane%4) + {0, 1, 8, 9}.
+      // Byte 2u (2u + 1) of a chunk is taken as the dim of row lane/4
+      // (lane/4 + 8) of m-tile u of the slab, so row i of m-tile u holds dim
+      // 16*(i%8) + 2u + i/8 (the epilogue puts each back); a byte permute
+      // pairs one dim of two tokens.
+      const int tv = 2 * (lane & 3);
+      const int t_a = t0 + tv;
+      const bool ok0 = stage_ok && t_a >= tlo && t_a < thi;
+      const bool ok1 = stage_ok && t_a + 1 >= tlo && t_a + 1 < thi;
+      const bool ok2 = stage_ok && t_a + 8 >= tlo && t_a + 8 < thi;
+      const bool ok3 = stage_ok && t_a + 9 >= tlo && t_a + 9 < thi;
+      const uint8_t* vstg = C::KVS ? stg : stg + C::KV_BYTES;
 #pragma unroll
-    for (int mt = 0; mt < C::MTILES; ++mt) {
-      uint32_t a[4];
-      ldmatrix_x4_trans(a, vt + (mt >> 2) * C::SLAB_BYTES + voff[mt & 3]);
-      mma_16816<C::KV8>(acc[mt], a, pb0, pb1);
+      for (int sl = 0; sl < C::TMA_SLABS; ++sl) {
+        const uint8_t* vp = vstg + sl * C::SLAB_BYTES;
+        const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+        // rows the sequence does not cover may hold any bits: e4m3 zero instead
+        uint4 r0 = *reinterpret_cast<const uint4*>(vp + tv * 128 + ((qh ^ tv) << 4));
+        uint4 r1 = *reinterpret_cast<const uint4*>(vp + (tv + 1) * 128 + ((qh ^ (tv + 1)) << 4));
+        uint4 r2 = *reinterpret_cast<const uint4*>(vp + (tv + 8) * 128 + ((qh ^ tv) << 4));
+        uint4 r3 = *reinterpret_cast<const uint4*>(vp + (tv + 9) * 128 + ((qh ^ (tv + 1)) << 4));
+        if (!ok0) r0 = zero;
+        if (!ok1) r1 = zero;
+        if (!ok2) r2 = zero;
+        if (!ok3) r3 = zero;
+        const uint32_t x0[4] = {r0.x, r0.y, r0.z, r0.w}, x1[4] = {r1.x, r1.y, r1.z, r1.w};
+        const uint32_t x2[4] = {r2.x, r2.y, r2.z, r2.w}, x3[4] = {r3.x, r3.y, r3.z, r3.w};
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+#pragma unroll
+          for (int u2 = 0; u2 < 2; ++u2) {
+            const uint32_t sel = u2 ? 0x7362u : 0x5140u;
+            uint32_t a[4];
+            e4m3x4_to_f16x4(__byte_perm(x0[w], x1[w], sel), a[0], a[1]);
+            e4m3x4_to_f16x4(__byte_perm(x2[w], x3[w], sel), a[2], a[3]);
+            mma_f16(acc[sl * 8 + w * 2 + u2], a, pb0, pb1);
+          }
+        }
+      }
+    } else {
+#pragma unroll
+      for (int mt = 0; mt < C::MTILES; ++mt) {
+        uint32_t a[4];
+        ldmatrix_x4_trans(a, vst + (mt >> 2) * C::SLAB_BYTES + voff[mt & 3]);
+        mma_bf16(acc[mt], a, pb0, pb1);
+      }
     }
 
     __syncwarp();
     asm volatile("" ::: "memory");
-    if constexpr (!C::KV8) {
-      if (lane == 0) mbar_arrive(&empty_bar[st]);
-    }
+    if (lane == 0) mbar_arrive(&empty_bar[st]);
   }
 
   // ---- merge the NW warp states --------------------------------------------------
@@ -512,11 +541,20 @@ __device__ __forceinline__ void stage1_cta(const Stage1Params& p, uint8_t* smem)
   for (int hh = 0; hh < 2; ++hh) {
     const int h = h0 + hh;
     if (h < C::G) {
-      float* dst = comb + (warp * C::G + h) * CS + qh;
+      if constexpr (C::KV8) {
+        // rows lane/4 and lane/4 + 8 of m-tile u of slab sl are dims
+        // sl*128 + 16*(lane/4) + 2u + {0, 1}
+        float* dst = comb + (warp * C::G + h) * CS + 16 * qh;
 #pragma unroll
-      for (int mt = 0; mt < C::MTILES; ++mt) {
-        dst[mt * 16] = acc[mt][hh];
-        dst[mt * 16 + 8] = acc[mt][2 + hh];
+        for (int mt = 0; mt < C::MTILES; ++mt)
+          *reinterpret_cast<float2*>(dst + (mt >> 3) * 128 + 2 * (mt & 7)) = make_float2(acc[mt][hh], acc[mt][2 + hh]);
+      } else {
+        float* dst = comb + (warp * C::G + h) * CS + qh;
+#pragma unroll
+        for (int mt = 0; mt < C::MTILES; ++mt) {
+          dst[mt * 16] = acc[mt][hh];
+          dst[mt * 16 + 8] = acc[mt][2 + hh];
+        }
       }
       if (qh == 0) warp_ml[warp * C::G + h] = make_float2(m_run[hh], l_run[hh]);
     }
