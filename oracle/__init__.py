@@ -2,9 +2,10 @@
 
 TEST INFRASTRUCTURE ONLY: the tests, the smoke check and the benchmark's CPU
 baseline may import this package; the product package never does. It shares
-no code with the CUDA path. The arithmetic lives in ``ref_decode.c`` (plain C,
-fp64, OpenMP over query rows); this module only compiles it with gcc and
-marshals numpy arrays into it.
+no code with the CUDA path. The arithmetic lives in ``ref_decode.c`` (decode
+attention; plain C, fp64, OpenMP over query rows) and ``ref_prepare.c`` (the
+per-token norm / RoPE / cache-slot step before it); this module only compiles
+them with gcc and marshals numpy arrays into them.
 
 bf16 tensors are passed as their raw bit patterns (numpy ``uint16``); the C
 code widens them exactly to fp64.
@@ -19,8 +20,9 @@ import threading
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRC = os.path.join(_HERE, "ref_decode.c")
+SOURCES = [os.path.join(_HERE, "ref_decode.c"), os.path.join(_HERE, "ref_prepare.c")]
 _LIB_PATH = os.path.join(_HERE, "libref_decode.so")
+CFLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fopenmp", "-shared", "-fPIC"]
 _lock = threading.Lock()
 _lib = None
 
@@ -38,12 +40,12 @@ class OracleError(RuntimeError):
 
 
 def build(force: bool = False) -> str:
-    """Compile ref_decode.c into libref_decode.so next to it (gcc, -fopenmp)."""
-    if not force and os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC):
+    """Compile the C sources into libref_decode.so next to them (gcc, -fopenmp)."""
+    if not force and os.path.exists(_LIB_PATH) and all(
+            os.path.getmtime(_LIB_PATH) >= os.path.getmtime(src) for src in SOURCES):
         return _LIB_PATH
     tmp = _LIB_PATH + f".tmp{os.getpid()}"
-    cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fopenmp",
-           "-shared", "-fPIC", "-o", tmp, _SRC, "-lm"]
+    cmd = ["gcc", *CFLAGS, "-o", tmp, *SOURCES, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
@@ -70,8 +72,19 @@ def _load():
             lib.ref_decode_rows_fp8.restype = i
             lib.ref_e4m3_to_f64.argtypes = [i]
             lib.ref_e4m3_to_f64.restype = d
+            set_prepare_signatures(lib)
             _lib = lib
     return _lib
+
+
+def set_prepare_signatures(lib):
+    p = ctypes.c_void_p
+    i = ctypes.c_int
+    d = ctypes.c_double
+    lib.ref_prepare_qkv.argtypes = [i, i, i, i, i, i, i, i, i, d, d] + [p] * 12
+    lib.ref_prepare_qkv.restype = i
+    lib.ref_rope_table.argtypes = [i, d, i, p]
+    lib.ref_rope_table.restype = i
 
 
 def _u16(a) -> np.ndarray:
@@ -202,3 +215,42 @@ def merge(o_part, lse_part):
     out = np.zeros(lead + (d,), dtype=np.float64)
     _check(lib.ref_merge(rows, S, d, _ptr(o_part), _ptr(lse_part), _ptr(out)))
     return out
+
+
+def rope_table(rot: int, theta: float, n_pos: int):
+    """float64 [n_pos, rot]: cos of the pair angles, then their sin."""
+    out = np.zeros((n_pos, rot), dtype=np.float64)
+    _check(_load().ref_rope_table(int(rot), float(theta), int(n_pos), _ptr(out)))
+    return out
+
+
+def prepare_qkv(q_in, k_in, v_in, q_w, k_w, v_w, block_tables, seq_lens, num_pages: int, page_size: int,
+                rot: int, theta: float, eps: float):
+    """The per-token step before decode, in fp64.
+
+    q_in uint16 [B, Hq, d]; k_in / v_in uint16 [B, Hkv, d] (v_in None = K=V
+    layer); weights uint16 [d] (v_w None = unit weight); block_tables int32
+    [B, max_pages]; seq_lens int32 [B] (including the new token).
+    Returns (q_out [B, Hq, d], k_out [B, Hkv, d], v_out [B, Hkv, d] or None,
+    slot_page [B] (-1 outside the pool), slot_row [B]).
+    """
+    lib = _load()
+    q_in, k_in, q_w, k_w = _u16(q_in), _u16(k_in), _u16(q_w), _u16(k_w)
+    v_in = None if v_in is None else _u16(v_in)
+    v_w = None if v_w is None else _u16(v_w)
+    block_tables, seq_lens = _i32(block_tables), _i32(seq_lens)
+    B, Hq, d = q_in.shape
+    Hkv = k_in.shape[1]
+    max_pages = block_tables.shape[1] if block_tables.ndim == 2 else 0
+    kv_shared = v_in is None
+    q_out = np.zeros((B, Hq, d), dtype=np.float64)
+    k_out = np.zeros((B, Hkv, d), dtype=np.float64)
+    v_out = None if kv_shared else np.zeros((B, Hkv, d), dtype=np.float64)
+    slot_page = np.zeros(B, dtype=np.int32)
+    slot_row = np.zeros(B, dtype=np.int32)
+    st = lib.ref_prepare_qkv(B, Hq, Hkv, d, int(page_size), int(num_pages), max_pages, int(kv_shared), int(rot),
+                             float(theta), float(eps), _ptr(q_in), _ptr(k_in), _ptr(v_in), _ptr(q_w), _ptr(k_w),
+                             _ptr(v_w), _ptr(block_tables), _ptr(seq_lens), _ptr(q_out), _ptr(k_out), _ptr(v_out),
+                             _ptr(slot_page), _ptr(slot_row))
+    _check(st)
+    return q_out, k_out, v_out, slot_page, slot_row

@@ -297,3 +297,65 @@ def quantize_kv_fp8(li: LayerInputs) -> Fp8LayerInputs:
     v8, vs = (None, None) if li.v_pool is None else _quantize_pool(li.v_pool)
     return Fp8LayerInputs(li.name + "-fp8", li.q, k8, v8, ks, vs, li.block_tables, li.seq_lens, li.window,
                           li.scale)
+
+
+# --------------------------------------------------------------------------
+# The step before decode: the new token's raw q / k / v and the layer's norm
+# weights and RoPE parameters
+# --------------------------------------------------------------------------
+
+# Per layer kind: RoPE base and the number of rotated dims (sliding layers
+# rotate every dim with base 1e4; global layers rotate a quarter of d with
+# base 1e6). The pages only say that the two kinds carry their own RoPE
+# parameters; these values are inputs, not part of the method.
+ROPE_PARAMS = {"global": (1.0e6, 0.25), "sliding": (1.0e4, 1.0)}
+NORM_EPS = 1e-6
+
+
+@dataclass
+class PrepareInputs:
+    """The new token of every request of one layer, before normalisation."""
+    layer: LayerInputs        # pools, block tables, seq_lens (including the new token)
+    q_in: torch.Tensor        # bf16 [B, Hq, d]
+    k_in: torch.Tensor        # bf16 [B, Hkv, d]
+    v_in: Optional[torch.Tensor]  # bf16 [B, Hkv, d]; None on a K=V layer
+    q_w: torch.Tensor         # bf16 [d]
+    k_w: torch.Tensor         # bf16 [d]
+    v_w: Optional[torch.Tensor]   # bf16 [d] or None (unit weight)
+    rot: int                  # rotated dims (even, <= d; 0 = none)
+    theta: float              # RoPE base
+    eps: float
+    max_positions: int        # rows of the layer's RoPE table
+
+    def rows_bytes(self) -> int:
+        """Bytes of the head rows read and written per call (q in/out, k/v in, cache rows)."""
+        li = self.layer
+        d, B = li.head_dim, li.batch
+        kv_rows = li.num_kv_heads * (1 if self.v_in is None else 2)
+        return 2 * B * (li.num_q_heads + kv_rows) * d * 2
+
+
+def make_prepare(li: LayerInputs, *, rot: Optional[int] = None, theta: Optional[float] = None,
+                 eps: float = NORM_EPS, in_std: float = 3.0, seed: int = 0, with_v_weight: bool = True,
+                 max_positions: Optional[int] = None) -> PrepareInputs:
+    """Raw new-token rows (N(0, in_std), bf16) and norm weights (N(1, 0.25), bf16)
+    for layer `li`; RoPE parameters from the layer kind unless given."""
+    kind = "sliding" if li.window > 0 else "global"
+    th, frac = ROPE_PARAMS[kind]
+    theta = th if theta is None else theta
+    rot = int(li.head_dim * frac) if rot is None else rot
+    device = li.q.device
+    gen = _dev_gen(seed + 104729, device)
+    B, Hq, Hkv, d = li.batch, li.num_q_heads, li.num_kv_heads, li.head_dim
+    q_in = _randn_bf16((B, Hq, d), in_std, gen, device)
+    k_in = _randn_bf16((B, Hkv, d), in_std, gen, device)
+    v_in = None if li.v_pool is None else _randn_bf16((B, Hkv, d), in_std, gen, device)
+
+    def weight():
+        return (1.0 + 0.25 * torch.randn(d, generator=gen, device=device)).to(torch.bfloat16)
+
+    q_w, k_w = weight(), weight()
+    v_w = weight() if (with_v_weight and v_in is not None) else None
+    if max_positions is None:
+        max_positions = li.block_tables.shape[1] * li.page_size
+    return PrepareInputs(li, q_in, k_in, v_in, q_w, k_w, v_w, rot, theta, eps, max_positions)

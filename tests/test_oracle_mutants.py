@@ -1,10 +1,14 @@
 """The pins are strong enough: plausible mistakes planted in a copy of the
-oracle's C source (on the CPU) must each fail at least one pin.
+oracle's C sources (on the CPU) must each fail at least one pin.
 
-Each mutant is the oracle with one edit: a wrong GQA head mapping, a window
-off by one, a swapped page index, a dropped scale or normalisation, K used as
-V, a sign error in the merge weights, a log-sum-exp without its log term, a
-split that forgets where the attended range starts.
+Each decode mutant is the oracle with one edit: a wrong GQA head mapping, a
+window off by one, a swapped page index, a dropped scale or normalisation, K
+used as V, a sign error in the merge weights, a log-sum-exp without its log
+term, a split that forgets where the attended range starts, FP8 decoding
+mistakes. Each mutant of the step before decode: a sum instead of a mean in
+the norm, a dropped eps, a RoPE sign or partner error, a wrong frequency
+exponent, the length used as the position, a swapped slot row, k normalised
+with q's weight.
 """
 import ctypes
 import os
@@ -16,8 +20,10 @@ import pytest
 
 import oracle
 import test_oracle_pins as pins
+import test_oracle_prepare_pins as prep
 
-SRC = os.path.join(os.path.dirname(oracle.__file__), "ref_decode.c")
+DECODE_SRC = os.path.join(os.path.dirname(oracle.__file__), "ref_decode.c")
+PREPARE_SRC = os.path.join(os.path.dirname(oracle.__file__), "ref_prepare.c")
 
 MUTANTS = {
     "gqa_head_mapping": ("const int g = h / G;", "const int g = h % ly->Hkv;"),
@@ -35,6 +41,41 @@ MUTANTS = {
     "split_ignores_range_start": ("long long plo = (long long)lo + (long long)k * chunk;",
                                   "long long plo = (long long)k * chunk;"),
 }
+
+
+PREPARE_MUTANTS = {
+    "norm_sum_not_mean": ("sqrt(ms / d + eps)", "sqrt(ms + eps)"),
+    "norm_eps_dropped": ("sqrt(ms / d + eps)", "sqrt(ms / d)"),
+    "rope_sign": ("y[i] = x1 * c - x2 * s;", "y[i] = x1 * c + x2 * s;"),
+    "rope_partner": ("const double x1 = y[i], x2 = y[i + half];", "const double x1 = y[i], x2 = y[i + 1];"),
+    "rope_frequency": ("pow(theta, -2.0 * i / rot)", "pow(theta, -1.0 * i / rot)"),
+    "position_is_length": ("const int pos = seq_lens[b] - 1;", "const int pos = seq_lens[b];"),
+    "slot_row_swapped": ("slot_row[b] = pos % P;", "slot_row[b] = pos / P;"),
+    "k_norm_with_q_weight": ("rms_norm(k_in + ((size_t)b * Hkv + g) * d, k_w,",
+                             "rms_norm(k_in + ((size_t)b * Hkv + g) * d, q_w,"),
+}
+
+
+def _prepare_battery():
+    """Run the pins of the step before decode; return the names of those that fail."""
+    failed = []
+    checks = {
+        "hand_examples": prep.test_hand_examples,
+        "complex_full": lambda: prep.test_rotation_equals_complex_multiplication(8, 8, 100.0, [1, 2, 9]),
+        "complex_partial": lambda: prep.test_rotation_equals_complex_multiplication(256, 64, 1e6, [77, 65536]),
+        "relative_position": prep.test_rotated_dot_depends_only_on_distance,
+        "unit_mean_square": prep.test_normalised_rows_have_unit_mean_square,
+        "pass_through": prep.test_pass_through_dims_beyond_rot,
+        "slot": lambda: prep.test_slot_holds_the_newest_position(False, 16, [1, 16, 17, 100]),
+        "slot_kv_shared": lambda: prep.test_slot_holds_the_newest_position(True, 16, [33, 2]),
+        "rope_table": prep.test_rope_table_matches_closed_form,
+    }
+    for name, fn in checks.items():
+        try:
+            fn()
+        except (AssertionError, oracle.OracleError, IndexError):
+            failed.append(name)
+    return failed
 
 
 def _battery():
@@ -63,34 +104,57 @@ def _battery():
     return failed
 
 
-def _load_variant(src_text, workdir, tag):
-    path_c = os.path.join(workdir, f"{tag}.c")
+def _load_variant(mutated_src, src_text, workdir, tag):
+    """Build the oracle library with `mutated_src` replaced by `src_text`."""
+    paths = []
+    for src in oracle.SOURCES:
+        path = os.path.join(workdir, f"{tag}_{os.path.basename(src)}")
+        with open(path, "w") as f:
+            if src == mutated_src:
+                f.write(src_text)
+            else:
+                with open(src) as g:
+                    f.write(g.read())
+        paths.append(path)
     path_so = os.path.join(workdir, f"{tag}.so")
-    with open(path_c, "w") as f:
-        f.write(src_text)
-    subprocess.run(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fopenmp", "-shared", "-fPIC",
-                    "-o", path_so, path_c, "-lm"], check=True)
+    subprocess.run(["gcc", *oracle.CFLAGS, "-o", path_so, *paths, "-lm"], check=True)
     lib = ctypes.CDLL(path_so)
     ref = oracle._load()
     for fn in ("ref_decode_rows", "ref_decode_split", "ref_merge", "ref_max_threads", "ref_decode_rows_fp8",
                "ref_e4m3_to_f64"):
         getattr(lib, fn).argtypes = getattr(ref, fn).argtypes
         getattr(lib, fn).restype = getattr(ref, fn).restype
+    oracle.set_prepare_signatures(lib)
     return lib
 
 
 def test_unmutated_oracle_passes_battery():
     assert _battery() == []
+    assert _prepare_battery() == []
+
+
+def _mutate(src, old, new):
+    with open(src) as f:
+        text = f.read()
+    assert text.count(old) == 1, f"mutation site {old!r} not unique"
+    return text.replace(old, new)
 
 
 @pytest.mark.parametrize("name", sorted(MUTANTS))
 def test_mutant_is_caught(name, monkeypatch):
-    with open(SRC) as f:
-        text = f.read()
-    old, new = MUTANTS[name]
-    assert text.count(old) == 1, f"mutation site for {name} not unique"
+    text = _mutate(DECODE_SRC, *MUTANTS[name])
     with tempfile.TemporaryDirectory() as tmp:
-        lib = _load_variant(text.replace(old, new), tmp, name)
+        lib = _load_variant(DECODE_SRC, text, tmp, name)
         monkeypatch.setattr(oracle, "_lib", lib)
         failed = _battery()
+    assert failed, f"mutant {name} passed every pin"
+
+
+@pytest.mark.parametrize("name", sorted(PREPARE_MUTANTS))
+def test_prepare_mutant_is_caught(name, monkeypatch):
+    text = _mutate(PREPARE_SRC, *PREPARE_MUTANTS[name])
+    with tempfile.TemporaryDirectory() as tmp:
+        lib = _load_variant(PREPARE_SRC, text, tmp, name)
+        monkeypatch.setattr(oracle, "_lib", lib)
+        failed = _prepare_battery()
     assert failed, f"mutant {name} passed every pin"
