@@ -249,6 +249,80 @@ pd_status paged_decode_noalloc(const pd_plan* plan, const void* q, const void* k
                                const int32_t* block_tables, const int32_t* seq_lens, int32_t window, float scale,
                                void* out, uint32_t* device_flags, void* stream);
 
+/* ---- The step before decode: QKV norm, RoPE, paged-cache write -----------------
+ *
+ * Gemma 4 layers normalise the new token's q, k and v per head and apply RoPE
+ * to q and k with the layer's own parameters (sliding-window and global layers
+ * differ); the normalised, rotated k and the normalised v then go into the
+ * paged cache (Sparse-vLLM PR #27 "feat: support Gemma 4 and native multimodal
+ * inference", sections "Gemma 4 文本推理" and "专用算子与性能优化"; the vLLM
+ * concepts page "模型库与算子层 — 概念" describes folding norm / RoPE into the
+ * paged KV-cache write). One launch does all three for a batch of new tokens.
+ */
+
+/*
+ * Fill a layer's RoPE table: cos_sin[p * rotary_dim + i] = cos(p * f_i) and
+ * cos_sin[p * rotary_dim + rotary_dim/2 + i] = sin(p * f_i), with
+ * f_i = theta^(-2i / rotary_dim), for p < num_positions and i < rotary_dim / 2.
+ * The angles and their sine / cosine are evaluated in fp64 and rounded to fp32.
+ *   theta          RoPE base (> 0, finite)
+ *   rotary_dim     even, 2..512
+ *   num_positions  rows of the table (>= 1)
+ *   cos_sin        device fp32 [num_positions, rotary_dim], caller-owned
+ *   stream         cudaStream_t as void*
+ * Once per layer kind, before the first paged_decode_qkv_norm_rope_write.
+ * Returns PD_ERR_INVALID_ARG for a bad argument, PD_ERR_CUDA if the launch fails.
+ */
+pd_status paged_decode_rope_table(double theta, int32_t rotary_dim, int32_t num_positions, float* cos_sin,
+                                  void* stream);
+
+/*
+ * For every request b, with pos = seq_lens[b] - 1 (the new token's position;
+ * seq_lens counts it, as in decode):
+ *   q_out[b, h]                    = rope(norm(q_in[b, h], q_norm_weight), pos)
+ *   k_pool[page, g, pos % P, :]    = rope(norm(k_in[b, g], k_norm_weight), pos)
+ *   v_pool[page, g, pos % P, :]    = norm(v_in[b, g], v_norm_weight)   (K != V layers)
+ * with page = block_tables[b][pos / P], norm(x, w)_i = x_i / sqrt(mean(x^2) +
+ * eps) * w_i (a model that scales by 1 + w passes 1 + w), and rope turning the
+ * pairs (i, i + rotary_dim/2), i < rotary_dim/2, by the angles of table row
+ * pos: (y_i, y_j) -> (y_i cos - y_j sin, y_j cos + y_i sin); dims past
+ * rotary_dim pass through. Arithmetic in fp32, results rounded once to bf16.
+ *   layer          the decode layer descriptor (bf16 cache only: an FP8 cache
+ *                  keeps one scale per page, which a single appended row
+ *                  cannot set -> PD_ERR_UNSUPPORTED; head_dim 256 or 512)
+ *   batch          requests (0: nothing is launched)
+ *   rotary_dim     even, 0..head_dim (0: no rotation, cos_sin may be NULL)
+ *   num_positions  rows of cos_sin
+ *   eps            >= 0, finite
+ *   q_in           device bf16 [batch, Hq, d]
+ *   k_in, v_in     device bf16 [batch, Hkv, d]; v_in unused (may be NULL) when
+ *                  layer->kv_shared (the cached row is the rotated k)
+ *   q_norm_weight, k_norm_weight  device bf16 [d]
+ *   v_norm_weight  device bf16 [d], or NULL for unit weights
+ *   cos_sin        device fp32 [num_positions, rotary_dim] (paged_decode_rope_table)
+ *   block_tables, seq_lens: as for decode
+ *   q_out          device bf16 [batch, Hq, d] (the decode call's q)
+ *   k_pool, v_pool device bf16 pools [num_pages, Hkv, P, d]; v_pool unused when
+ *                  layer->kv_shared
+ *   device_flags   device uint32 word, caller-owned and zeroed by the caller;
+ *                  PD_DEVFLAG_BAD_SEQLEN is or-ed in (and nothing of that
+ *                  request is written) when seq_lens[b] is outside
+ *                  [1, max_pages * P] or pos >= num_positions while rotating;
+ *                  PD_DEVFLAG_BAD_PAGE (and the cache rows are not written,
+ *                  q_out is) when the page id is outside the pool
+ *   stream         cudaStream_t as void*
+ * q_in / k_in / v_in / q_out / pools must be 16-byte aligned. Only the new
+ * token's rows of the pools are written. Requests must not share a slot.
+ * Returns PD_ERR_INVALID_ARG / PD_ERR_UNSUPPORTED without launching, PD_ERR_CUDA
+ * if the launch fails.
+ */
+pd_status paged_decode_qkv_norm_rope_write(const pd_layer_desc* layer, int32_t batch, int32_t rotary_dim,
+                                           int32_t num_positions, float eps, const void* q_in, const void* k_in,
+                                           const void* v_in, const void* q_norm_weight, const void* k_norm_weight,
+                                           const void* v_norm_weight, const float* cos_sin,
+                                           const int32_t* block_tables, const int32_t* seq_lens, void* q_out,
+                                           void* k_pool, void* v_pool, uint32_t* device_flags, void* stream);
+
 /* Static, human-readable name of a status. */
 const char* paged_decode_status_string(pd_status status);
 

@@ -41,6 +41,8 @@ EXPORTED = (
     "paged_decode_noalloc",
     "paged_decode_global_fp8",
     "paged_decode_window_fp8",
+    "paged_decode_rope_table",
+    "paged_decode_qkv_norm_rope_write",
 )
 
 
@@ -134,6 +136,10 @@ def load_library(path: Optional[str] = None):
         lib.paged_decode_window_fp8.argtypes = [ctypes.POINTER(Plan), vp, vp, vp, vp, vp, vp, vp, i32, f32, vp, u64,
                                                 vp, vp]
         lib.paged_decode_window_fp8.restype = ctypes.c_int
+        lib.paged_decode_rope_table.argtypes = [ctypes.c_double, i32, i32, vp, vp]
+        lib.paged_decode_rope_table.restype = ctypes.c_int
+        lib.paged_decode_qkv_norm_rope_write.argtypes = [ctypes.POINTER(LayerDesc), i32, i32, i32, f32] + [vp] * 14
+        lib.paged_decode_qkv_norm_rope_write.restype = ctypes.c_int
         if path is None:
             _lib = lib
         return lib
@@ -326,3 +332,23 @@ class LayerStep:
 
 def default_scale(head_dim: int) -> float:
     return 1.0 / math.sqrt(head_dim)
+
+
+def paged_decode_rope_table(theta: float, rotary_dim: int, num_positions: int, cos_sin, stream=None) -> None:
+    """Fill cos_sin (fp32 [num_positions, rotary_dim], device) with the layer's RoPE table."""
+    st = load_library().paged_decode_rope_table(float(theta), int(rotary_dim), int(num_positions), _ptr(cos_sin),
+                                                _stream_ptr(stream))
+    _check(st, "paged_decode_rope_table")
+
+
+def paged_decode_qkv_norm_rope_write(desc: LayerDesc, rotary_dim: int, num_positions: int, eps: float, q_in, k_in,
+                                     v_in, q_norm_weight, k_norm_weight, v_norm_weight, cos_sin, block_tables,
+                                     seq_lens, q_out, k_pool, v_pool, device_flags, stream=None) -> None:
+    """QKV norm + RoPE of the new tokens, k / v rows written into the pools, q into q_out."""
+    batch = q_in.shape[0]
+    st = load_library().paged_decode_qkv_norm_rope_write(
+        ctypes.byref(desc), int(batch), int(rotary_dim), int(num_positions), float(eps), _ptr(q_in), _ptr(k_in),
+        _ptr(v_in), _ptr(q_norm_weight), _ptr(k_norm_weight), _ptr(v_norm_weight), _ptr(cos_sin),
+        _ptr(block_tables), _ptr(seq_lens), _ptr(q_out), _ptr(k_pool), _ptr(v_pool), _ptr(device_flags),
+        _stream_ptr(stream))
+    _check(st, "paged_decode_qkv_norm_rope_write")

@@ -142,3 +142,31 @@ def test_no_gpu_calls_fail_cleanly_without_a_device(lib):
     # a host-side argument error is reported before anything touches CUDA
     st = lib.paged_decode_global(ctypes.byref(pl), None, None, None, None, None, 1.0, None, 0, None, None)
     assert st == b.PD_ERR_INVALID_ARG
+
+
+def test_prepare_rejects_bad_arguments_without_launching(lib):
+    """Host checks of the fused norm / RoPE / cache-write entry point (nothing is launched)."""
+    fake = 1 << 20  # an aligned address that is never touched: every call below is refused first
+    desc = b.layer_desc(16, 4, 512, 16, 64, 8, 0, False)
+
+    def call(desc=desc, rot=128, n_pos=128, eps=1e-6, batch=2, q_in=fake, flags=fake):
+        ptrs = [q_in, fake, fake, fake, fake, None, fake, fake, fake, fake, fake, fake, flags, None]
+        return lib.paged_decode_qkv_norm_rope_write(ctypes.byref(desc), batch, rot, n_pos, eps, *ptrs)
+
+    fp8 = b.layer_desc(16, 4, 512, 16, 64, 8, 0, False, b.PD_KV_FP8_E4M3)
+    assert call(desc=fp8) == b.PD_ERR_UNSUPPORTED
+    assert call(desc=b.layer_desc(16, 4, 128, 16, 64, 8, 0, False)) == b.PD_ERR_UNSUPPORTED
+    assert call(desc=b.layer_desc(16, 3, 512, 16, 64, 8, 0, False)) == b.PD_ERR_INVALID_ARG
+    assert call(rot=3) == b.PD_ERR_INVALID_ARG
+    assert call(rot=1024) == b.PD_ERR_INVALID_ARG
+    assert call(eps=-1.0) == b.PD_ERR_INVALID_ARG
+    assert call(eps=float("nan")) == b.PD_ERR_INVALID_ARG
+    assert call(n_pos=0) == b.PD_ERR_INVALID_ARG
+    assert call(batch=-1) == b.PD_ERR_INVALID_ARG
+    assert call(q_in=None) == b.PD_ERR_INVALID_ARG
+    assert call(q_in=fake + 2) == b.PD_ERR_INVALID_ARG
+    assert call(flags=None) == b.PD_ERR_INVALID_ARG
+    assert lib.paged_decode_rope_table(1e4, 63, 10, fake, None) == b.PD_ERR_INVALID_ARG
+    assert lib.paged_decode_rope_table(-1.0, 64, 10, fake, None) == b.PD_ERR_INVALID_ARG
+    assert lib.paged_decode_rope_table(1e4, 64, 0, fake, None) == b.PD_ERR_INVALID_ARG
+    assert lib.paged_decode_rope_table(1e4, 64, 10, None, None) == b.PD_ERR_INVALID_ARG
