@@ -423,11 +423,224 @@ def oracle_baseline(li_cpu, budget_s=10.0):
 
 
 # ----------------------------------------------------------------------------
+# the step before decode: QKV norm + RoPE + paged-cache write (--op prepare)
+# ----------------------------------------------------------------------------
+
+PREP_METRIC = "qkv-norm-rope-cache-write µs/layer-step and HBM GB/s, 1 GPU"
+
+
+def prepare_bytes(pi) -> int:
+    """Algorithmic bytes of one fused call: head rows in and out, the three norm
+    weights, one RoPE table row per request, one block-table entry and one length
+    per request."""
+    li = pi.layer
+    d = li.head_dim
+    weights = d * 2 * (2 + (1 if pi.v_w is not None else 0))
+    return pi.rows_bytes() + weights + li.batch * (pi.rot * 4 + 4 + 4)
+
+
+def run_prepare(args, world, rank, local):
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (the library has no CPU path)")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    pd_build.build()
+    pdb.load_library()
+    if args.kv != "bf16":
+        raise SystemExit("--op prepare writes a bf16 cache")
+    li = workload_layer(args.workload, args.part, dev)
+    pi = synth.make_prepare(li, seed=synth.seed_of(args.workload))
+    desc = pdb.layer_desc(li.num_q_heads, li.num_kv_heads, li.head_dim, li.page_size, li.num_pages,
+                          li.block_tables.shape[1], li.window, li.kv_shared)
+    cos_sin = torch.empty(pi.max_positions, max(2, pi.rot), dtype=torch.float32, device=dev)
+    pdb.paged_decode_rope_table(pi.theta, pi.rot, pi.max_positions, cos_sin)
+    # Each step reads its own copy of the new rows and writes its k / v rows to
+    # a different page (its own block table), so the copies of all steps of a
+    # cycle exceed 4x L2 and every step reaches HBM.
+    per_step = prepare_bytes(pi)
+    replicas = max(1, min(8192, math.ceil(4 * L2_BYTES / per_step)))
+    q_in = pi.q_in.unsqueeze(0).repeat(replicas, 1, 1, 1)
+    k_in = pi.k_in.unsqueeze(0).repeat(replicas, 1, 1, 1)
+    v_in = None if pi.v_in is None else pi.v_in.unsqueeze(0).repeat(replicas, 1, 1, 1)
+    q_out = torch.empty_like(q_in)
+    g = torch.Generator(device="cpu")
+    g.manual_seed(synth.seed_of(args.workload) + 31)
+    perm = torch.randperm(li.num_pages, generator=g).to(torch.int32)
+    tables = li.block_tables.cpu().unsqueeze(0).repeat(replicas, 1, 1)
+    last = ((li.seq_lens.cpu() - 1) // li.page_size).long()
+    for r in range(replicas):
+        tables[r, torch.arange(li.batch), last] = perm[(r * li.batch + torch.arange(li.batch)) % li.num_pages]
+    tables = tables.to(dev)
+    flags = torch.zeros(1, dtype=torch.int32, device=dev)
+    k_pool, v_pool = li.k_pool, li.v_pool
+    stream = torch.cuda.Stream(device=dev)
+
+    def one(i, qi=None, ki=None, vi=None, qo=None, seq=None):
+        r = i % replicas
+        pdb.paged_decode_qkv_norm_rope_write(
+            desc, pi.rot, pi.max_positions, pi.eps, q_in[r] if qi is None else qi, k_in[r] if ki is None else ki,
+            (None if v_in is None else v_in[r]) if vi is None else vi, pi.q_w, pi.k_w, pi.v_w, cos_sin, tables[r],
+            li.seq_lens if seq is None else seq, q_out[r] if qo is None else qo, k_pool, v_pool, flags, stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(max(3, args.warmup)):
+            one(i)
+    torch.cuda.synchronize()
+    if int(flags.item()) != 0:
+        raise SystemExit(f"device flags 0x{int(flags.item()):x}")
+
+    def graphs_of(fn, n):
+        out, left, i0 = [], n, 0
+        while left > 0:
+            m = min(1000, left)
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=stream):
+                for i in range(m):
+                    fn(i0 + i)
+            out.append(gr)
+            left -= m
+            i0 += m
+        return out
+
+    def timed(graphs, sample_clocks=False):
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            graphs[0].replay()
+        torch.cuda.synchronize()
+        barrier(world)
+        sampler = ClockSampler(local) if sample_clocks else None
+        if sampler:
+            sampler.__enter__()
+        with torch.cuda.stream(stream):
+            start.record(stream)
+            for gr in graphs:
+                gr.replay()
+            end.record(stream)
+        torch.cuda.synchronize()
+        if sampler:
+            sampler.__exit__(None, None, None)
+        barrier(world)
+        return start.elapsed_time(end), (sampler.summary() if sampler else None)
+
+    K = args.steps
+    ms, clocks = timed(graphs_of(one, K), sample_clocks=True)
+    ms = max_over_ranks(ms, world)
+    us = ms * 1e3 / K
+    peak, peak_kind = measured_peaks()
+    achieved = per_step / (us * 1e-6) / 1e9
+
+    e2e = None
+    if not args.no_e2e:
+        # host rows in (q, k, v, lengths) through one pinned staging copy; q out back to the host
+        parts = [pi.q_in, pi.k_in] + ([pi.v_in] if pi.v_in is not None else []) + [li.seq_lens]
+        offs, total = [], 0
+        for t in parts:
+            offs.append(total)
+            total += (t.numel() * t.element_size() + 255) // 256 * 256
+        stage_h = torch.zeros(total, dtype=torch.uint8, pin_memory=True)
+        stage_d = torch.empty(total, dtype=torch.uint8, device=dev)
+        views = []
+        for t, o in zip(parts, offs):
+            n = t.numel() * t.element_size()
+            stage_h[o:o + n].view(t.dtype).view(t.shape).copy_(t.cpu())
+            views.append(stage_d[o:o + n].view(t.dtype).view(t.shape))
+        qo_h = torch.empty(pi.q_in.shape, dtype=torch.bfloat16, pin_memory=True)
+        qo_d = torch.empty_like(pi.q_in)
+
+        def e2e_one(i):
+            stage_d.copy_(stage_h, non_blocking=True)
+            one(i, qi=views[0], ki=views[1], vi=views[2] if pi.v_in is not None else None, qo=qo_d, seq=views[-1])
+            qo_h.copy_(qo_d, non_blocking=True)
+
+        with torch.cuda.stream(stream):
+            for i in range(3):
+                e2e_one(i)
+        torch.cuda.synchronize()
+        e_ms, _ = timed(graphs_of(e2e_one, K))
+        e_ms = max_over_ranks(e_ms, world)
+        e2e = {"value": round(e_ms * 1e3 / K, 3), "unit": UNIT, "h2d_bytes_per_step": int(stage_h.numel()),
+               "d2h_bytes_per_step": qo_h.numel() * 2, "steps": K,
+               "launch": "CUDA graph replay of: one H2D copy of the new q / k / v rows + lengths from a pinned "
+                         "staging buffer, the C-ABI call, one D2H copy of q to pinned host memory"}
+    if int(flags.item()) != 0:
+        raise SystemExit(f"device flags 0x{int(flags.item()):x}")
+
+    cpu_baseline = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        pc = synth.make_prepare(li.to("cpu"), seed=synth.seed_of(args.workload))
+        a = [synth.bits_u16(pc.q_in), synth.bits_u16(pc.k_in), None if pc.v_in is None else synth.bits_u16(pc.v_in),
+             synth.bits_u16(pc.q_w), synth.bits_u16(pc.k_w), None if pc.v_w is None else synth.bits_u16(pc.v_w),
+             pc.layer.block_tables.numpy(), pc.layer.seq_lens.numpy(), li.num_pages, li.page_size, pc.rot, pc.theta,
+             pc.eps]
+        times, t_end = [], time.perf_counter() + args.cpu_seconds
+        while True:
+            t0 = time.perf_counter()
+            oracle.prepare_qkv(*a)
+            times.append(time.perf_counter() - t0)
+            if time.perf_counter() > t_end and len(times) >= 3:
+                break
+        cpu_baseline = {"value": round(statistics.median(times) * 1e6, 1), "unit": UNIT, "cores": 1,
+                        "kind": "oracle", "sample": f"full layer-step, median of {len(times)} runs, fp64 C"}
+
+    if rank == 0:
+        line = {
+            "metric": PREP_METRIC, "value": round(us, 3), "unit": UNIT, "n_gpus": world, "steps": K,
+            "warmup": max(3, args.warmup), "ms_per_step": round(us / 1e3, 6), "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "io_dtype": "bf16", "data": "synthetic",
+            "config": {"workload": synth.WORKLOADS[args.workload] + f" [{li.name}], new-token step",
+                       "batch": li.batch, "num_q_heads": li.num_q_heads, "num_kv_heads": li.num_kv_heads,
+                       "head_dim": li.head_dim, "kv_shared": li.kv_shared, "rotary_dim": pi.rot,
+                       "rope_theta": pi.theta,
+                       "l2": f"{replicas} input copies and block tables, {replicas * per_step / 1e6:.0f} MB per "
+                             "cycle (> 4x L2)",
+                       "launch": "CUDA graph replay, one stream"},
+            "roofline": {"bound": "hbm", "kernel": "qkv_norm_rope_write", "achieved": round(achieved, 1),
+                         "peak": peak, "peak_source": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                         "traffic": None, "algorithmic_bytes": per_step, "kernel_us": round(us, 3)},
+            "cpu_baseline": cpu_baseline, "e2e": e2e, "gpu_launches": K, "clocks": clocks,
+            "device": torch.cuda.get_device_name(dev),
+        }
+        print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------
 # reference arm: the oracle on the host cores
 # ----------------------------------------------------------------------------
 
+def run_reference_prepare(args, world):
+    """The oracle of the fused new-token step, full layer-steps on the host."""
+    import oracle
+    li = workload_layer(args.workload, args.part, "cpu")
+    pc = synth.make_prepare(li, seed=synth.seed_of(args.workload))
+    a = [synth.bits_u16(pc.q_in), synth.bits_u16(pc.k_in), None if pc.v_in is None else synth.bits_u16(pc.v_in),
+         synth.bits_u16(pc.q_w), synth.bits_u16(pc.k_w), None if pc.v_w is None else synth.bits_u16(pc.v_w),
+         li.block_tables.numpy(), li.seq_lens.numpy(), li.num_pages, li.page_size, pc.rot, pc.theta, pc.eps]
+    for _ in range(args.warmup):
+        oracle.prepare_qkv(*a)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.prepare_qkv(*a)
+    us = (time.perf_counter() - t0) / max(1, args.steps) * 1e6
+    line = {
+        "impl": "reference", "metric": PREP_METRIC, "value": round(us, 3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(us / 1e3, 6), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": synth.WORKLOADS[args.workload] + f" [{li.name}], new-token step", "batch": li.batch,
+                   "head_dim": li.head_dim},
+        "cpu_baseline": {"value": round(us, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": "full layer-step per step, fp64 C"},
+        "e2e": {"value": round(us, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
 def run_reference(args, world, rank):
     if rank != 0:
+        return
+    if args.op == "prepare":
+        run_reference_prepare(args, world)
         return
     import numpy as np
     import oracle
@@ -488,6 +701,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--kv", default="bf16", choices=["bf16", "fp8"],
                     help="KV-cache element type (fp8: e4m3 with per-(page, KV head) scales)")
+    ap.add_argument("--op", default="decode", choices=["decode", "prepare"],
+                    help="decode: the decode layer-step (default); prepare: the fused QKV norm + RoPE + "
+                         "paged-cache write of the new tokens")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -503,6 +719,8 @@ def main():
     try:
         if args.impl == "reference":
             run_reference(args, world, rank)
+        elif args.op == "prepare":
+            run_prepare(args, world, rank, local)
         else:
             run_ours(args, world, rank, local)
     finally:

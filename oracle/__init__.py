@@ -72,6 +72,8 @@ def _load():
             lib.ref_decode_rows_fp8.restype = i
             lib.ref_e4m3_to_f64.argtypes = [i]
             lib.ref_e4m3_to_f64.restype = d
+            lib.ref_decode_multi.argtypes = [i, i, i, i, i, i, i, i, p, p, p, p, p, i, d, p, p, i]
+            lib.ref_decode_multi.restype = i
             set_prepare_signatures(lib)
             _lib = lib
     return _lib
@@ -175,6 +177,32 @@ def decode_fp8(q, k8, v8, k_scale, v_scale, block_tables, seq_lens, scale: float
     st = lib.ref_decode_rows_fp8(B, Hq, Hkv, d, P, num_pages, max_pages, _ptr(q), _ptr(k8), _ptr(v8),
                                  _ptr(k_scale), _ptr(v_scale), _ptr(block_tables), _ptr(seq_lens), int(window),
                                  float(scale), _ptr(rows_arr), n_rows, _ptr(out), _ptr(lse), int(nthreads))
+    _check(st)
+    return (out, lse) if return_lse else out
+
+
+def decode_multi(q, k_pool, v_pool, block_tables, seq_lens, scale: float, window: int = 0, nthreads: int = 0,
+                 return_lse: bool = False):
+    """T new tokens per request, causal over the paged cache, in fp64.
+
+    q: uint16 [B, T, Hq, d], the last T positions of each request (seq_lens
+    counts them); otherwise as `decode`. Returns float64 [B, T, Hq, d] (and the
+    log-sum-exp [B, T, Hq] if return_lse).
+    """
+    lib = _load()
+    q, k_pool = _u16(q), _u16(k_pool)
+    v_pool = None if v_pool is None else _u16(v_pool)
+    block_tables, seq_lens = _i32(block_tables), _i32(seq_lens)
+    B, T, Hq, d = q.shape
+    num_pages, Hkv, P, d2 = k_pool.shape
+    if d2 != d or (v_pool is not None and v_pool.shape != k_pool.shape):
+        raise ValueError("shapes disagree")
+    max_pages = block_tables.shape[1] if block_tables.ndim == 2 else 0
+    out = np.zeros((B, T, Hq, d), dtype=np.float64)
+    lse = np.full((B, T, Hq), -np.inf, dtype=np.float64)
+    st = lib.ref_decode_multi(B, T, Hq, Hkv, d, P, num_pages, max_pages, _ptr(q), _ptr(k_pool), _ptr(v_pool),
+                              _ptr(block_tables), _ptr(seq_lens), int(window), float(scale), _ptr(out), _ptr(lse),
+                              int(nthreads))
     _check(st)
     return (out, lse) if return_lse else out
 

@@ -137,17 +137,17 @@ static int load_row(const ref_layer *ly, int which, int b, int g, int t, double 
 }
 
 /*
- * Attention of query head h of request b over the token positions [lo, hi):
+ * Attention of query row qrow (query head h of request b) over the token
+ * positions [lo, hi):
  * writes o[0..d) (normalised by the softmax denominator) and returns the
  * natural-log log-sum-exp of the scaled scores through *lse (-inf, o = 0 when
  * the range is empty).
  */
-static int attend_range(const ref_layer *ly, int b, int h, int lo, int hi, double *o, double *lse,
-                        double *s /* scratch, >= hi - lo */, double *row /* scratch, d */) {
+static int attend_range(const ref_layer *ly, int b, int h, const uint16_t *qrow, int lo, int hi, double *o,
+                        double *lse, double *s /* scratch, >= hi - lo */, double *row /* scratch, d */) {
   const int G = ly->Hq / ly->Hkv;
   const int g = h / G;
   const int d = ly->d;
-  const uint16_t *qrow = ly->q + ((size_t)b * ly->Hq + h) * d;
 
   for (int i = 0; i < d; ++i) o[i] = 0.0;
   if (hi <= lo) {
@@ -227,7 +227,7 @@ static int decode_rows(const ref_layer *ly, const int32_t *rows, int n_rows, dou
       int lo, hi;
       attended_range(ly, b, &lo, &hi);
       double lse;
-      int rs = attend_range(ly, b, h, lo, hi, out + (size_t)rix * d, &lse, s, row);
+      int rs = attend_range(ly, b, h, ly->q + (size_t)rix * d, lo, hi, out + (size_t)rix * d, &lse, s, row);
       if (lse_out) lse_out[rix] = lse;
       if (rs != REF_OK) {
 #pragma omp critical
@@ -272,6 +272,65 @@ int ref_decode_rows_fp8(int B, int Hq, int Hkv, int d, int P, int num_pages, int
   return decode_rows(&ly, rows, n_rows, out, lse_out, nthreads);
 }
 
+/*
+ * Several new tokens per request (speculative-decode verification, or a chunk
+ * of prefill, over the paged cache): request b has T query tokens, the last T
+ * of its L_b cached positions, all already in the cache. Query token j sits at
+ * position pos_j = L_b - T + j and attends causally: positions [lo_j, pos_j]
+ * with lo_j = 0 on a global layer and max(0, pos_j + 1 - W) on a window layer
+ * (the last W positions up to and including its own) -- for every j, the
+ * single-token decode of q[b, j] at length pos_j + 1.
+ *   q [B, T, Hq, d] (bf16 bits), out [B, T, Hq, d] fp64, lse_out [B, T, Hq]
+ *   (may be NULL). Returns REF_BAD_LEN if some L_b < T.
+ * Sources: the pages reuse a paged prefill plan next to decode (Sparse-vLLM
+ * PR #27, section "专用算子与性能优化") and list causal multi-token
+ * verification for speculative decoding over a paged cache (vLLM concepts
+ * page, section "MLA 与 Sparse MLA（DSA）").
+ */
+int ref_decode_multi(int B, int T, int Hq, int Hkv, int d, int P, int num_pages, int max_pages, const uint16_t *q,
+                     const uint16_t *k_pool, const uint16_t *v_pool, const int32_t *block_tables,
+                     const int32_t *seq_lens, int window, double scale, double *out, double *lse_out, int nthreads) {
+  ref_layer ly = {B, Hq, Hkv, d, P, num_pages, max_pages, q, k_pool, v_pool,
+                  block_tables, seq_lens, window, scale, 0, NULL, NULL, NULL, NULL};
+  int st = check_layer(&ly);
+  if (st != REF_OK) return st;
+  if (T < 1 || !out) return REF_BAD_ARG;
+  for (int b = 0; b < B; ++b)
+    if (seq_lens[b] < T) return REF_BAD_LEN;
+  const int max_len = max_seq_len(&ly);
+  const int total = B * T * Hq;
+
+  int status = REF_OK;
+  set_threads(nthreads);
+#pragma omp parallel
+  {
+    double *s = (double *)malloc(sizeof(double) * (size_t)(max_len > 0 ? max_len : 1));
+    double *row = (double *)malloc(sizeof(double) * (size_t)d);
+    if (!s || !row) {
+#pragma omp critical
+      status = REF_NO_MEM;
+    }
+#pragma omp for schedule(dynamic, 1)
+    for (int r = 0; r < total; ++r) {
+      if (!s || !row) continue;
+      const int b = r / (T * Hq), j = (r / Hq) % T, h = r % Hq;
+      const int pos = seq_lens[b] - T + j;
+      const int hi = pos + 1;
+      const int lo = (window > 0 && hi > window) ? hi - window : 0;
+      double lse;
+      int rs = attend_range(&ly, b, h, q + (size_t)r * d, lo, hi, out + (size_t)r * d, &lse, s, row);
+      if (lse_out) lse_out[r] = lse;
+      if (rs != REF_OK) {
+#pragma omp critical
+        status = rs;
+      }
+    }
+    free(s);
+    free(row);
+  }
+  return status;
+}
+
 /* e4m3 byte -> fp64 (exposed for the tests that pin the decoder). */
 double ref_e4m3_to_f64(int x) { return e4m3_to_f64((uint8_t)x); }
 
@@ -313,7 +372,8 @@ int ref_decode_split(int B, int Hq, int Hkv, int d, int P, int num_pages, int ma
         if (plo > hi) plo = hi;
         if (phi > hi) phi = hi;
         const size_t idx = (size_t)row * num_splits + k;
-        int rs = attend_range(&ly, b, h, (int)plo, (int)phi, o_part + idx * d, lse_part + idx, s, rowbuf);
+        int rs = attend_range(&ly, b, h, ly.q + ((size_t)b * Hq + h) * d, (int)plo, (int)phi, o_part + idx * d,
+                              lse_part + idx, s, rowbuf);
         if (rs != REF_OK) {
 #pragma omp critical
           status = rs;

@@ -72,6 +72,27 @@ __global__ void __launch_bounds__(32 * kRowsPerCta) qkv_norm_rope_write_kernel(c
   const int r = blockIdx.y * kRowsPerCta + warp;
   if (r >= p.rows) return;
 
+  // The source row and its weight do not depend on the length: their loads
+  // go out first, the length and the page id (which place the result) in
+  // their shadow.
+  const int Hq = p.num_q_heads, Hkv = p.num_kv_heads;
+  const bool is_q = r < Hq, is_k = !is_q && r < Hq + Hkv;
+  const int head = is_q ? r : (is_k ? r - Hq : r - Hq - Hkv);
+  const uint16_t* src = is_q ? p.q_in + ((size_t)b * Hq + head) * D
+                             : (is_k ? p.k_in : p.v_in) + ((size_t)b * Hkv + head) * D;
+  const uint16_t* w = is_q ? p.q_w : (is_k ? p.k_w : p.v_w);
+  float x[NCH][8], wf[NCH][8];
+#pragma unroll
+  for (int c = 0; c < NCH; ++c) {
+    unpack8(__ldg(reinterpret_cast<const uint4*>(src + c * 256 + lane * 8)), x[c]);
+    if (w) {
+      unpack8(__ldg(reinterpret_cast<const uint4*>(w + c * 256 + lane * 8)), wf[c]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) wf[c][i] = 1.f;
+    }
+  }
+
   const int L = p.seq_lens[b];
   const long long cap = (long long)p.max_pages * p.page_size;
   if (L < 1 || L > cap || (p.rot > 0 && L - 1 >= p.num_positions)) {
@@ -79,54 +100,31 @@ __global__ void __launch_bounds__(32 * kRowsPerCta) qkv_norm_rope_write_kernel(c
     return;
   }
   const int pos = L - 1;
-  const int Hq = p.num_q_heads, Hkv = p.num_kv_heads;
-  // which row: q head, k head or v head
-  const uint16_t* src;
-  const uint16_t* w;
   uint16_t* dst;
-  bool rotate;
-  if (r < Hq) {
-    src = p.q_in + ((size_t)b * Hq + r) * D;
-    w = p.q_w;
-    dst = p.q_out + ((size_t)b * Hq + r) * D;
-    rotate = true;
+  if (is_q) {
+    dst = p.q_out + ((size_t)b * Hq + head) * D;
   } else {
-    const bool is_k = r < Hq + Hkv;
-    const int g = is_k ? r - Hq : r - Hq - Hkv;
     const int page = p.block_tables[(size_t)b * p.max_pages + pos / p.page_size];
     if ((unsigned)page >= (unsigned)p.num_pages) {
       if (lane == 0) atomicOr(p.flags, kErrBadPage);
       return;
     }
-    src = (is_k ? p.k_in : p.v_in) + ((size_t)b * Hkv + g) * D;
-    w = is_k ? p.k_w : p.v_w;
-    dst = (is_k ? p.k_pool : p.v_pool) + (((size_t)page * Hkv + g) * p.page_size + pos % p.page_size) * D;
-    rotate = is_k;
+    dst = (is_k ? p.k_pool : p.v_pool) + (((size_t)page * Hkv + head) * p.page_size + pos % p.page_size) * D;
   }
+  const bool rotate = is_q || is_k;  // v is not rotated
 
-  float x[NCH][8];
   float ss = 0.f;
 #pragma unroll
-  for (int c = 0; c < NCH; ++c) {
-    unpack8(__ldg(reinterpret_cast<const uint4*>(src + c * 256 + lane * 8)), x[c]);
+  for (int c = 0; c < NCH; ++c)
 #pragma unroll
     for (int i = 0; i < 8; ++i) ss = fmaf(x[c][i], x[c][i], ss);
-  }
 #pragma unroll
   for (int m = 16; m > 0; m >>= 1) ss += __shfl_xor_sync(kFullMask, ss, m);
   const float inv_rms = 1.f / sqrtf(ss / D + p.eps);
 #pragma unroll
-  for (int c = 0; c < NCH; ++c) {
-    float wf[8];
-    if (w) {
-      unpack8(__ldg(reinterpret_cast<const uint4*>(w + c * 256 + lane * 8)), wf);
-    } else {
+  for (int c = 0; c < NCH; ++c)
 #pragma unroll
-      for (int i = 0; i < 8; ++i) wf[i] = 1.f;
-    }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) x[c][i] = x[c][i] * inv_rms * wf[i];
-  }
+    for (int i = 0; i < 8; ++i) x[c][i] = x[c][i] * inv_rms * wf[c][i];
 
   if (rotate && p.rot > 0) {
     float* y = ybuf[warp];

@@ -20,6 +20,7 @@ import pytest
 
 import oracle
 import test_oracle_pins as pins
+import test_oracle_multi_pins as multi
 import test_oracle_prepare_pins as prep
 
 DECODE_SRC = os.path.join(os.path.dirname(oracle.__file__), "ref_decode.c")
@@ -40,6 +41,10 @@ MUTANTS = {
     "lse_without_log": ("*lse = m + log(l);", "*lse = m;"),
     "split_ignores_range_start": ("long long plo = (long long)lo + (long long)k * chunk;",
                                   "long long plo = (long long)k * chunk;"),
+    "multi_position_off_by_one": ("const int pos = seq_lens[b] - T + j;", "const int pos = seq_lens[b] - T + j - 1;"),
+    "multi_window_from_length": ("const int lo = (window > 0 && hi > window) ? hi - window : 0;",
+                                 "const int lo = (window > 0 && seq_lens[b] > window) ? seq_lens[b] - window : 0;"),
+    "multi_q_row_ignores_token": ("q + (size_t)r * d, lo, hi,", "q + ((size_t)b * T * Hq + h) * d, lo, hi,"),
 }
 
 
@@ -95,6 +100,9 @@ def _battery():
         "e4m3_codes": pins.test_e4m3_decoder_matches_torch_for_every_code,
         "fp8_sdpa": lambda: pins.test_fp8_decode_matches_sdpa_on_dequantized_kv(False, 0),
         "fp8_sdpa_kvshared": lambda: pins.test_fp8_decode_matches_sdpa_on_dequantized_kv(True, 9),
+        "multi_sdpa": lambda: multi.test_multi_matches_library_sdpa_with_causal_mask(8, 4, 5, 3, 2, False),
+        "multi_sdpa_global": lambda: multi.test_multi_matches_library_sdpa_with_causal_mask(8, 2, 0, 4, 16, False),
+        "multi_is_decode": lambda: multi.test_token_j_is_decode_at_its_own_length(7),
     }
     for name, fn in checks.items():
         try:
@@ -121,7 +129,7 @@ def _load_variant(mutated_src, src_text, workdir, tag):
     lib = ctypes.CDLL(path_so)
     ref = oracle._load()
     for fn in ("ref_decode_rows", "ref_decode_split", "ref_merge", "ref_max_threads", "ref_decode_rows_fp8",
-               "ref_e4m3_to_f64"):
+               "ref_e4m3_to_f64", "ref_decode_multi"):
         getattr(lib, fn).argtypes = getattr(ref, fn).argtypes
         getattr(lib, fn).restype = getattr(ref, fn).restype
     oracle.set_prepare_signatures(lib)
