@@ -125,10 +125,11 @@ typedef struct {
   int32_t test_stall_bytes;  /* 0. Tests set it > 0 to make stage 1 expect more bytes per stage
                                 than its copies deliver, so its pipeline waits run out (~1 s) and
                                 report PD_DEVFLAG_WAIT_TIMEOUT without any fault */
-  int32_t reserved[2];
+  int32_t query_tokens;     /* T: query tokens per request (1 = decode; > 1 = paged_decode_plan_multi) */
+  int32_t reserved;
   uint64_t workspace_bytes; /* bytes the caller must provide */
-  uint64_t lse_offset;      /* byte offset of the fp32 [batch, Hq, S] log-sum-exp part */
-  uint64_t opart_offset;    /* byte offset of the fp32 [batch, Hq, S, d] partial outputs */
+  uint64_t lse_offset;      /* byte offset of the fp32 [batch, T, Hq, S] log-sum-exp part */
+  uint64_t opart_offset;    /* byte offset of the fp32 [batch, T, Hq, S, d] partial outputs */
   uint32_t magic;
   uint32_t version;
 } pd_plan;
@@ -149,6 +150,30 @@ typedef struct {
  */
 pd_status paged_decode_plan(const pd_layer_desc* layer, int32_t batch, const int32_t* seq_lens_host,
                             int32_t sm_count, pd_plan* plan);
+
+/*
+ * Plan for several new tokens per request: speculative-decode verification or
+ * a chunk of prefill over the paged cache (Sparse-vLLM PR #27, section
+ * "专用算子与性能优化", reuses a paged prefill plan next to decode; the vLLM
+ * concepts page, section "MLA 与 Sparse MLA（DSA）", lists causal multi-token
+ * verification over a paged cache). Request b's T query tokens are its last T
+ * cached positions (their K/V already written; seq_lens counts them); token j
+ * at position L_b - T + j attends causally: positions up to its own, and on a
+ * window layer only the last `window` of them (its own included) -- for each
+ * token, exactly the decode of that token at length L_b - T + 1 + j.
+ *   query_tokens  T, 1..256 (T = 1 is paged_decode_plan)
+ *   seq_lens_host each in [T, max_pages_per_seq * page_size]
+ *   other arguments as for paged_decode_plan
+ * With such a plan, paged_decode_global / paged_decode_window /
+ * paged_decode_merge / paged_decode_noalloc take q and out as bf16
+ * [batch, T, Hq, d]; a device length below T sets PD_DEVFLAG_BAD_SEQLEN and the
+ * tokens before position 0 attend nothing (zero output). The (token, head)
+ * pairs of one KV head are served 8 per CTA, so for T * group <= 8 every KV
+ * byte is still read once. bf16 caches only (an FP8 layer returns
+ * PD_ERR_UNSUPPORTED); group Hq / Hkv up to 8.
+ */
+pd_status paged_decode_plan_multi(const pd_layer_desc* layer, int32_t batch, int32_t query_tokens,
+                                  const int32_t* seq_lens_host, int32_t sm_count, pd_plan* plan);
 
 /*
  * Stage 1 on a global layer (plan->layer.window == 0): for every (request,

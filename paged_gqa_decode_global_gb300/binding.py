@@ -41,6 +41,7 @@ EXPORTED = (
     "paged_decode_noalloc",
     "paged_decode_global_fp8",
     "paged_decode_window_fp8",
+    "paged_decode_plan_multi",
     "paged_decode_rope_table",
     "paged_decode_qkv_norm_rope_write",
 )
@@ -77,7 +78,8 @@ class Plan(ctypes.Structure):
         ("max_seq_len", ctypes.c_int32),
         ("merge_mode", ctypes.c_int32),
         ("test_stall_bytes", ctypes.c_int32),
-        ("reserved", ctypes.c_int32 * 2),
+        ("query_tokens", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
         ("workspace_bytes", ctypes.c_uint64),
         ("lse_offset", ctypes.c_uint64),
         ("opart_offset", ctypes.c_uint64),
@@ -136,6 +138,8 @@ def load_library(path: Optional[str] = None):
         lib.paged_decode_window_fp8.argtypes = [ctypes.POINTER(Plan), vp, vp, vp, vp, vp, vp, vp, i32, f32, vp, u64,
                                                 vp, vp]
         lib.paged_decode_window_fp8.restype = ctypes.c_int
+        lib.paged_decode_plan_multi.argtypes = [ctypes.POINTER(LayerDesc), i32, i32, vp, i32, ctypes.POINTER(Plan)]
+        lib.paged_decode_plan_multi.restype = ctypes.c_int
         lib.paged_decode_rope_table.argtypes = [ctypes.c_double, i32, i32, vp, vp]
         lib.paged_decode_rope_table.restype = ctypes.c_int
         lib.paged_decode_qkv_norm_rope_write.argtypes = [ctypes.POINTER(LayerDesc), i32, i32, i32, f32] + [vp] * 14
@@ -189,6 +193,20 @@ def paged_decode_plan(desc: LayerDesc, seq_lens_host: Sequence[int], sm_count: i
     st = lib.paged_decode_plan(ctypes.byref(desc), n, ctypes.cast(arr, ctypes.c_void_p) if n else None,
                                int(sm_count), ctypes.byref(plan))
     _check(st, "paged_decode_plan")
+    return plan
+
+
+def paged_decode_plan_multi(desc: LayerDesc, query_tokens: int, seq_lens_host: Sequence[int],
+                            sm_count: int) -> Plan:
+    """Plan for `query_tokens` new tokens per request (q / out [B, T, Hq, d])."""
+    lib = load_library()
+    n = len(seq_lens_host)
+    arr = (ctypes.c_int32 * max(1, n))(*[int(x) for x in seq_lens_host])
+    plan = Plan()
+    st = lib.paged_decode_plan_multi(ctypes.byref(desc), n, int(query_tokens),
+                                     ctypes.cast(arr, ctypes.c_void_p) if n else None, int(sm_count),
+                                     ctypes.byref(plan))
+    _check(st, "paged_decode_plan_multi")
     return plan
 
 

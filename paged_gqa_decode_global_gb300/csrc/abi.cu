@@ -171,6 +171,9 @@ pd_status stage1(const pd_plan* plan, const void* q, const void* k_pool, const v
   p.num_kv_heads = ly.num_kv_heads;
   p.num_splits = plan->num_splits;
   p.chunk_tokens = plan->chunk_tokens;
+  p.query_tokens = plan->query_tokens;
+  p.group = ly.num_q_heads / ly.num_kv_heads;
+  p.col_tiles = plan->grid_y / ly.num_kv_heads;
 
   void* args[] = {&p};
   cudaLaunchConfig_t cfg = {};
@@ -250,8 +253,9 @@ pd_status paged_decode_merge(const pd_plan* plan, const void* workspace, size_t 
   p.out = out;
   p.num_splits = plan->num_splits;
   p.head_dim = plan->layer.head_dim;
-  const int rows = plan->batch * plan->layer.num_q_heads;
-  if (pd::launch_merge(p, rows, stream) != 0) return PD_ERR_CUDA;
+  const long long rows = (long long)plan->batch * plan->query_tokens * plan->layer.num_q_heads;
+  if (rows > 0x7fffffffLL) return PD_ERR_UNSUPPORTED;
+  if (pd::launch_merge(p, (int)rows, stream) != 0) return PD_ERR_CUDA;
   return PD_OK;
 }
 

@@ -16,7 +16,7 @@ struct Stage1Params {
   CUtensorMap kmap;
   CUtensorMap vmap;
   int32_t tma_rank;
-  const uint16_t* q;            // bf16 [B, Hq, D]
+  const uint16_t* q;            // bf16 [B, Hq, D] ([B, T, Hq, D] on multi-token variants)
   const uint16_t* k_pool;       // bf16 [num_pages, Hkv, P, D] (FP8: e4m3 bytes, read only by TMA)
   const uint16_t* v_pool;       // bf16, == k_pool for a K=V layer
   const float* k_scale;         // FP8: [num_pages, Hkv] scale of each (page, KV head) of K
@@ -34,6 +34,10 @@ struct Stage1Params {
   int32_t num_pages, max_pages, page_size;
   int32_t num_q_heads, num_kv_heads;
   int32_t num_splits, chunk_tokens;
+  // multi-token variants: T query tokens per request (q and out [B, T, Hq, D]),
+  // the GQA group at run time, and the CTAs (column tiles of 8 (token, head)
+  // pairs) per KV head: blockIdx.y = KV head * col_tiles + tile
+  int32_t query_tokens, group, col_tiles;
 };
 
 struct MergeParams {

@@ -21,7 +21,10 @@ constexpr uint64_t kWorkspaceHeader = 256;
 //                              head) scales) instead of bf16
 //   NW  consumer warps (+1 producer warp)
 //   SPW ring stages owned by each consumer warp
-template <int D_, int G_, bool KVS_, bool KV8_, int NW_, int SPW_>
+//   MQ  several query tokens per request: the G = 8 MMA columns hold (token,
+//       head) pairs of the request's T x group pairs, token-major, and each
+//       column is masked causally by its own token's position
+template <int D_, int G_, bool KVS_, bool KV8_, int NW_, int SPW_, bool MQ_ = false>
 struct Stage1Cfg {
   static constexpr int D = D_;
   static constexpr int G = G_;
@@ -29,6 +32,7 @@ struct Stage1Cfg {
   static constexpr bool KV8 = KV8_;
   static constexpr int NW = NW_;
   static constexpr int SPW = SPW_;
+  static constexpr bool MQ = MQ_;
   static constexpr int TB = 16;                  // tokens per stage = the MMA's 16-row side
   static constexpr int KSTEPS = D / 16;          // QK k-steps
   static constexpr int MTILES = D / 16;          // PV m-tiles (head dims)
@@ -73,51 +77,57 @@ struct Stage1Cfg {
   static_assert(STAGE_BYTES % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
   static_assert(SCALE_OFFSET % 8 == 0 && ML_OFFSET % 8 == 0, "float2 arrays need 8-byte alignment");
+  static_assert(!MQ || (G == 8 && !KV8), "multi-token variants use all 8 columns, bf16 cache");
 };
 
 // The instances this library is built with, by variant id:
-// X(id, head_dim, group, K=V, FP8, consumer warps, stages per warp).
+// X(id, head_dim, group, K=V, FP8, consumer warps, stages per warp, multi-token).
 // bf16: three consumer warps (the tensor cores leave the CUDA cores mostly
 // idle) plus the producer; rings of 192 KiB: 32 KiB stages x 6 (d512 K!=V),
 // 16 KiB x 12 (d512 K=V, d256 K!=V), 8 KiB x 24 (d256 K=V). FP8: seven
 // consumer warps (two per SM sub-partition hide the latency of widening e4m3
-// fragments to f16) and rings of 196-224 KiB.
-#define PD_FOR_EACH_VARIANT(X)        \
-  X(0, 512, 1, false, false, 3, 2)    \
-  X(1, 512, 2, false, false, 3, 2)    \
-  X(2, 512, 4, false, false, 3, 2)    \
-  X(3, 512, 8, false, false, 3, 2)    \
-  X(4, 512, 1, true, false, 3, 4)     \
-  X(5, 512, 2, true, false, 3, 4)     \
-  X(6, 512, 4, true, false, 3, 4)     \
-  X(7, 512, 8, true, false, 3, 4)     \
-  X(8, 256, 1, false, false, 3, 4)    \
-  X(9, 256, 2, false, false, 3, 4)    \
-  X(10, 256, 4, false, false, 3, 4)   \
-  X(11, 256, 8, false, false, 3, 4)   \
-  X(12, 256, 1, true, false, 3, 8)    \
-  X(13, 256, 2, true, false, 3, 8)    \
-  X(14, 256, 4, true, false, 3, 8)    \
-  X(15, 256, 8, true, false, 3, 8)    \
-  X(16, 512, 1, false, true, 7, 2)  \
-  X(17, 512, 2, false, true, 7, 2)  \
-  X(18, 512, 4, false, true, 7, 2)  \
-  X(19, 512, 8, false, true, 7, 2)  \
-  X(20, 512, 1, true, true, 7, 4)   \
-  X(21, 512, 2, true, true, 7, 4)   \
-  X(22, 512, 4, true, true, 7, 4)   \
-  X(23, 512, 8, true, true, 7, 4)   \
-  X(24, 256, 1, false, true, 7, 4)  \
-  X(25, 256, 2, false, true, 7, 4)  \
-  X(26, 256, 4, false, true, 7, 4)  \
-  X(27, 256, 8, false, true, 7, 4)  \
-  X(28, 256, 1, true, true, 7, 7)   \
-  X(29, 256, 2, true, true, 7, 7)   \
-  X(30, 256, 4, true, true, 7, 7)   \
-  X(31, 256, 8, true, true, 7, 7)
+// fragments to f16) and rings of 196-224 KiB. Multi-token (ids 32-35): the
+// group-8 geometry, any group <= 8 at run time.
+#define PD_FOR_EACH_VARIANT(X)             \
+  X(0, 512, 1, false, false, 3, 2, false)  \
+  X(1, 512, 2, false, false, 3, 2, false)  \
+  X(2, 512, 4, false, false, 3, 2, false)  \
+  X(3, 512, 8, false, false, 3, 2, false)  \
+  X(4, 512, 1, true, false, 3, 4, false)   \
+  X(5, 512, 2, true, false, 3, 4, false)   \
+  X(6, 512, 4, true, false, 3, 4, false)   \
+  X(7, 512, 8, true, false, 3, 4, false)   \
+  X(8, 256, 1, false, false, 3, 4, false)  \
+  X(9, 256, 2, false, false, 3, 4, false)  \
+  X(10, 256, 4, false, false, 3, 4, false) \
+  X(11, 256, 8, false, false, 3, 4, false) \
+  X(12, 256, 1, true, false, 3, 8, false)  \
+  X(13, 256, 2, true, false, 3, 8, false)  \
+  X(14, 256, 4, true, false, 3, 8, false)  \
+  X(15, 256, 8, true, false, 3, 8, false)  \
+  X(16, 512, 1, false, true, 7, 2, false)  \
+  X(17, 512, 2, false, true, 7, 2, false)  \
+  X(18, 512, 4, false, true, 7, 2, false)  \
+  X(19, 512, 8, false, true, 7, 2, false)  \
+  X(20, 512, 1, true, true, 7, 4, false)   \
+  X(21, 512, 2, true, true, 7, 4, false)   \
+  X(22, 512, 4, true, true, 7, 4, false)   \
+  X(23, 512, 8, true, true, 7, 4, false)   \
+  X(24, 256, 1, false, true, 7, 4, false)  \
+  X(25, 256, 2, false, true, 7, 4, false)  \
+  X(26, 256, 4, false, true, 7, 4, false)  \
+  X(27, 256, 8, false, true, 7, 4, false)  \
+  X(28, 256, 1, true, true, 7, 7, false)   \
+  X(29, 256, 2, true, true, 7, 7, false)   \
+  X(30, 256, 4, true, true, 7, 7, false)   \
+  X(31, 256, 8, true, true, 7, 7, false)   \
+  X(32, 512, 8, false, false, 3, 2, true)  \
+  X(33, 512, 8, true, false, 3, 4, true)   \
+  X(34, 256, 8, false, false, 3, 4, true)  \
+  X(35, 256, 8, true, false, 3, 8, true)
 
 struct VariantInfo {
-  int id, head_dim, group, kv_shared, kv_fp8, nw, spw, block_tokens, threads, smem_bytes, max_cluster;
+  int id, head_dim, group, kv_shared, kv_fp8, nw, spw, block_tokens, threads, smem_bytes, max_cluster, multi;
 };
 
 // Host-visible table, defined in plan.cu.

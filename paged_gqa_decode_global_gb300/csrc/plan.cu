@@ -18,10 +18,10 @@
 
 namespace pd {
 
-#define PD_VARIANT_ROW(ID, D, G, KVS, KV8, NW, SPW)                                                  \
-  VariantInfo{ID, D, G, KVS ? 1 : 0, KV8 ? 1 : 0, NW, SPW, Stage1Cfg<D, G, KVS, KV8, NW, SPW>::TB,      \
-              Stage1Cfg<D, G, KVS, KV8, NW, SPW>::THREADS, Stage1Cfg<D, G, KVS, KV8, NW, SPW>::SMEM_BYTES, \
-              Stage1Cfg<D, G, KVS, KV8, NW, SPW>::MAX_CLUSTER},
+#define PD_VARIANT_ROW(ID, D, G, KVS, KV8, NW, SPW, MQ)                                                    \
+  VariantInfo{ID, D, G, KVS ? 1 : 0, KV8 ? 1 : 0, NW, SPW, Stage1Cfg<D, G, KVS, KV8, NW, SPW, MQ>::TB,      \
+              Stage1Cfg<D, G, KVS, KV8, NW, SPW, MQ>::THREADS, Stage1Cfg<D, G, KVS, KV8, NW, SPW, MQ>::SMEM_BYTES, \
+              Stage1Cfg<D, G, KVS, KV8, NW, SPW, MQ>::MAX_CLUSTER, MQ ? 1 : 0},
 const VariantInfo kVariants[] = {PD_FOR_EACH_VARIANT(PD_VARIANT_ROW)};
 #undef PD_VARIANT_ROW
 const int kNumVariants = sizeof(kVariants) / sizeof(kVariants[0]);
@@ -31,18 +31,28 @@ const int kNumVariants = sizeof(kVariants) / sizeof(kVariants[0]);
 namespace {
 
 constexpr uint32_t kPlanMagic = 0x50444543u;  // "PDEC"
-constexpr int32_t kAbiVersion = 3;
+constexpr int32_t kAbiVersion = 4;
 // Pieces per (request, KV head) are capped (the merge stages their weights in
 // shared memory).
 constexpr int kMaxSplits = 1024;
 
-const pd::VariantInfo* find_variant(int head_dim, int group, int kv_shared, int kv_fp8) {
+// Query tokens per request a plan may carry (multi-token variants).
+constexpr int kMaxQueryTokens = 256;
+
+// Decode (one query token): the instance of exactly this group. Several query
+// tokens: the multi-token instance (8 columns of (token, head) pairs), which
+// serves any group up to 8.
+const pd::VariantInfo* find_variant(int head_dim, int group, int kv_shared, int kv_fp8, int multi) {
   for (int i = 0; i < pd::kNumVariants; ++i) {
     const pd::VariantInfo& v = pd::kVariants[i];
-    if (v.head_dim == head_dim && v.group == group && v.kv_shared == kv_shared && v.kv_fp8 == kv_fp8) return &v;
+    if (v.head_dim != head_dim || v.kv_shared != kv_shared || v.kv_fp8 != kv_fp8 || v.multi != multi) continue;
+    if (multi ? group <= v.group : v.group == group) return &v;
   }
   return nullptr;
 }
+
+// Column tiles (CTAs per KV head and piece) of a multi-token plan.
+int col_tiles(int query_tokens, int group) { return (query_tokens * group + 7) / 8; }
 
 uint64_t align_up(uint64_t x, uint64_t a) { return (x + a - 1) / a * a; }
 
@@ -144,7 +154,14 @@ const char* paged_decode_status_string(pd_status status) {
 
 pd_status paged_decode_plan(const pd_layer_desc* layer, int32_t batch, const int32_t* seq_lens_host,
                             int32_t sm_count, pd_plan* plan) {
+  return paged_decode_plan_multi(layer, batch, 1, seq_lens_host, sm_count, plan);
+}
+
+pd_status paged_decode_plan_multi(const pd_layer_desc* layer, int32_t batch, int32_t query_tokens,
+                                  const int32_t* seq_lens_host, int32_t sm_count, pd_plan* plan) {
   if (!layer || !plan) return PD_ERR_INVALID_ARG;
+  if (query_tokens < 1 || query_tokens > kMaxQueryTokens) return PD_ERR_INVALID_ARG;
+  const int T = query_tokens;
   const pd_layer_desc& ly = *layer;
   if (ly.num_q_heads <= 0 || ly.num_kv_heads <= 0 || ly.num_q_heads % ly.num_kv_heads != 0)
     return PD_ERR_INVALID_ARG;
@@ -160,21 +177,28 @@ pd_status paged_decode_plan(const pd_layer_desc* layer, int32_t batch, const int
   if ((long long)ly.num_pages * ly.num_kv_heads * ly.page_size > 0x7fffffffLL) return PD_ERR_UNSUPPORTED;
   int32_t max_len = 0;
   for (int b = 0; b < batch; ++b) {
-    if (seq_lens_host[b] < 0 || seq_lens_host[b] > cap) return PD_ERR_INVALID_ARG;
+    if (seq_lens_host[b] < (T > 1 ? T : 0) || seq_lens_host[b] > cap) return PD_ERR_INVALID_ARG;
     max_len = std::max(max_len, seq_lens_host[b]);
   }
   const int group = ly.num_q_heads / ly.num_kv_heads;
-  const pd::VariantInfo* v = find_variant(ly.head_dim, group, ly.kv_shared, ly.kv_dtype == PD_KV_FP8_E4M3);
+  const pd::VariantInfo* v =
+      find_variant(ly.head_dim, group, ly.kv_shared, ly.kv_dtype == PD_KV_FP8_E4M3, T > 1 ? 1 : 0);
   if (!v) return PD_ERR_UNSUPPORTED;
   const int TB = v->block_tokens;
+  // CTAs per (piece, KV head): one, or the column tiles of a multi-token plan
+  const int tiles = T > 1 ? col_tiles(T, group) : 1;
+  if ((long long)ly.num_kv_heads * tiles > 65535) return PD_ERR_UNSUPPORTED;
+  const int hkv_ctas = ly.num_kv_heads * tiles;
 
-  // block-aligned attended span of each request
+  // block-aligned attended span of each request (several query tokens: the
+  // union of their ranges, from the first token's window start)
   std::vector<int> n_tok(batch);
   int max_n = 0;
   long long total = 0;
   for (int b = 0; b < batch; ++b) {
     const int L = seq_lens_host[b];
-    const int lo = (ly.window > 0 && L > ly.window) ? L - ly.window : 0;
+    const int first_hi = L - T + 1;
+    const int lo = (ly.window > 0 && first_hi > ly.window) ? first_hi - ly.window : 0;
     n_tok[b] = L > 0 ? L - (lo / TB) * TB : 0;
     max_n = std::max(max_n, n_tok[b]);
     total += n_tok[b];
@@ -198,7 +222,7 @@ pd_status paged_decode_plan(const pd_layer_desc* layer, int32_t batch, const int
   if (max_n > 0) {
     // candidates: multiples of 16 on a geometric grid, from the point where the
     // launch would need more than ~8 waves up to one piece per request
-    const long long work = total * ly.num_kv_heads;
+    const long long work = total * hkv_ctas;
     const int c_min = (int)std::max<long long>(64, align_up((uint64_t)(work / (8LL * cm.slots) + 1), 16));
     const int c_max = (int)align_up((uint64_t)max_n, 16);
     std::vector<int> cands;
@@ -206,7 +230,7 @@ pd_status paged_decode_plan(const pd_layer_desc* layer, int32_t batch, const int
     for (int w = 1; w <= 8; ++w) {
       // pieces sized so B * Hkv * S lands on exactly w waves for the longest request
       const long long per_wave = (long long)w * cm.slots;
-      const long long pairs = (long long)batch * ly.num_kv_heads;
+      const long long pairs = (long long)batch * hkv_ctas;
       const long long s = std::max<long long>(1, per_wave / std::max<long long>(1, pairs));
       cands.push_back((int)align_up((uint64_t)((max_n + s - 1) / s), 16));
     }
@@ -218,11 +242,11 @@ pd_status paged_decode_plan(const pd_layer_desc* layer, int32_t batch, const int
       if (c < 16) continue;
       const int s = (max_n + c - 1) / c;
       if (s > kMaxSplits) continue;
-      const uint64_t merge_bytes = (uint64_t)batch * ly.num_q_heads * s * (ly.head_dim + 1) * 4ull * 2ull;
-      double cost = simulate(n_tok, ly.num_kv_heads, c, s, cm, merge_bytes);
+      const uint64_t merge_bytes = (uint64_t)batch * T * ly.num_q_heads * s * (ly.head_dim + 1) * 4ull * 2ull;
+      double cost = simulate(n_tok, hkv_ctas, c, s, cm, merge_bytes);
       bool cluster = false;
       if (s >= 2 && s <= std::min(kMaxClusterSplits, v->max_cluster)) {
-        const double cc = simulate_clusters(n_tok, ly.num_kv_heads, c, s, cm, kAssumedGpcs);
+        const double cc = simulate_clusters(n_tok, hkv_ctas, c, s, cm, kAssumedGpcs);
         if (cc < cost) {
           cost = cc;
           cluster = true;
@@ -245,13 +269,14 @@ pd_status paged_decode_plan(const pd_layer_desc* layer, int32_t batch, const int
   plan->block_tokens = TB;
   plan->variant = v->id;
   plan->grid_x = best_splits;
-  plan->grid_y = ly.num_kv_heads;
+  plan->grid_y = hkv_ctas;
+  plan->query_tokens = T;
   plan->grid_z = batch;
   plan->threads_per_cta = v->threads;
   plan->smem_bytes = v->smem_bytes;
   plan->sm_count = sm_count;
   plan->max_seq_len = max_len;
-  const uint64_t rows = (uint64_t)batch * ly.num_q_heads;
+  const uint64_t rows = (uint64_t)batch * T * ly.num_q_heads;
   if (best_splits > 1 && best_cluster) {
     // merged inside each cluster: the workspace holds only the error word
     plan->merge_mode = 2;
@@ -283,7 +308,14 @@ bool plan_is_valid(const pd_plan* plan) {
   if (plan->variant < 0 || plan->variant >= kNumVariants) return false;
   const VariantInfo& v = kVariants[plan->variant];
   const pd_layer_desc& ly = plan->layer;
-  if (ly.num_kv_heads <= 0 || ly.num_q_heads != ly.num_kv_heads * v.group) return false;
+  if (ly.num_kv_heads <= 0 || ly.num_q_heads % ly.num_kv_heads != 0) return false;
+  const int group = ly.num_q_heads / ly.num_kv_heads;
+  if (v.multi) {
+    if (group > v.group || plan->query_tokens < 2 || plan->query_tokens > kMaxQueryTokens) return false;
+    if (plan->grid_y != ly.num_kv_heads * col_tiles(plan->query_tokens, group)) return false;
+  } else {
+    if (group != v.group || plan->query_tokens != 1 || plan->grid_y != ly.num_kv_heads) return false;
+  }
   if (ly.head_dim != v.head_dim || ly.kv_shared != v.kv_shared) return false;
   if ((ly.kv_dtype == PD_KV_FP8_E4M3) != (v.kv_fp8 == 1)) return false;
   if (plan->num_splits < 1 || plan->chunk_tokens < 16 || plan->chunk_tokens % 16 != 0) return false;

@@ -115,6 +115,43 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 
 }  // namespace
 
+// The query rows behind the 8 MMA columns of a CTA. Decode variants: column c
+// is query head g*G + c of request b. Multi-token variants: column c is pair
+// tile*8 + c of the request's T x group (token, head) pairs, token-major, i.e.
+// token j = pair / group, head g*group + pair % group, row (b*T + j)*Hq + head
+// of q and out; pairs past T x group are unused columns.
+template <class C>
+struct ColMap {
+  int b, g, tile, T, group, Hq;
+  __device__ __forceinline__ ColMap(const Stage1Params& p) {
+    b = blockIdx.z;
+    Hq = p.num_q_heads;
+    if constexpr (C::MQ) {
+      g = blockIdx.y / p.col_tiles;
+      tile = blockIdx.y % p.col_tiles;
+      T = p.query_tokens;
+      group = p.group;
+    } else {
+      g = blockIdx.y;
+      tile = 0;
+      T = 1;
+      group = C::G;
+    }
+  }
+  __device__ __forceinline__ bool valid(int c) const {
+    return C::MQ ? (c < C::G && tile * C::G + c < T * group) : c < C::G;
+  }
+  __device__ __forceinline__ int token(int c) const { return C::MQ ? (tile * C::G + c) / group : 0; }
+  __device__ __forceinline__ size_t row(int c) const {
+    if constexpr (C::MQ) {
+      const int pr = tile * C::G + c;
+      return ((size_t)b * T + pr / group) * Hq + (size_t)g * group + pr % group;
+    } else {
+      return (size_t)b * Hq + (size_t)g * C::G + c;
+    }
+  }
+};
+
 // One CTA's piece: stream, attend, merge the warps, and leave the piece's result
 // in `out` (one piece), in the workspace (pieces merged by a later launch) or in
 // this CTA's shared memory (pieces merged across the cluster). Threads return
@@ -127,9 +164,10 @@ __device__ __forceinline__ void stage1_cta(const Stage1Params& p, uint8_t* smem)
   float2* stage_scale = reinterpret_cast<float2*>(smem + C::SCALE_OFFSET);  // FP8: (K, V) scale per stage
   float2* warp_ml = reinterpret_cast<float2*>(smem + C::ML_OFFSET);
 
+  const ColMap<C> cm(p);
   const int split = blockIdx.x;
-  const int g = blockIdx.y;
-  const int b = blockIdx.z;
+  const int g = cm.g;
+  const int b = cm.b;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
@@ -144,35 +182,49 @@ __device__ __forceinline__ void stage1_cta(const Stage1Params& p, uint8_t* smem)
     if (t < cap) page_spec = __ldg(table + t / p.page_size);
   }
   int L = p.seq_lens[b];
-  if (L < 0 || L > cap) {
+  if (L < 0 || L > cap || (C::MQ && L < cm.T)) {
     if (threadIdx.x == 0) atomicOr(p.err, kErrBadSeqLen);
-    L = L < 0 ? 0 : cap;
+    L = L < 0 ? 0 : (L > cap ? cap : L);
   }
-  const int lo = (p.window > 0 && L > p.window) ? L - p.window : 0;
+  // attended range [lo, hi) of this CTA's query rows: decode, the last W (or
+  // all) positions; multi-token, the union of its tokens' causal ranges, token
+  // j ending at its own position L - T + j (inclusive)
+  int hi = L, lo;
+  if constexpr (C::MQ) {
+    const int j_first = cm.token(0);
+    int j_last = cm.token(C::G - 1);
+    if (j_last > cm.T - 1) j_last = cm.T - 1;
+    hi = L - cm.T + j_last + 1;
+    if (hi < 0) hi = 0;
+    const int first_hi = L - cm.T + j_first + 1;
+    lo = (p.window > 0 && first_hi > p.window) ? first_hi - p.window : 0;
+  } else {
+    lo = (p.window > 0 && L > p.window) ? L - p.window : 0;
+  }
   const int base = (lo / C::TB) * C::TB;
   const long long piece_lo = (long long)base + (long long)split * p.chunk_tokens;
   const int tlo = (int)(piece_lo > lo ? piece_lo : lo);
   // the last piece takes whatever remains, so a device length longer than the
   // planned one is still attended in full
-  const long long piece_hi = (split == p.num_splits - 1) ? (long long)L : piece_lo + p.chunk_tokens;
-  const int thi = (int)(piece_hi < L ? piece_hi : L);
+  const long long piece_hi = (split == p.num_splits - 1) ? (long long)hi : piece_lo + p.chunk_tokens;
+  const int thi = (int)(piece_hi < hi ? piece_hi : hi);
   const int blk_lo = (tlo / C::TB) * C::TB;
   const int nblk = (thi > tlo) ? (thi - blk_lo + C::TB - 1) / C::TB : 0;
-
-  const size_t row_hq = (size_t)b * p.num_q_heads + (size_t)g * C::G;  // first query head row
 
   if (nblk == 0) {
     // nothing attended in this piece
     if (p.cluster_merge) {
       if (threadIdx.x < C::G) reinterpret_cast<float*>(smem + C::CTA_LSE_OFFSET)[threadIdx.x] = -INFINITY;
     } else if (p.num_splits == 1) {
-      __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out) + row_hq * C::D;
-      for (int i = threadIdx.x; i < C::G * C::D; i += C::THREADS) o[i] = __float2bfloat16_rn(0.f);
+      for (int i = threadIdx.x; i < C::G * C::D; i += C::THREADS)
+        if (cm.valid(i / C::D))
+          reinterpret_cast<__nv_bfloat16*>(p.out)[cm.row(i / C::D) * C::D + i % C::D] = __float2bfloat16_rn(0.f);
     } else {
       // weight 0 and a zero partial row, so the merge needs no special case
       for (int i = threadIdx.x; i < C::G * C::D; i += C::THREADS)
-        p.o_part[((row_hq + i / C::D) * p.num_splits + split) * C::D + i % C::D] = 0.f;
-      if (threadIdx.x < C::G) p.lse_part[(row_hq + threadIdx.x) * p.num_splits + split] = -INFINITY;
+        if (cm.valid(i / C::D)) p.o_part[(cm.row(i / C::D) * p.num_splits + split) * C::D + i % C::D] = 0.f;
+      if (threadIdx.x < C::G && cm.valid(threadIdx.x))
+        p.lse_part[cm.row(threadIdx.x) * p.num_splits + split] = -INFINITY;
     }
     return;
   }
@@ -191,15 +243,15 @@ __device__ __forceinline__ void stage1_cta(const Stage1Params& p, uint8_t* smem)
   } else {
 #pragma unroll
     for (int ks = 0; ks < C::KSTEPS; ++ks) {
-      if (qh < C::G) {
+      if (cm.valid(qh)) {
         if constexpr (C::KV8) {
           // dims in the FP8 QK order (see the consumer loop); the products run
           // in f16, so q rounds to f16 once here
-          const uint2 x = __ldg(reinterpret_cast<const uint2*>(p.q + (row_hq + qh) * C::D + kv8_qk_dim(ks, lane)));
+          const uint2 x = __ldg(reinterpret_cast<const uint2*>(p.q + cm.row(qh) * C::D + kv8_qk_dim(ks, lane)));
           qb[ks][0] = pack_f16x2(__uint_as_float(x.x << 16), __uint_as_float(x.x & 0xffff0000u));
           qb[ks][1] = pack_f16x2(__uint_as_float(x.y << 16), __uint_as_float(x.y & 0xffff0000u));
         } else {
-          const uint16_t* qrow = p.q + (row_hq + qh) * C::D + ks * 16 + qk;
+          const uint16_t* qrow = p.q + cm.row(qh) * C::D + ks * 16 + qk;
           qb[ks][0] = __ldg(reinterpret_cast<const unsigned int*>(qrow));
           qb[ks][1] = __ldg(reinterpret_cast<const unsigned int*>(qrow + 8));
         }
@@ -322,6 +374,19 @@ __device__ __forceinline__ void stage1_cta(const Stage1Params& p, uint8_t* smem)
 #pragma unroll
     for (int i = 0; i < 4; ++i) acc[mt][i] = 0.f;
 
+  // multi-token: the causal range [col_lo, col_hi) of this lane's two columns
+  int col_lo[2] = {0, 0}, col_hi[2] = {0, 0};
+  if constexpr (C::MQ) {
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc) {
+      const int c = (lane & 3) * 2 + cc;
+      if (cm.valid(c)) {
+        col_hi[cc] = L - cm.T + cm.token(c) + 1;
+        col_lo[cc] = (p.window > 0 && col_hi[cc] > p.window) ? col_hi[cc] - p.window : 0;
+      }
+    }
+  }
+
   // this lane's two heads and their running max / sum (base-2 logits)
   float m_run[2] = {-INFINITY, -INFINITY};
   float l_run[2] = {0.f, 0.f};
@@ -409,8 +474,16 @@ __device__ __forceinline__ void stage1_cta(const Stage1Params& p, uint8_t* smem)
     const int ta = t0 + qh;
     const bool va = stage_ok && ta >= tlo && ta < thi;
     const bool vb = stage_ok && ta + 8 >= tlo && ta + 8 < thi;
-    if (!va) s[0] = s[1] = -INFINITY;
-    if (!vb) s[2] = s[3] = -INFINITY;
+    if constexpr (C::MQ) {
+      // each column is also cut at its own token's causal range
+      if (!(va && ta >= col_lo[0] && ta < col_hi[0])) s[0] = -INFINITY;
+      if (!(va && ta >= col_lo[1] && ta < col_hi[1])) s[1] = -INFINITY;
+      if (!(vb && ta + 8 >= col_lo[0] && ta + 8 < col_hi[0])) s[2] = -INFINITY;
+      if (!(vb && ta + 8 >= col_lo[1] && ta + 8 < col_hi[1])) s[3] = -INFINITY;
+    } else {
+      if (!va) s[0] = s[1] = -INFINITY;
+      if (!vb) s[2] = s[3] = -INFINITY;
+    }
 
     // online softmax: max and sum over the block's 16 tokens (lane/4 and the two rows)
     float bm0 = fmaxf(s[0], s[2]), bm1 = fmaxf(s[1], s[3]);
@@ -588,6 +661,7 @@ __device__ __forceinline__ void stage1_cta(const Stage1Params& p, uint8_t* smem)
   for (int e = tid; e < C::G * D4; e += C::NW * 32) {
     const int h = e / D4;
     const int d4 = e % D4;
+    if (C::MQ && !cm.valid(h)) continue;
     float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int w = 0; w < C::NW; ++w) {
@@ -600,7 +674,7 @@ __device__ __forceinline__ void stage1_cta(const Stage1Params& p, uint8_t* smem)
     }
     if (p.num_splits == 1) {
       __nv_bfloat162* dst =
-          reinterpret_cast<__nv_bfloat162*>(reinterpret_cast<__nv_bfloat16*>(p.out) + (row_hq + h) * C::D) + d4 * 2;
+          reinterpret_cast<__nv_bfloat162*>(reinterpret_cast<__nv_bfloat16*>(p.out) + cm.row(h) * C::D) + d4 * 2;
       uint2 packed;
       packed.x = pack_bf16x2(o.x, o.y);
       packed.y = pack_bf16x2(o.z, o.w);
@@ -610,7 +684,7 @@ __device__ __forceinline__ void stage1_cta(const Stage1Params& p, uint8_t* smem)
       reinterpret_cast<float4*>(smem + C::CTA_OUT_OFFSET)[h * D4 + d4] = o;
       if (d4 == 0) reinterpret_cast<float*>(smem + C::CTA_LSE_OFFSET)[h] = coef[C::NW * C::G + h];
     } else {
-      const size_t prow = (row_hq + h) * p.num_splits + split;
+      const size_t prow = cm.row(h) * p.num_splits + split;
       reinterpret_cast<float4*>(p.o_part + prow * C::D)[d4] = o;
       if (d4 == 0) p.lse_part[prow] = coef[C::NW * C::G + h];
     }
@@ -669,10 +743,11 @@ __device__ __forceinline__ void cluster_merge(const Stage1Params& p, uint8_t* sm
       if (r < S) wts[r * C::G + tid] = l[r] * inv;
   }
   __syncthreads();
-  const size_t row_hq = (size_t)blockIdx.z * p.num_q_heads + (size_t)blockIdx.y * C::G;
+  const ColMap<C> cm(p);
 #pragma unroll 2
   for (int e = tid; e < C::G * D4; e += C::THREADS) {
     const int h = e / D4;
+    if (C::MQ && !cm.valid(h)) continue;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int r = 0; r < C::MAX_CLUSTER; ++r) {
@@ -688,8 +763,7 @@ __device__ __forceinline__ void cluster_merge(const Stage1Params& p, uint8_t* sm
     uint2 packed;
     packed.x = pack_bf16x2(acc.x, acc.y);
     packed.y = pack_bf16x2(acc.z, acc.w);
-    *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.out) + (row_hq + h) * C::D + (e % D4) * 4) =
-        packed;
+    *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.out) + cm.row(h) * C::D + (e % D4) * 4) = packed;
   }
 }
 
@@ -704,16 +778,16 @@ __global__ void __launch_bounds__(C::THREADS, 1) stage1_kernel(const __grid_cons
 
 // ---- instantiation and dispatch -------------------------------------------------
 
-#define PD_STAGE1_INSTANCE(ID, D, G, KVS, KV8, NW, SPW) \
-  template __global__ void stage1_kernel<Stage1Cfg<D, G, KVS, KV8, NW, SPW>>(const __grid_constant__ Stage1Params);
+#define PD_STAGE1_INSTANCE(ID, D, G, KVS, KV8, NW, SPW, MQ) \
+  template __global__ void stage1_kernel<Stage1Cfg<D, G, KVS, KV8, NW, SPW, MQ>>(const __grid_constant__ Stage1Params);
 PD_FOR_EACH_VARIANT(PD_STAGE1_INSTANCE)
 #undef PD_STAGE1_INSTANCE
 
 const void* stage1_kernel_ptr(int variant) {
   switch (variant) {
-#define PD_STAGE1_CASE(ID, D, G, KVS, KV8, NW, SPW) \
-  case ID:                                          \
-    return reinterpret_cast<const void*>(&stage1_kernel<Stage1Cfg<D, G, KVS, KV8, NW, SPW>>);
+#define PD_STAGE1_CASE(ID, D, G, KVS, KV8, NW, SPW, MQ) \
+  case ID:                                              \
+    return reinterpret_cast<const void*>(&stage1_kernel<Stage1Cfg<D, G, KVS, KV8, NW, SPW, MQ>>);
     PD_FOR_EACH_VARIANT(PD_STAGE1_CASE)
 #undef PD_STAGE1_CASE
     default:
