@@ -39,6 +39,7 @@ from paged_gqa_decode_global_gb300 import build as pd_build  # noqa: E402
 from paged_gqa_decode_global_gb300 import inputs as synth  # noqa: E402
 
 METRIC = "decode-attn µs/layer-step and KV HBM GB/s (% of GB300 peak), 1 GPU"
+MULTI_METRIC = "{T}-token-per-request (verification) attn µs/layer-step and KV HBM GB/s, 1 GPU"
 UNIT = "us/layer-step"
 L2_BYTES = 129 * 1000 * 1000
 FALLBACK_HBM_GBS = 6800.0
@@ -200,14 +201,19 @@ def run_ours(args, world, rank, local):
 
     li = workload_layer(args.workload, args.part, dev)
     fp8 = args.kv == "fp8"
+    T = args.query_tokens
+    if fp8 and T > 1:
+        raise SystemExit("several query tokens per request need a bf16 cache")
     if fp8:
         li = synth.quantize_kv_fp8(li)
-    step = pdb.LayerStep.for_inputs(li)
+    step = pdb.LayerStep.for_inputs(li, query_tokens=T)
+    # the step's query rows: q [B, Hq, d], or [B, T, Hq, d] for T tokens per request
+    q_rows = li.q if T == 1 else synth.make_query_tokens(li, T, seed=synth.seed_of(args.workload))
     plan = step.plan
     S = int(plan.num_splits)
     launches_per_step = 1 + (1 if int(plan.merge_mode) == 1 else 0)  # mode 2 merges inside stage 1
 
-    touched = max(1, li.kv_bytes())
+    touched = max(1, li.kv_bytes() if T == 1 else synth.multi_kv_bytes(li, T))
     replicas = max(1, min(16, math.ceil(4 * L2_BYTES / touched)))
     kp, vp = (li.k8, li.v8) if fp8 else (li.k_pool, li.v_pool)
     pools = [(kp, vp)]
@@ -215,22 +221,22 @@ def run_ours(args, world, rank, local):
         pools.append((kp.clone(), None if vp is None else vp.clone()))
     k_sc = li.k_scale if fp8 else None
     v_sc = li.v_scale if fp8 else None
-    out = torch.empty_like(li.q)
+    out = torch.empty_like(q_rows)
     stream = torch.cuda.Stream(device=dev)
 
     def one_step(i, stage1_only=False):
         k, v = pools[i % replicas]
         if fp8 and li.window > 0:
-            pdb.paged_decode_window_fp8(plan, li.q, k, v, k_sc, v_sc, li.block_tables, li.seq_lens, li.window,
+            pdb.paged_decode_window_fp8(plan, q_rows, k, v, k_sc, v_sc, li.block_tables, li.seq_lens, li.window,
                                         li.scale, step.workspace, out, stream)
         elif fp8:
-            pdb.paged_decode_global_fp8(plan, li.q, k, v, k_sc, v_sc, li.block_tables, li.seq_lens, li.scale,
+            pdb.paged_decode_global_fp8(plan, q_rows, k, v, k_sc, v_sc, li.block_tables, li.seq_lens, li.scale,
                                         step.workspace, out, stream)
         elif li.window > 0:
-            pdb.paged_decode_window(plan, li.q, k, v, li.block_tables, li.seq_lens, li.window, li.scale,
+            pdb.paged_decode_window(plan, q_rows, k, v, li.block_tables, li.seq_lens, li.window, li.scale,
                                     step.workspace, out, stream)
         else:
-            pdb.paged_decode_global(plan, li.q, k, v, li.block_tables, li.seq_lens, li.scale, step.workspace,
+            pdb.paged_decode_global(plan, q_rows, k, v, li.block_tables, li.seq_lens, li.scale, step.workspace,
                                     out, stream)
         if not stage1_only:
             pdb.paged_decode_merge(plan, step.workspace, out, stream)
@@ -295,12 +301,13 @@ def run_ours(args, world, rank, local):
 
     us_per_step = elapsed_ms * 1e3 / K
     s1_us = s1_ms * 1e3 / K
-    alg_bytes = li.algorithmic_bytes()
+    alg_bytes = li.algorithmic_bytes() if T == 1 else synth.multi_algorithmic_bytes(li, T)
     peak, peak_kind = measured_peaks()
     achieved = alg_bytes / (s1_us * 1e-6) / 1e9
-    kv_gbs = li.kv_bytes() / (us_per_step * 1e-6) / 1e9
+    kv_gbs = touched / (us_per_step * 1e-6) / 1e9
     src_hash = kernel_source_hash()
-    traffic = NCU_TRAFFIC.get(src_hash, {}).get(f"w{args.workload}{args.part or ''}{'-fp8' if fp8 else ''}")
+    traffic = NCU_TRAFFIC.get(src_hash, {}).get(
+        f"w{args.workload}{args.part or ''}{'-fp8' if fp8 else ''}{f'-t{T}' if T > 1 else ''}")
 
 
     # end to end: every step copies its inputs (q, block table, seq_lens) from
@@ -310,7 +317,7 @@ def run_ours(args, world, rank, local):
     e2e = None
     if not args.no_e2e:
         # the step's inputs travel in one pinned staging buffer (one copy each way)
-        parts = [li.q, li.block_tables, li.seq_lens]
+        parts = [q_rows, li.block_tables, li.seq_lens]
         offs, total = [], 0
         for t in parts:
             offs.append(total)
@@ -324,8 +331,8 @@ def run_ours(args, world, rank, local):
             views_d.append(stage_d[o:o + n].view(t.dtype).view(t.shape))
             views_h[-1].copy_(t.cpu())
         q_d, bt_d, sl_d = views_d
-        out_h = torch.empty(li.q.shape, dtype=li.q.dtype, pin_memory=True)
-        out_d = torch.empty_like(li.q)
+        out_h = torch.empty(q_rows.shape, dtype=q_rows.dtype, pin_memory=True)
+        out_d = torch.empty_like(q_rows)
 
         def e2e_step(i):
             k, v = pools[i % replicas]
@@ -375,15 +382,18 @@ def run_ours(args, world, rank, local):
 
     cpu_baseline = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not fp8:
-        cpu_baseline = oracle_baseline(li.to("cpu"), budget_s=args.cpu_seconds)
+        cpu_baseline = oracle_baseline(li.to("cpu"), budget_s=args.cpu_seconds,
+                                       q_multi=None if T == 1 else q_rows.cpu())
 
     if rank == 0:
         line = {
-            "metric": METRIC, "value": round(us_per_step, 3), "unit": UNIT, "n_gpus": world, "steps": K,
+            "metric": METRIC if T == 1 else MULTI_METRIC.format(T=T), "value": round(us_per_step, 3), "unit": UNIT,
+            "n_gpus": world, "steps": K,
             "warmup": max(3, args.warmup), "ms_per_step": round(us_per_step / 1e3, 6),
             "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
             "dtype": "f32", "io_dtype": "bf16" if not fp8 else "bf16 q/out, e4m3 KV", "data": "synthetic",
-            "config": config_of(li, args.workload, args.part, replicas, plan),
+            "config": dict(config_of(li, args.workload, args.part, replicas, plan), query_tokens=T,
+                           kv_bytes_per_step=touched),
             "kv_gbs": round(kv_gbs, 1), "kv_hbm_frac": round(kv_gbs / peak, 4),
             "roofline": {"bound": "hbm", "kernel": "stage1", "achieved": round(achieved, 1), "peak": peak,
                          "peak_source": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
@@ -398,11 +408,11 @@ def run_ours(args, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
-def oracle_baseline(li_cpu, budget_s=10.0):
+def oracle_baseline(li_cpu, budget_s=10.0, q_multi=None):
     """The fp64 oracle, as it stands, on all host cores: full layer-steps
-    repeated for about `budget_s` seconds."""
+    repeated for about `budget_s` seconds (q_multi: [B, T, Hq, d] query tokens)."""
     import oracle
-    q = synth.bits_u16(li_cpu.q)
+    q = synth.bits_u16(li_cpu.q if q_multi is None else q_multi)
     k = synth.bits_u16(li_cpu.k_pool)
     v = None if li_cpu.v_pool is None else synth.bits_u16(li_cpu.v_pool)
     bt = li_cpu.block_tables.numpy()
@@ -412,7 +422,10 @@ def oracle_baseline(li_cpu, budget_s=10.0):
     t_end = time.perf_counter() + budget_s
     while True:
         t0 = time.perf_counter()
-        oracle.decode(q, k, v, bt, sl, li_cpu.scale, li_cpu.window)
+        if q_multi is None:
+            oracle.decode(q, k, v, bt, sl, li_cpu.scale, li_cpu.window)
+        else:
+            oracle.decode_multi(q, k, v, bt, sl, li_cpu.scale, li_cpu.window)
         times.append(time.perf_counter() - t0)
         if time.perf_counter() > t_end and len(times) >= 3:
             break
@@ -636,11 +649,60 @@ def run_reference_prepare(args, world):
     print(json.dumps(line), flush=True)
 
 
+def run_reference_multi(args, world):
+    """The multi-token oracle on the host cores: each step is the full set of
+    T x Hq query rows of one request (cycling through the batch), its time
+    scaled by the (row, attended position) pairs to a full layer-step."""
+    import numpy as np
+    import oracle
+    T = args.query_tokens
+    li = workload_layer(args.workload, args.part, "cpu")
+    q = synth.make_query_tokens(li, T, seed=synth.seed_of(args.workload))
+    k = synth.bits_u16(li.k_pool)
+    v = None if li.v_pool is None else synth.bits_u16(li.v_pool)
+    lens = li.seq_lens_list()
+
+    def pairs(L):
+        return sum(min(L - T + 1 + j, li.window) if li.window else L - T + 1 + j for j in range(T)) * li.num_q_heads
+
+    full = sum(pairs(L) for L in lens)
+
+    def sample(i):
+        bi = i % li.batch
+        t0 = time.perf_counter()
+        oracle.decode_multi(synth.bits_u16(q[bi:bi + 1]), k, v, li.block_tables[bi:bi + 1].numpy(),
+                            np.array([lens[bi]], np.int32), li.scale, li.window)
+        return time.perf_counter() - t0, pairs(lens[bi])
+
+    for i in range(args.warmup):
+        sample(i)
+    t_total, work = 0.0, 0
+    for i in range(args.steps):
+        dt, n = sample(i)
+        t_total += dt
+        work += n
+    us = t_total / work * full * 1e6
+    line = {
+        "impl": "reference", "metric": MULTI_METRIC.format(T=T), "value": round(us, 3), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(us / 1e3, 6),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": synth.WORKLOADS[args.workload], "batch": li.batch, "head_dim": li.head_dim,
+                   "query_tokens": T},
+        "cpu_baseline": {"value": round(us, 3), "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
+                         "sample": "one request's T x Hq rows per step, time scaled linearly to a full layer-step"},
+        "e2e": {"value": round(us, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
 def run_reference(args, world, rank):
     if rank != 0:
         return
     if args.op == "prepare":
         run_reference_prepare(args, world)
+        return
+    if args.query_tokens > 1:
+        run_reference_multi(args, world)
         return
     import numpy as np
     import oracle
@@ -704,6 +766,8 @@ def main():
     ap.add_argument("--op", default="decode", choices=["decode", "prepare"],
                     help="decode: the decode layer-step (default); prepare: the fused QKV norm + RoPE + "
                          "paged-cache write of the new tokens")
+    ap.add_argument("--query-tokens", type=int, default=1,
+                    help="decode op: query tokens per request (> 1: speculative-decode verification, causal)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)

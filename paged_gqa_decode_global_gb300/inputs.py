@@ -359,3 +359,26 @@ def make_prepare(li: LayerInputs, *, rot: Optional[int] = None, theta: Optional[
     if max_positions is None:
         max_positions = li.block_tables.shape[1] * li.page_size
     return PrepareInputs(li, q_in, k_in, v_in, q_w, k_w, v_w, rot, theta, eps, max_positions)
+
+
+# --------------------------------------------------------------------------
+# Several query tokens per request (speculative-decode verification)
+# --------------------------------------------------------------------------
+
+def make_query_tokens(li: LayerInputs, T: int, seed: int = 0, q_std: float = 1.0) -> torch.Tensor:
+    """q for the last T positions of each request: bf16 [B, T, Hq, d], N(0, q_std)."""
+    gen = _dev_gen(seed + 15485863, li.q.device)
+    return _randn_bf16((li.batch, T, li.num_q_heads, li.head_dim), q_std, gen, li.q.device)
+
+
+def multi_kv_bytes(li: LayerInputs, T: int) -> int:
+    """KV bytes T query tokens per request must read (the union of their
+    causal ranges: the whole sequence, or the last W + T - 1 positions)."""
+    per_token = li.num_kv_heads * li.head_dim * 2 * (1 if li.kv_shared else 2)
+    n = [min(L, li.window + T - 1) if li.window > 0 else L for L in li.seq_lens_list()]
+    return sum(n) * per_token
+
+
+def multi_algorithmic_bytes(li: LayerInputs, T: int) -> int:
+    """KV bytes plus q read and out written for T tokens per request (bf16)."""
+    return multi_kv_bytes(li, T) + 2 * li.batch * T * li.num_q_heads * li.head_dim * 2
