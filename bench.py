@@ -48,18 +48,27 @@ FALLBACK_HBM_GBS = 6800.0
 # hash of the kernel sources it was taken on; stale entries are ignored (the
 # captures and their commands are summarised under profiles/).
 NCU_TRAFFIC = {
-    "3d79665ed3dc2ee9": {"w2": 67293696 + 715520, "w3": 68264704 + 605952, "w4a": 1073913000 + 3876096},
+    "1684858954e9d269": {"w2": 67293696 + 653312, "w3": 68266496 + 590336, "w4a": 1073970176 + 3444736,
+                         "w4a-fp8": 537315584 + 3361280, "w2-t2": 67450112 + 619776},
 }
 
+
+# the same for the fused QKV norm + RoPE + cache-write kernel (--op prepare)
+PREP_NCU_TRAFFIC = {
+    "a7da2517b4107fce": {"w2": 216832},
+}
 
 STAGE1_SOURCES = ("stage1.cu", "pd_common.cuh", "pd_variants.h", "pd_kernels.h")
 
 
-def kernel_source_hash() -> str:
-    """Hash of the stage-1 kernel's sources (what an ncu capture describes)."""
+PREP_SOURCES = ("prepare.cu", "pd_common.cuh", "pd_variants.h")
+
+
+def kernel_source_hash(sources=STAGE1_SOURCES) -> str:
+    """Hash of a kernel's sources (what an ncu capture describes)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_gqa_decode_global_gb300", "csrc")
-    for name in STAGE1_SOURCES:
+    for name in sources:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
@@ -611,7 +620,10 @@ def run_prepare(args, world, rank, local):
                        "launch": "CUDA graph replay, one stream"},
             "roofline": {"bound": "hbm", "kernel": "qkv_norm_rope_write", "achieved": round(achieved, 1),
                          "peak": peak, "peak_source": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                         "traffic": None, "algorithmic_bytes": per_step, "kernel_us": round(us, 3)},
+                         "traffic": PREP_NCU_TRAFFIC.get(kernel_source_hash(PREP_SOURCES), {}).get(
+                             f"w{args.workload}{args.part or ''}"),
+                         "algorithmic_bytes": per_step, "kernel_us": round(us, 3),
+                         "kernel_source": kernel_source_hash(PREP_SOURCES)},
             "cpu_baseline": cpu_baseline, "e2e": e2e, "gpu_launches": K, "clocks": clocks,
             "device": torch.cuda.get_device_name(dev),
         }
