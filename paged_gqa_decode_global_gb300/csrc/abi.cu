@@ -160,7 +160,10 @@ pd_status stage1(const pd_plan* plan, const void* q, const void* k_pool, const v
   p.lse_part = reinterpret_cast<float*>(ws + plan->lse_offset);
   p.o_part = reinterpret_cast<float*>(ws + plan->opart_offset);
   p.err = reinterpret_cast<uint32_t*>(ws);
-  p.cluster_merge = plan->merge_mode == 2 ? 1 : 0;
+  if (plan->merge_mode == 2)
+    p.cluster_merge = (plan->num_splits - 1 <= pd::kVariants[plan->variant].ded_slots) ? 2 : 1;
+  else
+    p.cluster_merge = 0;
   p.stall_bytes = plan->test_stall_bytes;
   p.scale_log2 = scale * kLog2e;
   p.window = ly.window;

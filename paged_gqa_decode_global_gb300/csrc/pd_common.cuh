@@ -142,6 +142,16 @@ __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
 }
 
+// The two halves of a cluster barrier phase, for a phase that spans the
+// kernel: every thread arrives without ordering when it starts (so no CTA
+// touches another's shared memory before that CTA has started) and waits
+// (acquire) before its first distributed-shared-memory store.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire;" ::: "memory"); }
+
 // The shared::cluster address of this CTA's shared address `addr` in CTA `rank`.
 __device__ __forceinline__ uint32_t map_smem_rank(uint32_t addr, uint32_t rank) {
   uint32_t r;

@@ -27,7 +27,9 @@ struct Stage1Params {
   float* lse_part;              // [B, Hq, S] natural-log log-sum-exp of each piece
   float* o_part;                // [B, Hq, S, D] normalised partial outputs
   uint32_t* err;                // device error word
-  int32_t cluster_merge;        // the S pieces of a (request, KV head) are one cluster; rank 0 merges
+  int32_t cluster_merge;        // the S pieces of a (request, KV head) are one cluster; rank 0 merges:
+                                // 1 = they push into rank 0's drained ring (two cluster barriers),
+                                // 2 = into rank 0's region of its own (one barrier; S - 1 <= DED_SLOTS)
   int32_t stall_bytes;          // tests only: bytes expected per stage beyond what the copies deliver
   float scale_log2;             // softmax scale * log2(e)
   int32_t window;               // 0 = global layer

@@ -68,8 +68,18 @@ struct Stage1Cfg {
   static constexpr int SCALE_OFFSET = (VALID_OFFSET + NST * 4 + 7) / 8 * 8;  // float2 (k, v) scale[NST] (FP8)
   static constexpr int ML_OFFSET = SCALE_OFFSET + NST * 8;     // float2 ml[NW][G]
   static constexpr int COEF_OFFSET = ML_OFFSET + NW * G * 8;   // float coef[NW][G], lse[G]
+  static constexpr int TAIL_END = (COEF_OFFSET + (NW * G + G) * 4 + 15) / 16 * 16;
+  // Pieces that can push into a region of their own, outside the ring (what
+  // is left of the 227 KiB): with them the cluster merge needs one cluster
+  // barrier (other ranks may store while rank 0 still streams); larger
+  // clusters push into rank 0's drained ring after a first barrier.
+  static constexpr int DED_ROOM = 227 * 1024 - 1024 - TAIL_END - 8 * G * 4;
+  static constexpr int DED_FIT = DED_ROOM > 0 ? DED_ROOM / (G * D * 4) : 0;
+  static constexpr int DED_SLOTS = DED_FIT < MAX_CLUSTER - 1 ? DED_FIT : MAX_CLUSTER - 1;
+  static constexpr int DED_OFFSET = TAIL_END;                  // float [DED_SLOTS][G][D]
+  static constexpr int DED_LSE_OFFSET = DED_OFFSET + DED_SLOTS * G * D * 4;  // float [DED_SLOTS][G]
   // + 1 KiB so the ring can start on a 1024-byte boundary (the swizzle period)
-  static constexpr int SMEM_BYTES = COEF_OFFSET + (NW * G + G) * 4 + 1024;
+  static constexpr int SMEM_BYTES = DED_LSE_OFFSET + (DED_SLOTS > 0 ? DED_SLOTS * G * 4 : 0) + 1024;
   static constexpr int THREADS = 32 * (NW + 1);
   static_assert(D % 128 == 0, "head_dim must be a multiple of 128");
   static_assert(G >= 1 && G <= 8, "the GQA group is the MMA's 8-wide side");
@@ -127,7 +137,8 @@ struct Stage1Cfg {
   X(35, 256, 8, true, false, 3, 8, true)
 
 struct VariantInfo {
-  int id, head_dim, group, kv_shared, kv_fp8, nw, spw, block_tokens, threads, smem_bytes, max_cluster, multi;
+  int id, head_dim, group, kv_shared, kv_fp8, nw, spw, block_tokens, threads, smem_bytes, max_cluster, multi,
+      ded_slots;
 };
 
 // Host-visible table, defined in plan.cu.

@@ -21,7 +21,8 @@ namespace pd {
 #define PD_VARIANT_ROW(ID, D, G, KVS, KV8, NW, SPW, MQ)                                                    \
   VariantInfo{ID, D, G, KVS ? 1 : 0, KV8 ? 1 : 0, NW, SPW, Stage1Cfg<D, G, KVS, KV8, NW, SPW, MQ>::TB,      \
               Stage1Cfg<D, G, KVS, KV8, NW, SPW, MQ>::THREADS, Stage1Cfg<D, G, KVS, KV8, NW, SPW, MQ>::SMEM_BYTES, \
-              Stage1Cfg<D, G, KVS, KV8, NW, SPW, MQ>::MAX_CLUSTER, MQ ? 1 : 0},
+              Stage1Cfg<D, G, KVS, KV8, NW, SPW, MQ>::MAX_CLUSTER, MQ ? 1 : 0,                           \
+              Stage1Cfg<D, G, KVS, KV8, NW, SPW, MQ>::DED_SLOTS},
 const VariantInfo kVariants[] = {PD_FOR_EACH_VARIANT(PD_VARIANT_ROW)};
 #undef PD_VARIANT_ROW
 const int kNumVariants = sizeof(kVariants) / sizeof(kVariants[0]);

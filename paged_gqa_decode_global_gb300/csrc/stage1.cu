@@ -262,7 +262,11 @@ __device__ __forceinline__ void stage1_cta(const Stage1Params& p, uint8_t* smem)
     }
   }
 
-  if (threadIdx.x == 0) {
+  // the producer's lane 0 (no q loads queued ahead of it) prefetches the
+  // tensor maps and sets up the ring's barriers
+  if (threadIdx.x == C::NW * 32) {
+    prefetch_tensormap(&p.kmap);
+    if (!C::KVS) prefetch_tensormap(&p.vmap);
 #pragma unroll 1
     for (int s = 0; s < C::NST; ++s) {
       mbar_init(&full_bar[s], 1);
@@ -277,10 +281,6 @@ __device__ __forceinline__ void stage1_cta(const Stage1Params& p, uint8_t* smem)
   // ---- producer ------------------------------------------------------------------
   if (warp == C::NW) {
     const uint64_t policy = l2_evict_first_policy();
-    if (lane == 0) {
-      prefetch_tensormap(&p.kmap);
-      if (!C::KVS) prefetch_tensormap(&p.vmap);
-    }
     // The whole warp walks the blocks 32 at a time: each lane holds one block's
     // page id (fetched a round ahead), lane 0 waits for the stage and issues
     // the copies, so page-id loads never serialise the issue of copies.
@@ -694,9 +694,12 @@ __device__ __forceinline__ void stage1_cta(const Stage1Params& p, uint8_t* smem)
 // Stage 2 inside the cluster (vLLM concepts page, "MLA 与 Sparse MLA（DSA）":
 // the pieces' partial results, each with its log-sum-exp, are merged). The S
 // CTAs of one (request, KV head) form a cluster; each holds its normalised
-// result and log-sum-exp in shared memory. Once every CTA is done with its ring,
-// ranks 1..S-1 push theirs into rank 0's ring area with posted distributed-
-// shared-memory stores; after a second cluster barrier rank 0 merges locally:
+// result and log-sum-exp in shared memory. Ranks 1..S-1 push theirs into rank
+// 0 with posted distributed-shared-memory stores -- into a region of rank 0's
+// own when S - 1 results fit beside the ring (every CTA arrived at a cluster
+// barrier when it started, which the pushers wait for), else into rank 0's
+// ring once a first cluster barrier shows every CTA done with it; after the
+// next cluster barrier rank 0 merges locally:
 //   out = sum_r w_r o_r,  w_r = exp(lse_r - M) / sum_r' exp(lse_r' - M),  M = max_r lse_r
 // in piece order; pieces with no attended token (lse = -inf) weigh nothing.
 template <class C>
@@ -707,10 +710,18 @@ __device__ __forceinline__ void cluster_merge(const Stage1Params& p, uint8_t* sm
   constexpr int D4 = C::D / 4;
   const float* my_lse = reinterpret_cast<const float*>(smem + C::CTA_LSE_OFFSET);
   const float4* my_out = reinterpret_cast<const float4*>(smem + C::CTA_OUT_OFFSET);
-  cluster_sync_all();  // every CTA of the cluster is done with its ring
+  const bool own_region = C::DED_SLOTS > 0 && p.cluster_merge == 2;
+  const int push_off = own_region ? C::DED_OFFSET : C::PUSH_OFFSET;
+  const int push_lse_off = own_region ? C::DED_LSE_OFFSET : C::PUSH_LSE_OFFSET;
+  if (own_region) {
+    __syncthreads();  // this CTA's result is complete
+    cluster_wait();   // every CTA of the cluster has started (it arrived at kernel entry)
+  } else {
+    cluster_sync_all();  // every CTA of the cluster is done with its ring
+  }
   if (rank != 0) {
-    const uint32_t slot = smem_u32(smem + C::PUSH_OFFSET) + (rank - 1) * (C::G * C::D * 4);
-    const uint32_t lse_slot = smem_u32(smem + C::PUSH_LSE_OFFSET) + (rank - 1) * (C::G * 4);
+    const uint32_t slot = smem_u32(smem + push_off) + (rank - 1) * (C::G * C::D * 4);
+    const uint32_t lse_slot = smem_u32(smem + push_lse_off) + (rank - 1) * (C::G * 4);
     if (tid < C::G) st_dsmem_f32(map_smem_rank(lse_slot + tid * 4, 0), my_lse[tid]);
     const uint32_t remote = map_smem_rank(slot, 0);
     for (int e = tid; e < C::G * D4; e += C::THREADS) {
@@ -720,8 +731,8 @@ __device__ __forceinline__ void cluster_merge(const Stage1Params& p, uint8_t* sm
   }
   cluster_sync_all();  // the pushes are visible in rank 0
   if (rank != 0) return;
-  const float* push_lse = reinterpret_cast<const float*>(smem + C::PUSH_LSE_OFFSET);
-  const float4* push_out = reinterpret_cast<const float4*>(smem + C::PUSH_OFFSET);
+  const float* push_lse = reinterpret_cast<const float*>(smem + push_lse_off);
+  const float4* push_out = reinterpret_cast<const float4*>(smem + push_off);
   float* wts = reinterpret_cast<float*>(smem + C::CTA_W_OFFSET);  // [S][G]
   if (tid < C::G) {
     float l[C::MAX_CLUSTER];
@@ -772,6 +783,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) stage1_kernel(const __grid_cons
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // the swizzle pattern repeats every 1024 bytes of shared address: start there
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  if (C::DED_SLOTS > 0 && p.cluster_merge == 2) cluster_arrive_relaxed();  // this CTA has started
   stage1_cta<C>(p, smem);
   if (p.cluster_merge) cluster_merge<C>(p, smem);
 }
