@@ -48,8 +48,8 @@ FALLBACK_HBM_GBS = 6800.0
 # hash of the kernel sources it was taken on; stale entries are ignored (the
 # captures and their commands are summarised under profiles/).
 NCU_TRAFFIC = {
-    "1684858954e9d269": {"w2": 67293696 + 653312, "w3": 68266496 + 590336, "w4a": 1073970176 + 3444736,
-                         "w4a-fp8": 537315584 + 3361280, "w2-t2": 67450112 + 619776},
+    "efc72d0cc09cccaa": {"w2": 67293696 + 632064, "w3": 68267264 + 603392, "w4a": 1073914368 + 3418624,
+                         "w4a-fp8": 537362432 + 3399168, "w2-t2": 67450112 + 626176},
 }
 
 
