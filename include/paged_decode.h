@@ -126,7 +126,7 @@ typedef struct {
                                 than its copies deliver, so its pipeline waits run out (~1 s) and
                                 report PD_DEVFLAG_WAIT_TIMEOUT without any fault */
   int32_t query_tokens;     /* T: query tokens per request (1 = decode; > 1 = paged_decode_plan_multi) */
-  int32_t reserved;
+  int32_t partial;          /* 1: made by paged_decode_plan_partial (fp32 pieces always left for a merge) */
   uint64_t workspace_bytes; /* bytes the caller must provide */
   uint64_t lse_offset;      /* byte offset of the fp32 [batch, T, Hq, S] log-sum-exp part */
   uint64_t opart_offset;    /* byte offset of the fp32 [batch, T, Hq, S, d] partial outputs */
@@ -273,6 +273,54 @@ pd_status paged_decode_check_device_error(const pd_plan* plan, void* workspace,
 pd_status paged_decode_noalloc(const pd_plan* plan, const void* q, const void* k_pool, const void* v_pool,
                                const int32_t* block_tables, const int32_t* seq_lens, int32_t window, float scale,
                                void* out, uint32_t* device_flags, void* stream);
+
+/* ---- Sequence-sharded decode: partial results and their combine ----------------
+ *
+ * Decode context parallelism (vLLM concepts page "模型库与算子层 — 概念", sections
+ * on the MLA backends: DCP, an all-gather of each rank's partial outputs and
+ * log-sum-exps ahead of the merge): the cached tokens of every request are
+ * spread over R ranks, each rank attends its own tokens and produces a
+ * normalised fp32 partial output plus its log-sum-exp, the ranks exchange
+ * them (an all-gather, the caller's collective), and every rank merges the R
+ * partials. The split of one request's tokens over several pieces inside a
+ * rank and the merge across ranks are the same log-sum-exp arithmetic.
+ */
+
+/*
+ * Plan for paged_decode_global_partial: as paged_decode_plan for a global bf16
+ * layer (window 0; PD_ERR_UNSUPPORTED otherwise), with fp32 pieces always left
+ * in the workspace (no in-cluster merge).
+ */
+pd_status paged_decode_plan_partial(const pd_layer_desc* layer, int32_t batch, const int32_t* seq_lens_host,
+                                    int32_t sm_count, pd_plan* plan);
+
+/*
+ * This rank's part of a sharded decode: attention of q over the tokens of this
+ * rank's cache (k_pool, v_pool, block_tables, seq_lens describe the local
+ * tokens, as for paged_decode_global), written as
+ *   o_out   device fp32 [batch, Hq, d]: the normalised partial output,
+ *   lse_out device fp32 [batch, Hq]: its natural-log log-sum-exp (-inf and a
+ *           zero row where the rank holds no token of the request).
+ * plan from paged_decode_plan_partial; o_out 16-byte aligned. Errors as for
+ * paged_decode_global.
+ */
+pd_status paged_decode_global_partial(const pd_plan* plan, const void* q, const void* k_pool, const void* v_pool,
+                                      const int32_t* block_tables, const int32_t* seq_lens, float scale,
+                                      void* workspace, size_t workspace_bytes, float* o_out, float* lse_out,
+                                      void* stream);
+
+/*
+ * Merge num_parts partial results of the same rows (one per rank, gathered):
+ *   o_parts   device fp32 [num_parts, rows, head_dim] (16-byte aligned)
+ *   lse_parts device fp32 [num_parts, rows]
+ *   out       device bf16 [rows, head_dim]
+ * out = sum_r w_r o_r, w_r = exp(lse_r - M) / sum_r' exp(lse_r' - M), M =
+ * max_r lse_r; parts with lse = -inf weigh nothing (a row with none is zero).
+ * num_parts 1..1024, head_dim a multiple of 4. Returns PD_ERR_INVALID_ARG for a
+ * bad argument, PD_ERR_CUDA if the launch fails.
+ */
+pd_status paged_decode_combine(int32_t num_parts, int32_t rows, int32_t head_dim, const float* o_parts,
+                               const float* lse_parts, void* out, void* stream);
 
 /* ---- The step before decode: QKV norm, RoPE, paged-cache write -----------------
  *

@@ -42,6 +42,9 @@ EXPORTED = (
     "paged_decode_global_fp8",
     "paged_decode_window_fp8",
     "paged_decode_plan_multi",
+    "paged_decode_plan_partial",
+    "paged_decode_global_partial",
+    "paged_decode_combine",
     "paged_decode_rope_table",
     "paged_decode_qkv_norm_rope_write",
 )
@@ -79,7 +82,7 @@ class Plan(ctypes.Structure):
         ("merge_mode", ctypes.c_int32),
         ("test_stall_bytes", ctypes.c_int32),
         ("query_tokens", ctypes.c_int32),
-        ("reserved", ctypes.c_int32),
+        ("partial", ctypes.c_int32),
         ("workspace_bytes", ctypes.c_uint64),
         ("lse_offset", ctypes.c_uint64),
         ("opart_offset", ctypes.c_uint64),
@@ -140,6 +143,12 @@ def load_library(path: Optional[str] = None):
         lib.paged_decode_window_fp8.restype = ctypes.c_int
         lib.paged_decode_plan_multi.argtypes = [ctypes.POINTER(LayerDesc), i32, i32, vp, i32, ctypes.POINTER(Plan)]
         lib.paged_decode_plan_multi.restype = ctypes.c_int
+        lib.paged_decode_plan_partial.argtypes = [ctypes.POINTER(LayerDesc), i32, vp, i32, ctypes.POINTER(Plan)]
+        lib.paged_decode_plan_partial.restype = ctypes.c_int
+        lib.paged_decode_global_partial.argtypes = [ctypes.POINTER(Plan), vp, vp, vp, vp, vp, f32, vp, u64, vp, vp, vp]
+        lib.paged_decode_global_partial.restype = ctypes.c_int
+        lib.paged_decode_combine.argtypes = [i32, i32, i32, vp, vp, vp, vp]
+        lib.paged_decode_combine.restype = ctypes.c_int
         lib.paged_decode_rope_table.argtypes = [ctypes.c_double, i32, i32, vp, vp]
         lib.paged_decode_rope_table.restype = ctypes.c_int
         lib.paged_decode_qkv_norm_rope_write.argtypes = [ctypes.POINTER(LayerDesc), i32, i32, i32, f32] + [vp] * 14
@@ -377,3 +386,35 @@ def paged_decode_qkv_norm_rope_write(desc: LayerDesc, rotary_dim: int, num_posit
         _ptr(block_tables), _ptr(seq_lens), _ptr(q_out), _ptr(k_pool), _ptr(v_pool), _ptr(device_flags),
         _stream_ptr(stream))
     _check(st, "paged_decode_qkv_norm_rope_write")
+
+
+def paged_decode_plan_partial(desc: LayerDesc, seq_lens_host: Sequence[int], sm_count: int) -> Plan:
+    """Plan for paged_decode_global_partial (a global bf16 layer's local tokens)."""
+    lib = load_library()
+    n = len(seq_lens_host)
+    arr = (ctypes.c_int32 * max(1, n))(*[int(x) for x in seq_lens_host])
+    plan = Plan()
+    st = lib.paged_decode_plan_partial(ctypes.byref(desc), n, ctypes.cast(arr, ctypes.c_void_p) if n else None,
+                                       int(sm_count), ctypes.byref(plan))
+    _check(st, "paged_decode_plan_partial")
+    return plan
+
+
+def paged_decode_global_partial(plan: Plan, q, k_pool, v_pool, block_tables, seq_lens, scale: float, workspace,
+                                o_out, lse_out, stream=None, workspace_bytes: Optional[int] = None) -> None:
+    """This rank's normalised fp32 partial output o_out [B, Hq, d] and its log-sum-exp lse_out [B, Hq]."""
+    wb = workspace.numel() * workspace.element_size() if workspace_bytes is None else workspace_bytes
+    st = load_library().paged_decode_global_partial(
+        ctypes.byref(plan), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables), _ptr(seq_lens), float(scale),
+        _ptr(workspace), int(wb), _ptr(o_out), _ptr(lse_out), _stream_ptr(stream))
+    _check(st, "paged_decode_global_partial")
+
+
+def paged_decode_combine(o_parts, lse_parts, out, stream=None) -> None:
+    """Merge gathered partials o_parts [R, rows..., d] fp32, lse_parts [R, rows...] into bf16 out [rows..., d]."""
+    R = o_parts.shape[0]
+    d = o_parts.shape[-1]
+    rows = o_parts[0].numel() // d
+    st = load_library().paged_decode_combine(int(R), int(rows), int(d), _ptr(o_parts), _ptr(lse_parts), _ptr(out),
+                                             _stream_ptr(stream))
+    _check(st, "paged_decode_combine")

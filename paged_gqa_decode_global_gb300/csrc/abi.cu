@@ -160,6 +160,7 @@ pd_status stage1(const pd_plan* plan, const void* q, const void* k_pool, const v
   p.lse_part = reinterpret_cast<float*>(ws + plan->lse_offset);
   p.o_part = reinterpret_cast<float*>(ws + plan->opart_offset);
   p.err = reinterpret_cast<uint32_t*>(ws);
+  p.direct_out = (plan->num_splits == 1 && !plan->partial) ? 1 : 0;
   if (plan->merge_mode == 2)
     p.cluster_merge = (plan->num_splits - 1 <= pd::kVariants[plan->variant].ded_slots) ? 2 : 1;
   else
@@ -199,6 +200,27 @@ pd_status stage1(const pd_plan* plan, const void* q, const void* k_pool, const v
     (void)cudaGetLastError();
     return PD_ERR_CUDA;
   }
+  return PD_OK;
+}
+
+// The merge of a plan's workspace ([rows][S] pieces) into bf16 `out`, or into
+// fp32 `o_f32` with the merged log-sum-exp `lse`.
+pd_status merge_workspace(const pd_plan* plan, const uint8_t* ws, void* out, float* o_f32, float* lse, void* stream) {
+  pd::MergeParams p = {};
+  p.lse_part = reinterpret_cast<const float*>(ws + plan->lse_offset);
+  p.o_part = reinterpret_cast<const float*>(ws + plan->opart_offset);
+  p.row_stride = (int64_t)plan->num_splits * plan->layer.head_dim;
+  p.piece_stride = plan->layer.head_dim;
+  p.lse_row_stride = plan->num_splits;
+  p.lse_piece_stride = 1;
+  p.out = out;
+  p.out_f32 = o_f32;
+  p.out_lse = lse;
+  p.num_splits = plan->num_splits;
+  p.head_dim = plan->layer.head_dim;
+  const long long rows = (long long)plan->batch * plan->query_tokens * plan->layer.num_q_heads;
+  if (rows > 0x7fffffffLL) return PD_ERR_UNSUPPORTED;
+  if (pd::launch_merge(p, (int)rows, stream) != 0) return PD_ERR_CUDA;
   return PD_OK;
 }
 
@@ -250,15 +272,40 @@ pd_status paged_decode_merge(const pd_plan* plan, const void* workspace, size_t 
   if (!workspace || !aligned(workspace, 256) || !out || !aligned(out, 16)) return PD_ERR_INVALID_ARG;
   if (workspace_bytes < plan->workspace_bytes) return PD_ERR_WORKSPACE_TOO_SMALL;
   const uint8_t* ws = static_cast<const uint8_t*>(workspace);
-  pd::MergeParams p;
-  p.lse_part = reinterpret_cast<const float*>(ws + plan->lse_offset);
-  p.o_part = reinterpret_cast<const float*>(ws + plan->opart_offset);
+  return merge_workspace(plan, ws, out, nullptr, nullptr, stream);
+}
+
+pd_status paged_decode_global_partial(const pd_plan* plan, const void* q, const void* k_pool, const void* v_pool,
+                                      const int32_t* block_tables, const int32_t* seq_lens, float scale,
+                                      void* workspace, size_t workspace_bytes, float* o_out, float* lse_out,
+                                      void* stream) {
+  if (!plan || !pd::plan_is_valid(plan) || !plan->partial) return PD_ERR_INVALID_ARG;
+  if (plan->batch > 0 && (!o_out || !lse_out || !aligned(o_out, 16) || !aligned(lse_out, 4)))
+    return PD_ERR_INVALID_ARG;
+  // stage 1 writes only the workspace for a partial plan; its `out` is not touched
+  pd_status st = stage1(plan, q, k_pool, v_pool, nullptr, nullptr, block_tables, seq_lens, 0, scale, workspace,
+                        workspace_bytes, o_out, stream);
+  if (st != PD_OK || plan->batch == 0) return st;
+  return merge_workspace(plan, static_cast<const uint8_t*>(workspace), nullptr, o_out, lse_out, stream);
+}
+
+pd_status paged_decode_combine(int32_t num_parts, int32_t rows, int32_t head_dim, const float* o_parts,
+                               const float* lse_parts, void* out, void* stream) {
+  if (num_parts < 1 || num_parts > 1024 || rows < 0 || head_dim <= 0 || head_dim % 4 != 0) return PD_ERR_INVALID_ARG;
+  if (rows == 0) return PD_OK;
+  if (!o_parts || !lse_parts || !out || !aligned(o_parts, 16) || !aligned(lse_parts, 4) || !aligned(out, 8))
+    return PD_ERR_INVALID_ARG;
+  pd::MergeParams p = {};
+  p.lse_part = lse_parts;
+  p.o_part = o_parts;
+  p.row_stride = head_dim;
+  p.piece_stride = (int64_t)rows * head_dim;
+  p.lse_row_stride = 1;
+  p.lse_piece_stride = rows;
   p.out = out;
-  p.num_splits = plan->num_splits;
-  p.head_dim = plan->layer.head_dim;
-  const long long rows = (long long)plan->batch * plan->query_tokens * plan->layer.num_q_heads;
-  if (rows > 0x7fffffffLL) return PD_ERR_UNSUPPORTED;
-  if (pd::launch_merge(p, (int)rows, stream) != 0) return PD_ERR_CUDA;
+  p.num_splits = num_parts;
+  p.head_dim = head_dim;
+  if (pd::launch_merge(p, rows, stream) != 0) return PD_ERR_CUDA;
   return PD_OK;
 }
 

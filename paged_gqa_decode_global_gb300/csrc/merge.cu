@@ -6,8 +6,10 @@
 // （DSA）" — split-KV decode whose pieces each produce partial results carrying a
 // log-sum-exp, combined afterwards:
 //   M = max_s lse_s,  w_s = exp(lse_s - M) / sum_s' exp(lse_s' - M),  out = sum_s w_s o_s.
-// Empty pieces carry lse = -inf (weight 0) and zero partial rows; a row with no
-// piece at all is zero.
+// Empty pieces carry lse = -inf (weight 0; their rows are not read); a row with
+// no piece at all is zero, with lse -inf. The same kernel merges a stage-1
+// workspace ([rows][S] pieces) and partial results gathered from several ranks
+// ([S][rows]), to bf16, or to fp32 with the merged log-sum-exp.
 //
 // Grid (row, 128-dim slice of the row), one warp each, launched behind stage 1
 // as a programmatic dependent (it waits for stage 1 before reading). The warp stages the
@@ -31,10 +33,10 @@ __global__ void __launch_bounds__(32) merge_kernel(const MergeParams p) {
   const size_t row = blockIdx.x;
   const int lane = threadIdx.x;
   const int S = p.num_splits;
-  const float* lse = p.lse_part + row * S;
+  const float* lse = p.lse_part + row * p.lse_row_stride;
   float M = -INFINITY;
   for (int s = lane; s < S; s += 32) {
-    const float l = lse[s];
+    const float l = lse[s * p.lse_piece_stride];
     w[s] = l;
     M = fmaxf(M, l);
   }
@@ -51,22 +53,28 @@ __global__ void __launch_bounds__(32) merge_kernel(const MergeParams p) {
   const float inv = sum > 0.f ? 1.f / sum : 0.f;
   __syncwarp();
   const int D4 = p.head_dim / 4;
+  if (p.out_lse && blockIdx.y == 0 && lane == 0) p.out_lse[row] = sum > 0.f ? M + logf(sum) : -INFINITY;
   const int d4 = blockIdx.y * 32 + lane;
   if (d4 >= D4) return;
-  const float4* src = reinterpret_cast<const float4*>(p.o_part + row * S * p.head_dim) + d4;
+  const float* src = p.o_part + row * p.row_stride + d4 * 4;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 8
   for (int s = 0; s < S; ++s) {
     const float ws = w[s] * inv;
-    const float4 o = src[(size_t)s * D4];
+    if (ws == 0.f) continue;  // an empty piece (its row may never have been written)
+    const float4 o = *reinterpret_cast<const float4*>(src + (size_t)s * p.piece_stride);
     acc.x = fmaf(ws, o.x, acc.x);
     acc.y = fmaf(ws, o.y, acc.y);
     acc.z = fmaf(ws, o.z, acc.z);
     acc.w = fmaf(ws, o.w, acc.w);
   }
-  __nv_bfloat162* out = reinterpret_cast<__nv_bfloat162*>(reinterpret_cast<__nv_bfloat16*>(p.out) + row * p.head_dim) + d4 * 2;
-  out[0] = __floats2bfloat162_rn(acc.x, acc.y);
-  out[1] = __floats2bfloat162_rn(acc.z, acc.w);
+  if (p.out) {
+    __nv_bfloat162* out =
+        reinterpret_cast<__nv_bfloat162*>(reinterpret_cast<__nv_bfloat16*>(p.out) + row * p.head_dim) + d4 * 2;
+    out[0] = __floats2bfloat162_rn(acc.x, acc.y);
+    out[1] = __floats2bfloat162_rn(acc.z, acc.w);
+  }
+  if (p.out_f32) reinterpret_cast<float4*>(p.out_f32 + row * p.head_dim)[d4] = acc;
 }
 
 }  // namespace

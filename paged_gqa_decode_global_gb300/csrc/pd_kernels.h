@@ -27,6 +27,7 @@ struct Stage1Params {
   float* lse_part;              // [B, Hq, S] natural-log log-sum-exp of each piece
   float* o_part;                // [B, Hq, S, D] normalised partial outputs
   uint32_t* err;                // device error word
+  int32_t direct_out;           // one piece and a bf16 result wanted: the CTA writes `out` itself
   int32_t cluster_merge;        // the S pieces of a (request, KV head) are one cluster; rank 0 merges:
                                 // 1 = they push into rank 0's drained ring (two cluster barriers),
                                 // 2 = into rank 0's region of its own (one barrier; S - 1 <= DED_SLOTS)
@@ -43,9 +44,15 @@ struct Stage1Params {
 };
 
 struct MergeParams {
-  const float* lse_part;  // [B, Hq, S]
-  const float* o_part;    // [B, Hq, S, D]
-  void* out;              // bf16 [B, Hq, D]
+  // piece s of row r: o_part[r * row_stride + s * piece_stride + d] (floats),
+  // lse_part[r * lse_row_stride + s * lse_piece_stride]; stage 1's workspace
+  // is [rows][S][D] / [rows][S], a cross-rank combine's input [S][rows][D] / [S][rows]
+  const float* lse_part;
+  const float* o_part;
+  int64_t row_stride, piece_stride, lse_row_stride, lse_piece_stride;
+  void* out;              // bf16 [rows, D], or null
+  float* out_f32;         // fp32 [rows, D], or null
+  float* out_lse;         // fp32 [rows] natural-log log-sum-exp of the merged row, or null
   int32_t num_splits;
   int32_t head_dim;
 };

@@ -131,6 +131,11 @@ double simulate_clusters(const std::vector<int>& n_tok, int hkv, int chunk, int 
 
 }  // namespace
 
+namespace {
+pd_status plan_impl(const pd_layer_desc* layer, int32_t batch, int32_t query_tokens, const int32_t* seq_lens_host,
+                    int32_t sm_count, int partial, pd_plan* plan);
+}
+
 extern "C" {
 
 int32_t paged_decode_abi_version(void) { return kAbiVersion; }
@@ -160,6 +165,21 @@ pd_status paged_decode_plan(const pd_layer_desc* layer, int32_t batch, const int
 
 pd_status paged_decode_plan_multi(const pd_layer_desc* layer, int32_t batch, int32_t query_tokens,
                                   const int32_t* seq_lens_host, int32_t sm_count, pd_plan* plan) {
+  return plan_impl(layer, batch, query_tokens, seq_lens_host, sm_count, 0, plan);
+}
+
+pd_status paged_decode_plan_partial(const pd_layer_desc* layer, int32_t batch, const int32_t* seq_lens_host,
+                                    int32_t sm_count, pd_plan* plan) {
+  if (layer && (layer->window != 0 || layer->kv_dtype != PD_KV_BF16)) return PD_ERR_UNSUPPORTED;
+  return plan_impl(layer, batch, 1, seq_lens_host, sm_count, 1, plan);
+}
+
+}  // extern "C"
+
+namespace {
+
+pd_status plan_impl(const pd_layer_desc* layer, int32_t batch, int32_t query_tokens, const int32_t* seq_lens_host,
+                    int32_t sm_count, int partial, pd_plan* plan) {
   if (!layer || !plan) return PD_ERR_INVALID_ARG;
   if (query_tokens < 1 || query_tokens > kMaxQueryTokens) return PD_ERR_INVALID_ARG;
   const int T = query_tokens;
@@ -246,7 +266,7 @@ pd_status paged_decode_plan_multi(const pd_layer_desc* layer, int32_t batch, int
       const uint64_t merge_bytes = (uint64_t)batch * T * ly.num_q_heads * s * (ly.head_dim + 1) * 4ull * 2ull;
       double cost = simulate(n_tok, hkv_ctas, c, s, cm, merge_bytes);
       bool cluster = false;
-      if (s >= 2 && s <= std::min(kMaxClusterSplits, v->max_cluster)) {
+      if (!partial && s >= 2 && s <= std::min(kMaxClusterSplits, v->max_cluster)) {
         const double cc = simulate_clusters(n_tok, hkv_ctas, c, s, cm, kAssumedGpcs);
         if (cc < cost) {
           cost = cc;
@@ -284,7 +304,8 @@ pd_status paged_decode_plan_multi(const pd_layer_desc* layer, int32_t batch, int
     plan->lse_offset = pd::kWorkspaceHeader;
     plan->opart_offset = pd::kWorkspaceHeader;
     plan->workspace_bytes = pd::kWorkspaceHeader;
-  } else if (best_splits > 1) {
+  } else if (best_splits > 1 || partial) {
+    // (a partial plan always leaves fp32 pieces for the merge, even one)
     plan->merge_mode = 1;
     plan->lse_offset = pd::kWorkspaceHeader;
     plan->opart_offset = align_up(plan->lse_offset + rows * best_splits * 4ull, 256);
@@ -295,12 +316,13 @@ pd_status paged_decode_plan_multi(const pd_layer_desc* layer, int32_t batch, int
     plan->opart_offset = pd::kWorkspaceHeader;
     plan->workspace_bytes = pd::kWorkspaceHeader;
   }
+  plan->partial = partial;
   plan->magic = kPlanMagic;
   plan->version = kAbiVersion;
   return PD_OK;
 }
 
-}  // extern "C"
+}  // namespace
 
 namespace pd {
 
@@ -325,7 +347,10 @@ bool plan_is_valid(const pd_plan* plan) {
   if (plan->merge_mode < 0 || plan->merge_mode > 2) return false;
   if (plan->test_stall_bytes < 0 || plan->test_stall_bytes > (1 << 16) || plan->test_stall_bytes % 16 != 0)
     return false;
-  if ((plan->num_splits == 1) != (plan->merge_mode == 0)) return false;
+  if (plan->partial != 0 && plan->partial != 1) return false;
+  if (plan->partial ? (plan->merge_mode != 1 || plan->query_tokens != 1 || ly.window != 0)
+                    : ((plan->num_splits == 1) != (plan->merge_mode == 0)))
+    return false;
   if (plan->merge_mode == 2 && plan->num_splits > std::min(kMaxClusterSplits, v.max_cluster)) return false;
   return true;
 }

@@ -215,7 +215,7 @@ __device__ __forceinline__ void stage1_cta(const Stage1Params& p, uint8_t* smem)
     // nothing attended in this piece
     if (p.cluster_merge) {
       if (threadIdx.x < C::G) reinterpret_cast<float*>(smem + C::CTA_LSE_OFFSET)[threadIdx.x] = -INFINITY;
-    } else if (p.num_splits == 1) {
+    } else if (p.direct_out) {
       for (int i = threadIdx.x; i < C::G * C::D; i += C::THREADS)
         if (cm.valid(i / C::D))
           reinterpret_cast<__nv_bfloat16*>(p.out)[cm.row(i / C::D) * C::D + i % C::D] = __float2bfloat16_rn(0.f);
@@ -672,7 +672,7 @@ __device__ __forceinline__ void stage1_cta(const Stage1Params& p, uint8_t* smem)
       o.z = fmaf(c, a.z, o.z);
       o.w = fmaf(c, a.w, o.w);
     }
-    if (p.num_splits == 1) {
+    if (p.direct_out) {
       __nv_bfloat162* dst =
           reinterpret_cast<__nv_bfloat162*>(reinterpret_cast<__nv_bfloat16*>(p.out) + cm.row(h) * C::D) + d4 * 2;
       uint2 packed;

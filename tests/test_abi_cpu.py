@@ -170,3 +170,28 @@ def test_prepare_rejects_bad_arguments_without_launching(lib):
     assert lib.paged_decode_rope_table(-1.0, 64, 10, fake, None) == b.PD_ERR_INVALID_ARG
     assert lib.paged_decode_rope_table(1e4, 64, 0, fake, None) == b.PD_ERR_INVALID_ARG
     assert lib.paged_decode_rope_table(1e4, 64, 10, None, None) == b.PD_ERR_INVALID_ARG
+
+
+def test_combine_and_partial_reject_bad_arguments_without_launching(lib):
+    fake = 1 << 20
+    assert lib.paged_decode_combine(0, 4, 512, fake, fake, fake, None) == b.PD_ERR_INVALID_ARG
+    assert lib.paged_decode_combine(1025, 4, 512, fake, fake, fake, None) == b.PD_ERR_INVALID_ARG
+    assert lib.paged_decode_combine(2, 4, 510, fake, fake, fake, None) == b.PD_ERR_INVALID_ARG
+    assert lib.paged_decode_combine(2, -1, 512, fake, fake, fake, None) == b.PD_ERR_INVALID_ARG
+    assert lib.paged_decode_combine(2, 4, 512, fake + 4, fake, fake, None) == b.PD_ERR_INVALID_ARG
+    assert lib.paged_decode_combine(2, 4, 512, None, fake, fake, None) == b.PD_ERR_INVALID_ARG
+    assert lib.paged_decode_combine(2, 0, 512, None, None, None, None) == b.PD_OK  # nothing to do
+    win = b.layer_desc(16, 4, 512, 16, 64, 8, window=128)
+    pl = b.Plan()
+    arr = (ctypes.c_int32 * 1)(16)
+    assert lib.paged_decode_plan_partial(ctypes.byref(win), 1, ctypes.cast(arr, ctypes.c_void_p), 152,
+                                         ctypes.byref(pl)) == b.PD_ERR_UNSUPPORTED
+    desc = b.layer_desc(16, 4, 512, 16, 64, 8)
+    assert lib.paged_decode_plan_partial(ctypes.byref(desc), 1, ctypes.cast(arr, ctypes.c_void_p), 152,
+                                         ctypes.byref(pl)) == b.PD_OK
+    assert pl.partial == 1 and pl.merge_mode == 1
+    # a decode plan is not a partial plan
+    dec = b.paged_decode_plan(desc, [16], 152)
+    st = lib.paged_decode_global_partial(ctypes.byref(dec), fake, fake, fake, fake, fake, 1.0, fake, 1 << 20, fake,
+                                         fake, None)
+    assert st == b.PD_ERR_INVALID_ARG
