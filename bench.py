@@ -55,7 +55,7 @@ NCU_TRAFFIC = {
 
 # the same for the fused QKV norm + RoPE + cache-write kernel (--op prepare)
 PREP_NCU_TRAFFIC = {
-    "a7da2517b4107fce": {"w2": 216832},
+    "cb00505d54cd73e0": {"w2": 216576},
 }
 
 STAGE1_SOURCES = ("stage1.cu", "pd_common.cuh", "pd_variants.h", "pd_kernels.h")
@@ -631,6 +631,105 @@ def run_prepare(args, world, rank, local):
 
 
 # ----------------------------------------------------------------------------
+# one rank of a sequence-sharded decode (--dcp-ranks R)
+# ----------------------------------------------------------------------------
+
+DCP_METRIC = "sequence-sharded decode, per-rank µs/layer-step (partial over 1/R of the tokens + combine of R), 1 GPU"
+
+
+def run_dcp(args, world, rank, local):
+    """What one of R ranks computes per layer-step: its partial over its
+    interleaved shard of the cache, then the combine of the R gathered
+    partials. The all-gather between them needs R GPUs and is not timed."""
+    from paged_gqa_decode_global_gb300 import dcp
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (the library has no CPU path)")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    pd_build.build()
+    pdb.load_library()
+    R = args.dcp_ranks
+    li = workload_layer(args.workload, args.part, dev)
+    if li.window > 0 or args.kv != "bf16" or args.query_tokens != 1:
+        raise SystemExit("--dcp-ranks: global bf16 layers, one query token")
+    k, v, table, lens = dcp.shard_cache(li.k_pool, li.v_pool, li.block_tables, li.seq_lens_list(), R, 0)
+    per_token = li.num_kv_heads * li.head_dim * 2 * (1 if li.kv_shared else 2)
+    shard_bytes = int(lens.sum()) * per_token
+    replicas = max(1, min(16, math.ceil(4 * L2_BYTES / max(1, shard_bytes))))
+    pools = [(k, v)] + [(k.clone(), None if v is None else v.clone()) for _ in range(replicas - 1)]
+    desc = pdb.layer_desc(li.num_q_heads, li.num_kv_heads, li.head_dim, li.page_size, k.shape[0], table.shape[1],
+                          0, li.kv_shared)
+    step = dcp.PartialStep(desc, lens.tolist(), torch.cuda.get_device_properties(dev).multi_processor_count, dev)
+    B, Hq, d = li.q.shape
+    o_all = torch.zeros(R, B, Hq, d, dtype=torch.float32, device=dev)
+    lse_all = torch.full((R, B, Hq), -float("inf"), dtype=torch.float32, device=dev)
+    out = torch.empty(B, Hq, d, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def one(i):
+        kk, vv = pools[i % replicas]
+        # this rank's partial lands in its slot of the gathered buffers
+        pdb.paged_decode_global_partial(step.plan, li.q, kk, vv, table, lens, li.scale, step.workspace, o_all[0],
+                                        lse_all[0], stream)
+        pdb.paged_decode_combine(o_all, lse_all, out, stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(max(3, args.warmup)):
+            one(i)
+        for r in range(1, R):  # the other ranks' partials, as an all-gather would deliver them
+            o_all[r].copy_(o_all[0])
+            lse_all[r].copy_(lse_all[0])
+    torch.cuda.synchronize()
+    K = args.steps
+    graphs, left, i0 = [], K, 0
+    while left > 0:
+        m = min(500, left)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(m):
+                one(i0 + i)
+        graphs.append(g)
+        left -= m
+        i0 += m
+    with torch.cuda.stream(stream):
+        graphs[0].replay()
+    torch.cuda.synchronize()
+    barrier(world)
+    sampler = ClockSampler(local)
+    sampler.__enter__()
+    a = torch.cuda.Event(enable_timing=True)
+    z = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        a.record(stream)
+        for g in graphs:
+            g.replay()
+        z.record(stream)
+    torch.cuda.synchronize()
+    sampler.__exit__(None, None, None)
+    barrier(world)
+    us = max_over_ranks(a.elapsed_time(z), world) * 1e3 / K
+    peak, peak_kind = measured_peaks()
+    alg = shard_bytes + B * Hq * d * 2 + R * B * Hq * (d + 1) * 4 + B * Hq * d * 2
+    if rank == 0:
+        line = {
+            "metric": DCP_METRIC, "value": round(us, 3), "unit": UNIT, "n_gpus": world, "steps": K,
+            "warmup": max(3, args.warmup), "ms_per_step": round(us / 1e3, 6), "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "io_dtype": "bf16", "data": "synthetic",
+            "config": {"workload": synth.WORKLOADS[args.workload] + (f" [{li.name}]" if args.part else ""),
+                       "dcp_ranks": R, "shard": "interleaved positions, rank 0",
+                       "shard_kv_bytes": shard_bytes, "exchange": "all-gather of (o, lse) not timed (needs R GPUs)",
+                       "l2": f"{replicas} rotating shard replicas", "launch": "CUDA graph replay, one stream"},
+            "kv_gbs": round(shard_bytes / (us * 1e-6) / 1e9, 1),
+            "roofline": {"bound": "hbm", "kernel": "partial + combine", "achieved": round(alg / (us * 1e-6) / 1e9, 1),
+                         "peak": peak, "peak_source": peak_kind, "unit": "GB/s",
+                         "frac": round(alg / (us * 1e-6) / 1e9 / peak, 4), "traffic": None, "algorithmic_bytes": alg},
+            "cpu_baseline": None, "e2e": None, "gpu_launches": K * 3, "clocks": sampler.summary(),
+            "device": torch.cuda.get_device_name(dev),
+        }
+        print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------
 # reference arm: the oracle on the host cores
 # ----------------------------------------------------------------------------
 
@@ -780,6 +879,8 @@ def main():
                          "paged-cache write of the new tokens")
     ap.add_argument("--query-tokens", type=int, default=1,
                     help="decode op: query tokens per request (> 1: speculative-decode verification, causal)")
+    ap.add_argument("--dcp-ranks", type=int, default=1,
+                    help="decode op: time one rank of an R-way sequence-sharded decode (partial + combine)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -797,6 +898,8 @@ def main():
             run_reference(args, world, rank)
         elif args.op == "prepare":
             run_prepare(args, world, rank, local)
+        elif args.dcp_ranks > 1:
+            run_dcp(args, world, rank, local)
         else:
             run_ours(args, world, rank, local)
     finally:
