@@ -185,16 +185,24 @@ pd_status stage1(const pd_plan* plan, const void* q, const void* k_pool, const v
   cfg.blockDim = dim3(plan->threads_per_cta);
   cfg.dynamicSmemBytes = plan->smem_bytes;
   cfg.stream = static_cast<cudaStream_t>(stream);
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  // programmatic dependent launch: the grid may start (set up its barriers on
+  // free SMs) while the previous kernel on the stream drains; it touches no
+  // global memory before that kernel has finished (griddepcontrol.wait)
+  attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[na].val.programmaticStreamSerializationAllowed = 1;
+  ++na;
   if (p.cluster_merge) {
     // the S pieces of one (request, KV head) are consecutive in x: one cluster
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = plan->num_splits;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = plan->num_splits;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
   }
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
   cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
   if (e != cudaSuccess) {
     (void)cudaGetLastError();

@@ -67,6 +67,11 @@ template <int D>
 __global__ void __launch_bounds__(32 * kRowsPerCta) qkv_norm_rope_write_kernel(const PrepParams p) {
   constexpr int NCH = D / 256;
   __shared__ float ybuf[kRowsPerCta][D];
+  // launched as a programmatic dependent: wait for the kernel before this one
+  // (it may have written the new rows), then let the decode behind this one
+  // launch and set itself up while these rows are written
+  grid_dependency_wait();
+  grid_launch_dependents();
   const int b = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = blockIdx.y * kRowsPerCta + warp;
@@ -248,12 +253,19 @@ pd_status paged_decode_qkv_norm_rope_write(const pd_layer_desc* layer, int32_t b
   p.rows = ly.num_q_heads + ly.num_kv_heads * (kvs ? 1 : 2);
   const dim3 grid((unsigned)batch, (unsigned)((p.rows + pd::kRowsPerCta - 1) / pd::kRowsPerCta));
   if (grid.y > 65535) return PD_ERR_UNSUPPORTED;
-  const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (ly.head_dim == 512)
-    pd::qkv_norm_rope_write_kernel<512><<<grid, 32 * pd::kRowsPerCta, 0, s>>>(p);
-  else
-    pd::qkv_norm_rope_write_kernel<256><<<grid, 32 * pd::kRowsPerCta, 0, s>>>(p);
-  return cudaGetLastError() == cudaSuccess ? PD_OK : PD_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(32 * pd::kRowsPerCta);
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = ly.head_dim == 512 ? cudaLaunchKernelEx(&cfg, pd::qkv_norm_rope_write_kernel<512>, p)
+                                           : cudaLaunchKernelEx(&cfg, pd::qkv_norm_rope_write_kernel<256>, p);
+  if (e != cudaSuccess) (void)cudaGetLastError();
+  return e == cudaSuccess ? PD_OK : PD_ERR_CUDA;
 }
 
 }  // extern "C"

@@ -164,6 +164,22 @@ __device__ __forceinline__ void stage1_cta(const Stage1Params& p, uint8_t* smem)
   float2* stage_scale = reinterpret_cast<float2*>(smem + C::SCALE_OFFSET);  // FP8: (K, V) scale per stage
   float2* warp_ml = reinterpret_cast<float2*>(smem + C::ML_OFFSET);
 
+  // Prologue, before the previous kernel on the stream may have finished: the
+  // producer's lane 0 prefetches the tensor maps (kernel parameters) and sets
+  // up the ring's barriers. Then every thread waits for that kernel: nothing
+  // below reads or writes global memory before it has completed.
+  if (threadIdx.x == C::NW * 32) {
+    prefetch_tensormap(&p.kmap);
+    if (!C::KVS) prefetch_tensormap(&p.vmap);
+#pragma unroll 1
+    for (int s = 0; s < C::NST; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    fence_barrier_init();
+  }
+  grid_dependency_wait();
+
   const ColMap<C> cm(p);
   const int split = blockIdx.x;
   const int g = cm.g;
@@ -262,19 +278,7 @@ __device__ __forceinline__ void stage1_cta(const Stage1Params& p, uint8_t* smem)
     }
   }
 
-  // the producer's lane 0 (no q loads queued ahead of it) prefetches the
-  // tensor maps and sets up the ring's barriers
-  if (threadIdx.x == C::NW * 32) {
-    prefetch_tensormap(&p.kmap);
-    if (!C::KVS) prefetch_tensormap(&p.vmap);
-#pragma unroll 1
-    for (int s = 0; s < C::NST; ++s) {
-      mbar_init(&full_bar[s], 1);
-      mbar_init(&empty_bar[s], 1);
-    }
-    fence_barrier_init();
-  }
-  __syncthreads();
+  __syncthreads();  // the ring's barriers (set up at entry) are visible
   // a merge launched behind this kernel may start its (waiting) CTAs now
   grid_launch_dependents();
 
