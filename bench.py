@@ -48,14 +48,14 @@ FALLBACK_HBM_GBS = 6800.0
 # hash of the kernel sources it was taken on; stale entries are ignored (the
 # captures and their commands are summarised under profiles/).
 NCU_TRAFFIC = {
-    "efc72d0cc09cccaa": {"w2": 67293696 + 632064, "w3": 68267264 + 603392, "w4a": 1073914368 + 3418624,
-                         "w4a-fp8": 537362432 + 3399168, "w2-t2": 67450112 + 626176},
+    "dba6f99f58f953db": {"w2": 67294208 + 693248, "w3": 68266240 + 617216, "w4a": 1074000896 + 3794176,
+                         "w4a-fp8": 537292032 + 3443200, "w2-t2": 67455232 + 710912},
 }
 
 
 # the same for the fused QKV norm + RoPE + cache-write kernel (--op prepare)
 PREP_NCU_TRAFFIC = {
-    "cb00505d54cd73e0": {"w2": 216576},
+    "54fdfc74075eaf74": {"w2": 216832},
 }
 
 STAGE1_SOURCES = ("stage1.cu", "pd_common.cuh", "pd_variants.h", "pd_kernels.h")
