@@ -156,8 +156,14 @@ struct ColMap {
 // in `out` (one piece), in the workspace (pieces merged by a later launch) or in
 // this CTA's shared memory (pieces merged across the cluster). Threads return
 // from here at different points; none leaves the kernel early.
+// What a thread of stage1_cta has done towards the cluster merge when every
+// piece pushes into a region of rank 0's own (one cluster barrier):
+constexpr int kMergeNothing = 0;   // not waited at the cluster barrier; the CTA pushed nothing
+constexpr int kMergePushed = 1;    // waited there, and the CTA's result went out (rank 0: stayed local)
+constexpr int kMergeToWait = 2;    // not waited; the CTA's result went out (the producer warp)
+
 template <class C>
-__device__ __forceinline__ void stage1_cta(const Stage1Params& p, uint8_t* smem) {
+__device__ __forceinline__ int stage1_cta(const Stage1Params& p, uint8_t* smem) {
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + C::BAR_OFFSET);
   uint64_t* empty_bar = full_bar + C::NST;
   uint32_t* stage_valid = reinterpret_cast<uint32_t*>(smem + C::VALID_OFFSET);
@@ -242,7 +248,7 @@ __device__ __forceinline__ void stage1_cta(const Stage1Params& p, uint8_t* smem)
       if (threadIdx.x < C::G && cm.valid(threadIdx.x))
         p.lse_part[cm.row(threadIdx.x) * p.num_splits + split] = -INFINITY;
     }
-    return;
+    return kMergeNothing;
   }
 
   // Start each role's first global loads before the barrier set-up so their
@@ -367,7 +373,7 @@ __device__ __forceinline__ void stage1_cta(const Stage1Params& p, uint8_t* smem)
         }
       }
     }
-    return;
+    return (C::DED_SLOTS > 0 && p.cluster_merge == 2) ? kMergeToWait : kMergeNothing;
   }
 
   // ---- consumers -----------------------------------------------------------------
@@ -660,6 +666,22 @@ __device__ __forceinline__ void stage1_cta(const Stage1Params& p, uint8_t* smem)
   }
   named_bar_sync(1, C::NW * 32);
 
+  // One-barrier cluster merge: once every CTA of the cluster has started
+  // (each arrived at the barrier at kernel entry), ranks 1..S-1 store their
+  // rows and lse straight into rank 0's region; rank 0 keeps its own locally.
+  const bool fused = C::DED_SLOTS > 0 && p.cluster_merge == 2;
+  bool to_rank0 = false;
+  uint32_t remote_out = 0, remote_lse = 0;
+  if (fused) {
+    cluster_wait();
+    const uint32_t rank = cluster_ctarank();
+    if (rank != 0) {
+      to_rank0 = true;
+      remote_out = map_smem_rank(smem_u32(smem + C::DED_OFFSET) + (rank - 1) * (C::G * C::D * 4), 0);
+      remote_lse = map_smem_rank(smem_u32(smem + C::DED_LSE_OFFSET) + (rank - 1) * (C::G * 4), 0);
+    }
+  }
+
   constexpr int D4 = C::D / 4;
 #pragma unroll 2
   for (int e = tid; e < C::G * D4; e += C::NW * 32) {
@@ -683,8 +705,11 @@ __device__ __forceinline__ void stage1_cta(const Stage1Params& p, uint8_t* smem)
       packed.x = pack_bf16x2(o.x, o.y);
       packed.y = pack_bf16x2(o.z, o.w);
       *reinterpret_cast<uint2*>(dst) = packed;
+    } else if (to_rank0) {
+      st_dsmem_f32x4(remote_out + (h * D4 + d4) * 16, o);
+      if (d4 == 0) st_dsmem_f32(remote_lse + h * 4, coef[C::NW * C::G + h]);
     } else if (p.cluster_merge) {
-      // kept in shared memory for rank 0 of the cluster
+      // kept in shared memory for rank 0 of the cluster (or to push from)
       reinterpret_cast<float4*>(smem + C::CTA_OUT_OFFSET)[h * D4 + d4] = o;
       if (d4 == 0) reinterpret_cast<float*>(smem + C::CTA_LSE_OFFSET)[h] = coef[C::NW * C::G + h];
     } else {
@@ -693,6 +718,7 @@ __device__ __forceinline__ void stage1_cta(const Stage1Params& p, uint8_t* smem)
       if (d4 == 0) p.lse_part[prow] = coef[C::NW * C::G + h];
     }
   }
+  return fused ? kMergePushed : kMergeNothing;
 }
 
 // Stage 2 inside the cluster (vLLM concepts page, "MLA 与 Sparse MLA（DSA）":
@@ -707,7 +733,7 @@ __device__ __forceinline__ void stage1_cta(const Stage1Params& p, uint8_t* smem)
 //   out = sum_r w_r o_r,  w_r = exp(lse_r - M) / sum_r' exp(lse_r' - M),  M = max_r lse_r
 // in piece order; pieces with no attended token (lse = -inf) weigh nothing.
 template <class C>
-__device__ __forceinline__ void cluster_merge(const Stage1Params& p, uint8_t* smem) {
+__device__ __forceinline__ void cluster_merge(const Stage1Params& p, uint8_t* smem, int state) {
   const int S = p.num_splits;
   const uint32_t rank = cluster_ctarank();
   const int tid = threadIdx.x;
@@ -717,13 +743,16 @@ __device__ __forceinline__ void cluster_merge(const Stage1Params& p, uint8_t* sm
   const bool own_region = C::DED_SLOTS > 0 && p.cluster_merge == 2;
   const int push_off = own_region ? C::DED_OFFSET : C::PUSH_OFFSET;
   const int push_lse_off = own_region ? C::DED_LSE_OFFSET : C::PUSH_LSE_OFFSET;
+  // (with its own region a CTA that attended something has pushed already --
+  // all its threads have state kMergePushed or kMergeToWait -- and an empty
+  // one, all of whose threads have state kMergeNothing, pushes its lse here)
   if (own_region) {
-    __syncthreads();  // this CTA's result is complete
-    cluster_wait();   // every CTA of the cluster has started (it arrived at kernel entry)
+    if (state == kMergeNothing) __syncthreads();  // this CTA's lse is in place
+    if (state != kMergePushed) cluster_wait();    // every CTA of the cluster has started
   } else {
     cluster_sync_all();  // every CTA of the cluster is done with its ring
   }
-  if (rank != 0) {
+  if (rank != 0 && state == kMergeNothing) {
     const uint32_t slot = smem_u32(smem + push_off) + (rank - 1) * (C::G * C::D * 4);
     const uint32_t lse_slot = smem_u32(smem + push_lse_off) + (rank - 1) * (C::G * 4);
     if (tid < C::G) st_dsmem_f32(map_smem_rank(lse_slot + tid * 4, 0), my_lse[tid]);
@@ -788,8 +817,8 @@ __global__ void __launch_bounds__(C::THREADS, 1) stage1_kernel(const __grid_cons
   // the swizzle pattern repeats every 1024 bytes of shared address: start there
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   if (C::DED_SLOTS > 0 && p.cluster_merge == 2) cluster_arrive_relaxed();  // this CTA has started
-  stage1_cta<C>(p, smem);
-  if (p.cluster_merge) cluster_merge<C>(p, smem);
+  const int state = stage1_cta<C>(p, smem);
+  if (p.cluster_merge) cluster_merge<C>(p, smem, state);
 }
 
 // ---- instantiation and dispatch -------------------------------------------------
