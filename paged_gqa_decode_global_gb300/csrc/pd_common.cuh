@@ -171,6 +171,12 @@ __device__ __forceinline__ void st_dsmem_f32x4(uint32_t addr, float4 v) {
                : "memory");
 }
 
+// Arrive at named barrier `id` (counted with the threads that sync on it)
+// without waiting for it.
+__device__ __forceinline__ void named_bar_arrive(int id, int nthreads) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }

@@ -284,7 +284,14 @@ __device__ __forceinline__ int stage1_cta(const Stage1Params& p, uint8_t* smem) 
     }
   }
 
-  __syncthreads();  // the ring's barriers (set up at entry) are visible
+  // The ring's barriers (set up by the producer's lane 0 at entry) are
+  // visible to the consumers once they pass named barrier 2, at which the
+  // producer only arrives: it issues its first copies without waiting for
+  // the consumers' q loads.
+  if (warp == C::NW)
+    named_bar_arrive(2, C::THREADS);
+  else
+    named_bar_sync(2, C::THREADS);
   // a merge launched behind this kernel may start its (waiting) CTAs now
   grid_launch_dependents();
 
