@@ -93,7 +93,7 @@ typedef enum {
 typedef struct {
   int32_t num_q_heads;        /* Hq, a multiple of num_kv_heads */
   int32_t num_kv_heads;       /* Hkv */
-  int32_t head_dim;           /* d: 256 or 512 */
+  int32_t head_dim;           /* d: 256 or 512 (128: bf16 cache, one query token) */
   int32_t page_size;          /* P: tokens per page, a multiple of 16 */
   int32_t num_pages;          /* pages in the pool */
   int32_t max_pages_per_seq;  /* block-table row length */

@@ -97,7 +97,8 @@ struct Stage1Cfg {
 // 16 KiB x 12 (d512 K=V, d256 K!=V), 8 KiB x 24 (d256 K=V). FP8: seven
 // consumer warps (two per SM sub-partition hide the latency of widening e4m3
 // fragments to f16) and rings of 196-224 KiB. Multi-token (ids 32-35): the
-// group-8 geometry, any group <= 8 at run time.
+// group-8 geometry, any group <= 8 at run time. head_dim 128 (ids 36-43, bf16,
+// one query token): 8 KiB stages x 24 (K!=V), 4 KiB x 48 (K=V).
 #define PD_FOR_EACH_VARIANT(X)             \
   X(0, 512, 1, false, false, 3, 2, false)  \
   X(1, 512, 2, false, false, 3, 2, false)  \
@@ -134,7 +135,15 @@ struct Stage1Cfg {
   X(32, 512, 8, false, false, 3, 2, true)  \
   X(33, 512, 8, true, false, 3, 4, true)   \
   X(34, 256, 8, false, false, 3, 4, true)  \
-  X(35, 256, 8, true, false, 3, 8, true)
+  X(35, 256, 8, true, false, 3, 8, true)   \
+  X(36, 128, 1, false, false, 3, 8, false) \
+  X(37, 128, 2, false, false, 3, 8, false) \
+  X(38, 128, 4, false, false, 3, 8, false) \
+  X(39, 128, 8, false, false, 3, 8, false) \
+  X(40, 128, 1, true, false, 3, 16, false) \
+  X(41, 128, 2, true, false, 3, 16, false) \
+  X(42, 128, 4, true, false, 3, 16, false) \
+  X(43, 128, 8, true, false, 3, 16, false)
 
 struct VariantInfo {
   int id, head_dim, group, kv_shared, kv_fp8, nw, spw, block_tokens, threads, smem_bytes, max_cluster, multi,

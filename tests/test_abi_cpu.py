@@ -64,7 +64,7 @@ def _plan(lens, Hq=16, Hkv=4, d=512, P=16, pages=4096, maxp=None, window=0, kv_s
     (dict(window=-1), b.PD_ERR_INVALID_ARG),
     (dict(sms=0), b.PD_ERR_INVALID_ARG),
     (dict(d=384), b.PD_ERR_UNSUPPORTED),
-    (dict(d=128), b.PD_ERR_UNSUPPORTED),
+    (dict(d=192), b.PD_ERR_UNSUPPORTED),
     (dict(Hq=64, Hkv=4), b.PD_ERR_UNSUPPORTED),   # group of 16
     (dict(Hq=48, Hkv=4), b.PD_ERR_UNSUPPORTED),   # group of 12
 ])
@@ -195,3 +195,15 @@ def test_combine_and_partial_reject_bad_arguments_without_launching(lib):
     st = lib.paged_decode_global_partial(ctypes.byref(dec), fake, fake, fake, fake, fake, 1.0, fake, 1 << 20, fake,
                                          fake, None)
     assert st == b.PD_ERR_INVALID_ARG
+
+
+def test_head_dim_128_is_planned_for_bf16_single_token(lib):
+    pl = _plan([100, 2000], d=128)
+    assert pl.layer.head_dim == 128 and pl.threads_per_cta == 128
+    desc = b.layer_desc(16, 4, 128, 16, 4096, 64, kv_dtype=b.PD_KV_FP8_E4M3)
+    with pytest.raises(b.PagedDecodeError) as e:
+        b.paged_decode_plan(desc, [100], 152)
+    assert e.value.status == b.PD_ERR_UNSUPPORTED
+    with pytest.raises(b.PagedDecodeError) as e:
+        b.paged_decode_plan_multi(b.layer_desc(16, 4, 128, 16, 4096, 64), 2, [100], 152)
+    assert e.value.status == b.PD_ERR_UNSUPPORTED
