@@ -774,24 +774,26 @@ __device__ __forceinline__ void cluster_merge(const Stage1Params& p, uint8_t* sm
   const float* push_lse = reinterpret_cast<const float*>(smem + push_lse_off);
   const float4* push_out = reinterpret_cast<const float4*>(smem + push_off);
   float* wts = reinterpret_cast<float*>(smem + C::CTA_W_OFFSET);  // [S][G]
-  if (tid < C::G) {
+  // one thread per (piece, head): w = exp(lse - M) / sum_r exp(lse_r - M),
+  // every thread of a head reading that head's S log-sum-exps
+  if (tid < S * C::G) {
+    const int r = tid / C::G, h = tid % C::G;
     float l[C::MAX_CLUSTER];
     float M = -INFINITY;
 #pragma unroll
-    for (int r = 0; r < C::MAX_CLUSTER; ++r) {
-      l[r] = r >= S ? -INFINITY : (r == 0 ? my_lse[tid] : push_lse[(r - 1) * C::G + tid]);
-      M = fmaxf(M, l[r]);
+    for (int q = 0; q < C::MAX_CLUSTER; ++q) {
+      l[q] = q >= S ? -INFINITY : (q == 0 ? my_lse[h] : push_lse[(q - 1) * C::G + h]);
+      M = fmaxf(M, l[q]);
     }
-    float sum = 0.f;
+    float sum = 0.f, mine = 0.f;
+    constexpr float kLog2e = 1.4426950408889634f;
 #pragma unroll
-    for (int r = 0; r < C::MAX_CLUSTER; ++r) {
-      l[r] = (M == -INFINITY) ? 0.f : expf(l[r] - M);
-      sum += l[r];
+    for (int q = 0; q < C::MAX_CLUSTER; ++q) {
+      const float e = (M == -INFINITY || q >= S) ? 0.f : ex2((l[q] - M) * kLog2e);
+      sum += e;
+      if (q == r) mine = e;
     }
-    const float inv = sum > 0.f ? 1.f / sum : 0.f;
-#pragma unroll
-    for (int r = 0; r < C::MAX_CLUSTER; ++r)
-      if (r < S) wts[r * C::G + tid] = l[r] * inv;
+    wts[r * C::G + h] = sum > 0.f ? mine / sum : 0.f;
   }
   __syncthreads();
   const ColMap<C> cm(p);
