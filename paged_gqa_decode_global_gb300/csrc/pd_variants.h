@@ -89,6 +89,7 @@ struct Stage1Cfg {
   static_assert(SCALE_OFFSET % 8 == 0 && ML_OFFSET % 8 == 0, "float2 arrays need 8-byte alignment");
   static_assert(!MQ || (G == 8 && !KV8), "multi-token variants use all 8 columns, bf16 cache");
   static_assert(8 * G <= THREADS, "one thread per (piece, head) computes the cluster merge weights");
+  static_assert(NW * G <= NW * 32, "one consumer thread per (warp, head) computes the warp merge coefficients");
 };
 
 // The instances this library is built with, by variant id:

@@ -651,25 +651,26 @@ __device__ __forceinline__ int stage1_cta(const Stage1Params& p, uint8_t* smem) 
   }
   named_bar_sync(1, C::NW * 32);
 
-  // merge coefficients, once per head: c_w = 2^(m_w - M) / sum_w' 2^(m_w' - M) l_w'
+  // merge coefficients, one thread per (warp, head):
+  //   c_w = 2^(m_w - M) / sum_w' 2^(m_w' - M) l_w'  (0 for a warp that saw no token)
+  // and the piece's natural-log log-sum-exp per head
   const int tid = threadIdx.x;
   float* coef = reinterpret_cast<float*>(smem + C::COEF_OFFSET);  // [NW][G], then lse[G]
-  if (tid < C::G) {
+  if (tid < C::NW * C::G) {
+    const int w = tid / C::G, h = tid % C::G;
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < C::NW; ++w) M = fmaxf(M, warp_ml[w * C::G + tid].x);
-    float Lsum = 0.f;
-    float f[C::NW];
+    for (int v = 0; v < C::NW; ++v) M = fmaxf(M, warp_ml[v * C::G + h].x);
+    float Lsum = 0.f, mine = 0.f;
 #pragma unroll
-    for (int w = 0; w < C::NW; ++w) {
-      const float2 ml = warp_ml[w * C::G + tid];
-      f[w] = (M == -INFINITY) ? 0.f : ex2(ml.x - M);  // 0 for a warp that saw no token
-      Lsum = fmaf(f[w], ml.y, Lsum);
+    for (int v = 0; v < C::NW; ++v) {
+      const float2 ml = warp_ml[v * C::G + h];
+      const float f = (M == -INFINITY) ? 0.f : ex2(ml.x - M);
+      Lsum = fmaf(f, ml.y, Lsum);
+      if (v == w) mine = f;
     }
-    const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
-#pragma unroll
-    for (int w = 0; w < C::NW; ++w) coef[w * C::G + tid] = f[w] * inv;
-    coef[C::NW * C::G + tid] = (Lsum > 0.f) ? (M + log2f(Lsum)) * 0.69314718055994530942f : -INFINITY;
+    coef[w * C::G + h] = Lsum > 0.f ? mine / Lsum : 0.f;
+    if (w == 0) coef[C::NW * C::G + h] = (Lsum > 0.f) ? (M + __log2f(Lsum)) * 0.69314718055994530942f : -INFINITY;
   }
   named_bar_sync(1, C::NW * 32);
 
