@@ -43,8 +43,9 @@ __global__ void __launch_bounds__(32) merge_kernel(const MergeParams p) {
 #pragma unroll
   for (int m = 16; m >= 1; m >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, m));
   float sum = 0.f;
+  constexpr float kLog2e = 1.4426950408889634f;
   for (int s = lane; s < S; s += 32) {
-    const float e = (M == -INFINITY) ? 0.f : expf(w[s] - M);
+    const float e = (M == -INFINITY) ? 0.f : exp2f((w[s] - M) * kLog2e);
     w[s] = e;
     sum += e;
   }
@@ -53,7 +54,7 @@ __global__ void __launch_bounds__(32) merge_kernel(const MergeParams p) {
   const float inv = sum > 0.f ? 1.f / sum : 0.f;
   __syncwarp();
   const int D4 = p.head_dim / 4;
-  if (p.out_lse && blockIdx.y == 0 && lane == 0) p.out_lse[row] = sum > 0.f ? M + logf(sum) : -INFINITY;
+  if (p.out_lse && blockIdx.y == 0 && lane == 0) p.out_lse[row] = sum > 0.f ? M + __logf(sum) : -INFINITY;
   const int d4 = blockIdx.y * 32 + lane;
   if (d4 >= D4) return;
   const float* src = p.o_part + row * p.row_stride + d4 * 4;
