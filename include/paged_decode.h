@@ -169,8 +169,9 @@ pd_status paged_decode_plan(const pd_layer_desc* layer, int32_t batch, const int
  * [batch, T, Hq, d]; a device length below T sets PD_DEVFLAG_BAD_SEQLEN and the
  * tokens before position 0 attend nothing (zero output). The (token, head)
  * pairs of one KV head are served 8 per CTA, so for T * group <= 8 every KV
- * byte is still read once. bf16 caches only (an FP8 layer returns
- * PD_ERR_UNSUPPORTED); group Hq / Hkv up to 8.
+ * byte is still read once. bf16 or FP8 caches (an FP8 plan goes with
+ * paged_decode_global_fp8 / paged_decode_window_fp8), head_dim 256 or 512,
+ * group Hq / Hkv up to 8.
  */
 pd_status paged_decode_plan_multi(const pd_layer_desc* layer, int32_t batch, int32_t query_tokens,
                                   const int32_t* seq_lens_host, int32_t sm_count, pd_plan* plan);

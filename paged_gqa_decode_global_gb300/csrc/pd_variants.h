@@ -87,7 +87,7 @@ struct Stage1Cfg {
   static_assert(STAGE_BYTES % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
   static_assert(SCALE_OFFSET % 8 == 0 && ML_OFFSET % 8 == 0, "float2 arrays need 8-byte alignment");
-  static_assert(!MQ || (G == 8 && !KV8), "multi-token variants use all 8 columns, bf16 cache");
+  static_assert(!MQ || G == 8, "multi-token variants use all 8 columns");
   static_assert(8 * G <= THREADS, "one thread per (piece, head) computes the cluster merge weights");
   static_assert(NW * G <= NW * 32, "one consumer thread per (warp, head) computes the warp merge coefficients");
 };
@@ -99,8 +99,9 @@ struct Stage1Cfg {
 // 16 KiB x 12 (d512 K=V, d256 K!=V), 8 KiB x 24 (d256 K=V). FP8: seven
 // consumer warps (two per SM sub-partition hide the latency of widening e4m3
 // fragments to f16) and rings of 196-224 KiB. Multi-token (ids 32-35): the
-// group-8 geometry, any group <= 8 at run time. head_dim 128 (ids 36-43, bf16,
-// one query token): 8 KiB stages x 24 (K!=V), 4 KiB x 48 (K=V).
+// group-8 geometry, any group <= 8 at run time (ids 44-47: the same over an
+// FP8 cache). head_dim 128 (ids 36-43, bf16, one query token): 8 KiB stages x
+// 24 (K!=V), 4 KiB x 48 (K=V).
 #define PD_FOR_EACH_VARIANT(X)             \
   X(0, 512, 1, false, false, 3, 2, false)  \
   X(1, 512, 2, false, false, 3, 2, false)  \
@@ -145,7 +146,11 @@ struct Stage1Cfg {
   X(40, 128, 1, true, false, 3, 16, false) \
   X(41, 128, 2, true, false, 3, 16, false) \
   X(42, 128, 4, true, false, 3, 16, false) \
-  X(43, 128, 8, true, false, 3, 16, false)
+  X(43, 128, 8, true, false, 3, 16, false) \
+  X(44, 512, 8, false, true, 7, 2, true)   \
+  X(45, 512, 8, true, true, 7, 4, true)    \
+  X(46, 256, 8, false, true, 7, 4, true)   \
+  X(47, 256, 8, true, true, 7, 7, true)
 
 struct VariantInfo {
   int id, head_dim, group, kv_shared, kv_fp8, nw, spw, block_tokens, threads, smem_bytes, max_cluster, multi,

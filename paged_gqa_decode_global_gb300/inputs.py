@@ -371,14 +371,24 @@ def make_query_tokens(li: LayerInputs, T: int, seed: int = 0, q_std: float = 1.0
     return _randn_bf16((li.batch, T, li.num_q_heads, li.head_dim), q_std, gen, li.q.device)
 
 
-def multi_kv_bytes(li: LayerInputs, T: int) -> int:
-    """KV bytes T query tokens per request must read (the union of their
-    causal ranges: the whole sequence, or the last W + T - 1 positions)."""
-    per_token = li.num_kv_heads * li.head_dim * 2 * (1 if li.kv_shared else 2)
-    n = [min(L, li.window + T - 1) if li.window > 0 else L for L in li.seq_lens_list()]
-    return sum(n) * per_token
+def _multi_tokens(li, T: int) -> List[int]:
+    """Positions T query tokens per request attend (the union of their causal
+    ranges: the whole sequence, or the last W + T - 1 positions)."""
+    return [min(L, li.window + T - 1) if li.window > 0 else L for L in li.seq_lens_list()]
 
 
-def multi_algorithmic_bytes(li: LayerInputs, T: int) -> int:
-    """KV bytes plus q read and out written for T tokens per request (bf16)."""
-    return multi_kv_bytes(li, T) + 2 * li.batch * T * li.num_q_heads * li.head_dim * 2
+def multi_kv_bytes(li, T: int) -> int:
+    """KV bytes T query tokens per request must read (bf16 or e4m3 cache)."""
+    elem = 1 if hasattr(li, "k8") else 2
+    per_token = li.num_kv_heads * li.head_dim * elem * (1 if li.kv_shared else 2)
+    return sum(_multi_tokens(li, T)) * per_token
+
+
+def multi_algorithmic_bytes(li, T: int) -> int:
+    """KV bytes (and, for an e4m3 cache, the scales of the pages touched) plus
+    q read and out written (bf16) for T tokens per request."""
+    scales = 0
+    if hasattr(li, "k8"):
+        pages = sum((n + li.page_size - 1) // li.page_size for n in _multi_tokens(li, T))
+        scales = pages * li.num_kv_heads * 4 * (1 if li.kv_shared else 2)
+    return multi_kv_bytes(li, T) + scales + 2 * li.batch * T * li.num_q_heads * li.head_dim * 2

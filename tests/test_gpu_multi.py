@@ -158,7 +158,46 @@ def test_plan_rejections():
         with pytest.raises(b.PagedDecodeError) as e:
             b.paged_decode_plan_multi(desc, T, lens, 152)
         assert e.value.status == status
-    fp8 = b.layer_desc(16, 4, 512, 16, 100, 64, kv_dtype=b.PD_KV_FP8_E4M3)
+    d128 = b.layer_desc(16, 4, 128, 16, 100, 64)
     with pytest.raises(b.PagedDecodeError) as e:
-        b.paged_decode_plan_multi(fp8, 2, [10], 152)
+        b.paged_decode_plan_multi(d128, 2, [10], 152)
     assert e.value.status == b.PD_ERR_UNSUPPORTED
+
+
+FP8_CASES = [
+    # d, Hq, Hkv, kvs, window, T, lens
+    (512, 16, 4, False, 0, 2, [2, 17, 300, 1000]),
+    (512, 16, 4, True, 0, 3, [3, 64, 700]),
+    (256, 16, 8, False, 1024, 4, [4100, 4200, 5, 1030]),
+    (256, 8, 4, True, 37, 5, [5, 60, 333]),
+]
+
+
+@pytest.mark.parametrize("case", FP8_CASES, ids=[f"d{c[0]}-kvs{int(c[3])}-W{c[4]}-T{c[5]}" for c in FP8_CASES])
+def test_multi_over_fp8_cache_matches_per_token_oracle(case):
+    """Over an e4m3 cache, token j of T must equal the (pinned) single-token
+    FP8 oracle at length L - T + 1 + j."""
+    d, Hq, Hkv, kvs, W, T, lens = case
+    li, q = _layer(lens, T, Hq, Hkv, d, window=W, kvs=kvs, seed=d + T + W + 5)
+    f8 = synth.quantize_kv_fp8(li)
+    desc = b.layer_desc(Hq, Hkv, d, li.page_size, li.num_pages, li.block_tables.shape[1], W, kvs, b.PD_KV_FP8_E4M3)
+    plan = b.paged_decode_plan_multi(desc, T, lens, _sms())
+    ws = torch.zeros(max(256, plan.workspace_bytes), dtype=torch.uint8, device="cuda")
+    out = torch.full_like(q, float("nan"))
+    if W > 0:
+        b.paged_decode_window_fp8(plan, q, f8.k8, f8.v8, f8.k_scale, f8.v_scale, li.block_tables, li.seq_lens, W,
+                                  li.scale, ws, out)
+    else:
+        b.paged_decode_global_fp8(plan, q, f8.k8, f8.v8, f8.k_scale, f8.v_scale, li.block_tables, li.seq_lens,
+                                  li.scale, ws, out)
+    b.paged_decode_merge(plan, ws, out)
+    assert ctypes_flags(plan, ws) == 0
+    qh = q.cpu()
+    ref = np.zeros(tuple(q.shape), dtype=np.float64)
+    k8, v8 = f8.k8.cpu().numpy(), None if f8.v8 is None else f8.v8.cpu().numpy()
+    ks, vs = f8.k_scale.cpu().numpy(), None if f8.v_scale is None else f8.v_scale.cpu().numpy()
+    for j in range(T):
+        lens_j = np.array([L - T + 1 + j for L in lens], dtype=np.int32)
+        ref[:, j] = oracle.decode_fp8(synth.bits_u16(qh[:, j].contiguous()), k8, v8, ks, vs,
+                                      li.block_tables.cpu().numpy(), lens_j, li.scale, W)
+    compare(out, ref, f"fp8 S={plan.num_splits} mode={plan.merge_mode}")
