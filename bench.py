@@ -39,6 +39,7 @@ from paged_gqa_decode_global_gb300 import build as pd_build  # noqa: E402
 from paged_gqa_decode_global_gb300 import inputs as synth  # noqa: E402
 
 METRIC = "decode-attn µs/layer-step and KV HBM GB/s (% of GB300 peak), 1 GPU"
+LAYER_METRIC = "new-token step + decode-attn µs/layer-step and KV HBM GB/s, 1 GPU"
 MULTI_METRIC = "{T}-token-per-request (verification) attn µs/layer-step and KV HBM GB/s, 1 GPU"
 UNIT = "us/layer-step"
 L2_BYTES = 129 * 1000 * 1000
@@ -214,11 +215,38 @@ def run_ours(args, world, rank, local):
     if fp8:
         li = synth.quantize_kv_fp8(li)
     step = pdb.LayerStep.for_inputs(li, query_tokens=T)
+    stream = torch.cuda.Stream(device=dev)
     # the step's query rows: q [B, Hq, d], or [B, T, Hq, d] for T tokens per request
     q_rows = li.q if T == 1 else synth.make_query_tokens(li, T, seed=synth.seed_of(args.workload))
     plan = step.plan
+    plan.early_kv = 1 if args.early_kv else 0
     S = int(plan.num_splits)
     launches_per_step = 1 + (1 if int(plan.merge_mode) == 1 else 0)  # mode 2 merges inside stage 1
+
+    # --op layer: each step first runs the fused QKV norm + RoPE + cache write
+    # of the new token (into the pool replica the step decodes), whose q_out is
+    # the decode's q
+    layer_op = args.op == "layer"
+    prep = None
+    if layer_op:
+        if fp8 or T != 1:
+            raise SystemExit("--op layer: bf16 cache, one query token per request")
+        pi = synth.make_prepare(li, seed=synth.seed_of(args.workload))
+        cos_sin = torch.empty(pi.max_positions, max(2, pi.rot), dtype=torch.float32, device=dev)
+        pdb.paged_decode_rope_table(pi.theta, pi.rot, pi.max_positions, cos_sin)
+        prep_desc = pdb.layer_desc(li.num_q_heads, li.num_kv_heads, li.head_dim, li.page_size, li.num_pages,
+                                   li.block_tables.shape[1], li.window, li.kv_shared)
+        prep_flags = torch.zeros(1, dtype=torch.int32, device=dev)
+        q_rows = torch.empty_like(li.q)
+
+        def prep(k, v, q_in=None, k_in=None, v_in=None, bt=None, sl=None, q_out=None):
+            pdb.paged_decode_qkv_norm_rope_write(
+                prep_desc, pi.rot, pi.max_positions, pi.eps, pi.q_in if q_in is None else q_in,
+                pi.k_in if k_in is None else k_in, pi.v_in if v_in is None else v_in, pi.q_w, pi.k_w, pi.v_w,
+                cos_sin, li.block_tables if bt is None else bt, li.seq_lens if sl is None else sl,
+                q_rows if q_out is None else q_out, k, v, prep_flags, stream)
+
+        launches_per_step += 1
 
     touched = max(1, li.kv_bytes() if T == 1 else synth.multi_kv_bytes(li, T))
     replicas = max(1, min(16, math.ceil(4 * L2_BYTES / touched)))
@@ -229,10 +257,11 @@ def run_ours(args, world, rank, local):
     k_sc = li.k_scale if fp8 else None
     v_sc = li.v_scale if fp8 else None
     out = torch.empty_like(q_rows)
-    stream = torch.cuda.Stream(device=dev)
 
     def one_step(i, stage1_only=False):
         k, v = pools[i % replicas]
+        if prep is not None and not stage1_only:
+            prep(k, v)
         if fp8 and li.window > 0:
             pdb.paged_decode_window_fp8(plan, q_rows, k, v, k_sc, v_sc, li.block_tables, li.seq_lens, li.window,
                                         li.scale, step.workspace, out, stream)
@@ -324,7 +353,10 @@ def run_ours(args, world, rank, local):
     e2e = None
     if not args.no_e2e:
         # the step's inputs travel in one pinned staging buffer (one copy each way)
-        parts = [q_rows, li.block_tables, li.seq_lens]
+        if layer_op:  # the new token's raw q / k / v rows instead of q
+            parts = [pi.q_in, pi.k_in] + ([] if pi.v_in is None else [pi.v_in]) + [li.block_tables, li.seq_lens]
+        else:
+            parts = [q_rows, li.block_tables, li.seq_lens]
         offs, total = [], 0
         for t in parts:
             offs.append(total)
@@ -337,13 +369,17 @@ def run_ours(args, world, rank, local):
             views_h.append(stage_h[o:o + n].view(t.dtype).view(t.shape))
             views_d.append(stage_d[o:o + n].view(t.dtype).view(t.shape))
             views_h[-1].copy_(t.cpu())
-        q_d, bt_d, sl_d = views_d
+        bt_d, sl_d = views_d[-2:]
+        q_d = torch.empty_like(q_rows) if layer_op else views_d[0]
         out_h = torch.empty(q_rows.shape, dtype=q_rows.dtype, pin_memory=True)
         out_d = torch.empty_like(q_rows)
 
         def e2e_step(i):
             k, v = pools[i % replicas]
             stage_d.copy_(stage_h, non_blocking=True)
+            if layer_op:
+                prep(k, v, q_in=views_d[0], k_in=views_d[1], v_in=None if pi.v_in is None else views_d[2],
+                     bt=bt_d, sl=sl_d, q_out=q_d)
             step(q_d, k, v, bt_d, sl_d, li.scale, out_d, stream, k_scale=k_sc, v_scale=v_sc)
             out_h.copy_(out_d, non_blocking=True)
 
@@ -382,8 +418,11 @@ def run_ours(args, world, rank, local):
         e2e = {"value": round(e2e_ms * 1e3 / K, 3), "unit": UNIT,
                "h2d_bytes_per_step": int(stage_h.numel()),
                "d2h_bytes_per_step": out_h.numel() * 2, "steps": K,
-               "launch": "CUDA graph replay of: one H2D copy of q + block table + seq_lens from a pinned "
-                         "staging buffer, the C-ABI decode calls, one D2H copy of out to pinned host memory",
+               "launch": "CUDA graph replay of: one H2D copy of " +
+                         ("the new token's q/k/v rows" if layer_op else "q") +
+                         " + block table + seq_lens from a pinned staging buffer, the C-ABI " +
+                         ("new-token step and " if layer_op else "") +
+                         "decode calls, one D2H copy of out to pinned host memory",
                "eager_value": round(eager_ms * 1e3 / n_eager, 3), "eager_steps": n_eager}
         step.check(stream)
 
@@ -396,16 +435,24 @@ def run_ours(args, world, rank, local):
         else:
             cpu_baseline = oracle_baseline(li.to("cpu"), budget_s=args.cpu_seconds,
                                            q_multi=None if T == 1 else q_rows.cpu())
+            if layer_op:
+                prep_us = oracle_prepare_us(li.to("cpu"), synth.seed_of(args.workload))
+                cpu_baseline = dict(cpu_baseline, value=round(cpu_baseline["value"] + prep_us, 1),
+                                    sample=cpu_baseline["sample"] + f"; plus the new-token step, {prep_us:.0f} us "
+                                                                    "(full layer-step, median of 5, one core)")
 
     if rank == 0:
         line = {
-            "metric": METRIC if T == 1 else MULTI_METRIC.format(T=T), "value": round(us_per_step, 3), "unit": UNIT,
+            "metric": LAYER_METRIC if layer_op else METRIC if T == 1 else MULTI_METRIC.format(T=T),
+            "value": round(us_per_step, 3), "unit": UNIT,
             "n_gpus": world, "steps": K,
             "warmup": max(3, args.warmup), "ms_per_step": round(us_per_step / 1e3, 6),
             "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
             "dtype": "f32", "io_dtype": "bf16" if not fp8 else "bf16 q/out, e4m3 KV", "data": "synthetic",
             "config": dict(config_of(li, args.workload, args.part, replicas, plan), query_tokens=T,
-                           kv_bytes_per_step=touched),
+                           kv_bytes_per_step=touched, early_kv=bool(args.early_kv),
+                           **({"step": "fused QKV norm + RoPE + cache write of the new token, then decode"}
+                              if layer_op else {})),
             "kv_gbs": round(kv_gbs, 1), "kv_hbm_frac": round(kv_gbs / peak, 4),
             "roofline": {"bound": "hbm", "kernel": "stage1", "achieved": round(achieved, 1), "peak": peak,
                          "peak_source": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
@@ -445,6 +492,22 @@ def oracle_baseline(li_cpu, budget_s=10.0, q_multi=None):
     return {"value": round(t * 1e6, 1), "unit": UNIT, "cores": threads, "kind": "oracle",
             "sample": f"full layer-step ({li_cpu.batch}x{li_cpu.num_q_heads} rows, {sum(li_cpu.attended())} "
                       f"attended tokens), median of {len(times)} runs, fp64 C + OpenMP"}
+
+
+def oracle_prepare_us(li_cpu, seed) -> float:
+    """The oracle of the new-token step, one full layer-step on one core (median of 5), in us."""
+    import oracle
+    pc = synth.make_prepare(li_cpu, seed=seed)
+    a = [synth.bits_u16(pc.q_in), synth.bits_u16(pc.k_in), None if pc.v_in is None else synth.bits_u16(pc.v_in),
+         synth.bits_u16(pc.q_w), synth.bits_u16(pc.k_w), None if pc.v_w is None else synth.bits_u16(pc.v_w),
+         li_cpu.block_tables.numpy(), li_cpu.seq_lens.numpy(), li_cpu.num_pages, li_cpu.page_size, pc.rot,
+         pc.theta, pc.eps]
+    times = []
+    for _ in range(5):
+        t0 = time.perf_counter()
+        oracle.prepare_qkv(*a)
+        times.append(time.perf_counter() - t0)
+    return statistics.median(times) * 1e6
 
 
 def oracle_baseline_fp8(li, budget_s=10.0):
@@ -880,14 +943,20 @@ def run_reference(args, world, rank):
         t_total += dt
         work += done
     us_per_step = t_total / work * full_tokens * 1e6  # scaled to a full layer-step
+    sample = (f"{len(rows)} query rows over {frac:.4f} of each attended range per step, "
+              "time scaled linearly to a full layer-step")
+    if args.op == "layer":  # plus the oracle's new-token step, timed whole
+        prep_us = oracle_prepare_us(li, synth.seed_of(args.workload))
+        us_per_step += prep_us
+        sample += f"; plus the new-token step, {prep_us:.0f} us (full layer-step, median of 5, one core)"
     line = {
-        "impl": "reference", "metric": METRIC, "value": round(us_per_step, 3), "unit": UNIT, "n_gpus": world,
+        "impl": "reference", "metric": LAYER_METRIC if args.op == "layer" else METRIC,
+        "value": round(us_per_step, 3), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(us_per_step / 1e3, 6),
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": synth.WORKLOADS[args.workload], "batch": li.batch, "head_dim": li.head_dim},
         "cpu_baseline": {"value": round(us_per_step, 3), "unit": UNIT, "cores": len(rows), "kind": "oracle",
-                         "sample": f"{len(rows)} query rows over {frac:.4f} of each attended range per step, "
-                                   "time scaled linearly to a full layer-step"},
+                         "sample": sample},
         "e2e": {"value": round(us_per_step, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -903,13 +972,17 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--kv", default="bf16", choices=["bf16", "fp8"],
                     help="KV-cache element type (fp8: e4m3 with per-(page, KV head) scales)")
-    ap.add_argument("--op", default="decode", choices=["decode", "prepare"],
+    ap.add_argument("--op", default="decode", choices=["decode", "prepare", "layer"],
                     help="decode: the decode layer-step (default); prepare: the fused QKV norm + RoPE + "
-                         "paged-cache write of the new tokens")
+                         "paged-cache write of the new tokens; layer: both, the new-token step then the decode")
     ap.add_argument("--query-tokens", type=int, default=1,
                     help="decode op: query tokens per request (> 1: speculative-decode verification, causal)")
     ap.add_argument("--dcp-ranks", type=int, default=1,
                     help="decode op: time one rank of an R-way sequence-sharded decode (partial + combine)")
+    ap.add_argument("--early-kv", action=argparse.BooleanOptionalAction, default=True,
+                    help="decode / layer: set pd_plan.early_kv (stage 1 copies older cache rows while the "
+                         "previous kernel on the stream -- the last step's decode, or the new-token step -- "
+                         "is still running; default on)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)

@@ -127,6 +127,17 @@ typedef struct {
                                 report PD_DEVFLAG_WAIT_TIMEOUT without any fault */
   int32_t query_tokens;     /* T: query tokens per request (1 = decode; > 1 = paged_decode_plan_multi) */
   int32_t partial;          /* 1: made by paged_decode_plan_partial (fp32 pieces always left for a merge) */
+  int32_t early_kv;         /* 0 (as planned). A caller may set 1 when no kernel that can still be
+                               running as stage 1 starts writes block_tables, seq_lens, the FP8 scales
+                               or a cached row other than each request's newest query_tokens positions.
+                               Those kernels are the one launched just before stage 1 on its stream and,
+                               if that one lets its dependents start before it waits for its own
+                               predecessor (paged_decode_qkv_norm_rope_write does), the one before it,
+                               and so on; this library's decode and merge kernels let them start only
+                               after that wait. A decode behind the new-token step, or behind another
+                               layer's decode, qualifies. Stage 1 then copies the older rows of its first
+                               pipeline stages while those kernels run (programmatic dependent launch);
+                               q, the newest rows and every write wait for them as usual */
   uint64_t workspace_bytes; /* bytes the caller must provide */
   uint64_t lse_offset;      /* byte offset of the fp32 [batch, T, Hq, S] log-sum-exp part */
   uint64_t opart_offset;    /* byte offset of the fp32 [batch, T, Hq, S, d] partial outputs */
@@ -387,6 +398,10 @@ pd_status paged_decode_rope_table(double theta, int32_t rotary_dim, int32_t num_
  *   stream         cudaStream_t as void*
  * q_in / k_in / v_in / q_out / pools must be 16-byte aligned. Only the new
  * token's rows of the pools are written. Requests must not share a slot.
+ * Launched as a programmatic dependent that lets the kernel behind it start at
+ * once, before it waits for the kernel before it: a decode with
+ * pd_plan.early_kv behind it streams its older rows meanwhile (a kernel behind
+ * it that reads what this one writes must wait for it, griddepcontrol.wait).
  * Returns PD_ERR_INVALID_ARG / PD_ERR_UNSUPPORTED without launching, PD_ERR_CUDA
  * if the launch fails.
  */

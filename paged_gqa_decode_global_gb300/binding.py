@@ -83,6 +83,7 @@ class Plan(ctypes.Structure):
         ("test_stall_bytes", ctypes.c_int32),
         ("query_tokens", ctypes.c_int32),
         ("partial", ctypes.c_int32),
+        ("early_kv", ctypes.c_int32),
         ("workspace_bytes", ctypes.c_uint64),
         ("lse_offset", ctypes.c_uint64),
         ("opart_offset", ctypes.c_uint64),
@@ -305,7 +306,7 @@ class LayerStep:
 
     def __init__(self, num_q_heads, num_kv_heads, head_dim, page_size, num_pages, max_pages_per_seq,
                  seq_lens_host, *, window=0, kv_shared=False, kv_dtype=PD_KV_BF16, sm_count=None, device=None,
-                 query_tokens=1):
+                 query_tokens=1, early_kv=False):
         import torch
         device = torch.device("cuda") if device is None else torch.device(device)
         if sm_count is None:
@@ -318,20 +319,22 @@ class LayerStep:
             self.plan = paged_decode_plan_multi(self.desc, self.query_tokens, list(seq_lens_host), sm_count)
         else:
             self.plan = paged_decode_plan(self.desc, list(seq_lens_host), sm_count)
+        # the caller's promise about the kernel launched just before stage 1 (pd_plan.early_kv)
+        self.plan.early_kv = 1 if early_kv else 0
         nbytes = int(self.plan.workspace_bytes)
         # zeroed once: the first word is the device error flag
         self.workspace = torch.zeros((nbytes + 255) // 256 * 256, dtype=torch.uint8, device=device)
         self.window = window
 
     @classmethod
-    def for_inputs(cls, li, sm_count=None, query_tokens=1):
+    def for_inputs(cls, li, sm_count=None, query_tokens=1, early_kv=False):
         """A step for a LayerInputs (bf16 cache) or Fp8LayerInputs (e4m3 cache);
         query_tokens > 1: q and out are [B, T, Hq, d]."""
         fp8 = hasattr(li, "k8")
         return cls(li.num_q_heads, li.num_kv_heads, li.head_dim, li.page_size, li.num_pages, li.max_pages,
                    li.seq_lens_list(), window=li.window, kv_shared=li.kv_shared,
                    kv_dtype=PD_KV_FP8_E4M3 if fp8 else PD_KV_BF16, sm_count=sm_count, device=li.q.device,
-                   query_tokens=query_tokens)
+                   query_tokens=query_tokens, early_kv=early_kv)
 
     def __call__(self, q, k_pool, v_pool, block_tables, seq_lens, scale, out, stream=None, k_scale=None,
                  v_scale=None):

@@ -166,6 +166,7 @@ pd_status stage1(const pd_plan* plan, const void* q, const void* k_pool, const v
   else
     p.cluster_merge = 0;
   p.stall_bytes = plan->test_stall_bytes;
+  p.early_kv = plan->early_kv;
   p.scale_log2 = scale * kLog2e;
   p.window = ly.window;
   p.num_pages = ly.num_pages;

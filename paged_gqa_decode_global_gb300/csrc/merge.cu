@@ -11,10 +11,13 @@
 // workspace ([rows][S] pieces) and partial results gathered from several ranks
 // ([S][rows]), to bf16, or to fp32 with the merged log-sum-exp.
 //
-// Grid (row, 128-dim slice of the row), one warp each, launched behind stage 1
-// as a programmatic dependent (it waits for stage 1 before reading). The warp stages the
-// row's S weights in shared memory, then every lane sums its 4 dims over the
-// pieces with independent 16-byte loads in flight.
+// Grid (row, 512-dim slice of the row), head_dim / 4 threads (at most 128)
+// each, launched behind stage 1 as a programmatic dependent (it waits for stage
+// 1 before reading). Every warp reduces the row's S log-sum-exps itself, and
+// each lane sums its 4 dims over the pieces with independent 16-byte loads in
+// flight, taking the weights of 32 pieces at a time from the lanes that
+// computed them. The kernel holds no shared memory, so one of its CTAs fits
+// beside a stage-1 CTA of the next launch on the same SM.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -26,49 +29,51 @@ namespace pd {
 namespace {
 
 constexpr int kMergeMaxSplits = 1024;
+constexpr int kMergeThreads = 128;  // 4 dims a thread: 512 dims a CTA
 
-__global__ void __launch_bounds__(32) merge_kernel(const MergeParams p) {
-  __shared__ float w[kMergeMaxSplits];
+__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams p) {
   grid_dependency_wait();  // stage 1 (launched before this grid) has finished
+  // the next kernel on the stream may become resident now (it waits for this
+  // grid before it reads anything this grid writes)
+  grid_launch_dependents();
   const size_t row = blockIdx.x;
-  const int lane = threadIdx.x;
+  const int lane = threadIdx.x & 31;
   const int S = p.num_splits;
   const float* lse = p.lse_part + row * p.lse_row_stride;
   float M = -INFINITY;
-  for (int s = lane; s < S; s += 32) {
-    const float l = lse[s * p.lse_piece_stride];
-    w[s] = l;
-    M = fmaxf(M, l);
-  }
+  for (int s = lane; s < S; s += 32) M = fmaxf(M, lse[s * p.lse_piece_stride]);
 #pragma unroll
   for (int m = 16; m >= 1; m >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, m));
   float sum = 0.f;
   constexpr float kLog2e = 1.4426950408889634f;
-  for (int s = lane; s < S; s += 32) {
-    const float e = (M == -INFINITY) ? 0.f : exp2f((w[s] - M) * kLog2e);
-    w[s] = e;
-    sum += e;
-  }
+  if (M != -INFINITY)
+    for (int s = lane; s < S; s += 32) sum += exp2f((lse[s * p.lse_piece_stride] - M) * kLog2e);
 #pragma unroll
   for (int m = 16; m >= 1; m >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, m);
   const float inv = sum > 0.f ? 1.f / sum : 0.f;
-  __syncwarp();
   const int D4 = p.head_dim / 4;
-  if (p.out_lse && blockIdx.y == 0 && lane == 0) p.out_lse[row] = sum > 0.f ? M + __logf(sum) : -INFINITY;
-  const int d4 = blockIdx.y * 32 + lane;
-  if (d4 >= D4) return;
+  if (p.out_lse && blockIdx.y == 0 && threadIdx.x == 0) p.out_lse[row] = sum > 0.f ? M + __logf(sum) : -INFINITY;
+  const int d4 = blockIdx.y * kMergeThreads + threadIdx.x;
+  const bool active = d4 < D4;
   const float* src = p.o_part + row * p.row_stride + d4 * 4;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s0 = 0; s0 < S; s0 += 32) {
+    // lane k's weight is piece s0 + k's
+    const int s = s0 + lane;
+    const float wl = (s < S && M != -INFINITY) ? exp2f((lse[s * p.lse_piece_stride] - M) * kLog2e) * inv : 0.f;
+    const int n = min(32, S - s0);
 #pragma unroll 8
-  for (int s = 0; s < S; ++s) {
-    const float ws = w[s] * inv;
-    if (ws == 0.f) continue;  // an empty piece (its row may never have been written)
-    const float4 o = *reinterpret_cast<const float4*>(src + (size_t)s * p.piece_stride);
-    acc.x = fmaf(ws, o.x, acc.x);
-    acc.y = fmaf(ws, o.y, acc.y);
-    acc.z = fmaf(ws, o.z, acc.z);
-    acc.w = fmaf(ws, o.w, acc.w);
+    for (int k = 0; k < n; ++k) {
+      const float ws = __shfl_sync(0xffffffffu, wl, k);
+      if (ws == 0.f || !active) continue;  // an empty piece (its row may never have been written)
+      const float4 o = *reinterpret_cast<const float4*>(src + (size_t)(s0 + k) * p.piece_stride);
+      acc.x = fmaf(ws, o.x, acc.x);
+      acc.y = fmaf(ws, o.y, acc.y);
+      acc.z = fmaf(ws, o.z, acc.z);
+      acc.w = fmaf(ws, o.w, acc.w);
+    }
   }
+  if (!active) return;
   if (p.out) {
     __nv_bfloat162* out =
         reinterpret_cast<__nv_bfloat162*>(reinterpret_cast<__nv_bfloat16*>(p.out) + row * p.head_dim) + d4 * 2;
@@ -86,8 +91,9 @@ int launch_merge(const MergeParams& p, int rows, void* stream) {
   // launched with programmatic stream serialisation: its CTAs may become
   // resident while stage 1 drains and wait there for its completion
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(rows, (p.head_dim / 4 + 31) / 32);
-  cfg.blockDim = dim3(32);
+  const int d4 = p.head_dim / 4;
+  cfg.gridDim = dim3(rows, (d4 + kMergeThreads - 1) / kMergeThreads);
+  cfg.blockDim = dim3(d4 < kMergeThreads ? (d4 + 31) / 32 * 32 : kMergeThreads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = static_cast<cudaStream_t>(stream);
   cudaLaunchAttribute attr[1];

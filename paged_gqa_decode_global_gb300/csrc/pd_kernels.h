@@ -32,6 +32,9 @@ struct Stage1Params {
                                 // 1 = they push into rank 0's drained ring (two cluster barriers),
                                 // 2 = into rank 0's region of its own (one barrier; S - 1 <= DED_SLOTS)
   int32_t stall_bytes;          // tests only: bytes expected per stage beyond what the copies deliver
+  int32_t early_kv;             // no kernel still running when this grid starts writes a length,
+                                // page id, scale or cached row older than the newest query_tokens
+                                // positions: the producer copies such rows before its dependency wait
   float scale_log2;             // softmax scale * log2(e)
   int32_t window;               // 0 = global layer
   int32_t num_pages, max_pages, page_size;

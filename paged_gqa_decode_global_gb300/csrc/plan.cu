@@ -32,7 +32,7 @@ const int kNumVariants = sizeof(kVariants) / sizeof(kVariants[0]);
 namespace {
 
 constexpr uint32_t kPlanMagic = 0x50444543u;  // "PDEC"
-constexpr int32_t kAbiVersion = 4;
+constexpr int32_t kAbiVersion = 5;
 // Pieces per (request, KV head) are capped (the merge stages their weights in
 // shared memory).
 constexpr int kMaxSplits = 1024;
@@ -348,6 +348,7 @@ bool plan_is_valid(const pd_plan* plan) {
   if (plan->test_stall_bytes < 0 || plan->test_stall_bytes > (1 << 16) || plan->test_stall_bytes % 16 != 0)
     return false;
   if (plan->partial != 0 && plan->partial != 1) return false;
+  if (plan->early_kv != 0 && plan->early_kv != 1) return false;
   if (plan->partial ? (plan->merge_mode != 1 || plan->query_tokens != 1 || ly.window != 0)
                     : ((plan->num_splits == 1) != (plan->merge_mode == 0)))
     return false;

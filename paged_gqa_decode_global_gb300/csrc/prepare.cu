@@ -67,11 +67,13 @@ template <int D>
 __global__ void __launch_bounds__(32 * kRowsPerCta) qkv_norm_rope_write_kernel(const PrepParams p) {
   constexpr int NCH = D / 256;
   __shared__ float ybuf[kRowsPerCta][D];
-  // launched as a programmatic dependent: wait for the kernel before this one
-  // (it may have written the new rows), then let the decode behind this one
-  // launch and set itself up while these rows are written
-  grid_dependency_wait();
+  // launched as a programmatic dependent: let the decode behind this one
+  // launch at once (it waits for this grid, and so for everything before it,
+  // before it reads q or a new row; with early_kv its older rows stream in
+  // meanwhile), then wait for the kernel before this one, which may have
+  // written the new rows
   grid_launch_dependents();
+  grid_dependency_wait();
   const int b = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = blockIdx.y * kRowsPerCta + warp;

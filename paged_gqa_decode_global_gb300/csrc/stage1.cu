@@ -173,7 +173,13 @@ __device__ __forceinline__ int stage1_cta(const Stage1Params& p, uint8_t* smem) 
   // Prologue, before the previous kernel on the stream may have finished: the
   // producer's lane 0 prefetches the tensor maps (kernel parameters) and sets
   // up the ring's barriers. Then every thread waits for that kernel: nothing
-  // below reads or writes global memory before it has completed.
+  // below reads or writes global memory before it has completed -- except,
+  // with early_kv, the producer warp's reads of the lengths, page ids, FP8
+  // scales and the cached rows older than each request's newest query_tokens
+  // positions (data the caller guarantees that kernel does not write): it
+  // waits before the first copy of a block holding a newer row, before the
+  // first copy that has to wait for a free stage, and before it leaves.
+  const bool early = p.early_kv != 0 && threadIdx.x >= C::NW * 32;
   if (threadIdx.x == C::NW * 32) {
     prefetch_tensormap(&p.kmap);
     if (!C::KVS) prefetch_tensormap(&p.vmap);
@@ -184,7 +190,7 @@ __device__ __forceinline__ int stage1_cta(const Stage1Params& p, uint8_t* smem) 
     }
     fence_barrier_init();
   }
-  grid_dependency_wait();
+  if (!early) grid_dependency_wait();
 
   const ColMap<C> cm(p);
   const int split = blockIdx.x;
@@ -235,6 +241,7 @@ __device__ __forceinline__ int stage1_cta(const Stage1Params& p, uint8_t* smem) 
 
   if (nblk == 0) {
     // nothing attended in this piece
+    if (early) grid_dependency_wait();
     if (p.cluster_merge) {
       if (threadIdx.x < C::G) reinterpret_cast<float*>(smem + C::CTA_LSE_OFFSET)[threadIdx.x] = -INFINITY;
     } else if (p.direct_out) {
@@ -303,6 +310,9 @@ __device__ __forceinline__ int stage1_cta(const Stage1Params& p, uint8_t* smem) 
     // the copies, so page-id loads never serialise the issue of copies.
     int issued = 0;
     bool stop = false;
+    bool waited = !early;
+    // blocks ending after this position hold rows the previous kernel may write
+    const int fresh_from = L - p.query_tokens;
 #pragma unroll 1
     for (int j0 = 0; j0 < nblk && !stop; j0 += 32) {
       const int page_mine = page_next;
@@ -321,6 +331,10 @@ __device__ __forceinline__ int stage1_cta(const Stage1Params& p, uint8_t* smem) 
 #pragma unroll 1
       for (int k = 0; k < cnt; ++k) {
         const int j = j0 + k;
+        if (!waited && (j >= C::NST || blk_lo + (j + 1) * C::TB > fresh_from)) {
+          grid_dependency_wait();
+          waited = true;
+        }
         const int page = __shfl_sync(kFullMask, page_mine, k);
         float2 scale_blk;
         scale_blk.x = __shfl_sync(kFullMask, scale_mine.x, k);
@@ -367,6 +381,7 @@ __device__ __forceinline__ int stage1_cta(const Stage1Params& p, uint8_t* smem) 
         issued = j + 1;
       }
     }
+    if (!waited) grid_dependency_wait();
     // no copy may still be landing in shared memory when the CTA exits (one
     // deadline for all stages)
     if (lane == 0) {

@@ -49,7 +49,7 @@ def test_build_targets_sm103a_only():
 def test_status_strings_and_version(lib):
     assert b.status_string(b.PD_OK) == "ok"
     assert "workspace" in b.status_string(b.PD_ERR_WORKSPACE_TOO_SMALL)
-    assert b.abi_version() == 4
+    assert b.abi_version() == 5
 
 
 def _plan(lens, Hq=16, Hkv=4, d=512, P=16, pages=4096, maxp=None, window=0, kv_shared=False, sms=152):
@@ -207,3 +207,15 @@ def test_head_dim_128_is_planned_for_bf16_single_token(lib):
     with pytest.raises(b.PagedDecodeError) as e:
         b.paged_decode_plan_multi(b.layer_desc(16, 4, 128, 16, 4096, 64), 2, [100], 152)
     assert e.value.status == b.PD_ERR_UNSUPPORTED
+
+
+def test_early_kv_is_a_flag_the_caller_sets(lib):
+    """pd_plan.early_kv: 0 as planned; 1 accepted; anything else refused before any launch."""
+    fake = 1 << 20
+    desc = b.layer_desc(16, 4, 512, 16, 64, 8)
+    pl = b.paged_decode_plan(desc, [100], 152)
+    assert pl.early_kv == 0
+    pl.early_kv = 2
+    st = lib.paged_decode_global(ctypes.byref(pl), fake, fake, fake, fake, fake, 1.0, fake, 1 << 20, fake, None)
+    assert st == b.PD_ERR_INVALID_ARG
+    assert lib.paged_decode_merge(ctypes.byref(pl), fake, 1 << 20, fake, None) == b.PD_ERR_INVALID_ARG

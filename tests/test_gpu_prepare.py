@@ -65,13 +65,16 @@ class GpuPrepare:
             self.cos_sin = torch.empty(pi.max_positions, pi.rot, dtype=torch.float32, device="cuda")
             b.paged_decode_rope_table(pi.theta, pi.rot, pi.max_positions, self.cos_sin)
 
-    def run(self, seq=None, table=None):
+    def launch(self, seq=None, table=None, stream=None):
         pi, li = self.pi, self.pi.layer
         b.paged_decode_qkv_norm_rope_write(_desc(li), pi.rot, pi.max_positions, pi.eps, self.q_in, self.k_in,
                                            self.v_in, self.q_w, self.k_w, self.v_w, self.cos_sin,
                                            self.table if table is None else table,
                                            self.seq if seq is None else seq, self.q_out, self.k_pool,
-                                           self.v_pool, self.flags)
+                                           self.v_pool, self.flags, stream)
+
+    def run(self, seq=None, table=None):
+        self.launch(seq, table)
         torch.cuda.synchronize()
         return int(self.flags.item())
 
@@ -139,25 +142,10 @@ def test_unit_v_weight_and_repeat_determinism():
     assert torch.equal(first[0], g.q_out) and torch.equal(first[1], g.k_pool) and torch.equal(first[2], g.v_pool)
 
 
-@pytest.mark.parametrize("case", [LAYERS[0], LAYERS[2], LAYERS[1]], ids=["global", "sliding", "global K=V"])
-def test_prepare_then_decode_matches_oracle(case):
-    """GPU: fused step then decode. Oracle: its own step, rows rounded to bf16
-    into a host copy of the pools, then its decode."""
-    pi = _make(*case, seed=23)
+def _prepared_decode_oracle(pi):
+    """The oracle's step, its rows rounded to bf16 into a host copy of the
+    pools, then its decode."""
     li = pi.layer
-    g = GpuPrepare(pi)
-    assert g.run() == 0
-    desc = _desc(li)
-    plan = b.paged_decode_plan(desc, li.seq_lens.tolist(), torch.cuda.get_device_properties(0).multi_processor_count)
-    ws = torch.zeros(max(256, plan.workspace_bytes), dtype=torch.uint8, device="cuda")
-    out = torch.empty_like(g.q_out)
-    if li.window > 0:
-        b.paged_decode_window(plan, g.q_out, g.k_pool, g.v_pool, g.table, g.seq, li.window, li.scale, ws, out)
-    else:
-        b.paged_decode_global(plan, g.q_out, g.k_pool, g.v_pool, g.table, g.seq, li.scale, ws, out)
-    b.paged_decode_merge(plan, ws, out)
-    torch.cuda.synchronize()
-
     q, k, v, page, row = _oracle(pi)
     kpool = li.k_pool.clone()
     vpool = None if li.v_pool is None else li.v_pool.clone()
@@ -166,12 +154,71 @@ def test_prepare_then_decode_matches_oracle(case):
         if vpool is not None:
             vpool[page[bi], :, row[bi], :] = torch.from_numpy(v[bi]).to(torch.bfloat16)
     q16 = torch.from_numpy(q).to(torch.bfloat16)
-    exp = oracle.decode(synth.bits_u16(q16), synth.bits_u16(kpool), None if vpool is None else synth.bits_u16(vpool),
-                        li.block_tables.numpy(), li.seq_lens.numpy(), li.scale, li.window)
+    return oracle.decode(synth.bits_u16(q16), synth.bits_u16(kpool), None if vpool is None else synth.bits_u16(vpool),
+                         li.block_tables.numpy(), li.seq_lens.numpy(), li.scale, li.window)
+
+
+def _decode_after(g, early_kv, stream=None):
+    """Stage 1 (+ merge) on the prepared cache, launched behind whatever is
+    on the stream; plan.early_kv as given."""
+    li = g.pi.layer
+    plan = b.paged_decode_plan(_desc(li), li.seq_lens.tolist(), torch.cuda.get_device_properties(0).multi_processor_count)
+    plan.early_kv = early_kv
+    ws = torch.zeros(max(256, plan.workspace_bytes), dtype=torch.uint8, device="cuda")
+    out = torch.empty_like(g.q_out)
+    if li.window > 0:
+        b.paged_decode_window(plan, g.q_out, g.k_pool, g.v_pool, g.table, g.seq, li.window, li.scale, ws, out, stream)
+    else:
+        b.paged_decode_global(plan, g.q_out, g.k_pool, g.v_pool, g.table, g.seq, li.scale, ws, out, stream)
+    b.paged_decode_merge(plan, ws, out, stream)
+    return out, plan, ws
+
+
+def _check_decode(out, exp):
     got = out.float().cpu().double().numpy()
     assert np.abs(got - exp).max() <= 2e-2
     cos = (got * exp).sum() / np.sqrt((got * got).sum() * (exp * exp).sum())
     assert cos > 0.9995
+
+
+@pytest.mark.parametrize("case", [LAYERS[0], LAYERS[2], LAYERS[1]], ids=["global", "sliding", "global K=V"])
+def test_prepare_then_decode_matches_oracle(case):
+    """GPU: fused step, a host sync, then decode; against the oracle's step + decode."""
+    pi = _make(*case, seed=23)
+    g = GpuPrepare(pi)
+    assert g.run() == 0
+    out, _, _ = _decode_after(g, 0)
+    torch.cuda.synchronize()
+    _check_decode(out, _prepared_decode_oracle(pi))
+
+
+@pytest.mark.parametrize("case", [LAYERS[0], LAYERS[2], LAYERS[1], LAYERS[3]],
+                         ids=["global", "sliding", "global K=V", "sliding K=V P32"])
+def test_prepare_then_early_decode_matches_oracle(case):
+    """The fused step and an early_kv decode back to back on one stream, no
+    host sync between: stage 1 may copy older rows while the step runs, but
+    must read each request's new row (and q) only after it. The new rows hold
+    a large sentinel before the step, so a copy taken too early shows in the
+    output; short requests put the new row in the first pipeline stages."""
+    pi = _make(*case, seed=29)
+    li = pi.layer
+    g = GpuPrepare(pi)
+    P = li.page_size
+    for bi, L in enumerate(li.seq_lens.tolist()):
+        page = int(li.block_tables[bi, (L - 1) // P])
+        g.k_pool[page, :, (L - 1) % P, :] = 64.0
+        if g.v_pool is not None:
+            g.v_pool[page, :, (L - 1) % P, :] = -64.0
+    g.q_out.fill_(0.5)
+    exp = _prepared_decode_oracle(pi)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        g.launch(stream=s)
+        out, plan, ws = _decode_after(g, 1, stream=s)
+    s.synchronize()
+    assert int(g.flags.item()) == 0
+    assert b.paged_decode_check_device_error(plan, ws, s) == 0
+    _check_decode(out, exp)
 
 
 def test_bad_length_and_bad_page_flags():
