@@ -49,14 +49,14 @@ FALLBACK_HBM_GBS = 6800.0
 # hash of the kernel sources it was taken on; stale entries are ignored (the
 # captures and their commands are summarised under profiles/).
 NCU_TRAFFIC = {
-    "2789a6171b424b01": {"w2": 67293952 + 664064, "w3": 68266752 + 603136, "w4a": 1073914112 + 3917312,
-                         "w4a-fp8": 537308672 + 3651840, "w2-t2": 67450112 + 652032},
+    "3d95dc50144f4a12": {"w2": 67295744 + 710400, "w3": 68267008 + 591360, "w4a": 1073925888 + 3737600,
+                         "w4a-fp8": 537351168 + 3902208, "w2-t2": 67450880 + 662016},
 }
 
 
 # the same for the fused QKV norm + RoPE + cache-write kernel (--op prepare)
 PREP_NCU_TRAFFIC = {
-    "dc6a82492f0e753a": {"w2": 216576},
+    "fed05ad210b6d714": {"w2": 216832},
 }
 
 STAGE1_SOURCES = ("stage1.cu", "pd_common.cuh", "pd_variants.h", "pd_kernels.h")

@@ -36,7 +36,10 @@
 //     writes bf16 output (one piece), or keeps its normalised result and
 //     log-sum-exp for rank 0 of its thread-block cluster to merge over
 //     distributed shared memory (up to 8 pieces), or writes an fp32 partial +
-//     log-sum-exp for the merge kernel (more pieces).
+//     log-sum-exp for the merge kernel (more pieces);
+//   * the grid is a programmatic dependent of the kernel before it: barriers
+//     are set up while that kernel drains, and with early_kv the producer
+//     already copies the cached rows that kernel cannot be writing.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
