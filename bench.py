@@ -10,9 +10,13 @@ batch. Timing: W warm-up steps, then exactly K steps replayed from CUDA graphs
 on one stream, bracketed by CUDA events with a synchronize (and, for N > 1, a
 barrier) on both sides. Each step reads a different replica of the K/V pools,
 and the replicas together are larger than 4x L2, so every step streams its KV
-from HBM. Prints one JSON line (rank 0).
+from HBM. The plan's early_kv flag is set (--no-early-kv clears it): a step's
+stage 1 copies its first cached blocks while the step before it drains (each
+step's rows are written by no kernel of the loop). Prints one JSON line
+(rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 1..5] [--impl ours|reference]
+                  [--op decode|prepare|layer] [--kv bf16|fp8] [--query-tokens T] [--dcp-ranks R]
 
 Under torchrun (N > 1) every rank runs an independent replica of the step
 (decode attention needs no exchange); the reported time is the max over ranks.
