@@ -493,9 +493,17 @@ def oracle_baseline(li_cpu, budget_s=10.0, q_multi=None):
         if time.perf_counter() > t_end and len(times) >= 3:
             break
     t = statistics.median(times)
+    # and once on one core
+    t0 = time.perf_counter()
+    if q_multi is None:
+        oracle.decode(q, k, v, bt, sl, li_cpu.scale, li_cpu.window, nthreads=1)
+    else:
+        oracle.decode_multi(q, k, v, bt, sl, li_cpu.scale, li_cpu.window, nthreads=1)
+    t1 = time.perf_counter() - t0
     return {"value": round(t * 1e6, 1), "unit": UNIT, "cores": threads, "kind": "oracle",
             "sample": f"full layer-step ({li_cpu.batch}x{li_cpu.num_q_heads} rows, {sum(li_cpu.attended())} "
-                      f"attended tokens), median of {len(times)} runs, fp64 C + OpenMP"}
+                      f"attended tokens), median of {len(times)} runs, fp64 C + OpenMP",
+            "single_thread_value": round(t1 * 1e6, 1)}
 
 
 def oracle_prepare_us(li_cpu, seed) -> float:
