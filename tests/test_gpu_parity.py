@@ -51,7 +51,20 @@ def compare(gpu_out, ref, li, tag=""):
     cos = float(g @ r / (np.linalg.norm(g) * np.linalg.norm(r))) if g.size else 1.0
     assert err <= MAX_ABS, f"{tag}: max abs {err:.3e}"
     assert cos > MIN_COS, f"{tag}: cosine {cos:.7f}"
-    return err, cos
+    # per (request, head) row as well: at long contexts the outputs are small and
+    # max |err| alone says little. Two bf16 roundings of at most 2^-9 relative
+    # each (the probabilities entering PV, and the output) bound the relative
+    # L2 error near 2^-8 = 3.9e-3 (allowed: 5e-3), and so 1 - cosine of any row
+    # near (5e-3)^2 / 2 (allowed: 1e-4)
+    gr, rr = got[~empty], ref[~empty]
+    num = (gr * rr).sum(-1)
+    den = np.linalg.norm(gr, axis=-1) * np.linalg.norm(rr, axis=-1)
+    ok = den > 0
+    row_cos = float((num[ok] / den[ok]).min()) if ok.any() else 1.0
+    rel_l2 = float(np.linalg.norm(g - r) / np.linalg.norm(r)) if g.size and np.linalg.norm(r) > 0 else 0.0
+    assert row_cos > 0.9999, f"{tag}: worst row cosine {row_cos:.6f}"
+    assert rel_l2 < 5e-3, f"{tag}: relative L2 {rel_l2:.3e}"
+    return err, cos, row_cos, rel_l2
 
 
 # ---- the five named workloads at full size -------------------------------------
@@ -61,8 +74,9 @@ def compare(gpu_out, ref, li, tag=""):
 def test_workload_matches_oracle(cid, part):
     for li in synth.workload(cid, device="cuda", part=part):
         out, step = run_gpu(li)
-        err, cos = compare(out, run_oracle(li), li, f"{li.name} S={step.plan.num_splits}")
-        print(f"{li.name}: splits {step.plan.num_splits} chunk {step.plan.chunk_tokens} max_abs {err:.2e} cos {cos:.7f}")
+        err, cos, row_cos, rel = compare(out, run_oracle(li), li, f"{li.name} S={step.plan.num_splits}")
+        print(f"{li.name}: splits {step.plan.num_splits} chunk {step.plan.chunk_tokens} max_abs {err:.2e} "
+              f"cos {cos:.7f} worst row cos {row_cos:.6f} rel L2 {rel:.2e}")
 
 
 # ---- every kernel instance on ragged batches ----------------------------------
@@ -304,8 +318,9 @@ def test_fp8_workload_matches_oracle(cid, part):
     for li in synth.workload(cid, device="cuda", part=part):
         f = synth.quantize_kv_fp8(li)
         out, step = run_gpu(f)
-        err, cos = compare(out, run_oracle_fp8(f), f, f"{f.name} S={step.plan.num_splits}")
-        print(f"{f.name}: splits {step.plan.num_splits} max_abs {err:.2e} cos {cos:.7f}")
+        err, cos, row_cos, rel = compare(out, run_oracle_fp8(f), f, f"{f.name} S={step.plan.num_splits}")
+        print(f"{f.name}: splits {step.plan.num_splits} max_abs {err:.2e} cos {cos:.7f} worst row cos {row_cos:.6f} "
+              f"rel L2 {rel:.2e}")
 
 
 def test_fp8_nan_bytes_in_unattended_rows_do_not_leak():
