@@ -763,7 +763,8 @@ def run_dcp(args, world, rank, local):
     pools = [(k, v)] + [(k.clone(), None if v is None else v.clone()) for _ in range(replicas - 1)]
     desc = pdb.layer_desc(li.num_q_heads, li.num_kv_heads, li.head_dim, li.page_size, k.shape[0], table.shape[1],
                           0, li.kv_shared)
-    step = dcp.PartialStep(desc, lens.tolist(), torch.cuda.get_device_properties(dev).multi_processor_count, dev)
+    step = dcp.PartialStep(desc, lens.tolist(), torch.cuda.get_device_properties(dev).multi_processor_count, dev,
+                           early_kv=args.early_kv)
     B, Hq, d = li.q.shape
     o_all = torch.zeros(R, B, Hq, d, dtype=torch.float32, device=dev)
     lse_all = torch.full((R, B, Hq), -float("inf"), dtype=torch.float32, device=dev)
@@ -820,7 +821,7 @@ def run_dcp(args, world, rank, local):
             "warmup": max(3, args.warmup), "ms_per_step": round(us / 1e3, 6), "higher_is_better": False,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "io_dtype": "bf16", "data": "synthetic",
             "config": {"workload": synth.WORKLOADS[args.workload] + (f" [{li.name}]" if args.part else ""),
-                       "dcp_ranks": R, "shard": "interleaved positions, rank 0",
+                       "dcp_ranks": R, "shard": "interleaved positions, rank 0", "early_kv": bool(args.early_kv),
                        "shard_kv_bytes": shard_bytes, "exchange": "all-gather of (o, lse) not timed (needs R GPUs)",
                        "l2": f"{replicas} rotating shard replicas", "launch": "CUDA graph replay, one stream"},
             "kv_gbs": round(shard_bytes / (us * 1e-6) / 1e9, 1),

@@ -89,8 +89,11 @@ def exchange_partials(o: torch.Tensor, lse: torch.Tensor, group=None) -> Tuple[t
 class PartialStep:
     """Plan + workspace for this rank's partial decode of one global layer."""
 
-    def __init__(self, desc: binding.LayerDesc, local_lens: Sequence[int], sm_count: int, device):
+    def __init__(self, desc: binding.LayerDesc, local_lens: Sequence[int], sm_count: int, device,
+                 early_kv: bool = False):
         self.plan = binding.paged_decode_plan_partial(desc, list(local_lens), sm_count)
+        # the caller's promise about the kernels before each call (pd_plan.early_kv)
+        self.plan.early_kv = 1 if early_kv else 0
         nbytes = int(self.plan.workspace_bytes)
         self.workspace = torch.zeros((nbytes + 255) // 256 * 256, dtype=torch.uint8, device=device)
 

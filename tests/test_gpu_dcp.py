@@ -31,8 +31,8 @@ def _desc(li, num_pages, max_pages):
                         li.v_pool is None)
 
 
-def _partial(li, k, v, table, lens):
-    step = dcp.PartialStep(_desc(li, k.shape[0], table.shape[1]), lens.tolist(), _sms(), "cuda")
+def _partial(li, k, v, table, lens, early_kv=False):
+    step = dcp.PartialStep(_desc(li, k.shape[0], table.shape[1]), lens.tolist(), _sms(), "cuda", early_kv=early_kv)
     o, lse = step(li.q, k, v, table, lens, li.scale)
     torch.cuda.synchronize()
     return o, lse
@@ -99,3 +99,19 @@ def test_partial_plan_rules():
     with pytest.raises(b.PagedDecodeError) as e:
         b.paged_decode_plan_partial(win, [16], _sms())
     assert e.value.status == b.PD_ERR_UNSUPPORTED
+
+
+def test_early_kv_ranks_back_to_back():
+    """The virtual ranks' partials with early_kv, queued back to back with no
+    host sync (each rank's stage 1 copying while the previous rank's launches
+    drain), then combined: equal to the unsharded oracle."""
+    R = 3
+    pool = sum((L + 15) // 16 for L in LENS) + 3
+    li = synth.make_layer("dcp", LENS, 16, 4, 512, pool_pages=pool, seed=41, device="cuda")
+    shards = [dcp.shard_cache(li.k_pool, li.v_pool, li.block_tables, LENS, R, r, "interleaved") for r in range(R)]
+    steps = [dcp.PartialStep(_desc(li, k.shape[0], t.shape[1]), n.tolist(), _sms(), "cuda", early_kv=True)
+             for k, _, t, n in shards]
+    outs = [step(li.q, k, v, t, n, li.scale) for step, (k, v, t, n) in zip(steps, shards)]
+    out = dcp.combine(torch.stack([o for o, _ in outs]), torch.stack([lse for _, lse in outs]))
+    torch.cuda.synchronize()
+    _compare(out, _full_oracle(li), "early_kv ranks")
