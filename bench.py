@@ -54,7 +54,8 @@ FALLBACK_HBM_GBS = 6800.0
 # captures and their commands are summarised under profiles/).
 NCU_TRAFFIC = {
     "3d95dc50144f4a12": {"w2": 67295744 + 710400, "w3": 68267008 + 591360, "w4a": 1073925888 + 3737600,
-                         "w4a-fp8": 537351168 + 3902208, "w2-t2": 67450880 + 662016},
+                         "w4a-fp8": 537351168 + 3902208, "w2-t2": 67450880 + 662016,
+                         "w5global-fp8": 799140352 + 5286400},
 }
 
 
