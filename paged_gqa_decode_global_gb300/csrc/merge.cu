@@ -28,7 +28,7 @@ namespace pd {
 
 namespace {
 
-constexpr int kMergeMaxSplits = 1024;
+constexpr int kMergeMaxSplits = 1024;  // pieces of one row (the plan's cap, and the combine's rank limit)
 constexpr int kMergeThreads = 128;  // 4 dims a thread: 512 dims a CTA
 
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams p) {

@@ -33,8 +33,8 @@ namespace {
 
 constexpr uint32_t kPlanMagic = 0x50444543u;  // "PDEC"
 constexpr int32_t kAbiVersion = 5;
-// Pieces per (request, KV head) are capped (the merge stages their weights in
-// shared memory).
+// Pieces per (request, KV head) are capped at what the merge kernel takes
+// (and far above what the cost model ever picks: a few waves of the GPU).
 constexpr int kMaxSplits = 1024;
 
 // Query tokens per request a plan may carry (multi-token variants).
