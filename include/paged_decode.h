@@ -49,7 +49,14 @@
  * and out). The library allocates and frees nothing, keeps no state between
  * calls, and never synchronises except in paged_decode_check_device_error.
  * Every launch is ordered on the given stream (a cudaStream_t passed as void*;
- * NULL = the legacy default stream).
+ * NULL = the legacy default stream). The kernels go out as programmatic
+ * dependents (they may become resident while the kernel before them drains,
+ * and wait for it before touching what it may write; see pd_plan.early_kv for
+ * the one exception a caller can opt into), and each lets the launch behind it
+ * start early: a caller's kernel launched behind one of them with
+ * programmatic stream serialisation must wait for it (griddepcontrol.wait,
+ * cudaGridDependencySynchronize) before reading its output. Kernels launched
+ * without that attribute, copies and events are ordered as usual.
  *
  * Errors: no exception or trap crosses this boundary. Host-side argument checks
  * return a status without launching anything. Conditions only the GPU can see
