@@ -11,12 +11,13 @@
 // workspace ([rows][S] pieces) and partial results gathered from several ranks
 // ([S][rows]), to bf16, or to fp32 with the merged log-sum-exp.
 //
-// Grid (row, 512-dim slice of the row), head_dim / 4 threads (at most 128)
-// each, launched behind stage 1 as a programmatic dependent (it waits for stage
-// 1 before reading). Every warp reduces the row's S log-sum-exps itself, and
-// each lane sums its 4 dims over the pieces with independent 16-byte loads in
-// flight, taking the weights of 32 pieces at a time from the lanes that
-// computed them. The kernel holds no shared memory, so one of its CTAs fits
+// Grid (row, 128-dim slice of the row), 128 threads, launched behind stage 1
+// as a programmatic dependent (it waits for stage 1 before reading). Every
+// warp reduces the row's S log-sum-exps itself; then lane 4c + g of warp w
+// sums float4 column 8w + c of the slice over pieces g, g + 4, g + 8, ...
+// (eight lanes of one piece group read 128 contiguous bytes of a piece, and
+// all of a lane's loads are in flight together), and two shuffles add the
+// four groups. The kernel holds no shared memory, so one of its CTAs fits
 // beside a stage-1 CTA of the next launch on the same SM.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -29,7 +30,8 @@ namespace pd {
 namespace {
 
 constexpr int kMergeMaxSplits = 1024;  // pieces of one row (the plan's cap, and the combine's rank limit)
-constexpr int kMergeThreads = 128;  // 4 dims a thread: 512 dims a CTA
+constexpr int kMergeThreads = 128;  // 32 float4 columns x 4 piece groups: 128 dims a CTA
+constexpr int kMergeGroups = 4;
 
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams p) {
   grid_dependency_wait();  // stage 1 (launched before this grid) has finished
@@ -37,7 +39,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
   // grid before it reads anything this grid writes)
   grid_launch_dependents();
   const size_t row = blockIdx.x;
-  const int lane = threadIdx.x & 31;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int S = p.num_splits;
   const float* lse = p.lse_part + row * p.lse_row_stride;
   float M = -INFINITY;
@@ -53,27 +55,32 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
   const float inv = sum > 0.f ? 1.f / sum : 0.f;
   const int D4 = p.head_dim / 4;
   if (p.out_lse && blockIdx.y == 0 && threadIdx.x == 0) p.out_lse[row] = sum > 0.f ? M + __logf(sum) : -INFINITY;
-  const int d4 = blockIdx.y * kMergeThreads + threadIdx.x;
+  const int g = lane % kMergeGroups;
+  const int d4 = blockIdx.y * (kMergeThreads / kMergeGroups) + warp * (32 / kMergeGroups) + lane / kMergeGroups;
   const bool active = d4 < D4;
-  const float* src = p.o_part + row * p.row_stride + d4 * 4;
+  const float* src = p.o_part + row * p.row_stride + (size_t)d4 * 4;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int s0 = 0; s0 < S; s0 += 32) {
-    // lane k's weight is piece s0 + k's
-    const int s = s0 + lane;
-    const float wl = (s < S && M != -INFINITY) ? exp2f((lse[s * p.lse_piece_stride] - M) * kLog2e) * inv : 0.f;
-    const int n = min(32, S - s0);
-#pragma unroll 8
-    for (int k = 0; k < n; ++k) {
-      const float ws = __shfl_sync(0xffffffffu, wl, k);
-      if (ws == 0.f || !active) continue;  // an empty piece (its row may never have been written)
-      const float4 o = *reinterpret_cast<const float4*>(src + (size_t)(s0 + k) * p.piece_stride);
+  if (active && M != -INFINITY) {
+#pragma unroll 4
+    for (int s = g; s < S; s += kMergeGroups) {
+      const float ws = exp2f((lse[s * p.lse_piece_stride] - M) * kLog2e) * inv;
+      if (ws == 0.f) continue;  // an empty piece (its row may never have been written)
+      const float4 o = *reinterpret_cast<const float4*>(src + (size_t)s * p.piece_stride);
       acc.x = fmaf(ws, o.x, acc.x);
       acc.y = fmaf(ws, o.y, acc.y);
       acc.z = fmaf(ws, o.z, acc.z);
       acc.w = fmaf(ws, o.w, acc.w);
     }
   }
-  if (!active) return;
+  // the four piece groups of a column sit in four neighbouring lanes
+#pragma unroll
+  for (int m = 1; m < kMergeGroups; m <<= 1) {
+    acc.x += __shfl_xor_sync(0xffffffffu, acc.x, m);
+    acc.y += __shfl_xor_sync(0xffffffffu, acc.y, m);
+    acc.z += __shfl_xor_sync(0xffffffffu, acc.z, m);
+    acc.w += __shfl_xor_sync(0xffffffffu, acc.w, m);
+  }
+  if (!active || g != 0) return;
   if (p.out) {
     __nv_bfloat162* out =
         reinterpret_cast<__nv_bfloat162*>(reinterpret_cast<__nv_bfloat16*>(p.out) + row * p.head_dim) + d4 * 2;
@@ -91,9 +98,9 @@ int launch_merge(const MergeParams& p, int rows, void* stream) {
   // launched with programmatic stream serialisation: its CTAs may become
   // resident while stage 1 drains and wait there for its completion
   cudaLaunchConfig_t cfg = {};
-  const int d4 = p.head_dim / 4;
-  cfg.gridDim = dim3(rows, (d4 + kMergeThreads - 1) / kMergeThreads);
-  cfg.blockDim = dim3(d4 < kMergeThreads ? (d4 + 31) / 32 * 32 : kMergeThreads);
+  constexpr int kCols = kMergeThreads / kMergeGroups;  // float4 columns a CTA
+  cfg.gridDim = dim3(rows, (p.head_dim / 4 + kCols - 1) / kCols);
+  cfg.blockDim = dim3(kMergeThreads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = static_cast<cudaStream_t>(stream);
   cudaLaunchAttribute attr[1];
