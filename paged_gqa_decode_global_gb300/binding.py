@@ -23,6 +23,9 @@ PD_ERR_WORKSPACE_TOO_SMALL = 3
 PD_ERR_CUDA = 4
 PD_ERR_DEVICE_FAULT = 5
 
+# layout of pd_plan / pd_layer_desc this binding marshals (paged_decode_abi_version)
+ABI_VERSION = 5
+
 PD_KV_BF16 = 0
 PD_KV_FP8_E4M3 = 1
 
@@ -154,6 +157,10 @@ def load_library(path: Optional[str] = None):
         lib.paged_decode_rope_table.restype = ctypes.c_int
         lib.paged_decode_qkv_norm_rope_write.argtypes = [ctypes.POINTER(LayerDesc), i32, i32, i32, f32] + [vp] * 14
         lib.paged_decode_qkv_norm_rope_write.restype = ctypes.c_int
+        found = int(lib.paged_decode_abi_version())
+        if found != ABI_VERSION:
+            raise RuntimeError(f"{p} has ABI version {found}, this binding marshals version {ABI_VERSION}: rebuild it "
+                               "with `python -m paged_gqa_decode_global_gb300.build`")
         if path is None:
             _lib = lib
         return lib

@@ -49,7 +49,7 @@ def test_build_targets_sm103a_only():
 def test_status_strings_and_version(lib):
     assert b.status_string(b.PD_OK) == "ok"
     assert "workspace" in b.status_string(b.PD_ERR_WORKSPACE_TOO_SMALL)
-    assert b.abi_version() == 5
+    assert b.abi_version() == 5 == b.ABI_VERSION
 
 
 def _plan(lens, Hq=16, Hkv=4, d=512, P=16, pages=4096, maxp=None, window=0, kv_shared=False, sms=152):
