@@ -219,3 +219,55 @@ def test_early_kv_is_a_flag_the_caller_sets(lib):
     st = lib.paged_decode_global(ctypes.byref(pl), fake, fake, fake, fake, fake, 1.0, fake, 1 << 20, fake, None)
     assert st == b.PD_ERR_INVALID_ARG
     assert lib.paged_decode_merge(ctypes.byref(pl), fake, 1 << 20, fake, None) == b.PD_ERR_INVALID_ARG
+
+
+def test_planner_invariants_on_random_shapes(lib):
+    """300 seeded random layer shapes and batches, decode / multi-token / partial
+    plans, bf16 and FP8: every plan covers every attended token, its grid and
+    workspace match its merge mode, and stage 1 launches fit the hardware."""
+    import numpy as np
+    rng = np.random.default_rng(20261202)
+    shapes = [(512, 0), (256, 0), (256, 1024), (512, 64), (128, 0)]
+    made = {0: 0, 1: 0, 2: 0}
+    for _ in range(300):
+        d, window = shapes[rng.integers(len(shapes))]
+        Hkv = int(rng.choice([1, 2, 4, 8]))
+        G = int(rng.choice([1, 2, 4, 8]))
+        kvs = bool(rng.integers(2))
+        fp8 = d != 128 and bool(rng.integers(2))
+        T = 1 if d == 128 or rng.random() < 0.6 else int(rng.integers(2, 9))
+        partial = T == 1 and window == 0 and not fp8 and rng.random() < 0.2
+        B = int(rng.integers(1, 40))
+        lens = [int(x) for x in np.exp(rng.uniform(np.log(T), np.log(200000), B)).astype(int)]
+        lens = [max(L, T) for L in lens]
+        maxp = max((L + 15) // 16 for L in lens)
+        sms = int(rng.choice([1, 20, 148, 152, 1000]))
+        desc = b.layer_desc(Hkv * G, Hkv, d, 16, 10 ** 6, maxp, window, kvs,
+                            b.PD_KV_FP8_E4M3 if fp8 else b.PD_KV_BF16)
+        if partial:
+            pl = b.paged_decode_plan_partial(desc, lens, sms)
+        elif T > 1:
+            pl = b.paged_decode_plan_multi(desc, T, lens, sms)
+        else:
+            pl = b.paged_decode_plan(desc, lens, sms)
+        S, chunk, TB = pl.num_splits, pl.chunk_tokens, pl.block_tokens
+        assert chunk % 16 == 0 and 1 <= S <= 1024
+        for L in lens:
+            first_hi = L - T + 1
+            lo = first_hi - window if window and first_hi > window else 0
+            assert S * chunk >= L - (lo // TB) * TB  # every attended token is in some piece
+        tiles = (T * G + 7) // 8 if T > 1 else 1
+        assert (pl.grid_x, pl.grid_y, pl.grid_z) == (S, Hkv * tiles, B)
+        assert pl.threads_per_cta in (128, 256) and 0 < pl.smem_bytes <= 227 * 1024
+        assert pl.query_tokens == T and pl.partial == int(partial) and pl.early_kv == 0
+        rows = B * T * Hkv * G
+        if pl.merge_mode == 1:
+            assert pl.opart_offset >= pl.lse_offset + rows * S * 4 >= 256
+            assert pl.workspace_bytes >= pl.opart_offset + rows * S * d * 4
+        else:
+            assert not partial and pl.workspace_bytes >= 4
+            assert (pl.merge_mode == 0) == (S == 1)
+            if pl.merge_mode == 2:
+                assert 2 <= S <= 8
+        made[pl.merge_mode] += 1
+    assert all(made.values()), made  # every merge mode was planned for some shape
