@@ -72,9 +72,17 @@ def compare(gpu_out, ref, li, tag=""):
 @pytest.mark.parametrize("cid,part", [(1, None), (2, None), (3, None), (4, "a"), (4, "b"), (4, "c"),
                                       (5, "global"), (5, "sliding")])
 def test_workload_matches_oracle(cid, part):
+    """Full size, in the launch configuration bench.py times: the plan's
+    early_kv set, two steps queued back to back with no host sync (the second
+    copying its first blocks while the first drains); both against the oracle."""
     for li in synth.workload(cid, device="cuda", part=part):
-        out, step = run_gpu(li)
-        err, cos, row_cos, rel = compare(out, run_oracle(li), li, f"{li.name} S={step.plan.num_splits}")
+        step = b.LayerStep.for_inputs(li, early_kv=True)
+        first = step.run(li, torch.full_like(li.q, float("nan")))
+        out = step.run(li, torch.full_like(li.q, float("nan")))
+        assert step.check() == 0
+        ref = run_oracle(li)
+        compare(first, ref, li, f"{li.name} first step")
+        err, cos, row_cos, rel = compare(out, ref, li, f"{li.name} S={step.plan.num_splits}")
         print(f"{li.name}: splits {step.plan.num_splits} chunk {step.plan.chunk_tokens} max_abs {err:.2e} "
               f"cos {cos:.7f} worst row cos {row_cos:.6f} rel L2 {rel:.2e}")
 
@@ -317,8 +325,13 @@ def test_fp8_variants_ragged(d, G, kvs, window):
 def test_fp8_workload_matches_oracle(cid, part):
     for li in synth.workload(cid, device="cuda", part=part):
         f = synth.quantize_kv_fp8(li)
-        out, step = run_gpu(f)
-        err, cos, row_cos, rel = compare(out, run_oracle_fp8(f), f, f"{f.name} S={step.plan.num_splits}")
+        step = b.LayerStep.for_inputs(f, early_kv=True)
+        first = step.run(f, torch.full_like(f.q, float("nan")))
+        out = step.run(f, torch.full_like(f.q, float("nan")))
+        assert step.check() == 0
+        ref = run_oracle_fp8(f)
+        compare(first, ref, f, f"{f.name} first step")
+        err, cos, row_cos, rel = compare(out, ref, f, f"{f.name} S={step.plan.num_splits}")
         print(f"{f.name}: splits {step.plan.num_splits} max_abs {err:.2e} cos {cos:.7f} worst row cos {row_cos:.6f} "
               f"rel L2 {rel:.2e}")
 
