@@ -878,6 +878,11 @@ def run_reference_multi(args, world):
     k = synth.bits_u16(li.k_pool)
     v = None if li.v_pool is None else synth.bits_u16(li.v_pool)
     lens = li.seq_lens_list()
+    fp8 = args.kv == "fp8"
+    if fp8:  # token j of a request is the FP8 decode at length L - T + 1 + j (what the multi-token pins show)
+        f8 = synth.quantize_kv_fp8(li)
+        k8, v8 = f8.k8.numpy(), None if f8.v8 is None else f8.v8.numpy()
+        ks, vs = f8.k_scale.numpy(), None if f8.v_scale is None else f8.v_scale.numpy()
 
     def pairs(L):
         return sum(min(L - T + 1 + j, li.window) if li.window else L - T + 1 + j for j in range(T)) * li.num_q_heads
@@ -887,8 +892,13 @@ def run_reference_multi(args, world):
     def sample(i):
         bi = i % li.batch
         t0 = time.perf_counter()
-        oracle.decode_multi(synth.bits_u16(q[bi:bi + 1]), k, v, li.block_tables[bi:bi + 1].numpy(),
-                            np.array([lens[bi]], np.int32), li.scale, li.window)
+        if fp8:
+            for j in range(T):
+                oracle.decode_fp8(synth.bits_u16(q[bi:bi + 1, j]), k8, v8, ks, vs, li.block_tables[bi:bi + 1].numpy(),
+                                  np.array([lens[bi] - T + 1 + j], np.int32), li.scale, li.window)
+        else:
+            oracle.decode_multi(synth.bits_u16(q[bi:bi + 1]), k, v, li.block_tables[bi:bi + 1].numpy(),
+                                np.array([lens[bi]], np.int32), li.scale, li.window)
         return time.perf_counter() - t0, pairs(lens[bi])
 
     for i in range(args.warmup):
@@ -904,7 +914,7 @@ def run_reference_multi(args, world):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(us / 1e3, 6),
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": synth.WORKLOADS[args.workload], "batch": li.batch, "head_dim": li.head_dim,
-                   "query_tokens": T},
+                   "query_tokens": T, "kv": args.kv},
         "cpu_baseline": {"value": round(us, 3), "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
                          "sample": "one request's T x Hq rows per step, time scaled linearly to a full layer-step"},
         "e2e": {"value": round(us, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -925,8 +935,14 @@ def run_reference(args, world, rank):
     import oracle
     li = workload_layer(args.workload, args.part, "cpu")
     q = synth.bits_u16(li.q)
-    k = synth.bits_u16(li.k_pool)
-    v = None if li.v_pool is None else synth.bits_u16(li.v_pool)
+    fp8 = args.kv == "fp8"
+    if fp8:  # the FP8 oracle over the e4m3 cache the GPU arm decodes
+        f8 = synth.quantize_kv_fp8(li)
+        k8, v8 = f8.k8.numpy(), None if f8.v8 is None else f8.v8.numpy()
+        ks, vs = f8.k_scale.numpy(), None if f8.v_scale is None else f8.v_scale.numpy()
+    else:
+        k = synth.bits_u16(li.k_pool)
+        v = None if li.v_pool is None else synth.bits_u16(li.v_pool)
     bt = li.block_tables.numpy()
     full_lens = li.seq_lens.numpy().astype(np.int32)
     threads = oracle.max_threads()
@@ -939,7 +955,10 @@ def run_reference(args, world, rank):
         if li.window > 0:
             lens = full_lens  # the window bounds the work already
         t0 = time.perf_counter()
-        oracle.decode(q, k, v, bt, lens, li.scale, li.window, rows=rows)
+        if fp8:
+            oracle.decode_fp8(q, k8, v8, ks, vs, bt, lens, li.scale, li.window, rows=rows)
+        else:
+            oracle.decode(q, k, v, bt, lens, li.scale, li.window, rows=rows)
         dt = time.perf_counter() - t0
         att = [min(int(L), li.window) if li.window else int(L) for L in lens]
         done = sum(att[r // li.num_q_heads] for r in rows)
@@ -968,7 +987,8 @@ def run_reference(args, world, rank):
         "value": round(us_per_step, 3), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(us_per_step / 1e3, 6),
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": synth.WORKLOADS[args.workload], "batch": li.batch, "head_dim": li.head_dim},
+        "config": {"workload": synth.WORKLOADS[args.workload], "batch": li.batch, "head_dim": li.head_dim,
+                   "kv": args.kv},
         "cpu_baseline": {"value": round(us_per_step, 3), "unit": UNIT, "cores": len(rows), "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(us_per_step, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
