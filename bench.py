@@ -33,6 +33,8 @@ import subprocess
 import sys
 import time
 
+from typing import Optional
+
 import torch
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -80,14 +82,46 @@ def kernel_source_hash(sources=STAGE1_SOURCES) -> str:
     return h.hexdigest()[:16]
 
 
+def hbm_peak_from(data) -> Optional[float]:
+    """The measured HBM copy bandwidth (GB/s) in a peaks record: the number under
+    a key naming HBM and GB/s ("hbm_gbs", "hbm_GBs", "hbm_copy_gbs", ...), at the
+    top level or one level down, or such a key's {"value": ...}; None if absent."""
+    def number(v):
+        if isinstance(v, dict):
+            v = v.get("value", v.get("gbs"))
+        return float(v) if isinstance(v, (int, float)) and not isinstance(v, bool) and v > 0 else None
+
+    def scan(d):
+        for key, v in d.items():
+            k = key.lower()
+            if "hbm" in k and "gbs" in k.replace("/", "").replace("_", ""):
+                x = number(v)
+                if x is not None:
+                    return x
+        return None
+
+    if not isinstance(data, dict):
+        return None
+    x = scan(data)
+    if x is None:
+        for key, v in data.items():
+            if isinstance(v, dict):
+                x = scan(v) if "hbm" not in key.lower() else (number(v) or scan(v))
+                if x is not None:
+                    break
+    return x
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
-        with open(path) as f:
-            data = json.load(f)
-        for key in ("hbm_gbs", "hbm_GBs", "hbm_copy_gbs"):
-            if key in data:
-                return float(data[key]), "measured"
+        try:
+            with open(path) as f:
+                x = hbm_peak_from(json.load(f))
+        except (OSError, ValueError):
+            x = None
+        if x is not None:
+            return x, "measured"
     return FALLBACK_HBM_GBS, "fallback"
 
 
