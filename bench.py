@@ -32,7 +32,6 @@ import statistics
 import subprocess
 import sys
 import time
-
 from typing import Optional
 
 import torch
