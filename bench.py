@@ -1,16 +1,20 @@
 #!/usr/bin/env python
 """Benchmark of one decode layer-step (stage 1 + stage 2) of paged GQA decode.
 
-Default workload: global-layer decode, batch 8, 16 query / 4 KV heads,
-head_dim 512, 1024 cached tokens per request, 16-token pages shuffled across a
-4096-page pool, K and V in separate pools (bf16).
+Default workload: long-context global-layer decode with split-K, batch 4 x
+32768 cached tokens, 16 query / 4 KV heads, head_dim 512, 16-token pages
+shuffled across an 8192-page pool, K and V in separate pools (bf16), q with
+std 0.5: 1 GiB of KV per layer-step. --workload 1..5 (and --part) select the
+other workloads.
 
 A "step" is one layer-step: the stage-1 launch and the merge launch over one
-batch. Timing: W warm-up steps, then exactly K steps replayed from CUDA graphs
-on one stream, bracketed by CUDA events with a synchronize (and, for N > 1, a
-barrier) on both sides. Each step reads a different replica of the K/V pools,
-and the replicas together are larger than 4x L2, so every step streams its KV
-from HBM. The plan's early_kv flag is set (--no-early-kv clears it): a step's
+batch. Timing: W warm-up steps, then regions of exactly K steps replayed from
+CUDA graphs on one stream, each bracketed by CUDA events with a synchronize
+(and, for N > 1, a barrier) on both sides; the region is timed several times
+(at least 5, about 0.4 s in all) and the median is reported (max over ranks).
+Each step reads a different replica of the K/V pools when one step's KV is
+smaller than L2, and the replicas together are larger than 4x L2, so every
+step streams its KV from HBM. The plan's early_kv flag is set (--no-early-kv clears it): a step's
 stage 1 copies its first cached blocks while the step before it drains (each
 step's rows are written by no kernel of the loop). Prints one JSON line
 (rank 0).
@@ -246,6 +250,56 @@ def config_of(li, cid, part, replicas, plan):
     }
 
 
+def timed_regions(graphs, stream, world, local, sample_clocks=False, stats=None, min_regions=5,
+                  max_regions=400, budget_s=0.4):
+    """Time the K-step region (one replay of every graph in `graphs`, on
+    `stream`) several times and return the median region in ms, with the clock
+    samples taken meanwhile. Each region is bracketed by a synchronize and a
+    barrier on both sides and timed by CUDA events on `stream`. The number of
+    regions (at least min_regions, about budget_s of timed work, at most
+    max_regions) is agreed across ranks from the first region's time; the
+    median is then taken per rank and the max over ranks reported."""
+    # CUDAGraph.replay() launches on the current stream: make it `stream`,
+    # the stream the events are recorded on
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+
+    def region():
+        torch.cuda.synchronize()
+        barrier(world)
+        with torch.cuda.stream(stream):
+            start.record(stream)
+            for g in graphs:
+                g.replay()
+            end.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        return start.elapsed_time(end)
+
+    with torch.cuda.stream(stream):
+        for g in graphs[:1]:  # warm the graph exec once
+            g.replay()
+    torch.cuda.synchronize()
+    barrier(world)
+    sampler = ClockSampler(local) if sample_clocks else None
+    if sampler:
+        sampler.__enter__()
+    times = [region()]
+    n = int(min(max_regions, max(min_regions, math.ceil(budget_s * 1e3 / max(times[0], 1e-3)))))
+    n = int(max_over_ranks(float(n), world))
+    while len(times) < n:
+        times.append(region())
+    if sampler:
+        sampler.__exit__(None, None, None)
+    med = statistics.median(times)
+    if stats is not None:
+        stats.clear()
+        stats.update({"regions": len(times), "statistic": "median over regions of K steps (max over ranks)",
+                      "region_ms_min": round(min(times), 4), "region_ms_median": round(med, 4),
+                      "region_ms_max": round(max(times), 4)})
+    return med, (sampler.summary() if sampler else None)
+
+
 # ----------------------------------------------------------------------------
 # our arm
 # ----------------------------------------------------------------------------
@@ -349,38 +403,19 @@ def run_ours(args, world, rank, local):
         return graphs
 
     def timed(graphs, sample_clocks=False):
-        # CUDAGraph.replay() launches on the current stream: make it `stream`,
-        # the stream the events are recorded on
-        start = torch.cuda.Event(enable_timing=True)
-        end = torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            for g in graphs[:1]:  # warm the graph exec once
-                g.replay()
-        torch.cuda.synchronize()
-        barrier(world)
-        sampler = ClockSampler(local) if sample_clocks else None
-        if sampler:
-            sampler.__enter__()
-        torch.cuda.synchronize()
-        with torch.cuda.stream(stream):
-            start.record(stream)
-            for g in graphs:
-                g.replay()
-            end.record(stream)
-        torch.cuda.synchronize()
-        if sampler:
-            sampler.__exit__(None, None, None)
-        barrier(world)
-        return start.elapsed_time(end), (sampler.summary() if sampler else None)
+        return timed_regions(graphs, stream, world, local, sample_clocks, region_stats)
 
     K = args.steps
+    region_stats = {}
     step_graphs = capture(K)
     elapsed_ms, clocks = timed(step_graphs, sample_clocks=True)
+    step_regions = dict(region_stats)
     # a region with rejected clocks on any rank is measured once more, by every rank
     if max_over_ranks(1.0 if clocks_rejected(clocks) else 0.0, world) > 0:
         first = clocks
         elapsed_ms, clocks = timed(step_graphs, sample_clocks=True)
         clocks = dict(clocks, remeasured_after=first)
+        step_regions = dict(region_stats)
     elapsed_ms = max_over_ranks(elapsed_ms, world)
     del step_graphs
     s1_graphs = capture(K, stage1_only=True)
@@ -515,6 +550,7 @@ def run_ours(args, world, rank, local):
             "e2e": e2e,
             "gpu_launches": K * launches_per_step,
             "clocks": clocks,
+            "timing": step_regions,
             "device": torch.cuda.get_device_name(dev),
         }
         print(json.dumps(line), flush=True)
@@ -683,25 +719,7 @@ def run_prepare(args, world, rank, local):
         return out
 
     def timed(graphs, sample_clocks=False):
-        start = torch.cuda.Event(enable_timing=True)
-        end = torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            graphs[0].replay()
-        torch.cuda.synchronize()
-        barrier(world)
-        sampler = ClockSampler(local) if sample_clocks else None
-        if sampler:
-            sampler.__enter__()
-        with torch.cuda.stream(stream):
-            start.record(stream)
-            for gr in graphs:
-                gr.replay()
-            end.record(stream)
-        torch.cuda.synchronize()
-        if sampler:
-            sampler.__exit__(None, None, None)
-        barrier(world)
-        return start.elapsed_time(end), (sampler.summary() if sampler else None)
+        return timed_regions(graphs, stream, world, local, sample_clocks)
 
     K = args.steps
     ms, clocks = timed(graphs_of(one, K), sample_clocks=True)
@@ -1052,9 +1070,9 @@ def run_reference(args, world, rank):
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--workload", type=int, default=4, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--part", default=None, help="workload 4: a|b|c; workload 5: global|sliding")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--kv", default="bf16", choices=["bf16", "fp8"],

@@ -144,7 +144,8 @@ typedef struct {
                                after that wait. A decode behind the new-token step, or behind another
                                layer's decode, qualifies. Stage 1 then copies the older rows of its first
                                pipeline stages while those kernels run (programmatic dependent launch);
-                               q, the newest rows and every write wait for them as usual */
+                               q, the newest rows and every write (the device error word included)
+                               wait for them as usual */
   uint64_t workspace_bytes; /* bytes the caller must provide */
   uint64_t lse_offset;      /* byte offset of the fp32 [batch, T, Hq, S] log-sum-exp part */
   uint64_t opart_offset;    /* byte offset of the fp32 [batch, T, Hq, S, d] partial outputs */
@@ -163,8 +164,12 @@ typedef struct {
  *                 later call whose lengths do not exceed max(seq_lens_host)
  *   sm_count      streaming multiprocessors of the target GPU (> 0)
  *   plan          output
+ * Groups (Hq / Hkv) of 1..16 are served: up to 8 by one CTA per (request, KV
+ * head, piece) that reads each KV byte once for all query heads; 9..16 by
+ * CTAs of 8 query heads each (two per KV head, each reading the KV head's
+ * pages; head_dim 256 or 512).
  * Returns PD_ERR_INVALID_ARG for a malformed shape or length, PD_ERR_UNSUPPORTED
- * for a head_dim or group size (Hq / Hkv) this build has no kernel for.
+ * for a head_dim or group size this build has no kernel for (group > 16).
  */
 pd_status paged_decode_plan(const pd_layer_desc* layer, int32_t batch, const int32_t* seq_lens_host,
                             int32_t sm_count, pd_plan* plan);
@@ -189,7 +194,7 @@ pd_status paged_decode_plan(const pd_layer_desc* layer, int32_t batch, const int
  * pairs of one KV head are served 8 per CTA, so for T * group <= 8 every KV
  * byte is still read once. bf16 or FP8 caches (an FP8 plan goes with
  * paged_decode_global_fp8 / paged_decode_window_fp8), head_dim 256 or 512,
- * group Hq / Hkv up to 8.
+ * group Hq / Hkv up to 16.
  */
 pd_status paged_decode_plan_multi(const pd_layer_desc* layer, int32_t batch, int32_t query_tokens,
                                   const int32_t* seq_lens_host, int32_t sm_count, pd_plan* plan);
@@ -281,13 +286,18 @@ pd_status paged_decode_check_device_error(const pd_plan* plan, void* workspace,
  *   device_flags  optional device pointer: receives the device error word
  *                 (PD_DEVFLAG_*) of this call; NULL to ignore it
  *   stream        cudaStream_t as void*
- * Returns PD_ERR_WORKSPACE_TOO_SMALL, without launching, when the plan needs
- * more than 8 MiB of scratch (plan->workspace_bytes > 8 MiB); otherwise the
- * statuses of the calls it makes. The first call on a device looks up the
- * scratch array's device address, so make it before any stream capture. All
- * calls share the one array and each starts by clearing its error word: calls
- * that overlap on the GPU race, so order them on one stream. It allocates
- * nothing.
+ * Every argument is checked before anything is queued: PD_ERR_INVALID_ARG for
+ * what paged_decode_global / paged_decode_window refuse, and for an FP8 plan
+ * (its scales have no argument here) or a plan from paged_decode_plan_partial;
+ * PD_ERR_WORKSPACE_TOO_SMALL when the plan needs more than 8 MiB of scratch
+ * (plan->workspace_bytes > 8 MiB). With batch 0 nothing is launched and
+ * device_flags is not written. Otherwise it returns the statuses of the calls
+ * it makes. The array has one device address per CUDA context; the first call
+ * in a context (the device's primary context, another context made current by
+ * the caller, or a primary context made again after cudaDeviceReset) looks it
+ * up, so make that call before any stream capture. All calls share the one
+ * array and each starts by clearing its error word: calls that overlap on the
+ * GPU race, so order them on one stream. It allocates nothing.
  */
 pd_status paged_decode_noalloc(const pd_plan* plan, const void* q, const void* k_pool, const void* v_pool,
                                const int32_t* block_tables, const int32_t* seq_lens, int32_t window, float scale,

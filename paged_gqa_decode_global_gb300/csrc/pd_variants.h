@@ -21,8 +21,9 @@ constexpr uint64_t kWorkspaceHeader = 256;
 //                              head) scales) instead of bf16
 //   NW  consumer warps (+1 producer warp)
 //   SPW ring stages owned by each consumer warp
-//   MQ  several query tokens per request: the G = 8 MMA columns hold (token,
-//       head) pairs of the request's T x group pairs, token-major, and each
+//   MQ  column-tiled (several query tokens per request, or one token with a
+//       group of 9..16): the G = 8 MMA columns hold (token, head) pairs of
+//       the request's T x group pairs, token-major, 8 per CTA, and each
 //       column is masked causally by its own token's position
 template <int D_, int G_, bool KVS_, bool KV8_, int NW_, int SPW_, bool MQ_ = false>
 struct Stage1Cfg {
@@ -98,9 +99,9 @@ struct Stage1Cfg {
 // idle) plus the producer; rings of 192 KiB: 32 KiB stages x 6 (d512 K!=V),
 // 16 KiB x 12 (d512 K=V, d256 K!=V), 8 KiB x 24 (d256 K=V). FP8: seven
 // consumer warps (two per SM sub-partition hide the latency of widening e4m3
-// fragments to f16) and rings of 196-224 KiB. Multi-token (ids 32-35): the
-// group-8 geometry, any group <= 8 at run time (ids 44-47: the same over an
-// FP8 cache). head_dim 128 (ids 36-43, bf16, one query token): 8 KiB stages x
+// fragments to f16) and rings of 196-224 KiB. Column-tiled (ids 32-35): the
+// group-8 geometry, any group up to 16 and any number of query tokens at run
+// time (ids 44-47: the same over an FP8 cache). head_dim 128 (ids 36-43, bf16, one query token): 8 KiB stages x
 // 24 (K!=V), 4 KiB x 48 (K=V).
 #define PD_FOR_EACH_VARIANT(X)             \
   X(0, 512, 1, false, false, 3, 2, false)  \

@@ -40,14 +40,21 @@ constexpr int kMaxSplits = 1024;
 // Query tokens per request a plan may carry (multi-token variants).
 constexpr int kMaxQueryTokens = 256;
 
-// Decode (one query token): the instance of exactly this group. Several query
-// tokens: the multi-token instance (8 columns of (token, head) pairs), which
-// serves any group up to 8.
+// Largest GQA group (query heads per KV head) a plan accepts.
+constexpr int kMaxGroup = 16;
+
+// Decode (one query token) with a group of at most 8: the instance of exactly
+// this group. Several query tokens, or a group of 9..16: the column-tiled
+// instance (CTAs of 8 columns of (token, head) pairs), which serves any group
+// up to kMaxGroup.
+bool tiled(int query_tokens, int group) { return query_tokens > 1 || group > 8; }
+
 const pd::VariantInfo* find_variant(int head_dim, int group, int kv_shared, int kv_fp8, int multi) {
+  if (group < 1 || group > kMaxGroup) return nullptr;
   for (int i = 0; i < pd::kNumVariants; ++i) {
     const pd::VariantInfo& v = pd::kVariants[i];
     if (v.head_dim != head_dim || v.kv_shared != kv_shared || v.kv_fp8 != kv_fp8 || v.multi != multi) continue;
-    if (multi ? group <= v.group : v.group == group) return &v;
+    if (multi || v.group == group) return &v;
   }
   return nullptr;
 }
@@ -202,12 +209,12 @@ pd_status plan_impl(const pd_layer_desc* layer, int32_t batch, int32_t query_tok
     max_len = std::max(max_len, seq_lens_host[b]);
   }
   const int group = ly.num_q_heads / ly.num_kv_heads;
-  const pd::VariantInfo* v =
-      find_variant(ly.head_dim, group, ly.kv_shared, ly.kv_dtype == PD_KV_FP8_E4M3, T > 1 ? 1 : 0);
+  const bool multi = tiled(T, group);
+  const pd::VariantInfo* v = find_variant(ly.head_dim, group, ly.kv_shared, ly.kv_dtype == PD_KV_FP8_E4M3, multi);
   if (!v) return PD_ERR_UNSUPPORTED;
   const int TB = v->block_tokens;
-  // CTAs per (piece, KV head): one, or the column tiles of a multi-token plan
-  const int tiles = T > 1 ? col_tiles(T, group) : 1;
+  // CTAs per (piece, KV head): one, or the column tiles of a tiled plan
+  const int tiles = multi ? col_tiles(T, group) : 1;
   if ((long long)ly.num_kv_heads * tiles > 65535) return PD_ERR_UNSUPPORTED;
   const int hkv_ctas = ly.num_kv_heads * tiles;
 
@@ -334,7 +341,8 @@ bool plan_is_valid(const pd_plan* plan) {
   if (ly.num_kv_heads <= 0 || ly.num_q_heads % ly.num_kv_heads != 0) return false;
   const int group = ly.num_q_heads / ly.num_kv_heads;
   if (v.multi) {
-    if (group > v.group || plan->query_tokens < 2 || plan->query_tokens > kMaxQueryTokens) return false;
+    if (group > kMaxGroup || plan->query_tokens < 1 || plan->query_tokens > kMaxQueryTokens) return false;
+    if (!tiled(plan->query_tokens, group)) return false;
     if (plan->grid_y != ly.num_kv_heads * col_tiles(plan->query_tokens, group)) return false;
   } else {
     if (group != v.group || plan->query_tokens != 1 || plan->grid_y != ly.num_kv_heads) return false;

@@ -181,7 +181,9 @@ __device__ __forceinline__ int stage1_cta(const Stage1Params& p, uint8_t* smem) 
   // scales and the cached rows older than each request's newest query_tokens
   // positions (data the caller guarantees that kernel does not write): it
   // waits before the first copy of a block holding a newer row, before the
-  // first copy that has to wait for a free stage, and before it leaves.
+  // first copy that has to wait for a free stage, and before it leaves. It
+  // writes nothing to global memory before that wait: a bad page id it meets
+  // is recorded in a register and reaches the error word afterwards.
   const bool early = p.early_kv != 0 && threadIdx.x >= C::NW * 32;
   if (threadIdx.x == C::NW * 32) {
     prefetch_tensormap(&p.kmap);
@@ -213,7 +215,7 @@ __device__ __forceinline__ int stage1_cta(const Stage1Params& p, uint8_t* smem) 
     if (t < cap) page_spec = __ldg(table + t / p.page_size);
   }
   int L = p.seq_lens[b];
-  if (L < 0 || L > cap || (C::MQ && L < cm.T)) {
+  if (L < 0 || L > cap || (C::MQ && cm.T > 1 && L < cm.T)) {
     if (threadIdx.x == 0) atomicOr(p.err, kErrBadSeqLen);
     L = L < 0 ? 0 : (L > cap ? cap : L);
   }
@@ -314,6 +316,9 @@ __device__ __forceinline__ int stage1_cta(const Stage1Params& p, uint8_t* smem) 
     int issued = 0;
     bool stop = false;
     bool waited = !early;
+    // error bits seen by lane 0, published once this grid may write global
+    // memory (after its dependency wait)
+    uint32_t err_bits = 0;
     // blocks ending after this position hold rows the previous kernel may write
     const int fresh_from = L - p.query_tokens;
 #pragma unroll 1
@@ -347,7 +352,7 @@ __device__ __forceinline__ int stage1_cta(const Stage1Params& p, uint8_t* smem) 
           const int st = j % C::NST;
           const int round = j / C::NST;
           if (round > 0 && !mbar_wait(&empty_bar[st], (round - 1) & 1)) {
-            atomicOr(p.err, kErrTimeout);
+            err_bits |= kErrTimeout;
             go = 0;
           } else {
             const int t0 = blk_lo + j * C::TB;
@@ -372,7 +377,7 @@ __device__ __forceinline__ int stage1_cta(const Stage1Params& p, uint8_t* smem) 
                 }
               }
             } else {
-              atomicOr(p.err, kErrBadPage);
+              err_bits |= kErrBadPage;
               mbar_arrive(&full_bar[st]);
             }
           }
@@ -393,10 +398,11 @@ __device__ __forceinline__ int stage1_cta(const Stage1Params& p, uint8_t* smem) 
       for (int st = 0; st < C::NST && st < issued; ++st) {
         const int j_last = st + C::NST * ((issued - 1 - st) / C::NST);
         if (!mbar_wait_until(&full_bar[st], (j_last / C::NST) & 1, deadline)) {
-          atomicOr(p.err, kErrTimeout);
+          err_bits |= kErrTimeout;
           break;
         }
       }
+      if (err_bits) atomicOr(p.err, err_bits);
     }
     return (C::DED_SLOTS > 0 && p.cluster_merge == 2) ? kMergeToWait : kMergeNothing;
   }

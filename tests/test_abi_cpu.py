@@ -65,8 +65,9 @@ def _plan(lens, Hq=16, Hkv=4, d=512, P=16, pages=4096, maxp=None, window=0, kv_s
     (dict(sms=0), b.PD_ERR_INVALID_ARG),
     (dict(d=384), b.PD_ERR_UNSUPPORTED),
     (dict(d=192), b.PD_ERR_UNSUPPORTED),
-    (dict(Hq=64, Hkv=4), b.PD_ERR_UNSUPPORTED),   # group of 16
-    (dict(Hq=48, Hkv=4), b.PD_ERR_UNSUPPORTED),   # group of 12
+    (dict(Hq=128, Hkv=4), b.PD_ERR_UNSUPPORTED),  # group of 32
+    (dict(Hq=68, Hkv=4), b.PD_ERR_UNSUPPORTED),   # group of 17
+    (dict(Hq=64, Hkv=4, d=128), b.PD_ERR_UNSUPPORTED),  # group of 16 at head_dim 128
 ])
 def test_plan_rejects(lib, kw, status):
     with pytest.raises(b.PagedDecodeError) as e:
@@ -197,6 +198,54 @@ def test_combine_and_partial_reject_bad_arguments_without_launching(lib):
     assert st == b.PD_ERR_INVALID_ARG
 
 
+@pytest.mark.parametrize("G", [9, 12, 16])
+@pytest.mark.parametrize("d,window,kvs", [(512, 0, False), (512, 0, True), (256, 1024, False)])
+def test_groups_above_8_are_served_by_column_tiles(lib, G, d, window, kvs):
+    lens = [5000, 100, 0, 30000]
+    pl = _plan(lens, Hq=4 * G, Hkv=4, d=d, window=window, kv_shared=kvs, pages=10 ** 5)
+    tiles = (G + 7) // 8
+    assert pl.query_tokens == 1 and (pl.grid_y, pl.grid_z) == (4 * tiles, len(lens))
+    assert b.load_library().paged_decode_abi_version() == 5
+    # the same group over several query tokens: T x G pairs, 8 per CTA
+    desc = b.layer_desc(4 * G, 4, d, 16, 10 ** 5, 2000, window, kvs)
+    pm = b.paged_decode_plan_multi(desc, 3, [3000, 40], 152)
+    assert pm.grid_y == 4 * ((3 * G + 7) // 8)
+    # and its FP8 form
+    f8 = b.paged_decode_plan(b.layer_desc(4 * G, 4, d, 16, 10 ** 5, 2000, window, kvs, b.PD_KV_FP8_E4M3),
+                             [3000, 40], 152)
+    assert f8.grid_y == 4 * tiles
+
+
+def test_noalloc_checks_every_argument_before_queueing_work(lib):
+    """paged_decode_noalloc refuses bad calls with no CUDA call at all: on a
+    machine without a GPU, a call that got past its checks would fail with
+    PD_ERR_CUDA instead."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a device is present")
+    fake = 1 << 20
+    bf = b.paged_decode_plan(b.layer_desc(16, 4, 512, 16, 4096, 64), [1024] * 4, 152)
+    win = b.paged_decode_plan(b.layer_desc(16, 8, 256, 16, 4096, 300, 1024), [4000] * 4, 152)
+    f8 = b.paged_decode_plan(b.layer_desc(16, 4, 512, 16, 4096, 64, kv_dtype=b.PD_KV_FP8_E4M3), [1024] * 4, 152)
+    part = b.paged_decode_plan_partial(b.layer_desc(16, 4, 512, 16, 4096, 64), [1024] * 4, 152)
+
+    def call(plan, window=0, q=fake, k=fake, v=fake + 4096, scale=0.05):
+        return lib.paged_decode_noalloc(ctypes.byref(plan), q, k, v, fake, fake, window, ctypes.c_float(scale),
+                                        fake, None, None)
+
+    assert call(f8) == b.PD_ERR_INVALID_ARG           # FP8: no scales to pass
+    assert call(part) == b.PD_ERR_INVALID_ARG         # partial plans keep fp32 pieces for the caller
+    assert call(win, window=512) == b.PD_ERR_INVALID_ARG   # window differs from the plan's
+    assert call(bf, window=1024) == b.PD_ERR_INVALID_ARG   # a window on a global plan
+    assert call(bf, q=None) == b.PD_ERR_INVALID_ARG
+    assert call(bf, q=fake + 2) == b.PD_ERR_INVALID_ARG    # misaligned q
+    assert call(bf, v=fake) == b.PD_ERR_INVALID_ARG        # V aliasing K on a K != V layer
+    assert call(bf, scale=float("nan")) == b.PD_ERR_INVALID_ARG
+    big = b.paged_decode_plan(b.layer_desc(16, 4, 512, 16, 64 * 512 + 1, 512), [8192] * 64, 4000)
+    assert big.workspace_bytes > 8 << 20 and call(big) == b.PD_ERR_WORKSPACE_TOO_SMALL
+    assert call(bf) == b.PD_ERR_CUDA                  # valid: gets as far as CUDA, which is absent here
+
+
 def test_head_dim_128_is_planned_for_bf16_single_token(lib):
     pl = _plan([100, 2000], d=128)
     assert pl.layer.head_dim == 128 and pl.threads_per_cta == 128
@@ -232,7 +281,7 @@ def test_planner_invariants_on_random_shapes(lib):
     for _ in range(300):
         d, window = shapes[rng.integers(len(shapes))]
         Hkv = int(rng.choice([1, 2, 4, 8]))
-        G = int(rng.choice([1, 2, 4, 8]))
+        G = int(rng.choice([1, 2, 4, 8, 12, 16] if d != 128 else [1, 2, 4, 8]))
         kvs = bool(rng.integers(2))
         fp8 = d != 128 and bool(rng.integers(2))
         T = 1 if d == 128 or rng.random() < 0.6 else int(rng.integers(2, 9))
@@ -256,7 +305,7 @@ def test_planner_invariants_on_random_shapes(lib):
             first_hi = L - T + 1
             lo = first_hi - window if window and first_hi > window else 0
             assert S * chunk >= L - (lo // TB) * TB  # every attended token is in some piece
-        tiles = (T * G + 7) // 8 if T > 1 else 1
+        tiles = (T * G + 7) // 8 if T > 1 or G > 8 else 1
         assert (pl.grid_x, pl.grid_y, pl.grid_z) == (S, Hkv * tiles, B)
         assert pl.threads_per_cta in (128, 256) and 0 < pl.smem_bytes <= 227 * 1024
         assert pl.query_tokens == T and pl.partial == int(partial) and pl.early_kv == 0

@@ -107,6 +107,34 @@ def test_variants_ragged(d, G, kvs, window):
         compare(out, ref, li, f"d{d} G{G} kvs{kvs} W{window} sms{sms} S{step.plan.num_splits}")
 
 
+@pytest.mark.parametrize("d,G,kvs", [(512, 16, False), (512, 12, True), (256, 16, True), (256, 9, False)])
+@pytest.mark.parametrize("window", [0, 37, 1000])
+def test_groups_above_8_ragged(d, G, kvs, window):
+    """Groups of 9..16 query heads per KV head (served by CTAs of 8 query heads):
+    ragged lengths, windows, one piece / cluster merge / merge kernel."""
+    Hkv = 2
+    lens = [1, 17, 300, 0, 1000, 33]
+    li = synth.make_layer("g", lens, Hkv * G, Hkv, d, window=window, kv_shared=kvs,
+                          pool_pages=sum((L + 15) // 16 for L in lens) + 5, seed=7 * d + G + 100 * kvs + window,
+                          device="cuda")
+    ref = run_oracle(li)
+    modes = set()
+    for sms in (1, 3, 40, 152):
+        out, step = run_gpu(li, sm_count=sms)
+        assert step.plan.grid_y == Hkv * ((G + 7) // 8)
+        modes.add(int(step.plan.merge_mode))
+        compare(out, ref, li, f"d{d} G{G} kvs{kvs} W{window} sms{sms} S{step.plan.num_splits}")
+    assert 0 in modes and len(modes) >= 2, modes
+
+
+def test_group_16_single_token_is_bit_exact():
+    li = synth.make_layer("one16", [1, 1], 32, 2, 512, pool_pages=5, seed=13, device="cuda")
+    out, _ = run_gpu(li)
+    for bi in range(2):
+        page = int(li.block_tables[bi, 0])
+        assert torch.equal(out[bi], li.v_pool[page, :, 0, :].repeat_interleave(16, dim=0))
+
+
 def test_page_size_32():
     lens = [100, 64, 5]
     li = synth.make_layer("p32", lens, 8, 2, 512, page_size=32, pool_pages=12, seed=5, device="cuda")
@@ -179,11 +207,14 @@ def test_window_ignores_rows_before_the_window():
 
 # ---- device-side error reporting (the kernel's own checks; nothing faults) -------
 
-def test_bad_page_id_sets_flag_and_skips_the_page():
+@pytest.mark.parametrize("early_kv", [False, True])
+def test_bad_page_id_sets_flag_and_skips_the_page(early_kv):
+    # with early_kv the producer meets the bad page before its dependency wait;
+    # the flag still reaches the error word (written only after that wait)
     li = synth.make_layer("bad", [64, 64], 8, 2, 512, pool_pages=10, seed=9, device="cuda")
     bt = li.block_tables.clone()
     bt[1, 2] = 10 ** 6  # far outside the pool
-    step = b.LayerStep.for_inputs(li)
+    step = b.LayerStep.for_inputs(li, early_kv=early_kv)
     out = torch.empty_like(li.q)
     step(li.q, li.k_pool, li.v_pool, bt, li.seq_lens, li.scale, out)
     with pytest.raises(b.PagedDecodeError) as e:
@@ -306,7 +337,7 @@ def run_oracle_fp8(f):
                              f.seq_lens.cpu().numpy(), f.scale, f.window)
 
 
-@pytest.mark.parametrize("d,G,kvs", FP8_VARIANTS)
+@pytest.mark.parametrize("d,G,kvs", FP8_VARIANTS + [(512, 16, True), (256, 12, False)])
 @pytest.mark.parametrize("window", [0, 37])
 def test_fp8_variants_ragged(d, G, kvs, window):
     Hkv = 2

@@ -1,12 +1,15 @@
-"""The allocation-free entry point (paged_decode_noalloc) against the
-workspace entry points.
+"""The allocation-free entry point (paged_decode_noalloc) against the fp64
+oracle and against the workspace entry points.
 
 paged_decode_noalloc serves callers that may not allocate device memory, such
 as an engine plugin whose host owns all device memory or a serving loop that
 must not call cudaMalloc mid-step; it runs the same decode step on a scratch
-array inside the library. Its output must match the workspace path's on two
-calls in a row (the second call finds the first call's contents in the shared
-array).
+array inside the library. Each case makes two calls in a row with different
+queries: the second call finds the first call's partials in the shared array
+and must not be affected by them. The cases cover each merge mode: one piece
+(nothing in the array but the error word), pieces merged inside a
+thread-block cluster (likewise), and pieces merged by the merge kernel, whose
+fp32 partials and log-sum-exps live in the array.
 
 This file is named to be collected last.
 """
@@ -14,6 +17,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from paged_gqa_decode_global_gb300 import binding as b
 from paged_gqa_decode_global_gb300 import inputs as synth
 
@@ -31,32 +35,58 @@ def _built():
 
 
 def _close(a, ref, tag):
-    x = a.float().cpu().numpy().astype(np.float64).ravel()
-    y = ref.float().cpu().numpy().astype(np.float64).ravel()
+    x = a.float().cpu().numpy().astype(np.float64).ravel() if torch.is_tensor(a) else a.ravel()
+    y = ref.float().cpu().numpy().astype(np.float64).ravel() if torch.is_tensor(ref) else ref.ravel()
     assert np.isfinite(x).all(), tag
     err = np.abs(x - y).max()
     cos = float(x @ y / (np.linalg.norm(x) * np.linalg.norm(y)))
     assert err <= MAX_ABS and cos > MIN_COS, f"{tag}: max abs {err:.3e} cos {cos:.7f}"
 
 
-@pytest.mark.parametrize("window,kvs,d,G", [(0, False, 512, 4), (0, True, 512, 4), (1024, False, 256, 2)])
-def test_noalloc_matches_workspace_path_twice(window, kvs, d, G):
-    lens = [4097, 1500, 77, 0, 3000]
+def _oracle(li, q):
+    return oracle.decode(synth.bits_u16(q), synth.bits_u16(li.k_pool),
+                         None if li.v_pool is None else synth.bits_u16(li.v_pool),
+                         li.block_tables.cpu().numpy(), li.seq_lens.cpu().numpy(), li.scale, li.window)
+
+
+LENS = [4097, 1500, 77, 0, 3000]
+
+# (lengths, window, K=V, head_dim, group, SM count given to the planner, merge mode it must pick)
+CASES = [
+    (LENS, 0, False, 512, 4, 8, 0),
+    (LENS, 0, False, 512, 4, 152, 1),
+    (LENS, 0, True, 512, 4, 152, 1),
+    (LENS, 1024, False, 256, 2, 160, 1),
+    (LENS, 1024, False, 256, 2, 152, 2),
+    ([1024] * 8, 0, False, 512, 4, 152, 2),
+]
+
+
+@pytest.mark.parametrize("lens,window,kvs,d,G,sms,mode", CASES)
+def test_noalloc_matches_oracle_and_workspace_path_twice(lens, window, kvs, d, G, sms, mode):
     li = synth.make_layer("na", lens, 4 * G, 4, d, window=window, kv_shared=kvs,
-                          pool_pages=sum((L + 15) // 16 for L in lens) + 8, seed=21 + d + window + kvs,
+                          pool_pages=sum((L + 15) // 16 for L in lens) + 8, seed=21 + d + window + kvs + sms,
                           device="cuda")
-    step = b.LayerStep.for_inputs(li)
-    assert step.plan.num_splits > 1  # the scratch array really carries partials
-    ref = step.run(li)
-    assert step.check() == 0
+    step = b.LayerStep.for_inputs(li, sm_count=sms)
+    assert int(step.plan.merge_mode) == mode, (step.plan.merge_mode, step.plan.num_splits)
+    if mode == 1:
+        # the merge kernel reads partials from the scratch array
+        assert step.plan.workspace_bytes > 256 and step.plan.num_splits > 1
+    gen = torch.Generator(device="cuda").manual_seed(77 + sms)
+    queries = [li.q, torch.randn(li.q.shape, generator=gen, device="cuda").to(torch.bfloat16)]
     flags = torch.full((1,), -1, dtype=torch.int32, device="cuda")
-    for call in range(2):
-        out = torch.full_like(li.q, float("nan"))
-        b.paged_decode_noalloc(step.plan, li.q, li.k_pool, li.v_pool, li.block_tables, li.seq_lens, window,
+    for call, q in enumerate(queries):
+        ref_ws = torch.full_like(q, float("nan"))
+        step(q, li.k_pool, li.v_pool, li.block_tables, li.seq_lens, li.scale, ref_ws)
+        assert step.check() == 0
+        out = torch.full_like(q, float("nan"))
+        b.paged_decode_noalloc(step.plan, q, li.k_pool, li.v_pool, li.block_tables, li.seq_lens, window,
                                li.scale, out, device_flags=flags)
         torch.cuda.synchronize()
         assert int(flags.item()) == 0, f"call {call}: device flags {int(flags.item()):#x}"
-        _close(out, ref, f"call {call}")
+        tag = f"call {call}, merge mode {mode}, S={step.plan.num_splits}"
+        _close(out, ref_ws, tag + " vs the workspace path")
+        _close(out.float().cpu().numpy().astype(np.float64), _oracle(li, q), tag + " vs the oracle")
 
 
 def test_noalloc_rejects_plans_beyond_its_scratch():
