@@ -25,7 +25,10 @@ constexpr uint64_t kWorkspaceHeader = 256;
 //       group of 9..16): the G = 8 MMA columns hold (token, head) pairs of
 //       the request's T x group pairs, token-major, 8 per CTA, and each
 //       column is masked causally by its own token's position
-template <int D_, int G_, bool KVS_, bool KV8_, int NW_, int SPW_, bool MQ_ = false>
+//   NSUB 16-token blocks per ring stage: each block is one tiled copy of K (and
+//       one of V); the stage's blocks share its mbarrier round trip and one
+//       online-softmax update
+template <int D_, int G_, bool KVS_, bool KV8_, int NW_, int SPW_, bool MQ_ = false, int NSUB_ = 1>
 struct Stage1Cfg {
   static constexpr int D = D_;
   static constexpr int G = G_;
@@ -34,7 +37,8 @@ struct Stage1Cfg {
   static constexpr int NW = NW_;
   static constexpr int SPW = SPW_;
   static constexpr bool MQ = MQ_;
-  static constexpr int TB = 16;                  // tokens per stage = the MMA's 16-row side
+  static constexpr int NSUB = NSUB_;
+  static constexpr int TB = 16;                  // tokens per block = the MMA's 16-row side
   static constexpr int KSTEPS = D / 16;          // QK k-steps
   static constexpr int MTILES = D / 16;          // PV m-tiles (head dims)
   static constexpr int NST = NW * SPW;
@@ -44,9 +48,11 @@ struct Stage1Cfg {
   static constexpr int SLABS = D / 64;           // bf16 slabs
   static constexpr int ELEM = KV8 ? 1 : 2;
   static constexpr int TMA_SLABS = D * ELEM / 128;
-  static constexpr int KV_BYTES = TMA_SLABS * SLAB_BYTES;
-  static constexpr int STAGE_BYTES = KV_BYTES * (KVS ? 1 : 2);
-  static constexpr int TX_BYTES = STAGE_BYTES;                  // bytes the copies deliver
+  static constexpr int KV_BYTES = TMA_SLABS * SLAB_BYTES;       // one block of K (or V)
+  static constexpr int BLOCK_TX = KV_BYTES * (KVS ? 1 : 2);     // bytes the copies of one block deliver
+  // a stage: the K of its NSUB blocks, then (K != V) their V
+  static constexpr int V_OFFSET = NSUB * KV_BYTES;
+  static constexpr int STAGE_BYTES = NSUB * BLOCK_TX;
   static constexpr int RING_BYTES = NST * STAGE_BYTES;
   static constexpr int WORK_BYTES = RING_BYTES;
   static constexpr int COMB_STRIDE = D + 4;                    // floats per head row of the warp merge
@@ -65,9 +71,9 @@ struct Stage1Cfg {
   static constexpr int PUSH_LSE_OFFSET = PUSH_OFFSET + (MAX_CLUSTER - 1) * G * D * 4;
   static_assert(PUSH_LSE_OFFSET + (MAX_CLUSTER - 1) * G * 4 <= BODY_BYTES, "cluster merge buffers fit in the body");
   static constexpr int BAR_OFFSET = BODY_BYTES;                // full[NST], empty[NST]
-  static constexpr int VALID_OFFSET = BAR_OFFSET + NST * 16;   // u32 valid[NST]
-  static constexpr int SCALE_OFFSET = (VALID_OFFSET + NST * 4 + 7) / 8 * 8;  // float2 (k, v) scale[NST] (FP8)
-  static constexpr int ML_OFFSET = SCALE_OFFSET + NST * 8;     // float2 ml[NW][G]
+  static constexpr int VALID_OFFSET = BAR_OFFSET + NST * 16;   // u32 valid[NST]: one bit per block
+  static constexpr int SCALE_OFFSET = (VALID_OFFSET + NST * 4 + 7) / 8 * 8;  // float2 (k, v) scale[NST][NSUB] (FP8)
+  static constexpr int ML_OFFSET = SCALE_OFFSET + NST * NSUB * 8;  // float2 ml[NW][G]
   static constexpr int COEF_OFFSET = ML_OFFSET + NW * G * 8;   // float coef[NW][G], lse[G]
   static constexpr int TAIL_END = (COEF_OFFSET + (NW * G + G) * 4 + 15) / 16 * 16;
   // Pieces that can push into a region of their own, outside the ring (what
@@ -85,6 +91,7 @@ struct Stage1Cfg {
   static_assert(D % 128 == 0, "head_dim must be a multiple of 128");
   static_assert(G >= 1 && G <= 8, "the GQA group is the MMA's 8-wide side");
   static_assert(16 % TB == 0, "a block must lie inside one 16-token page slice");
+  static_assert(NSUB >= 1 && 32 % NSUB == 0, "a stage's blocks come from one batch of 32 page ids");
   static_assert(STAGE_BYTES % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
   static_assert(SCALE_OFFSET % 8 == 0 && ML_OFFSET % 8 == 0, "float2 arrays need 8-byte alignment");
@@ -94,68 +101,70 @@ struct Stage1Cfg {
 };
 
 // The instances this library is built with, by variant id:
-// X(id, head_dim, group, K=V, FP8, consumer warps, stages per warp, multi-token).
+// X(id, head_dim, group, K=V, FP8, consumer warps, stages per warp, multi-token,
+//   blocks per stage).
 // bf16: three consumer warps (the tensor cores leave the CUDA cores mostly
-// idle) plus the producer; rings of 192 KiB: 32 KiB stages x 6 (d512 K!=V),
-// 16 KiB x 12 (d512 K=V, d256 K!=V), 8 KiB x 24 (d256 K=V). FP8: seven
-// consumer warps (two per SM sub-partition hide the latency of widening e4m3
-// fragments to f16) and rings of 196-224 KiB. Column-tiled (ids 32-35): the
-// group-8 geometry, any group up to 16 and any number of query tokens at run
-// time (ids 44-47: the same over an FP8 cache). head_dim 128 (ids 36-43, bf16, one query token): 8 KiB stages x
-// 24 (K!=V), 4 KiB x 48 (K=V).
-#define PD_FOR_EACH_VARIANT(X)             \
-  X(0, 512, 1, false, false, 3, 2, false)  \
-  X(1, 512, 2, false, false, 3, 2, false)  \
-  X(2, 512, 4, false, false, 3, 2, false)  \
-  X(3, 512, 8, false, false, 3, 2, false)  \
-  X(4, 512, 1, true, false, 3, 4, false)   \
-  X(5, 512, 2, true, false, 3, 4, false)   \
-  X(6, 512, 4, true, false, 3, 4, false)   \
-  X(7, 512, 8, true, false, 3, 4, false)   \
-  X(8, 256, 1, false, false, 3, 4, false)  \
-  X(9, 256, 2, false, false, 3, 4, false)  \
-  X(10, 256, 4, false, false, 3, 4, false) \
-  X(11, 256, 8, false, false, 3, 4, false) \
-  X(12, 256, 1, true, false, 3, 8, false)  \
-  X(13, 256, 2, true, false, 3, 8, false)  \
-  X(14, 256, 4, true, false, 3, 8, false)  \
-  X(15, 256, 8, true, false, 3, 8, false)  \
-  X(16, 512, 1, false, true, 7, 2, false)  \
-  X(17, 512, 2, false, true, 7, 2, false)  \
-  X(18, 512, 4, false, true, 7, 2, false)  \
-  X(19, 512, 8, false, true, 7, 2, false)  \
-  X(20, 512, 1, true, true, 7, 4, false)   \
-  X(21, 512, 2, true, true, 7, 4, false)   \
-  X(22, 512, 4, true, true, 7, 4, false)   \
-  X(23, 512, 8, true, true, 7, 4, false)   \
-  X(24, 256, 1, false, true, 7, 4, false)  \
-  X(25, 256, 2, false, true, 7, 4, false)  \
-  X(26, 256, 4, false, true, 7, 4, false)  \
-  X(27, 256, 8, false, true, 7, 4, false)  \
-  X(28, 256, 1, true, true, 7, 7, false)   \
-  X(29, 256, 2, true, true, 7, 7, false)   \
-  X(30, 256, 4, true, true, 7, 7, false)   \
-  X(31, 256, 8, true, true, 7, 7, false)   \
-  X(32, 512, 8, false, false, 3, 2, true)  \
-  X(33, 512, 8, true, false, 3, 4, true)   \
-  X(34, 256, 8, false, false, 3, 4, true)  \
-  X(35, 256, 8, true, false, 3, 8, true)   \
-  X(36, 128, 1, false, false, 3, 8, false) \
-  X(37, 128, 2, false, false, 3, 8, false) \
-  X(38, 128, 4, false, false, 3, 8, false) \
-  X(39, 128, 8, false, false, 3, 8, false) \
-  X(40, 128, 1, true, false, 3, 16, false) \
-  X(41, 128, 2, true, false, 3, 16, false) \
-  X(42, 128, 4, true, false, 3, 16, false) \
-  X(43, 128, 8, true, false, 3, 16, false) \
-  X(44, 512, 8, false, true, 7, 2, true)   \
-  X(45, 512, 8, true, true, 7, 4, true)    \
-  X(46, 256, 8, false, true, 7, 4, true)   \
-  X(47, 256, 8, true, true, 7, 7, true)
+// idle) plus the producer; rings of 192 KiB: 32 KiB stages x 6 (d512 K!=V:
+// one block a stage; d256 K!=V: two blocks), 16 KiB x 12 (d512 K=V: one block;
+// d256 K=V and d128 K!=V: two blocks), 8 KiB x 24 (d128 K=V: two blocks).
+// FP8: seven consumer warps (two per SM sub-partition hide the latency of
+// widening e4m3 fragments to f16), one block a stage, rings of 196-224 KiB.
+// Column-tiled (ids 32-35): the group-8 geometry, any group up to 16 and any
+// number of query tokens at run time (ids 44-47: the same over an FP8 cache).
+// head_dim 128: ids 36-43 (bf16, one query token).
+#define PD_FOR_EACH_VARIANT(X) \
+  X(0, 512, 1, false, false, 3, 2, false, 1)  \
+  X(1, 512, 2, false, false, 3, 2, false, 1)  \
+  X(2, 512, 4, false, false, 3, 2, false, 1)  \
+  X(3, 512, 8, false, false, 3, 2, false, 1)  \
+  X(4, 512, 1, true, false, 3, 4, false, 1)   \
+  X(5, 512, 2, true, false, 3, 4, false, 1)   \
+  X(6, 512, 4, true, false, 3, 4, false, 1)   \
+  X(7, 512, 8, true, false, 3, 4, false, 1)   \
+  X(8, 256, 1, false, false, 3, 2, false, 2)  \
+  X(9, 256, 2, false, false, 3, 2, false, 2)  \
+  X(10, 256, 4, false, false, 3, 2, false, 2) \
+  X(11, 256, 8, false, false, 3, 2, false, 2) \
+  X(12, 256, 1, true, false, 3, 4, false, 2)  \
+  X(13, 256, 2, true, false, 3, 4, false, 2)  \
+  X(14, 256, 4, true, false, 3, 4, false, 2)  \
+  X(15, 256, 8, true, false, 3, 4, false, 2)  \
+  X(16, 512, 1, false, true, 7, 2, false, 1)  \
+  X(17, 512, 2, false, true, 7, 2, false, 1)  \
+  X(18, 512, 4, false, true, 7, 2, false, 1)  \
+  X(19, 512, 8, false, true, 7, 2, false, 1)  \
+  X(20, 512, 1, true, true, 7, 4, false, 1)   \
+  X(21, 512, 2, true, true, 7, 4, false, 1)   \
+  X(22, 512, 4, true, true, 7, 4, false, 1)   \
+  X(23, 512, 8, true, true, 7, 4, false, 1)   \
+  X(24, 256, 1, false, true, 7, 4, false, 1)  \
+  X(25, 256, 2, false, true, 7, 4, false, 1)  \
+  X(26, 256, 4, false, true, 7, 4, false, 1)  \
+  X(27, 256, 8, false, true, 7, 4, false, 1)  \
+  X(28, 256, 1, true, true, 7, 7, false, 1)   \
+  X(29, 256, 2, true, true, 7, 7, false, 1)   \
+  X(30, 256, 4, true, true, 7, 7, false, 1)   \
+  X(31, 256, 8, true, true, 7, 7, false, 1)   \
+  X(32, 512, 8, false, false, 3, 2, true, 1)  \
+  X(33, 512, 8, true, false, 3, 4, true, 1)   \
+  X(34, 256, 8, false, false, 3, 2, true, 2)  \
+  X(35, 256, 8, true, false, 3, 4, true, 2)   \
+  X(36, 128, 1, false, false, 3, 4, false, 2) \
+  X(37, 128, 2, false, false, 3, 4, false, 2) \
+  X(38, 128, 4, false, false, 3, 4, false, 2) \
+  X(39, 128, 8, false, false, 3, 4, false, 2) \
+  X(40, 128, 1, true, false, 3, 8, false, 2)  \
+  X(41, 128, 2, true, false, 3, 8, false, 2)  \
+  X(42, 128, 4, true, false, 3, 8, false, 2)  \
+  X(43, 128, 8, true, false, 3, 8, false, 2)  \
+  X(44, 512, 8, false, true, 7, 2, true, 1)   \
+  X(45, 512, 8, true, true, 7, 4, true, 1)    \
+  X(46, 256, 8, false, true, 7, 4, true, 1)   \
+  X(47, 256, 8, true, true, 7, 7, true, 1)
 
 struct VariantInfo {
   int id, head_dim, group, kv_shared, kv_fp8, nw, spw, block_tokens, threads, smem_bytes, max_cluster, multi,
-      ded_slots;
+      ded_slots, blocks_per_stage;
 };
 
 // Host-visible table, defined in plan.cu.

@@ -18,11 +18,12 @@
 
 namespace pd {
 
-#define PD_VARIANT_ROW(ID, D, G, KVS, KV8, NW, SPW, MQ)                                                    \
-  VariantInfo{ID, D, G, KVS ? 1 : 0, KV8 ? 1 : 0, NW, SPW, Stage1Cfg<D, G, KVS, KV8, NW, SPW, MQ>::TB,      \
-              Stage1Cfg<D, G, KVS, KV8, NW, SPW, MQ>::THREADS, Stage1Cfg<D, G, KVS, KV8, NW, SPW, MQ>::SMEM_BYTES, \
-              Stage1Cfg<D, G, KVS, KV8, NW, SPW, MQ>::MAX_CLUSTER, MQ ? 1 : 0,                           \
-              Stage1Cfg<D, G, KVS, KV8, NW, SPW, MQ>::DED_SLOTS},
+#define PD_VARIANT_ROW(ID, D, G, KVS, KV8, NW, SPW, MQ, NSUB)                                              \
+  VariantInfo{ID, D, G, KVS ? 1 : 0, KV8 ? 1 : 0, NW, SPW, Stage1Cfg<D, G, KVS, KV8, NW, SPW, MQ, NSUB>::TB, \
+              Stage1Cfg<D, G, KVS, KV8, NW, SPW, MQ, NSUB>::THREADS,                                       \
+              Stage1Cfg<D, G, KVS, KV8, NW, SPW, MQ, NSUB>::SMEM_BYTES,                                    \
+              Stage1Cfg<D, G, KVS, KV8, NW, SPW, MQ, NSUB>::MAX_CLUSTER, MQ ? 1 : 0,                       \
+              Stage1Cfg<D, G, KVS, KV8, NW, SPW, MQ, NSUB>::DED_SLOTS, NSUB},
 const VariantInfo kVariants[] = {PD_FOR_EACH_VARIANT(PD_VARIANT_ROW)};
 #undef PD_VARIANT_ROW
 const int kNumVariants = sizeof(kVariants) / sizeof(kVariants[0]);
@@ -244,6 +245,8 @@ pd_status plan_impl(const pd_layer_desc* layer, int32_t batch, int32_t query_tok
   cm.cluster_merge_us = 0.5;
   cm.slots = sm_count;  // one resident CTA per SM (shared memory bound)
 
+  // pieces are whole stages where possible (a stage holds blocks_per_stage blocks)
+  const uint64_t unit = 16ull * v->blocks_per_stage;
   int best_chunk = std::max(16, (int)align_up((uint64_t)std::max(max_n, 1), 16));
   int best_splits = 1;
   bool best_cluster = false;
@@ -251,16 +254,16 @@ pd_status plan_impl(const pd_layer_desc* layer, int32_t batch, int32_t query_tok
     // candidates: multiples of 16 on a geometric grid, from the point where the
     // launch would need more than ~8 waves up to one piece per request
     const long long work = total * hkv_ctas;
-    const int c_min = (int)std::max<long long>(64, align_up((uint64_t)(work / (8LL * cm.slots) + 1), 16));
+    const int c_min = (int)std::max<long long>(64, align_up((uint64_t)(work / (8LL * cm.slots) + 1), unit));
     const int c_max = (int)align_up((uint64_t)max_n, 16);
     std::vector<int> cands;
-    for (double c = c_min; c < c_max; c *= 1.08) cands.push_back((int)align_up((uint64_t)c, 16));
+    for (double c = c_min; c < c_max; c *= 1.08) cands.push_back((int)align_up((uint64_t)c, unit));
     for (int w = 1; w <= 8; ++w) {
       // pieces sized so B * Hkv * S lands on exactly w waves for the longest request
       const long long per_wave = (long long)w * cm.slots;
       const long long pairs = (long long)batch * hkv_ctas;
       const long long s = std::max<long long>(1, per_wave / std::max<long long>(1, pairs));
-      cands.push_back((int)align_up((uint64_t)((max_n + s - 1) / s), 16));
+      cands.push_back((int)align_up((uint64_t)((max_n + s - 1) / s), unit));
     }
     cands.push_back(c_max);
     std::sort(cands.begin(), cands.end());

@@ -170,7 +170,7 @@ __device__ __forceinline__ int stage1_cta(const Stage1Params& p, uint8_t* smem) 
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + C::BAR_OFFSET);
   uint64_t* empty_bar = full_bar + C::NST;
   uint32_t* stage_valid = reinterpret_cast<uint32_t*>(smem + C::VALID_OFFSET);
-  float2* stage_scale = reinterpret_cast<float2*>(smem + C::SCALE_OFFSET);  // FP8: (K, V) scale per stage
+  float2* stage_scale = reinterpret_cast<float2*>(smem + C::SCALE_OFFSET);  // FP8: (K, V) scale per block of a stage
   float2* warp_ml = reinterpret_cast<float2*>(smem + C::ML_OFFSET);
 
   // Prologue, before the previous kernel on the stream may have finished: the
@@ -336,48 +336,70 @@ __device__ __forceinline__ int stage1_cta(const Stage1Params& p, uint8_t* smem) 
       const int jn = j0 + 32 + lane;
       page_next = (jn < nblk) ? __ldg(table + (blk_lo + jn * C::TB) / p.page_size) : -1;
       const int cnt = min(32, nblk - j0);
+      // one stage per NSUB consecutive blocks (32 is a multiple of NSUB, so a
+      // stage never straddles two batches of page ids)
 #pragma unroll 1
-      for (int k = 0; k < cnt; ++k) {
-        const int j = j0 + k;
-        if (!waited && (j >= C::NST || blk_lo + (j + 1) * C::TB > fresh_from)) {
+      for (int k = 0; k < cnt; k += C::NSUB) {
+        const int jb = (j0 + k) / C::NSUB;  // stage block
+        if (!waited && (jb >= C::NST || blk_lo + (j0 + k + C::NSUB) * C::TB > fresh_from)) {
           grid_dependency_wait();
           waited = true;
         }
-        const int page = __shfl_sync(kFullMask, page_mine, k);
-        float2 scale_blk;
-        scale_blk.x = __shfl_sync(kFullMask, scale_mine.x, k);
-        scale_blk.y = __shfl_sync(kFullMask, scale_mine.y, k);
+        int page[C::NSUB];
+        float2 scale_blk[C::NSUB];
+#pragma unroll
+        for (int u = 0; u < C::NSUB; ++u) {
+          page[u] = __shfl_sync(kFullMask, page_mine, k + u);
+          scale_blk[u].x = __shfl_sync(kFullMask, scale_mine.x, k + u);
+          scale_blk[u].y = __shfl_sync(kFullMask, scale_mine.y, k + u);
+        }
         int go = 1;
         if (lane == 0) {
-          const int st = j % C::NST;
-          const int round = j / C::NST;
+          const int st = jb % C::NST;
+          const int round = jb / C::NST;
           if (round > 0 && !mbar_wait(&empty_bar[st], (round - 1) & 1)) {
             err_bits |= kErrTimeout;
             go = 0;
           } else {
-            const int t0 = blk_lo + j * C::TB;
-            const bool ok = (unsigned)page < (unsigned)p.num_pages;
-            stage_valid[st] = ok ? 1u : 0u;
-            if constexpr (C::KV8) stage_scale[st] = scale_blk;
-            if (ok) {
-              const int row0 = (page * p.num_kv_heads + g) * p.page_size + (t0 % p.page_size);
-              uint8_t* dst = smem + (size_t)st * C::STAGE_BYTES;
-              mbar_arrive_expect_tx(&full_bar[st], C::TX_BYTES + p.stall_bytes);
-              if (p.tma_rank == 3) {
-                tma_load_3d(dst, &p.kmap, 0, row0, 0, &full_bar[st], policy);
-                if (!C::KVS) tma_load_3d(dst + C::KV_BYTES, &p.vmap, 0, row0, 0, &full_bar[st], policy);
-              } else {
-                constexpr int SLAB_ELEMS = 128 / C::ELEM;
+            // blocks of this stage that exist and have a page in the pool
+            uint32_t bits = 0;
 #pragma unroll
-                for (int sl = 0; sl < C::TMA_SLABS; ++sl) {
-                  tma_load_2d(dst + sl * C::SLAB_BYTES, &p.kmap, sl * SLAB_ELEMS, row0, &full_bar[st], policy);
-                  if (!C::KVS)
-                    tma_load_2d(dst + C::KV_BYTES + sl * C::SLAB_BYTES, &p.vmap, sl * SLAB_ELEMS, row0,
-                                &full_bar[st], policy);
+            for (int u = 0; u < C::NSUB; ++u) {
+              if (j0 + k + u >= nblk) continue;
+              if ((unsigned)page[u] < (unsigned)p.num_pages)
+                bits |= 1u << u;
+              else
+                err_bits |= kErrBadPage;
+            }
+            stage_valid[st] = bits;
+            if constexpr (C::KV8) {
+#pragma unroll
+              for (int u = 0; u < C::NSUB; ++u) stage_scale[st * C::NSUB + u] = scale_blk[u];
+            }
+            if (bits) {
+              uint8_t* dst = smem + (size_t)st * C::STAGE_BYTES;
+              mbar_arrive_expect_tx(&full_bar[st], __popc(bits) * C::BLOCK_TX + p.stall_bytes);
+#pragma unroll
+              for (int u = 0; u < C::NSUB; ++u) {
+                if (!((bits >> u) & 1u)) continue;
+                const int t0 = blk_lo + (j0 + k + u) * C::TB;
+                const int row0 = (page[u] * p.num_kv_heads + g) * p.page_size + (t0 % p.page_size);
+                uint8_t* kd = dst + u * C::KV_BYTES;
+                uint8_t* vd = dst + C::V_OFFSET + u * C::KV_BYTES;
+                if (p.tma_rank == 3) {
+                  tma_load_3d(kd, &p.kmap, 0, row0, 0, &full_bar[st], policy);
+                  if (!C::KVS) tma_load_3d(vd, &p.vmap, 0, row0, 0, &full_bar[st], policy);
+                } else {
+                  constexpr int SLAB_ELEMS = 128 / C::ELEM;
+#pragma unroll
+                  for (int sl = 0; sl < C::TMA_SLABS; ++sl) {
+                    tma_load_2d(kd + sl * C::SLAB_BYTES, &p.kmap, sl * SLAB_ELEMS, row0, &full_bar[st], policy);
+                    if (!C::KVS)
+                      tma_load_2d(vd + sl * C::SLAB_BYTES, &p.vmap, sl * SLAB_ELEMS, row0, &full_bar[st], policy);
+                  }
                 }
               }
             } else {
-              err_bits |= kErrBadPage;
               mbar_arrive(&full_bar[st]);
             }
           }
@@ -386,7 +408,7 @@ __device__ __forceinline__ int stage1_cta(const Stage1Params& p, uint8_t* smem) 
           stop = true;
           break;
         }
-        issued = j + 1;
+        issued = jb + 1;
       }
     }
     if (!waited) grid_dependency_wait();
@@ -448,86 +470,115 @@ __device__ __forceinline__ int stage1_cta(const Stage1Params& p, uint8_t* smem) 
   }
   const uint32_t ring = smem_u32(smem);
 
+  // stages of this piece: NSUB consecutive 16-token blocks each (the last may
+  // hold fewer)
+  const int nstg = (nblk + C::NSUB - 1) / C::NSUB;
 #pragma unroll 1
-  for (int j = warp; j < nblk; j += C::NW) {
-    const int st = j % C::NST;
+  for (int jb = warp; jb < nstg; jb += C::NW) {
+    const int st = jb % C::NST;
     // every lane polls; the warp leaves together if any lane gave up
-    const bool landed = mbar_wait(&full_bar[st], (j / C::NST) & 1);
+    const bool landed = mbar_wait(&full_bar[st], (jb / C::NST) & 1);
     if (__any_sync(kFullMask, !landed)) {
       if (lane == 0) atomicOr(p.err, kErrTimeout);
       break;
     }
     const uint32_t kst = ring + st * C::STAGE_BYTES;
-    const uint32_t vst = C::KVS ? kst : kst + C::KV_BYTES;
-    const bool stage_ok = stage_valid[st] != 0;
-    const int t0 = blk_lo + j * C::TB;
+    const uint32_t vst = C::KVS ? kst : kst + C::V_OFFSET;
+    const uint32_t valid_bits = stage_valid[st];
+    const int t0 = blk_lo + jb * (C::NSUB * C::TB);  // first token of the stage
     const uint8_t* stg = smem + (size_t)st * C::STAGE_BYTES;
-    float k_sc = 1.f, v_sc = 1.f;
-    if constexpr (C::KV8) {
-      const float2 sc = stage_scale[st];
-      k_sc = sc.x;
-      v_sc = sc.y;
+    float k_sc[C::NSUB], v_sc[C::NSUB];
+#pragma unroll
+    for (int u = 0; u < C::NSUB; ++u) {
+      k_sc[u] = 1.f;
+      v_sc[u] = 1.f;
+      if constexpr (C::KV8) {
+        const float2 sc = stage_scale[st * C::NSUB + u];
+        k_sc[u] = sc.x;
+        v_sc[u] = sc.y;
+      }
     }
 
-    // QK on the tensor cores, four independent accumulation chains
-    float sacc[4][4];
+    // QK on the tensor cores, block by block, four independent accumulation
+    // chains each. s[u]: this lane's scores of block u: tokens t0 + 16u + lane/4
+    // (s[u][0], s[u][1]) and + 8 (s[u][2], s[u][3]); heads 2*(lane%4) (s[u][0],
+    // s[u][2]) and 2*(lane%4) + 1 (s[u][1], s[u][3])
+    float s[C::NSUB][4];
 #pragma unroll
-    for (int c = 0; c < 4; ++c)
+    for (int u = 0; u < C::NSUB; ++u) {
+      float sacc[4][4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) sacc[c][i] = 0.f;
-    if constexpr (C::KV8) {
-      // A fragments straight from the e4m3 rows: one 16-byte chunk of token
-      // rows lane/4 and lane/4 + 8 holds this lane's part of four k-steps
-      // (the dims are taken in the order kv8_qk_dim gives; q follows it)
+      for (int c = 0; c < 4; ++c)
 #pragma unroll
-      for (int sl = 0; sl < C::TMA_SLABS; ++sl) {
+        for (int i = 0; i < 4; ++i) sacc[c][i] = 0.f;
+      if constexpr (C::KV8) {
+        // A fragments straight from the e4m3 rows: one 16-byte chunk of token
+        // rows lane/4 and lane/4 + 8 holds this lane's part of four k-steps
+        // (the dims are taken in the order kv8_qk_dim gives; q follows it)
+        const uint8_t* kb = stg + u * C::KV_BYTES;
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          const uint8_t* sp = stg + sl * C::SLAB_BYTES + qh * 128 + (((2 * (lane & 3) + hf) ^ qh) << 4);
-          const uint4 ra = *reinterpret_cast<const uint4*>(sp);
-          const uint4 rb = *reinterpret_cast<const uint4*>(sp + 8 * 128);
-          const uint32_t wa[4] = {ra.x, ra.y, ra.z, ra.w};
-          const uint32_t wb[4] = {rb.x, rb.y, rb.z, rb.w};
+        for (int sl = 0; sl < C::TMA_SLABS; ++sl) {
 #pragma unroll
-          for (int jj = 0; jj < 4; ++jj) {
-            uint32_t a[4];
-            e4m3x4_to_f16x4(wa[jj], a[0], a[2]);
-            e4m3x4_to_f16x4(wb[jj], a[1], a[3]);
-            const int ks = sl * 8 + hf * 4 + jj;
-            mma_f16(sacc[jj], a, qb[ks][0], qb[ks][1]);
+          for (int hf = 0; hf < 2; ++hf) {
+            const uint8_t* sp = kb + sl * C::SLAB_BYTES + qh * 128 + (((2 * (lane & 3) + hf) ^ qh) << 4);
+            const uint4 ra = *reinterpret_cast<const uint4*>(sp);
+            const uint4 rb = *reinterpret_cast<const uint4*>(sp + 8 * 128);
+            const uint32_t wa[4] = {ra.x, ra.y, ra.z, ra.w};
+            const uint32_t wb[4] = {rb.x, rb.y, rb.z, rb.w};
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+              uint32_t a[4];
+              e4m3x4_to_f16x4(wa[jj], a[0], a[2]);
+              e4m3x4_to_f16x4(wb[jj], a[1], a[3]);
+              const int ks = sl * 8 + hf * 4 + jj;
+              mma_f16(sacc[jj], a, qb[ks][0], qb[ks][1]);
+            }
           }
         }
-      }
-    } else {
+      } else {
+        const uint32_t kb = kst + u * C::KV_BYTES;
 #pragma unroll
-      for (int ks = 0; ks < C::KSTEPS; ++ks) {
-        uint32_t a[4];
-        ldmatrix_x4(a, kst + (ks >> 2) * C::SLAB_BYTES + koff[ks & 3]);
-        mma_bf16(sacc[ks & 3], a, qb[ks][0], qb[ks][1]);
+        for (int ks = 0; ks < C::KSTEPS; ++ks) {
+          uint32_t a[4];
+          ldmatrix_x4(a, kb + (ks >> 2) * C::SLAB_BYTES + koff[ks & 3]);
+          mma_bf16(sacc[ks & 3], a, qb[ks][0], qb[ks][1]);
+        }
       }
-    }
-    // lane holds tokens t0 + lane/4 (s[0], s[1]) and t0 + lane/4 + 8 (s[2], s[3]);
-    // heads 2*(lane%4) (s[0], s[2]) and 2*(lane%4) + 1 (s[1], s[3])
-    float s[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-      s[i] = ((sacc[0][i] + sacc[1][i]) + (sacc[2][i] + sacc[3][i])) * (p.scale_log2 * k_sc);
-    const int ta = t0 + qh;
-    const bool va = stage_ok && ta >= tlo && ta < thi;
-    const bool vb = stage_ok && ta + 8 >= tlo && ta + 8 < thi;
-    if constexpr (C::MQ) {
-      // each column is also cut at its own token's causal range
-      if (!(va && ta >= col_lo[0] && ta < col_hi[0])) s[0] = -INFINITY;
-      if (!(va && ta >= col_lo[1] && ta < col_hi[1])) s[1] = -INFINITY;
-      if (!(vb && ta + 8 >= col_lo[0] && ta + 8 < col_hi[0])) s[2] = -INFINITY;
-      if (!(vb && ta + 8 >= col_lo[1] && ta + 8 < col_hi[1])) s[3] = -INFINITY;
-    } else {
-      if (!va) s[0] = s[1] = -INFINITY;
-      if (!vb) s[2] = s[3] = -INFINITY;
+      for (int i = 0; i < 4; ++i)
+        s[u][i] = ((sacc[0][i] + sacc[1][i]) + (sacc[2][i] + sacc[3][i])) * (p.scale_log2 * k_sc[u]);
     }
 
-    // online softmax: max and sum over the block's 16 tokens (lane/4 and the two rows)
-    float bm0 = fmaxf(s[0], s[2]), bm1 = fmaxf(s[1], s[3]);
+    // masks: rows outside the piece's range, of a skipped page, or (multi-token
+    // columns) outside the column's own causal range
+    bool va[C::NSUB], vb[C::NSUB];
+    bool all_in = true;
+#pragma unroll
+    for (int u = 0; u < C::NSUB; ++u) {
+      const bool ok = (valid_bits >> u) & 1u;
+      const int ta = t0 + u * C::TB + qh;
+      va[u] = ok && ta >= tlo && ta < thi;
+      vb[u] = ok && ta + 8 >= tlo && ta + 8 < thi;
+      all_in = all_in && va[u] && vb[u];
+      if constexpr (C::MQ) {
+        if (!(va[u] && ta >= col_lo[0] && ta < col_hi[0])) s[u][0] = -INFINITY;
+        if (!(va[u] && ta >= col_lo[1] && ta < col_hi[1])) s[u][1] = -INFINITY;
+        if (!(vb[u] && ta + 8 >= col_lo[0] && ta + 8 < col_hi[0])) s[u][2] = -INFINITY;
+        if (!(vb[u] && ta + 8 >= col_lo[1] && ta + 8 < col_hi[1])) s[u][3] = -INFINITY;
+      } else {
+        if (!va[u]) s[u][0] = s[u][1] = -INFINITY;
+        if (!vb[u]) s[u][2] = s[u][3] = -INFINITY;
+      }
+    }
+
+    // online softmax: max and sum over the stage's tokens (lane/4, the two
+    // rows and the NSUB blocks)
+    float bm0 = -INFINITY, bm1 = -INFINITY;
+#pragma unroll
+    for (int u = 0; u < C::NSUB; ++u) {
+      bm0 = fmaxf(bm0, fmaxf(s[u][0], s[u][2]));
+      bm1 = fmaxf(bm1, fmaxf(s[u][1], s[u][3]));
+    }
 #pragma unroll
     for (int mask = 4; mask < 32; mask <<= 1) {
       bm0 = fmaxf(bm0, __shfl_xor_sync(kFullMask, bm0, mask));
@@ -537,8 +588,17 @@ __device__ __forceinline__ int stage1_cta(const Stage1Params& p, uint8_t* smem) 
     const float alpha0 = (mn0 == -INFINITY) ? 1.f : ex2(m_run[0] - mn0);
     const float alpha1 = (mn1 == -INFINITY) ? 1.f : ex2(m_run[1] - mn1);
     const float ms0 = (mn0 == -INFINITY) ? 0.f : mn0, ms1 = (mn1 == -INFINITY) ? 0.f : mn1;
-    const float p0 = ex2(s[0] - ms0), p1 = ex2(s[1] - ms1), p2 = ex2(s[2] - ms0), p3 = ex2(s[3] - ms1);
-    float bs0 = p0 + p2, bs1 = p1 + p3;
+    float pr[C::NSUB][4];
+    float bs0 = 0.f, bs1 = 0.f;
+#pragma unroll
+    for (int u = 0; u < C::NSUB; ++u) {
+      pr[u][0] = ex2(s[u][0] - ms0);
+      pr[u][1] = ex2(s[u][1] - ms1);
+      pr[u][2] = ex2(s[u][2] - ms0);
+      pr[u][3] = ex2(s[u][3] - ms1);
+      bs0 += pr[u][0] + pr[u][2];
+      bs1 += pr[u][1] + pr[u][3];
+    }
 #pragma unroll
     for (int mask = 4; mask < 32; mask <<= 1) {
       bs0 += __shfl_xor_sync(kFullMask, bs0, mask);
@@ -558,84 +618,95 @@ __device__ __forceinline__ int stage1_cta(const Stage1Params& p, uint8_t* smem) 
       }
     }
 
-    // Edge block (window start, sequence end, skipped page): the masked rows
+    // Edge stage (window start, sequence end, skipped page): the masked rows
     // carry p = 0, but 0 * NaN is NaN, and a page's unused rows may hold any
     // bits. Zero those V rows before they enter the PV contraction.
     // (The FP8 path zeroes them in registers, below.)
     if constexpr (!C::KV8) {
-      const bool edge = __any_sync(kFullMask, !(va && vb));
-      if (edge) {
+      if (__any_sync(kFullMask, !all_in)) {
 #pragma unroll 1
-        for (int r = 0; r < C::TB; ++r) {
+        for (int r = 0; r < C::NSUB * C::TB; ++r) {
+          const int u = r / C::TB, rr = r % C::TB;
           const int t = t0 + r;
-          if (stage_ok && t >= tlo && t < thi) continue;
+          if (((valid_bits >> u) & 1u) && t >= tlo && t < thi) continue;
           for (int idx = lane; idx < C::SLABS * 8; idx += 32)
-            sts128_zero(vst + (idx >> 3) * C::SLAB_BYTES + r * 128 + (idx & 7) * 16);
+            sts128_zero(vst + u * C::KV_BYTES + (idx >> 3) * C::SLAB_BYTES + rr * 128 + (idx & 7) * 16);
         }
         fence_proxy_async_smem();  // these writes precede the next TMA fill
         __syncwarp();
       }
     }
 
-    // P^T as the B operand: transpose the (token x head) 16-bit fragments; on
-    // the FP8 path the block's V scale rides on P (sum_t p_t (v_sc v8_t))
-    uint32_t pb0, pb1;
-    if constexpr (C::KV8) {
-      pb0 = movmatrix_trans(pack_f16x2(p0 * v_sc, p1 * v_sc));  // tokens 0..7
-      pb1 = movmatrix_trans(pack_f16x2(p2 * v_sc, p3 * v_sc));  // tokens 8..15
-    } else {
-      pb0 = movmatrix_trans(pack_bf16x2(p0, p1));
-      pb1 = movmatrix_trans(pack_bf16x2(p2, p3));
+    // P^T as the B operand of each block: transpose the (token x head) 16-bit
+    // fragments; on the FP8 path the block's V scale rides on P
+    // (sum_t p_t (v_sc v8_t))
+    uint32_t pb[C::NSUB][2];
+#pragma unroll
+    for (int u = 0; u < C::NSUB; ++u) {
+      if constexpr (C::KV8) {
+        pb[u][0] = movmatrix_trans(pack_f16x2(pr[u][0] * v_sc[u], pr[u][1] * v_sc[u]));  // tokens 0..7
+        pb[u][1] = movmatrix_trans(pack_f16x2(pr[u][2] * v_sc[u], pr[u][3] * v_sc[u]));  // tokens 8..15
+      } else {
+        pb[u][0] = movmatrix_trans(pack_bf16x2(pr[u][0], pr[u][1]));
+        pb[u][1] = movmatrix_trans(pack_bf16x2(pr[u][2], pr[u][3]));
+      }
     }
 
     // PV on the tensor cores
     if constexpr (C::KV8) {
-      // A fragments (dims x tokens) straight from the e4m3 rows: this lane
-      // reads the 16-byte chunk lane/4 of tokens 2*(lane%4) + {0, 1, 8, 9}.
-      // Byte 2u (2u + 1) of a chunk is taken as the dim of row lane/4
-      // (lane/4 + 8) of m-tile u of the slab, so row i of m-tile u holds dim
-      // 16*(i%8) + 2u + i/8 (the epilogue puts each back); a byte permute
-      // pairs one dim of two tokens.
-      const int tv = 2 * (lane & 3);
-      const int t_a = t0 + tv;
-      const bool ok0 = stage_ok && t_a >= tlo && t_a < thi;
-      const bool ok1 = stage_ok && t_a + 1 >= tlo && t_a + 1 < thi;
-      const bool ok2 = stage_ok && t_a + 8 >= tlo && t_a + 8 < thi;
-      const bool ok3 = stage_ok && t_a + 9 >= tlo && t_a + 9 < thi;
-      const uint8_t* vstg = C::KVS ? stg : stg + C::KV_BYTES;
 #pragma unroll
-      for (int sl = 0; sl < C::TMA_SLABS; ++sl) {
-        const uint8_t* vp = vstg + sl * C::SLAB_BYTES;
-        const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
-        // rows the sequence does not cover may hold any bits: e4m3 zero instead
-        uint4 r0 = *reinterpret_cast<const uint4*>(vp + tv * 128 + ((qh ^ tv) << 4));
-        uint4 r1 = *reinterpret_cast<const uint4*>(vp + (tv + 1) * 128 + ((qh ^ (tv + 1)) << 4));
-        uint4 r2 = *reinterpret_cast<const uint4*>(vp + (tv + 8) * 128 + ((qh ^ tv) << 4));
-        uint4 r3 = *reinterpret_cast<const uint4*>(vp + (tv + 9) * 128 + ((qh ^ (tv + 1)) << 4));
-        if (!ok0) r0 = zero;
-        if (!ok1) r1 = zero;
-        if (!ok2) r2 = zero;
-        if (!ok3) r3 = zero;
-        const uint32_t x0[4] = {r0.x, r0.y, r0.z, r0.w}, x1[4] = {r1.x, r1.y, r1.z, r1.w};
-        const uint32_t x2[4] = {r2.x, r2.y, r2.z, r2.w}, x3[4] = {r3.x, r3.y, r3.z, r3.w};
+      for (int u = 0; u < C::NSUB; ++u) {
+        // A fragments (dims x tokens) straight from the e4m3 rows: this lane
+        // reads the 16-byte chunk lane/4 of tokens 2*(lane%4) + {0, 1, 8, 9}.
+        // Byte 2w (2w + 1) of a chunk is taken as the dim of row lane/4
+        // (lane/4 + 8) of m-tile w of the slab, so row i of m-tile w holds dim
+        // 16*(i%8) + 2w + i/8 (the epilogue puts each back); a byte permute
+        // pairs one dim of two tokens.
+        const int tv = 2 * (lane & 3);
+        const int t_a = t0 + u * C::TB + tv;
+        const bool ok = (valid_bits >> u) & 1u;
+        const bool ok0 = ok && t_a >= tlo && t_a < thi;
+        const bool ok1 = ok && t_a + 1 >= tlo && t_a + 1 < thi;
+        const bool ok2 = ok && t_a + 8 >= tlo && t_a + 8 < thi;
+        const bool ok3 = ok && t_a + 9 >= tlo && t_a + 9 < thi;
+        const uint8_t* vstg = (C::KVS ? stg : stg + C::V_OFFSET) + u * C::KV_BYTES;
 #pragma unroll
-        for (int w = 0; w < 4; ++w) {
+        for (int sl = 0; sl < C::TMA_SLABS; ++sl) {
+          const uint8_t* vp = vstg + sl * C::SLAB_BYTES;
+          const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+          // rows the sequence does not cover may hold any bits: e4m3 zero instead
+          uint4 r0 = *reinterpret_cast<const uint4*>(vp + tv * 128 + ((qh ^ tv) << 4));
+          uint4 r1 = *reinterpret_cast<const uint4*>(vp + (tv + 1) * 128 + ((qh ^ (tv + 1)) << 4));
+          uint4 r2 = *reinterpret_cast<const uint4*>(vp + (tv + 8) * 128 + ((qh ^ tv) << 4));
+          uint4 r3 = *reinterpret_cast<const uint4*>(vp + (tv + 9) * 128 + ((qh ^ (tv + 1)) << 4));
+          if (!ok0) r0 = zero;
+          if (!ok1) r1 = zero;
+          if (!ok2) r2 = zero;
+          if (!ok3) r3 = zero;
+          const uint32_t x0[4] = {r0.x, r0.y, r0.z, r0.w}, x1[4] = {r1.x, r1.y, r1.z, r1.w};
+          const uint32_t x2[4] = {r2.x, r2.y, r2.z, r2.w}, x3[4] = {r3.x, r3.y, r3.z, r3.w};
 #pragma unroll
-          for (int u2 = 0; u2 < 2; ++u2) {
-            const uint32_t sel = u2 ? 0x7362u : 0x5140u;
-            uint32_t a[4];
-            e4m3x4_to_f16x4(__byte_perm(x0[w], x1[w], sel), a[0], a[1]);
-            e4m3x4_to_f16x4(__byte_perm(x2[w], x3[w], sel), a[2], a[3]);
-            mma_f16(acc[sl * 8 + w * 2 + u2], a, pb0, pb1);
+          for (int w = 0; w < 4; ++w) {
+#pragma unroll
+            for (int u2 = 0; u2 < 2; ++u2) {
+              const uint32_t sel = u2 ? 0x7362u : 0x5140u;
+              uint32_t a[4];
+              e4m3x4_to_f16x4(__byte_perm(x0[w], x1[w], sel), a[0], a[1]);
+              e4m3x4_to_f16x4(__byte_perm(x2[w], x3[w], sel), a[2], a[3]);
+              mma_f16(acc[sl * 8 + w * 2 + u2], a, pb[u][0], pb[u][1]);
+            }
           }
         }
       }
     } else {
 #pragma unroll
       for (int mt = 0; mt < C::MTILES; ++mt) {
-        uint32_t a[4];
-        ldmatrix_x4_trans(a, vst + (mt >> 2) * C::SLAB_BYTES + voff[mt & 3]);
-        mma_bf16(acc[mt], a, pb0, pb1);
+#pragma unroll
+        for (int u = 0; u < C::NSUB; ++u) {
+          uint32_t a[4];
+          ldmatrix_x4_trans(a, vst + u * C::KV_BYTES + (mt >> 2) * C::SLAB_BYTES + voff[mt & 3]);
+          mma_bf16(acc[mt], a, pb[u][0], pb[u][1]);
+        }
       }
     }
 
@@ -857,16 +928,17 @@ __global__ void __launch_bounds__(C::THREADS, 1) stage1_kernel(const __grid_cons
 
 // ---- instantiation and dispatch -------------------------------------------------
 
-#define PD_STAGE1_INSTANCE(ID, D, G, KVS, KV8, NW, SPW, MQ) \
-  template __global__ void stage1_kernel<Stage1Cfg<D, G, KVS, KV8, NW, SPW, MQ>>(const __grid_constant__ Stage1Params);
+#define PD_STAGE1_INSTANCE(ID, D, G, KVS, KV8, NW, SPW, MQ, NSUB)                       \
+  template __global__ void stage1_kernel<Stage1Cfg<D, G, KVS, KV8, NW, SPW, MQ, NSUB>>( \
+      const __grid_constant__ Stage1Params);
 PD_FOR_EACH_VARIANT(PD_STAGE1_INSTANCE)
 #undef PD_STAGE1_INSTANCE
 
 const void* stage1_kernel_ptr(int variant) {
   switch (variant) {
-#define PD_STAGE1_CASE(ID, D, G, KVS, KV8, NW, SPW, MQ) \
-  case ID:                                              \
-    return reinterpret_cast<const void*>(&stage1_kernel<Stage1Cfg<D, G, KVS, KV8, NW, SPW, MQ>>);
+#define PD_STAGE1_CASE(ID, D, G, KVS, KV8, NW, SPW, MQ, NSUB) \
+  case ID:                                                    \
+    return reinterpret_cast<const void*>(&stage1_kernel<Stage1Cfg<D, G, KVS, KV8, NW, SPW, MQ, NSUB>>);
     PD_FOR_EACH_VARIANT(PD_STAGE1_CASE)
 #undef PD_STAGE1_CASE
     default:

@@ -124,7 +124,8 @@ def test_groups_above_8_ragged(d, G, kvs, window):
         assert step.plan.grid_y == Hkv * ((G + 7) // 8)
         modes.add(int(step.plan.merge_mode))
         compare(out, ref, li, f"d{d} G{G} kvs{kvs} W{window} sms{sms} S{step.plan.num_splits}")
-    assert 0 in modes and len(modes) >= 2, modes
+    if window == 0:  # short windows always fit one piece
+        assert 0 in modes and len(modes) >= 2, modes
 
 
 def test_group_16_single_token_is_bit_exact():
