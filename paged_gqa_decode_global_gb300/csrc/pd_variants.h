@@ -75,7 +75,11 @@ struct Stage1Cfg {
   static constexpr int SCALE_OFFSET = (VALID_OFFSET + NST * 4 + 7) / 8 * 8;  // float2 (k, v) scale[NST][NSUB] (FP8)
   static constexpr int ML_OFFSET = SCALE_OFFSET + NST * NSUB * 8;  // float2 ml[NW][G]
   static constexpr int COEF_OFFSET = ML_OFFSET + NW * G * 8;   // float coef[NW][G], lse[G]
-  static constexpr int TAIL_END = (COEF_OFFSET + (NW * G + G) * 4 + 15) / 16 * 16;
+  // the producer's batch of 32 blocks: pool row of each (or a negative code)
+  // and, FP8, its (K, V) scales
+  static constexpr int BATCH_ROW_OFFSET = (COEF_OFFSET + (NW * G + G) * 4 + 7) / 8 * 8;  // int [32]
+  static constexpr int BATCH_SCALE_OFFSET = BATCH_ROW_OFFSET + 32 * 4;                    // float2 [32]
+  static constexpr int TAIL_END = (BATCH_SCALE_OFFSET + 32 * 8 + 15) / 16 * 16;
   // Pieces that can push into a region of their own, outside the ring (what
   // is left of the 227 KiB): with them the cluster merge needs one cluster
   // barrier (other ranks may store while rank 0 still streams); larger

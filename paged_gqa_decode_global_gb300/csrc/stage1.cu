@@ -310,108 +310,107 @@ __device__ __forceinline__ int stage1_cta(const Stage1Params& p, uint8_t* smem) 
   // ---- producer ------------------------------------------------------------------
   if (warp == C::NW) {
     const uint64_t policy = l2_evict_first_policy();
-    // The whole warp walks the blocks 32 at a time: each lane holds one block's
-    // page id (fetched a round ahead), lane 0 waits for the stage and issues
-    // the copies, so page-id loads never serialise the issue of copies.
-    int issued = 0;
+    int* batch_row = reinterpret_cast<int*>(smem + C::BATCH_ROW_OFFSET);
+    float2* batch_scale = reinterpret_cast<float2*>(smem + C::BATCH_SCALE_OFFSET);
+    // The warp walks the blocks 32 at a time: lane k turns block j0 + k's page
+    // id (fetched a batch ahead) into the pool row its copies start at (and,
+    // FP8, fetches its scales) and leaves them in shared memory; lane 0 alone
+    // then waits for each stage and issues its copies, with no warp-wide step
+    // per block.
+    int issued = 0;  // stage blocks issued (lane 0)
     bool stop = false;
-    bool waited = !early;
+    bool waited = !early;  // lane 0's dependency wait
     // error bits seen by lane 0, published once this grid may write global
     // memory (after its dependency wait)
     uint32_t err_bits = 0;
     // blocks ending after this position hold rows the previous kernel may write
     const int fresh_from = L - p.query_tokens;
+    constexpr int kNoBlock = -1, kBadPage = -2;
 #pragma unroll 1
     for (int j0 = 0; j0 < nblk && !stop; j0 += 32) {
-      const int page_mine = page_next;
-      // FP8: each lane also fetches its block's (K, V) scales
-      float2 scale_mine = make_float2(1.f, 1.f);
-      if constexpr (C::KV8) {
-        if ((unsigned)page_mine < (unsigned)p.num_pages) {
-          const size_t si = (size_t)page_mine * p.num_kv_heads + g;
-          scale_mine.x = __ldg(p.k_scale + si);
-          scale_mine.y = C::KVS ? scale_mine.x : __ldg(p.v_scale + si);
+      const int jk = j0 + lane;
+      int row = kNoBlock;
+      float2 sc = make_float2(1.f, 1.f);
+      if (jk < nblk) {
+        if ((unsigned)page_next < (unsigned)p.num_pages) {
+          row = (page_next * p.num_kv_heads + g) * p.page_size + ((blk_lo + jk * C::TB) % p.page_size);
+          if constexpr (C::KV8) {
+            const size_t si = (size_t)page_next * p.num_kv_heads + g;
+            sc.x = __ldg(p.k_scale + si);
+            sc.y = C::KVS ? sc.x : __ldg(p.v_scale + si);
+          }
+        } else {
+          row = kBadPage;
         }
       }
       const int jn = j0 + 32 + lane;
       page_next = (jn < nblk) ? __ldg(table + (blk_lo + jn * C::TB) / p.page_size) : -1;
-      const int cnt = min(32, nblk - j0);
-      // one stage per NSUB consecutive blocks (32 is a multiple of NSUB, so a
-      // stage never straddles two batches of page ids)
+      batch_row[lane] = row;
+      if constexpr (C::KV8) batch_scale[lane] = sc;
+      __syncwarp();
+      if (lane == 0) {
+        const int cnt = min(32, nblk - j0);
+        // one stage per NSUB consecutive blocks (32 is a multiple of NSUB, so
+        // a stage never straddles two batches)
 #pragma unroll 1
-      for (int k = 0; k < cnt; k += C::NSUB) {
-        const int jb = (j0 + k) / C::NSUB;  // stage block
-        if (!waited && (jb >= C::NST || blk_lo + (j0 + k + C::NSUB) * C::TB > fresh_from)) {
-          grid_dependency_wait();
-          waited = true;
-        }
-        int page[C::NSUB];
-        float2 scale_blk[C::NSUB];
-#pragma unroll
-        for (int u = 0; u < C::NSUB; ++u) {
-          page[u] = __shfl_sync(kFullMask, page_mine, k + u);
-          scale_blk[u].x = __shfl_sync(kFullMask, scale_mine.x, k + u);
-          scale_blk[u].y = __shfl_sync(kFullMask, scale_mine.y, k + u);
-        }
-        int go = 1;
-        if (lane == 0) {
+        for (int k = 0; k < cnt; k += C::NSUB) {
+          const int jb = (j0 + k) / C::NSUB;  // stage block
+          if (!waited && (jb >= C::NST || blk_lo + (j0 + k + C::NSUB) * C::TB > fresh_from)) {
+            grid_dependency_wait();
+            waited = true;
+          }
           const int st = jb % C::NST;
           const int round = jb / C::NST;
           if (round > 0 && !mbar_wait(&empty_bar[st], (round - 1) & 1)) {
             err_bits |= kErrTimeout;
-            go = 0;
-          } else {
-            // blocks of this stage that exist and have a page in the pool
-            uint32_t bits = 0;
+            stop = true;
+            break;
+          }
+          // blocks of this stage that exist and have a page in the pool
+          int rows[C::NSUB];
+          uint32_t bits = 0;
+#pragma unroll
+          for (int u = 0; u < C::NSUB; ++u) {
+            rows[u] = (k + u < cnt) ? batch_row[k + u] : kNoBlock;
+            if (rows[u] >= 0) bits |= 1u << u;
+            if (rows[u] == kBadPage) err_bits |= kErrBadPage;
+          }
+          stage_valid[st] = bits;
+          if constexpr (C::KV8) {
+#pragma unroll
+            for (int u = 0; u < C::NSUB; ++u) stage_scale[st * C::NSUB + u] = batch_scale[(k + u) & 31];
+          }
+          if (bits) {
+            uint8_t* dst = smem + (size_t)st * C::STAGE_BYTES;
+            mbar_arrive_expect_tx(&full_bar[st], __popc(bits) * C::BLOCK_TX + p.stall_bytes);
 #pragma unroll
             for (int u = 0; u < C::NSUB; ++u) {
-              if (j0 + k + u >= nblk) continue;
-              if ((unsigned)page[u] < (unsigned)p.num_pages)
-                bits |= 1u << u;
-              else
-                err_bits |= kErrBadPage;
-            }
-            stage_valid[st] = bits;
-            if constexpr (C::KV8) {
+              if (!((bits >> u) & 1u)) continue;
+              uint8_t* kd = dst + u * C::KV_BYTES;
+              uint8_t* vd = dst + C::V_OFFSET + u * C::KV_BYTES;
+              if (p.tma_rank == 3) {
+                tma_load_3d(kd, &p.kmap, 0, rows[u], 0, &full_bar[st], policy);
+                if (!C::KVS) tma_load_3d(vd, &p.vmap, 0, rows[u], 0, &full_bar[st], policy);
+              } else {
+                constexpr int SLAB_ELEMS = 128 / C::ELEM;
 #pragma unroll
-              for (int u = 0; u < C::NSUB; ++u) stage_scale[st * C::NSUB + u] = scale_blk[u];
-            }
-            if (bits) {
-              uint8_t* dst = smem + (size_t)st * C::STAGE_BYTES;
-              mbar_arrive_expect_tx(&full_bar[st], __popc(bits) * C::BLOCK_TX + p.stall_bytes);
-#pragma unroll
-              for (int u = 0; u < C::NSUB; ++u) {
-                if (!((bits >> u) & 1u)) continue;
-                const int t0 = blk_lo + (j0 + k + u) * C::TB;
-                const int row0 = (page[u] * p.num_kv_heads + g) * p.page_size + (t0 % p.page_size);
-                uint8_t* kd = dst + u * C::KV_BYTES;
-                uint8_t* vd = dst + C::V_OFFSET + u * C::KV_BYTES;
-                if (p.tma_rank == 3) {
-                  tma_load_3d(kd, &p.kmap, 0, row0, 0, &full_bar[st], policy);
-                  if (!C::KVS) tma_load_3d(vd, &p.vmap, 0, row0, 0, &full_bar[st], policy);
-                } else {
-                  constexpr int SLAB_ELEMS = 128 / C::ELEM;
-#pragma unroll
-                  for (int sl = 0; sl < C::TMA_SLABS; ++sl) {
-                    tma_load_2d(kd + sl * C::SLAB_BYTES, &p.kmap, sl * SLAB_ELEMS, row0, &full_bar[st], policy);
-                    if (!C::KVS)
-                      tma_load_2d(vd + sl * C::SLAB_BYTES, &p.vmap, sl * SLAB_ELEMS, row0, &full_bar[st], policy);
-                  }
+                for (int sl = 0; sl < C::TMA_SLABS; ++sl) {
+                  tma_load_2d(kd + sl * C::SLAB_BYTES, &p.kmap, sl * SLAB_ELEMS, rows[u], &full_bar[st], policy);
+                  if (!C::KVS)
+                    tma_load_2d(vd + sl * C::SLAB_BYTES, &p.vmap, sl * SLAB_ELEMS, rows[u], &full_bar[st], policy);
                 }
               }
-            } else {
-              mbar_arrive(&full_bar[st]);
             }
+          } else {
+            mbar_arrive(&full_bar[st]);
           }
+          issued = jb + 1;
         }
-        if (__shfl_sync(kFullMask, go, 0) == 0) {
-          stop = true;
-          break;
-        }
-        issued = jb + 1;
       }
+      // lane 0 is done with this batch's entries before they are rewritten
+      stop = __shfl_sync(kFullMask, stop, 0);
     }
-    if (!waited) grid_dependency_wait();
+    if (early && !(lane == 0 && waited)) grid_dependency_wait();
     // no copy may still be landing in shared memory when the CTA exits (one
     // deadline for all stages)
     if (lane == 0) {
