@@ -75,11 +75,15 @@ struct Stage1Cfg {
   static constexpr int SCALE_OFFSET = (VALID_OFFSET + NST * 4 + 7) / 8 * 8;  // float2 (k, v) scale[NST][NSUB] (FP8)
   static constexpr int ML_OFFSET = SCALE_OFFSET + NST * NSUB * 8;  // float2 ml[NW][G]
   static constexpr int COEF_OFFSET = ML_OFFSET + NW * G * 8;   // float coef[NW][G], lse[G]
-  // the producer's batch of 32 blocks: pool row of each (or a negative code)
-  // and, FP8, its (K, V) scales
+  // Rings of 24..32 stages are fed by one producer lane per stage (each lane
+  // waits for its own stage and issues its copies); other rings by the
+  // producer warp's batch walk, lane 0 issuing in order.
+  static constexpr bool LANE_PER_STAGE = NST >= 24 && NST <= 32;
+  // the batch walk's 32 blocks: pool row of each (or a negative code) and,
+  // FP8, its (K, V) scales
   static constexpr int BATCH_ROW_OFFSET = (COEF_OFFSET + (NW * G + G) * 4 + 7) / 8 * 8;  // int [32]
-  static constexpr int BATCH_SCALE_OFFSET = BATCH_ROW_OFFSET + 32 * 4;                    // float2 [32]
-  static constexpr int TAIL_END = (BATCH_SCALE_OFFSET + 32 * 8 + 15) / 16 * 16;
+  static constexpr int BATCH_SCALE_OFFSET = BATCH_ROW_OFFSET + (LANE_PER_STAGE ? 0 : 32 * 4);  // float2 [32]
+  static constexpr int TAIL_END = (BATCH_SCALE_OFFSET + (LANE_PER_STAGE ? 0 : 32 * 8) + 15) / 16 * 16;
   // Pieces that can push into a region of their own, outside the ring (what
   // is left of the 227 KiB): with them the cluster merge needs one cluster
   // barrier (other ranks may store while rank 0 still streams); larger
@@ -112,7 +116,8 @@ struct Stage1Cfg {
 // one block a stage; d256 K!=V: two blocks), 16 KiB x 12 (d512 K=V: one block;
 // d256 K=V and d128 K!=V: two blocks), 8 KiB x 24 (d128 K=V: two blocks).
 // FP8: seven consumer warps (two per SM sub-partition hide the latency of
-// widening e4m3 fragments to f16), one block a stage, rings of 196-224 KiB.
+// widening e4m3 fragments to f16), one block a stage (two for d256 K=V),
+// rings of 168-224 KiB.
 // Column-tiled (ids 32-35): the group-8 geometry, any group up to 16 and any
 // number of query tokens at run time (ids 44-47: the same over an FP8 cache).
 // head_dim 128: ids 36-43 (bf16, one query token).
@@ -145,10 +150,10 @@ struct Stage1Cfg {
   X(25, 256, 2, false, true, 7, 4, false, 1)  \
   X(26, 256, 4, false, true, 7, 4, false, 1)  \
   X(27, 256, 8, false, true, 7, 4, false, 1)  \
-  X(28, 256, 1, true, true, 7, 7, false, 1)   \
-  X(29, 256, 2, true, true, 7, 7, false, 1)   \
-  X(30, 256, 4, true, true, 7, 7, false, 1)   \
-  X(31, 256, 8, true, true, 7, 7, false, 1)   \
+  X(28, 256, 1, true, true, 7, 3, false, 2)   \
+  X(29, 256, 2, true, true, 7, 3, false, 2)   \
+  X(30, 256, 4, true, true, 7, 3, false, 2)   \
+  X(31, 256, 8, true, true, 7, 3, false, 2)   \
   X(32, 512, 8, false, false, 3, 2, true, 1)  \
   X(33, 512, 8, true, false, 3, 4, true, 1)   \
   X(34, 256, 8, false, false, 3, 2, true, 2)  \
@@ -164,7 +169,7 @@ struct Stage1Cfg {
   X(44, 512, 8, false, true, 7, 2, true, 1)   \
   X(45, 512, 8, true, true, 7, 4, true, 1)    \
   X(46, 256, 8, false, true, 7, 4, true, 1)   \
-  X(47, 256, 8, true, true, 7, 7, true, 1)
+  X(47, 256, 8, true, true, 7, 3, true, 2)
 
 struct VariantInfo {
   int id, head_dim, group, kv_shared, kv_fp8, nw, spw, block_tokens, threads, smem_bytes, max_cluster, multi,

@@ -208,11 +208,19 @@ __device__ __forceinline__ int stage1_cta(const Stage1Params& p, uint8_t* smem) 
   const int cap = p.max_pages * p.page_size;
   const int32_t* table = p.block_tables + (size_t)b * p.max_pages;
   // On a global layer a piece starts at split * chunk whatever the length, so
-  // the producer fetches its first 32 page ids while the length is in flight.
-  int page_spec = -1;
-  if (warp == C::NW && p.window == 0) {
-    const long long t = (long long)split * p.chunk_tokens + (long long)lane * C::TB;
-    if (t < cap) page_spec = __ldg(table + t / p.page_size);
+  // the producer fetches its first page ids while the length is in flight:
+  // with one lane per stage, lane st those of stage block st; with the batch
+  // walk, lane k that of block k.
+  constexpr bool kLanePerStage = C::LANE_PER_STAGE;
+  int page_spec[C::NSUB];
+#pragma unroll
+  for (int u = 0; u < C::NSUB; ++u) {
+    page_spec[u] = -1;
+    const int blk = kLanePerStage ? lane * C::NSUB + u : (u == 0 ? lane : -1);
+    if (warp == C::NW && p.window == 0 && blk >= 0 && (!kLanePerStage || lane < C::NST)) {
+      const long long t = (long long)split * p.chunk_tokens + (long long)blk * C::TB;
+      if (t < cap) page_spec[u] = __ldg(table + t / p.page_size);
+    }
   }
   int L = p.seq_lens[b];
   if (L < 0 || L > cap || (C::MQ && cm.T > 1 && L < cm.T)) {
@@ -243,6 +251,8 @@ __device__ __forceinline__ int stage1_cta(const Stage1Params& p, uint8_t* smem) 
   const int thi = (int)(piece_hi < hi ? piece_hi : hi);
   const int blk_lo = (tlo / C::TB) * C::TB;
   const int nblk = (thi > tlo) ? (thi - blk_lo + C::TB - 1) / C::TB : 0;
+  // stages of this piece: NSUB consecutive blocks each (the last may hold fewer)
+  const int nstg = (nblk + C::NSUB - 1) / C::NSUB;
 
   if (nblk == 0) {
     // nothing attended in this piece
@@ -263,18 +273,14 @@ __device__ __forceinline__ int stage1_cta(const Stage1Params& p, uint8_t* smem) 
     return kMergeNothing;
   }
 
-  // Start each role's first global loads before the barrier set-up so their
-  // latency overlaps it: the producer warp fetches the page ids of its first 32
-  // blocks (one per lane), the consumers their q fragments.
-  int page_next = -1;
+  // The consumers start their q loads before the barrier set-up so their
+  // latency overlaps it.
   // B fragments of q (heads on N, dims on K): lane holds head lane/4, dims
   // 2*(lane%4) + {0,1} and + {8,9} of every 16-dim step; heads past G are zero.
   const int qh = lane >> 2;
   const int qk = (lane & 3) * 2;
   uint32_t qb[C::KSTEPS][2];
-  if (warp == C::NW) {
-    if (lane < nblk) page_next = (p.window == 0) ? page_spec : __ldg(table + (blk_lo + lane * C::TB) / p.page_size);
-  } else {
+  if (warp != C::NW) {
 #pragma unroll
     for (int ks = 0; ks < C::KSTEPS; ++ks) {
       if (cm.valid(qh)) {
@@ -309,7 +315,131 @@ __device__ __forceinline__ int stage1_cta(const Stage1Params& p, uint8_t* smem) 
 
   // ---- producer ------------------------------------------------------------------
   if (warp == C::NW) {
+    if constexpr (kLanePerStage) {
+    // Lane st owns ring stage st: it walks the stage blocks st, st + NST, ...
+    // of the piece on its own, fetching the next one's page ids (and FP8
+    // scales) while it waits for the stage to be released, then issuing that
+    // block's copies. Stages never wait for one another, and each lane waits
+    // only for the use of its stage it issued itself.
     const uint64_t policy = l2_evict_first_policy();
+    bool waited = !early;  // this lane's dependency wait
+    // error bits seen by this lane, published once this grid may write global
+    // memory (after its dependency wait)
+    uint32_t err_bits = 0;
+    int last_jb = -1;  // the last stage block this lane issued
+    // blocks ending after this position hold rows the previous kernel may write
+    const int fresh_from = L - p.query_tokens;
+    if (lane < C::NST) {
+      const int st = lane;
+      uint8_t* dst = smem + (size_t)st * C::STAGE_BYTES;
+      // page ids (and scales) of stage block jb, fetched one use ahead
+      auto fetch = [&](int jb, int (&pg)[C::NSUB], float2 (&sc)[C::NSUB]) {
+#pragma unroll
+        for (int u = 0; u < C::NSUB; ++u) {
+          const int j = jb * C::NSUB + u;
+          pg[u] = (jb < nstg && j < nblk) ? __ldg(table + (blk_lo + j * C::TB) / p.page_size) : -1;
+          sc[u] = make_float2(1.f, 1.f);
+          if constexpr (C::KV8) {
+            if ((unsigned)pg[u] < (unsigned)p.num_pages) {
+              const size_t si = (size_t)pg[u] * p.num_kv_heads + g;
+              sc[u].x = __ldg(p.k_scale + si);
+              sc[u].y = C::KVS ? sc[u].x : __ldg(p.v_scale + si);
+            }
+          }
+        }
+      };
+      int pg[C::NSUB];
+      float2 sc[C::NSUB];
+      if (p.window == 0) {
+        // the ids fetched before the length (a piece of a global layer starts at split * chunk)
+#pragma unroll
+        for (int u = 0; u < C::NSUB; ++u) {
+          pg[u] = (st * C::NSUB + u < nblk) ? page_spec[u] : -1;
+          sc[u] = make_float2(1.f, 1.f);
+          if constexpr (C::KV8) {
+            if ((unsigned)pg[u] < (unsigned)p.num_pages) {
+              const size_t si = (size_t)pg[u] * p.num_kv_heads + g;
+              sc[u].x = __ldg(p.k_scale + si);
+              sc[u].y = C::KVS ? sc[u].x : __ldg(p.v_scale + si);
+            }
+          }
+        }
+      } else {
+        fetch(st, pg, sc);
+      }
+#pragma unroll 1
+      for (int jb = st; jb < nstg; jb += C::NST) {
+        int pg_next[C::NSUB];
+        float2 sc_next[C::NSUB];
+        fetch(jb + C::NST, pg_next, sc_next);
+        if (!waited && (jb >= C::NST || blk_lo + (jb + 1) * C::NSUB * C::TB > fresh_from)) {
+          grid_dependency_wait();
+          waited = true;
+        }
+        const int round = jb / C::NST;
+        if (round > 0 && !mbar_wait(&empty_bar[st], (round - 1) & 1)) {
+          err_bits |= kErrTimeout;
+          break;
+        }
+        // blocks of this stage that exist and have a page in the pool
+        uint32_t bits = 0;
+#pragma unroll
+        for (int u = 0; u < C::NSUB; ++u) {
+          if (jb * C::NSUB + u >= nblk) continue;
+          if ((unsigned)pg[u] < (unsigned)p.num_pages)
+            bits |= 1u << u;
+          else
+            err_bits |= kErrBadPage;
+        }
+        stage_valid[st] = bits;
+        if constexpr (C::KV8) {
+#pragma unroll
+          for (int u = 0; u < C::NSUB; ++u) stage_scale[st * C::NSUB + u] = sc[u];
+        }
+        if (bits) {
+          mbar_arrive_expect_tx(&full_bar[st], __popc(bits) * C::BLOCK_TX + p.stall_bytes);
+#pragma unroll
+          for (int u = 0; u < C::NSUB; ++u) {
+            if (!((bits >> u) & 1u)) continue;
+            const int t0 = blk_lo + (jb * C::NSUB + u) * C::TB;
+            const int row0 = (pg[u] * p.num_kv_heads + g) * p.page_size + (t0 % p.page_size);
+            uint8_t* kd = dst + u * C::KV_BYTES;
+            uint8_t* vd = dst + C::V_OFFSET + u * C::KV_BYTES;
+            if (p.tma_rank == 3) {
+              tma_load_3d(kd, &p.kmap, 0, row0, 0, &full_bar[st], policy);
+              if (!C::KVS) tma_load_3d(vd, &p.vmap, 0, row0, 0, &full_bar[st], policy);
+            } else {
+              constexpr int SLAB_ELEMS = 128 / C::ELEM;
+#pragma unroll
+              for (int sl = 0; sl < C::TMA_SLABS; ++sl) {
+                tma_load_2d(kd + sl * C::SLAB_BYTES, &p.kmap, sl * SLAB_ELEMS, row0, &full_bar[st], policy);
+                if (!C::KVS)
+                  tma_load_2d(vd + sl * C::SLAB_BYTES, &p.vmap, sl * SLAB_ELEMS, row0, &full_bar[st], policy);
+              }
+            }
+          }
+        } else {
+          mbar_arrive(&full_bar[st]);
+        }
+        last_jb = jb;
+#pragma unroll
+        for (int u = 0; u < C::NSUB; ++u) {
+          pg[u] = pg_next[u];
+          sc[u] = sc_next[u];
+        }
+      }
+    }
+    if (!waited) grid_dependency_wait();
+    // no copy may still be landing in shared memory when the CTA exits: each
+    // lane waits for its stage's last copies
+    if (last_jb >= 0 && !mbar_wait(&full_bar[lane], (last_jb / C::NST) & 1)) err_bits |= kErrTimeout;
+    err_bits = __reduce_or_sync(kFullMask, err_bits);
+    if (lane == 0 && err_bits) atomicOr(p.err, err_bits);
+    } else {
+    const uint64_t policy = l2_evict_first_policy();
+    // page id of block `lane` of the first batch
+    int page_next = -1;
+    if (lane < nblk) page_next = (p.window == 0) ? page_spec[0] : __ldg(table + (blk_lo + lane * C::TB) / p.page_size);
     int* batch_row = reinterpret_cast<int*>(smem + C::BATCH_ROW_OFFSET);
     float2* batch_scale = reinterpret_cast<float2*>(smem + C::BATCH_SCALE_OFFSET);
     // The warp walks the blocks 32 at a time: lane k turns block j0 + k's page
@@ -425,6 +555,7 @@ __device__ __forceinline__ int stage1_cta(const Stage1Params& p, uint8_t* smem) 
       }
       if (err_bits) atomicOr(p.err, err_bits);
     }
+    }
     return (C::DED_SLOTS > 0 && p.cluster_merge == 2) ? kMergeToWait : kMergeNothing;
   }
 
@@ -469,9 +600,6 @@ __device__ __forceinline__ int stage1_cta(const Stage1Params& p, uint8_t* smem) 
   }
   const uint32_t ring = smem_u32(smem);
 
-  // stages of this piece: NSUB consecutive 16-token blocks each (the last may
-  // hold fewer)
-  const int nstg = (nblk + C::NSUB - 1) / C::NSUB;
 #pragma unroll 1
   for (int jb = warp; jb < nstg; jb += C::NW) {
     const int st = jb % C::NST;
