@@ -58,11 +58,10 @@ FALLBACK_HBM_GBS = 6800.0
 # hash of the kernel sources it was taken on; stale entries are ignored (the
 # captures and their commands are summarised under profiles/).
 NCU_TRAFFIC = {
-    "3d95dc50144f4a12": {"w2": 67295744 + 710400, "w3": 68267008 + 591360, "w4a": 1073925888 + 3737600,
-                         "w4a-fp8": 537351168 + 3902208, "w2-t2": 67450880 + 662016,
-                         "w5global-fp8": 799140352 + 5286400},
+    "cf4afb6b93f92e43": {"w4a": 1073912832 + 3335168, "w2": 67298816 + 441088, "w3": 68275200 + 333568,
+                         "w4a-fp8": 537299968 + 3247616, "w5global": 1596612864 + 4693504,
+                         "w5global-fp8": 798941952 + 5015808, "w5sliding": 68171776 + 550144},
 }
-
 
 # the same for the fused QKV norm + RoPE + cache-write kernel (--op prepare)
 PREP_NCU_TRAFFIC = {
