@@ -18,12 +18,22 @@
 
 namespace pd {
 
-#define PD_VARIANT_ROW(ID, D, G, KVS, KV8, NW, SPW, MQ, NSUB)                                              \
-  VariantInfo{ID, D, G, KVS ? 1 : 0, KV8 ? 1 : 0, NW, SPW, Stage1Cfg<D, G, KVS, KV8, NW, SPW, MQ, NSUB>::TB, \
-              Stage1Cfg<D, G, KVS, KV8, NW, SPW, MQ, NSUB>::THREADS,                                       \
-              Stage1Cfg<D, G, KVS, KV8, NW, SPW, MQ, NSUB>::SMEM_BYTES,                                    \
-              Stage1Cfg<D, G, KVS, KV8, NW, SPW, MQ, NSUB>::MAX_CLUSTER, MQ ? 1 : 0,                       \
-              Stage1Cfg<D, G, KVS, KV8, NW, SPW, MQ, NSUB>::DED_SLOTS, NSUB},
+#define PD_VARIANT_ROW(ID, D, G, KVS, KV8, NW, SPW, MQ, NSUB, TW)                                         \
+  VariantInfo{ID,                                                                                         \
+              D,                                                                                          \
+              G,                                                                                          \
+              KVS ? 1 : 0,                                                                                \
+              KV8 ? 1 : 0,                                                                                \
+              NW,                                                                                         \
+              SPW,                                                                                        \
+              Stage1Cfg<D, G, KVS, KV8, NW, SPW, MQ, NSUB, TW>::TB,                                        \
+              Stage1Cfg<D, G, KVS, KV8, NW, SPW, MQ, NSUB, TW>::THREADS,                                   \
+              Stage1Cfg<D, G, KVS, KV8, NW, SPW, MQ, NSUB, TW>::SMEM_BYTES,                                \
+              Stage1Cfg<D, G, KVS, KV8, NW, SPW, MQ, NSUB, TW>::MAX_CLUSTER,                               \
+              MQ ? 1 : 0,                                                                                 \
+              Stage1Cfg<D, G, KVS, KV8, NW, SPW, MQ, NSUB, TW>::DED_SLOTS,                                 \
+              NSUB,                                                                                       \
+              TW},
 const VariantInfo kVariants[] = {PD_FOR_EACH_VARIANT(PD_VARIANT_ROW)};
 #undef PD_VARIANT_ROW
 const int kNumVariants = sizeof(kVariants) / sizeof(kVariants[0]);
@@ -50,18 +60,27 @@ constexpr int kMaxGroup = 16;
 // up to kMaxGroup.
 bool tiled(int query_tokens, int group) { return query_tokens > 1 || group > 8; }
 
-const pd::VariantInfo* find_variant(int head_dim, int group, int kv_shared, int kv_fp8, int multi) {
+// Column-tiled plans with more than one 8-column tile use, over a bf16 cache,
+// the instances whose CTA serves two tiles from one ring (one copy of every
+// block for both); other plans those with one tile per CTA.
+const pd::VariantInfo* find_variant(int head_dim, int group, int kv_shared, int kv_fp8, int multi, int tiles) {
   if (group < 1 || group > kMaxGroup) return nullptr;
   for (int i = 0; i < pd::kNumVariants; ++i) {
     const pd::VariantInfo& v = pd::kVariants[i];
     if (v.head_dim != head_dim || v.kv_shared != kv_shared || v.kv_fp8 != kv_fp8 || v.multi != multi) continue;
+    if (v.tiles != tiles) continue;
     if (multi || v.group == group) return &v;
   }
   return nullptr;
 }
 
-// Column tiles (CTAs per KV head and piece) of a multi-token plan.
+// 8-column tiles of a column-tiled plan: its T x group (token, head) pairs, 8 at a time.
 int col_tiles(int query_tokens, int group) { return (query_tokens * group + 7) / 8; }
+
+// CTAs per (KV head, piece) of a plan on instance v.
+int col_groups(const pd::VariantInfo& v, int query_tokens, int group) {
+  return v.multi ? (col_tiles(query_tokens, group) + v.tiles - 1) / v.tiles : 1;
+}
 
 uint64_t align_up(uint64_t x, uint64_t a) { return (x + a - 1) / a * a; }
 
@@ -211,13 +230,29 @@ pd_status plan_impl(const pd_layer_desc* layer, int32_t batch, int32_t query_tok
   }
   const int group = ly.num_q_heads / ly.num_kv_heads;
   const bool multi = tiled(T, group);
-  const pd::VariantInfo* v = find_variant(ly.head_dim, group, ly.kv_shared, ly.kv_dtype == PD_KV_FP8_E4M3, multi);
+  const bool fp8 = ly.kv_dtype == PD_KV_FP8_E4M3;
+  // Two tiles per CTA read each block once for both; separate CTAs read it
+  // once each, the second read an L2 hit when the context is short. Measured
+  // (16 query / 4 KV heads, d 512): 4 tiles over 8 x 1024 tokens 22.1 us with
+  // two tiles a CTA against 25.7 us; 2 tiles over 4 x 32768 tokens 165 us
+  // against 192 us; 2 tiles over 8 x 1024 tokens 21.3 us against 20.2 us.
+  int longest_span = 0;
+  for (int b = 0; b < batch; ++b) {
+    const int L = seq_lens_host[b];
+    const int first_hi = L - T + 1;
+    const int lo = (ly.window > 0 && first_hi > ly.window) ? first_hi - ly.window : 0;
+    longest_span = std::max(longest_span, L - lo);
+  }
+  const int tiles_needed = multi ? col_tiles(T, group) : 1;
+  const int want_tiles = (multi && !fp8 && (tiles_needed >= 3 || (tiles_needed == 2 && longest_span >= 4096))) ? 2 : 1;
+  const pd::VariantInfo* v = find_variant(ly.head_dim, group, ly.kv_shared, fp8, multi, want_tiles);
+  if (!v && want_tiles > 1) v = find_variant(ly.head_dim, group, ly.kv_shared, fp8, multi, 1);
   if (!v) return PD_ERR_UNSUPPORTED;
   const int TB = v->block_tokens;
-  // CTAs per (piece, KV head): one, or the column tiles of a tiled plan
-  const int tiles = multi ? col_tiles(T, group) : 1;
-  if ((long long)ly.num_kv_heads * tiles > 65535) return PD_ERR_UNSUPPORTED;
-  const int hkv_ctas = ly.num_kv_heads * tiles;
+  // CTAs per (piece, KV head): one, or the column groups of a tiled plan
+  const int groups = col_groups(*v, T, group);
+  if ((long long)ly.num_kv_heads * groups > 65535) return PD_ERR_UNSUPPORTED;
+  const int hkv_ctas = ly.num_kv_heads * groups;
 
   // block-aligned attended span of each request (several query tokens: the
   // union of their ranges, from the first token's window start)
@@ -346,7 +381,7 @@ bool plan_is_valid(const pd_plan* plan) {
   if (v.multi) {
     if (group > kMaxGroup || plan->query_tokens < 1 || plan->query_tokens > kMaxQueryTokens) return false;
     if (!tiled(plan->query_tokens, group)) return false;
-    if (plan->grid_y != ly.num_kv_heads * col_tiles(plan->query_tokens, group)) return false;
+    if (plan->grid_y != ly.num_kv_heads * col_groups(v, plan->query_tokens, group)) return false;
   } else {
     if (group != v.group || plan->query_tokens != 1 || plan->grid_y != ly.num_kv_heads) return false;
   }

@@ -118,11 +118,13 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 
 }  // namespace
 
-// The query rows behind the 8 MMA columns of a CTA. Decode variants: column c
-// is query head g*G + c of request b. Multi-token variants: column c is pair
-// tile*8 + c of the request's T x group (token, head) pairs, token-major, i.e.
-// token j = pair / group, head g*group + pair % group, row (b*T + j)*Hq + head
-// of q and out; pairs past T x group are unused columns.
+// The query rows behind the CC columns of a CTA (CC = 8 MMA columns for each
+// of its TW tiles). Decode variants: column c is query head g*G + c of
+// request b. Column-tiled variants: column c is pair tile*8 + c of the
+// request's T x group (token, head) pairs, token-major, where tile is the
+// CTA's first 8-column tile: token j = pair / group, head g*group + pair %
+// group, row (b*T + j)*Hq + head of q and out; pairs past T x group are unused
+// columns.
 template <class C>
 struct ColMap {
   int b, g, tile, T, group, Hq;
@@ -131,7 +133,7 @@ struct ColMap {
     Hq = p.num_q_heads;
     if constexpr (C::MQ) {
       g = blockIdx.y / p.col_tiles;
-      tile = blockIdx.y % p.col_tiles;
+      tile = (blockIdx.y % p.col_tiles) * C::TW;
       T = p.query_tokens;
       group = p.group;
     } else {
@@ -142,7 +144,7 @@ struct ColMap {
     }
   }
   __device__ __forceinline__ bool valid(int c) const {
-    return C::MQ ? (c < C::G && tile * C::G + c < T * group) : c < C::G;
+    return C::MQ ? (c < C::CC && tile * C::G + c < T * group) : c < C::G;
   }
   __device__ __forceinline__ int token(int c) const { return C::MQ ? (tile * C::G + c) / group : 0; }
   __device__ __forceinline__ size_t row(int c) const {
@@ -191,7 +193,7 @@ __device__ __forceinline__ int stage1_cta(const Stage1Params& p, uint8_t* smem) 
 #pragma unroll 1
     for (int s = 0; s < C::NST; ++s) {
       mbar_init(&full_bar[s], 1);
-      mbar_init(&empty_bar[s], 1);
+      mbar_init(&empty_bar[s], C::TW);  // each team's warp for the stage releases it
     }
     fence_barrier_init();
   }
@@ -203,6 +205,10 @@ __device__ __forceinline__ int stage1_cta(const Stage1Params& p, uint8_t* smem) 
   const int b = cm.b;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // consumer warps form TW teams of WB; team t serves the CTA's columns
+  // [8t, 8t + 8) and its warps split the stage blocks
+  const int team = warp / C::WB;
+  const int cb = team * C::G;  // first CTA column of this warp's team
 
   // ---- attended range of this request and this piece -------------------------
   const int cap = p.max_pages * p.page_size;
@@ -233,7 +239,7 @@ __device__ __forceinline__ int stage1_cta(const Stage1Params& p, uint8_t* smem) 
   int hi = L, lo;
   if constexpr (C::MQ) {
     const int j_first = cm.token(0);
-    int j_last = cm.token(C::G - 1);
+    int j_last = cm.token(C::CC - 1);
     if (j_last > cm.T - 1) j_last = cm.T - 1;
     hi = L - cm.T + j_last + 1;
     if (hi < 0) hi = 0;
@@ -258,16 +264,16 @@ __device__ __forceinline__ int stage1_cta(const Stage1Params& p, uint8_t* smem) 
     // nothing attended in this piece
     if (early) grid_dependency_wait();
     if (p.cluster_merge) {
-      if (threadIdx.x < C::G) reinterpret_cast<float*>(smem + C::CTA_LSE_OFFSET)[threadIdx.x] = -INFINITY;
+      if (threadIdx.x < C::CC) reinterpret_cast<float*>(smem + C::CTA_LSE_OFFSET)[threadIdx.x] = -INFINITY;
     } else if (p.direct_out) {
-      for (int i = threadIdx.x; i < C::G * C::D; i += C::THREADS)
+      for (int i = threadIdx.x; i < C::CC * C::D; i += C::THREADS)
         if (cm.valid(i / C::D))
           reinterpret_cast<__nv_bfloat16*>(p.out)[cm.row(i / C::D) * C::D + i % C::D] = __float2bfloat16_rn(0.f);
     } else {
       // weight 0 and a zero partial row, so the merge needs no special case
-      for (int i = threadIdx.x; i < C::G * C::D; i += C::THREADS)
+      for (int i = threadIdx.x; i < C::CC * C::D; i += C::THREADS)
         if (cm.valid(i / C::D)) p.o_part[(cm.row(i / C::D) * p.num_splits + split) * C::D + i % C::D] = 0.f;
-      if (threadIdx.x < C::G && cm.valid(threadIdx.x))
+      if (threadIdx.x < C::CC && cm.valid(threadIdx.x))
         p.lse_part[cm.row(threadIdx.x) * p.num_splits + split] = -INFINITY;
     }
     return kMergeNothing;
@@ -283,15 +289,15 @@ __device__ __forceinline__ int stage1_cta(const Stage1Params& p, uint8_t* smem) 
   if (warp != C::NW) {
 #pragma unroll
     for (int ks = 0; ks < C::KSTEPS; ++ks) {
-      if (cm.valid(qh)) {
+      if (cm.valid(cb + qh)) {
         if constexpr (C::KV8) {
           // dims in the FP8 QK order (see the consumer loop); the products run
           // in f16, so q rounds to f16 once here
-          const uint2 x = __ldg(reinterpret_cast<const uint2*>(p.q + cm.row(qh) * C::D + kv8_qk_dim(ks, lane)));
+          const uint2 x = __ldg(reinterpret_cast<const uint2*>(p.q + cm.row(cb + qh) * C::D + kv8_qk_dim(ks, lane)));
           qb[ks][0] = pack_f16x2(__uint_as_float(x.x << 16), __uint_as_float(x.x & 0xffff0000u));
           qb[ks][1] = pack_f16x2(__uint_as_float(x.y << 16), __uint_as_float(x.y & 0xffff0000u));
         } else {
-          const uint16_t* qrow = p.q + cm.row(qh) * C::D + ks * 16 + qk;
+          const uint16_t* qrow = p.q + cm.row(cb + qh) * C::D + ks * 16 + qk;
           qb[ks][0] = __ldg(reinterpret_cast<const unsigned int*>(qrow));
           qb[ks][1] = __ldg(reinterpret_cast<const unsigned int*>(qrow + 8));
         }
@@ -572,7 +578,7 @@ __device__ __forceinline__ int stage1_cta(const Stage1Params& p, uint8_t* smem) 
   if constexpr (C::MQ) {
 #pragma unroll
     for (int cc = 0; cc < 2; ++cc) {
-      const int c = (lane & 3) * 2 + cc;
+      const int c = cb + (lane & 3) * 2 + cc;
       if (cm.valid(c)) {
         col_hi[cc] = L - cm.T + cm.token(c) + 1;
         col_lo[cc] = (p.window > 0 && col_hi[cc] > p.window) ? col_hi[cc] - p.window : 0;
@@ -601,7 +607,7 @@ __device__ __forceinline__ int stage1_cta(const Stage1Params& p, uint8_t* smem) 
   const uint32_t ring = smem_u32(smem);
 
 #pragma unroll 1
-  for (int jb = warp; jb < nstg; jb += C::NW) {
+  for (int jb = warp % C::WB; jb < nstg; jb += C::WB) {
     const int st = jb % C::NST;
     // every lane polls; the warp leaves together if any lane gave up
     const bool landed = mbar_wait(&full_bar[st], (jb / C::NST) & 1);
@@ -747,20 +753,23 @@ __device__ __forceinline__ int stage1_cta(const Stage1Params& p, uint8_t* smem) 
 
     // Edge stage (window start, sequence end, skipped page): the masked rows
     // carry p = 0, but 0 * NaN is NaN, and a page's unused rows may hold any
-    // bits. Zero those V rows before they enter the PV contraction.
-    // (The FP8 path zeroes them in registers, below.)
+    // bits, so their V values are zeroed in registers before the PV
+    // contraction (several teams may read one stage: shared memory is left
+    // as it landed). This lane's PV fragments of block u hold tokens
+    // 2*(lane%4) + {0, 1} (halves of words 0 and 1) and + {8, 9} (words 2, 3).
+    // (The FP8 path masks its own fragments in the PV loop.)
+    bool edge = false;
+    uint32_t vmask[C::NSUB][2];
     if constexpr (!C::KV8) {
-      if (__any_sync(kFullMask, !all_in)) {
-#pragma unroll 1
-        for (int r = 0; r < C::NSUB * C::TB; ++r) {
-          const int u = r / C::TB, rr = r % C::TB;
-          const int t = t0 + r;
-          if (((valid_bits >> u) & 1u) && t >= tlo && t < thi) continue;
-          for (int idx = lane; idx < C::SLABS * 8; idx += 32)
-            sts128_zero(vst + u * C::KV_BYTES + (idx >> 3) * C::SLAB_BYTES + rr * 128 + (idx & 7) * 16);
-        }
-        fence_proxy_async_smem();  // these writes precede the next TMA fill
-        __syncwarp();
+      edge = __any_sync(kFullMask, !all_in);
+#pragma unroll
+      for (int u = 0; u < C::NSUB; ++u) {
+        const bool ok = (valid_bits >> u) & 1u;
+        const int tv = t0 + u * C::TB + 2 * (lane & 3);
+        const bool k0 = ok && tv >= tlo && tv < thi, k1 = ok && tv + 1 >= tlo && tv + 1 < thi;
+        const bool k8 = ok && tv + 8 >= tlo && tv + 8 < thi, k9 = ok && tv + 9 >= tlo && tv + 9 < thi;
+        vmask[u][0] = (k0 ? 0x0000ffffu : 0u) | (k1 ? 0xffff0000u : 0u);
+        vmask[u][1] = (k8 ? 0x0000ffffu : 0u) | (k9 ? 0xffff0000u : 0u);
       }
     }
 
@@ -825,6 +834,20 @@ __device__ __forceinline__ int stage1_cta(const Stage1Params& p, uint8_t* smem) 
           }
         }
       }
+    } else if (edge) {
+#pragma unroll
+      for (int mt = 0; mt < C::MTILES; ++mt) {
+#pragma unroll
+        for (int u = 0; u < C::NSUB; ++u) {
+          uint32_t a[4];
+          ldmatrix_x4_trans(a, vst + u * C::KV_BYTES + (mt >> 2) * C::SLAB_BYTES + voff[mt & 3]);
+          a[0] &= vmask[u][0];
+          a[1] &= vmask[u][0];
+          a[2] &= vmask[u][1];
+          a[3] &= vmask[u][1];
+          mma_bf16(acc[mt], a, pb[u][0], pb[u][1]);
+        }
+      }
     } else {
 #pragma unroll
       for (int mt = 0; mt < C::MTILES; ++mt) {
@@ -873,28 +896,32 @@ __device__ __forceinline__ int stage1_cta(const Stage1Params& p, uint8_t* smem) 
   }
   named_bar_sync(1, C::NW * 32);
 
-  // merge coefficients, one thread per (warp, head):
+  // merge coefficients, one thread per (warp, head), over the warps of its team:
   //   c_w = 2^(m_w - M) / sum_w' 2^(m_w' - M) l_w'  (0 for a warp that saw no token)
-  // and the piece's natural-log log-sum-exp per head
+  // and the piece's natural-log log-sum-exp per CTA column
   const int tid = threadIdx.x;
-  float* coef = reinterpret_cast<float*>(smem + C::COEF_OFFSET);  // [NW][G], then lse[G]
+  float* coef = reinterpret_cast<float*>(smem + C::COEF_OFFSET);  // [NW][G], then lse[CC]
   if (tid < C::NW * C::G) {
     const int w = tid / C::G, h = tid % C::G;
+    const int w0 = (w / C::WB) * C::WB;  // the team's first warp
     float M = -INFINITY;
 #pragma unroll
-    for (int v = 0; v < C::NW; ++v) M = fmaxf(M, warp_ml[v * C::G + h].x);
+    for (int v = 0; v < C::WB; ++v) M = fmaxf(M, warp_ml[(w0 + v) * C::G + h].x);
     float Lsum = 0.f, mine = 0.f;
 #pragma unroll
-    for (int v = 0; v < C::NW; ++v) {
-      const float2 ml = warp_ml[v * C::G + h];
+    for (int v = 0; v < C::WB; ++v) {
+      const float2 ml = warp_ml[(w0 + v) * C::G + h];
       const float f = (M == -INFINITY) ? 0.f : ex2(ml.x - M);
       Lsum = fmaf(f, ml.y, Lsum);
-      if (v == w) mine = f;
+      if (w0 + v == w) mine = f;
     }
     coef[w * C::G + h] = Lsum > 0.f ? mine / Lsum : 0.f;
-    if (w == 0) coef[C::NW * C::G + h] = (Lsum > 0.f) ? (M + __log2f(Lsum)) * 0.69314718055994530942f : -INFINITY;
+    if (w == w0)
+      coef[C::NW * C::G + (w / C::WB) * C::G + h] =
+          (Lsum > 0.f) ? (M + __log2f(Lsum)) * 0.69314718055994530942f : -INFINITY;
   }
   named_bar_sync(1, C::NW * 32);
+  const float* col_lse = coef + C::NW * C::G;  // [CC]
 
   // One-barrier cluster merge: once every CTA of the cluster has started
   // (each arrived at the barrier at kernel entry), ranks 1..S-1 store their
@@ -907,22 +934,23 @@ __device__ __forceinline__ int stage1_cta(const Stage1Params& p, uint8_t* smem) 
     const uint32_t rank = cluster_ctarank();
     if (rank != 0) {
       to_rank0 = true;
-      remote_out = map_smem_rank(smem_u32(smem + C::DED_OFFSET) + (rank - 1) * (C::G * C::D * 4), 0);
-      remote_lse = map_smem_rank(smem_u32(smem + C::DED_LSE_OFFSET) + (rank - 1) * (C::G * 4), 0);
+      remote_out = map_smem_rank(smem_u32(smem + C::DED_OFFSET) + (rank - 1) * (C::CC * C::D * 4), 0);
+      remote_lse = map_smem_rank(smem_u32(smem + C::DED_LSE_OFFSET) + (rank - 1) * (C::CC * 4), 0);
     }
   }
 
   constexpr int D4 = C::D / 4;
 #pragma unroll 2
-  for (int e = tid; e < C::G * D4; e += C::NW * 32) {
-    const int h = e / D4;
+  for (int e = tid; e < C::CC * D4; e += C::NW * 32) {
+    const int h = e / D4;  // CTA column
     const int d4 = e % D4;
     if (C::MQ && !cm.valid(h)) continue;
+    const int w0 = (h / C::G) * C::WB, hc = h % C::G;  // its team's first warp, its MMA column
     float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int w = 0; w < C::NW; ++w) {
-      const float c = coef[w * C::G + h];
-      const float4 a = *reinterpret_cast<const float4*>(comb + (w * C::G + h) * CS + d4 * 4);
+    for (int v = 0; v < C::WB; ++v) {
+      const float c = coef[(w0 + v) * C::G + hc];
+      const float4 a = *reinterpret_cast<const float4*>(comb + ((w0 + v) * C::G + hc) * CS + d4 * 4);
       o.x = fmaf(c, a.x, o.x);
       o.y = fmaf(c, a.y, o.y);
       o.z = fmaf(c, a.z, o.z);
@@ -937,15 +965,15 @@ __device__ __forceinline__ int stage1_cta(const Stage1Params& p, uint8_t* smem) 
       *reinterpret_cast<uint2*>(dst) = packed;
     } else if (to_rank0) {
       st_dsmem_f32x4(remote_out + (h * D4 + d4) * 16, o);
-      if (d4 == 0) st_dsmem_f32(remote_lse + h * 4, coef[C::NW * C::G + h]);
+      if (d4 == 0) st_dsmem_f32(remote_lse + h * 4, col_lse[h]);
     } else if (p.cluster_merge) {
       // kept in shared memory for rank 0 of the cluster (or to push from)
       reinterpret_cast<float4*>(smem + C::CTA_OUT_OFFSET)[h * D4 + d4] = o;
-      if (d4 == 0) reinterpret_cast<float*>(smem + C::CTA_LSE_OFFSET)[h] = coef[C::NW * C::G + h];
+      if (d4 == 0) reinterpret_cast<float*>(smem + C::CTA_LSE_OFFSET)[h] = col_lse[h];
     } else {
       const size_t prow = cm.row(h) * p.num_splits + split;
       reinterpret_cast<float4*>(p.o_part + prow * C::D)[d4] = o;
-      if (d4 == 0) p.lse_part[prow] = coef[C::NW * C::G + h];
+      if (d4 == 0) p.lse_part[prow] = col_lse[h];
     }
   }
   return fused ? kMergePushed : kMergeNothing;
@@ -983,11 +1011,11 @@ __device__ __forceinline__ void cluster_merge(const Stage1Params& p, uint8_t* sm
     cluster_sync_all();  // every CTA of the cluster is done with its ring
   }
   if (rank != 0 && state == kMergeNothing) {
-    const uint32_t slot = smem_u32(smem + push_off) + (rank - 1) * (C::G * C::D * 4);
-    const uint32_t lse_slot = smem_u32(smem + push_lse_off) + (rank - 1) * (C::G * 4);
-    if (tid < C::G) st_dsmem_f32(map_smem_rank(lse_slot + tid * 4, 0), my_lse[tid]);
+    const uint32_t slot = smem_u32(smem + push_off) + (rank - 1) * (C::CC * C::D * 4);
+    const uint32_t lse_slot = smem_u32(smem + push_lse_off) + (rank - 1) * (C::CC * 4);
+    if (tid < C::CC) st_dsmem_f32(map_smem_rank(lse_slot + tid * 4, 0), my_lse[tid]);
     const uint32_t remote = map_smem_rank(slot, 0);
-    for (int e = tid; e < C::G * D4; e += C::THREADS) {
+    for (int e = tid; e < C::CC * D4; e += C::THREADS) {
       if (my_lse[e / D4] == -INFINITY) continue;  // nothing attended: only the lse is pushed
       st_dsmem_f32x4(remote + e * 16, my_out[e]);
     }
@@ -996,16 +1024,16 @@ __device__ __forceinline__ void cluster_merge(const Stage1Params& p, uint8_t* sm
   if (rank != 0) return;
   const float* push_lse = reinterpret_cast<const float*>(smem + push_lse_off);
   const float4* push_out = reinterpret_cast<const float4*>(smem + push_off);
-  float* wts = reinterpret_cast<float*>(smem + C::CTA_W_OFFSET);  // [S][G]
+  float* wts = reinterpret_cast<float*>(smem + C::CTA_W_OFFSET);  // [S][CC]
   // one thread per (piece, head): w = exp(lse - M) / sum_r exp(lse_r - M),
   // every thread of a head reading that head's S log-sum-exps
-  if (tid < S * C::G) {
-    const int r = tid / C::G, h = tid % C::G;
+  if (tid < S * C::CC) {
+    const int r = tid / C::CC, h = tid % C::CC;
     float l[C::MAX_CLUSTER];
     float M = -INFINITY;
 #pragma unroll
     for (int q = 0; q < C::MAX_CLUSTER; ++q) {
-      l[q] = q >= S ? -INFINITY : (q == 0 ? my_lse[h] : push_lse[(q - 1) * C::G + h]);
+      l[q] = q >= S ? -INFINITY : (q == 0 ? my_lse[h] : push_lse[(q - 1) * C::CC + h]);
       M = fmaxf(M, l[q]);
     }
     float sum = 0.f, mine = 0.f;
@@ -1016,21 +1044,21 @@ __device__ __forceinline__ void cluster_merge(const Stage1Params& p, uint8_t* sm
       sum += e;
       if (q == r) mine = e;
     }
-    wts[r * C::G + h] = sum > 0.f ? mine / sum : 0.f;
+    wts[r * C::CC + h] = sum > 0.f ? mine / sum : 0.f;
   }
   __syncthreads();
   const ColMap<C> cm(p);
 #pragma unroll 2
-  for (int e = tid; e < C::G * D4; e += C::THREADS) {
+  for (int e = tid; e < C::CC * D4; e += C::THREADS) {
     const int h = e / D4;
     if (C::MQ && !cm.valid(h)) continue;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int r = 0; r < C::MAX_CLUSTER; ++r) {
       if (r >= S) break;
-      const float w = wts[r * C::G + h];
+      const float w = wts[r * C::CC + h];
       if (w == 0.f) continue;  // an empty piece pushed no result
-      const float4 v = r == 0 ? my_out[e] : push_out[(r - 1) * C::G * D4 + e];
+      const float4 v = r == 0 ? my_out[e] : push_out[(r - 1) * C::CC * D4 + e];
       acc.x = fmaf(w, v.x, acc.x);
       acc.y = fmaf(w, v.y, acc.y);
       acc.z = fmaf(w, v.z, acc.z);
@@ -1055,17 +1083,17 @@ __global__ void __launch_bounds__(C::THREADS, 1) stage1_kernel(const __grid_cons
 
 // ---- instantiation and dispatch -------------------------------------------------
 
-#define PD_STAGE1_INSTANCE(ID, D, G, KVS, KV8, NW, SPW, MQ, NSUB)                       \
-  template __global__ void stage1_kernel<Stage1Cfg<D, G, KVS, KV8, NW, SPW, MQ, NSUB>>( \
+#define PD_STAGE1_INSTANCE(ID, D, G, KVS, KV8, NW, SPW, MQ, NSUB, TW)                       \
+  template __global__ void stage1_kernel<Stage1Cfg<D, G, KVS, KV8, NW, SPW, MQ, NSUB, TW>>( \
       const __grid_constant__ Stage1Params);
 PD_FOR_EACH_VARIANT(PD_STAGE1_INSTANCE)
 #undef PD_STAGE1_INSTANCE
 
 const void* stage1_kernel_ptr(int variant) {
   switch (variant) {
-#define PD_STAGE1_CASE(ID, D, G, KVS, KV8, NW, SPW, MQ, NSUB) \
-  case ID:                                                    \
-    return reinterpret_cast<const void*>(&stage1_kernel<Stage1Cfg<D, G, KVS, KV8, NW, SPW, MQ, NSUB>>);
+#define PD_STAGE1_CASE(ID, D, G, KVS, KV8, NW, SPW, MQ, NSUB, TW) \
+  case ID:                                                        \
+    return reinterpret_cast<const void*>(&stage1_kernel<Stage1Cfg<D, G, KVS, KV8, NW, SPW, MQ, NSUB, TW>>);
     PD_FOR_EACH_VARIANT(PD_STAGE1_CASE)
 #undef PD_STAGE1_CASE
     default:

@@ -204,13 +204,18 @@ def test_groups_above_8_are_served_by_column_tiles(lib, G, d, window, kvs):
     lens = [5000, 100, 0, 30000]
     pl = _plan(lens, Hq=4 * G, Hkv=4, d=d, window=window, kv_shared=kvs, pages=10 ** 5)
     tiles = (G + 7) // 8
-    assert pl.query_tokens == 1 and (pl.grid_y, pl.grid_z) == (4 * tiles, len(lens))
+    # bf16 over a long context (a span of 4096 tokens or more): one CTA per KV
+    # head serves both 8-column tiles (one copy of each block); a short one
+    # (the 1024-token window) keeps a CTA per tile
+    per_cta = 2 if window == 0 else 1
+    assert pl.query_tokens == 1 and (pl.grid_y, pl.grid_z) == (4 * tiles // per_cta, len(lens))
     assert b.load_library().paged_decode_abi_version() == 5
-    # the same group over several query tokens: T x G pairs, 8 per CTA
+    # the same group over several query tokens: T x G pairs, 16 per CTA
     desc = b.layer_desc(4 * G, 4, d, 16, 10 ** 5, 2000, window, kvs)
     pm = b.paged_decode_plan_multi(desc, 3, [3000, 40], 152)
-    assert pm.grid_y == 4 * ((3 * G + 7) // 8)
-    # and its FP8 form
+    t3 = (3 * G + 7) // 8
+    assert pm.grid_y == 4 * ((t3 + 1) // 2 if t3 >= 3 else t3)
+    # and its FP8 form: 8 columns per CTA
     f8 = b.paged_decode_plan(b.layer_desc(4 * G, 4, d, 16, 10 ** 5, 2000, window, kvs, b.PD_KV_FP8_E4M3),
                              [3000, 40], 152)
     assert f8.grid_y == 4 * tiles
@@ -306,8 +311,11 @@ def test_planner_invariants_on_random_shapes(lib):
             lo = first_hi - window if window and first_hi > window else 0
             assert S * chunk >= L - (lo // TB) * TB  # every attended token is in some piece
         tiles = (T * G + 7) // 8 if T > 1 or G > 8 else 1
-        assert (pl.grid_x, pl.grid_y, pl.grid_z) == (S, Hkv * tiles, B)
-        assert pl.threads_per_cta in (128, 256) and 0 < pl.smem_bytes <= 227 * 1024
+        spans = [L - ((L - T + 1 - window) if window and L - T + 1 > window else 0) for L in lens]
+        # bf16 CTAs serve two 8-column tiles for 3+ tiles, or 2 over a span of 4096+ tokens
+        per_cta = 2 if not fp8 and (tiles >= 3 or (tiles == 2 and max(spans) >= 4096)) else 1
+        assert (pl.grid_x, pl.grid_y, pl.grid_z) == (S, Hkv * ((tiles + per_cta - 1) // per_cta), B)
+        assert pl.threads_per_cta in (128, 224, 256) and 0 < pl.smem_bytes <= 227 * 1024
         assert pl.query_tokens == T and pl.partial == int(partial) and pl.early_kv == 0
         rows = B * T * Hkv * G
         if pl.merge_mode == 1:

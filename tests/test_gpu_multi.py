@@ -85,6 +85,10 @@ CASES = [
     (512, 16, 2, False, 0, 3, [3, 100, 2000]),             # G = 8: one token per tile
     (256, 12, 4, False, 5, 6, [6, 40, 97]),                # G = 3: pairs straddle tiles
     (512, 8, 4, False, 16, 5, [5, 16, 17, 48]),            # window shorter than T's span
+    (512, 16, 4, False, 0, 8, [8, 100, 1024, 3000]),       # four tiles: two CTAs of two
+    (256, 16, 8, True, 1024, 6, [4100, 6, 1500]),          # two tiles, K=V, window
+    (512, 12, 4, False, 37, 7, [7, 300, 2000]),            # three tiles: the last CTA's second tile unused
+    (256, 64, 4, False, 0, 2, [2, 900, 33]),               # G = 16, two query tokens: four tiles
 ]
 
 
@@ -98,26 +102,32 @@ def test_multi_matches_oracle(case):
     compare(out, run_oracle(li, q), f"S={plan.num_splits} mode={plan.merge_mode}")
 
 
-MODE_CASES = [([64, 64], 4), ([1024] * 8, 152), ([60000], 152)]
+# (lengths, SM count, query tokens): each merge mode, for one-tile CTAs (T = 2:
+# 8 columns) and two-tile CTAs (T = 4, 8: 16 and 32 columns)
+MODE_CASES = [([64, 64], 4, 8), ([1024] * 8, 152, 8), ([60000], 152, 4), ([64, 64], 4, 2), ([1024] * 8, 152, 2),
+              ([60000], 152, 2)]
+MODE_IDS = ["one-piece-2tiles", "cluster-merge-2tiles", "merge-kernel-2tiles", "one-piece", "cluster-merge",
+            "merge-kernel"]
 
 
-@pytest.mark.parametrize("lens,sms", MODE_CASES,
-                         ids=["one-piece", "cluster-merge", "merge-kernel"])
-def test_multi_merge_modes(lens, sms):
+def _mode_plan(lens, sms, T):
+    desc = b.layer_desc(16, 4, 512, 16, sum((L + 15) // 16 for L in lens) + 3, max((L + 15) // 16 for L in lens))
+    return b.paged_decode_plan_multi(desc, T, lens, sms)
+
+
+@pytest.mark.parametrize("lens,sms,T", MODE_CASES, ids=MODE_IDS)
+def test_multi_merge_modes(lens, sms, T):
     """Lengths and SM counts that lead the planner to each of its merge modes."""
-    T = 4
-    li, q = _layer(lens, T, 16, 4, 512, seed=len(lens) + sms, q_std=0.5)
+    li, q = _layer(lens, T, 16, 4, 512, seed=len(lens) + sms + T, q_std=0.5)
     out, plan, flags = run_gpu(li, q, T, sms=sms)
     assert flags == 0
     compare(out, run_oracle(li, q), f"S={plan.num_splits} mode={plan.merge_mode}")
 
 
 def test_merge_modes_are_all_reached():
-    modes = set()
-    for lens, sms in MODE_CASES:
-        desc = b.layer_desc(16, 4, 512, 16, sum((L + 15) // 16 for L in lens) + 3, max((L + 15) // 16 for L in lens))
-        modes.add(int(b.paged_decode_plan_multi(desc, 4, lens, sms).merge_mode))
-    assert modes == {0, 1, 2}
+    for tiles in ((4, 8), (2,)):
+        modes = {int(_mode_plan(lens, sms, T).merge_mode) for lens, sms, T in MODE_CASES if T in tiles}
+        assert modes == {0, 1, 2}, (tiles, modes)
 
 
 def test_first_token_of_a_fresh_sequence_returns_its_value_row():

@@ -109,11 +109,13 @@ def test_variants_ragged(d, G, kvs, window):
 
 @pytest.mark.parametrize("d,G,kvs", [(512, 16, False), (512, 12, True), (256, 16, True), (256, 9, False)])
 @pytest.mark.parametrize("window", [0, 37, 1000])
-def test_groups_above_8_ragged(d, G, kvs, window):
-    """Groups of 9..16 query heads per KV head (served by CTAs of 8 query heads):
+@pytest.mark.parametrize("long", [False, True])
+def test_groups_above_8_ragged(d, G, kvs, window, long):
+    """Groups of 9..16 query heads per KV head (two 8-column tiles: a CTA per
+    tile over short contexts, one CTA for both over a span of 4096+ tokens):
     ragged lengths, windows, one piece / cluster merge / merge kernel."""
     Hkv = 2
-    lens = [1, 17, 300, 0, 1000, 33]
+    lens = [1, 17, 300, 0, 1000, 33] + ([5000] if long else [])
     li = synth.make_layer("g", lens, Hkv * G, Hkv, d, window=window, kv_shared=kvs,
                           pool_pages=sum((L + 15) // 16 for L in lens) + 5, seed=7 * d + G + 100 * kvs + window,
                           device="cuda")
@@ -121,7 +123,8 @@ def test_groups_above_8_ragged(d, G, kvs, window):
     modes = set()
     for sms in (1, 3, 40, 152):
         out, step = run_gpu(li, sm_count=sms)
-        assert step.plan.grid_y == Hkv * ((G + 7) // 8)
+        span = max(min(L, window) if window else L for L in lens)
+        assert step.plan.grid_y == (Hkv if span >= 4096 else 2 * Hkv)
         modes.add(int(step.plan.merge_mode))
         compare(out, ref, li, f"d{d} G{G} kvs{kvs} W{window} sms{sms} S{step.plan.num_splits}")
     if window == 0:  # short windows always fit one piece
