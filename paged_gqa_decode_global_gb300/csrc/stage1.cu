@@ -759,19 +759,7 @@ __device__ __forceinline__ int stage1_cta(const Stage1Params& p, uint8_t* smem) 
     // 2*(lane%4) + {0, 1} (halves of words 0 and 1) and + {8, 9} (words 2, 3).
     // (The FP8 path masks its own fragments in the PV loop.)
     bool edge = false;
-    uint32_t vmask[C::NSUB][2];
-    if constexpr (!C::KV8) {
-      edge = __any_sync(kFullMask, !all_in);
-#pragma unroll
-      for (int u = 0; u < C::NSUB; ++u) {
-        const bool ok = (valid_bits >> u) & 1u;
-        const int tv = t0 + u * C::TB + 2 * (lane & 3);
-        const bool k0 = ok && tv >= tlo && tv < thi, k1 = ok && tv + 1 >= tlo && tv + 1 < thi;
-        const bool k8 = ok && tv + 8 >= tlo && tv + 8 < thi, k9 = ok && tv + 9 >= tlo && tv + 9 < thi;
-        vmask[u][0] = (k0 ? 0x0000ffffu : 0u) | (k1 ? 0xffff0000u : 0u);
-        vmask[u][1] = (k8 ? 0x0000ffffu : 0u) | (k9 ? 0xffff0000u : 0u);
-      }
-    }
+    if constexpr (!C::KV8) edge = __any_sync(kFullMask, !all_in);
 
     // P^T as the B operand of each block: transpose the (token x head) 16-bit
     // fragments; on the FP8 path the block's V scale rides on P
@@ -835,6 +823,16 @@ __device__ __forceinline__ int stage1_cta(const Stage1Params& p, uint8_t* smem) 
         }
       }
     } else if (edge) {
+      uint32_t vmask[C::NSUB][2];
+#pragma unroll
+      for (int u = 0; u < C::NSUB; ++u) {
+        const bool ok = (valid_bits >> u) & 1u;
+        const int tv = t0 + u * C::TB + 2 * (lane & 3);
+        const bool k0 = ok && tv >= tlo && tv < thi, k1 = ok && tv + 1 >= tlo && tv + 1 < thi;
+        const bool k8 = ok && tv + 8 >= tlo && tv + 8 < thi, k9 = ok && tv + 9 >= tlo && tv + 9 < thi;
+        vmask[u][0] = (k0 ? 0x0000ffffu : 0u) | (k1 ? 0xffff0000u : 0u);
+        vmask[u][1] = (k8 ? 0x0000ffffu : 0u) | (k9 ? 0xffff0000u : 0u);
+      }
 #pragma unroll
       for (int mt = 0; mt < C::MTILES; ++mt) {
 #pragma unroll
