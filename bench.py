@@ -440,7 +440,13 @@ def run_ours(args, world, rank, local):
     # decode loop runs), and, for reference, as eager calls.
     e2e = None
     if not args.no_e2e:
-        # the step's inputs travel in one pinned staging buffer (one copy each way)
+        # Every step copies its inputs (q -- or the new token's raw rows --,
+        # block table, seq_lens) from one pinned host staging buffer and its
+        # result back to pinned host memory. The decode loop a caller writes
+        # pipelines this: two device copies of the staging buffer and of out,
+        # the input copy of step i + 1 and the result copy of step i on copy
+        # streams of their own while step i's kernels run, each step's kernels
+        # waiting for its inputs and each result buffer for its copy-out.
         if layer_op:  # the new token's raw q / k / v rows instead of q
             parts = [pi.q_in, pi.k_in] + ([] if pi.v_in is None else [pi.v_in]) + [li.block_tables, li.seq_lens]
         else:
@@ -450,67 +456,115 @@ def run_ours(args, world, rank, local):
             offs.append(total)
             total += (t.numel() * t.element_size() + 255) // 256 * 256
         stage_h = torch.zeros(total, dtype=torch.uint8, pin_memory=True)
-        stage_d = torch.empty(total, dtype=torch.uint8, device=dev)
-        views_h, views_d = [], []
         for t, o in zip(parts, offs):
             n = t.numel() * t.element_size()
-            views_h.append(stage_h[o:o + n].view(t.dtype).view(t.shape))
-            views_d.append(stage_d[o:o + n].view(t.dtype).view(t.shape))
-            views_h[-1].copy_(t.cpu())
-        bt_d, sl_d = views_d[-2:]
-        q_d = torch.empty_like(q_rows) if layer_op else views_d[0]
-        out_h = torch.empty(q_rows.shape, dtype=q_rows.dtype, pin_memory=True)
-        out_d = torch.empty_like(q_rows)
+            stage_h[o:o + n].view(t.dtype).view(t.shape).copy_(t.cpu())
+        bufs = []
+        for _ in range(2):
+            sd = torch.empty(total, dtype=torch.uint8, device=dev)
+            vd = [sd[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape) for t, o in zip(parts, offs)]
+            bufs.append({"stage": sd, "views": vd, "q": torch.empty_like(q_rows) if layer_op else vd[0],
+                         "out": torch.empty_like(q_rows),
+                         "out_h": torch.empty(q_rows.shape, dtype=q_rows.dtype, pin_memory=True),
+                         "in_done": torch.cuda.Event(), "comp_done": torch.cuda.Event(),
+                         "out_done": torch.cuda.Event()})
+        h2d = torch.cuda.Stream(device=dev)
+        d2h = torch.cuda.Stream(device=dev)
 
-        def e2e_step(i):
+        def compute(i, bf):
             k, v = pools[i % replicas]
-            stage_d.copy_(stage_h, non_blocking=True)
+            vd = bf["views"]
             if layer_op:
-                prep(k, v, q_in=views_d[0], k_in=views_d[1], v_in=None if pi.v_in is None else views_d[2],
-                     bt=bt_d, sl=sl_d, q_out=q_d)
-            step(q_d, k, v, bt_d, sl_d, li.scale, out_d, stream, k_scale=k_sc, v_scale=v_sc)
-            out_h.copy_(out_d, non_blocking=True)
+                prep(k, v, q_in=vd[0], k_in=vd[1], v_in=None if pi.v_in is None else vd[2],
+                     bt=vd[-2], sl=vd[-1], q_out=bf["q"])
+            step(bf["q"], k, v, vd[-2], vd[-1], li.scale, bf["out"], stream, k_scale=k_sc, v_scale=v_sc)
 
-        with torch.cuda.stream(stream):
-            for i in range(3):
-                e2e_step(i)
-        torch.cuda.synchronize()
-        graphs = []
-        left, i0 = K, 0
-        while left > 0:
-            m = min(500, left)
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                for i in range(m):
-                    e2e_step(i0 + i)
-            graphs.append(g)
-            left -= m
-            i0 += m
+        def serial_steps(i0, m):
+            bf = bufs[0]
+            for i in range(i0, i0 + m):
+                bf["stage"].copy_(stage_h, non_blocking=True)
+                compute(i, bf)
+                bf["out_h"].copy_(bf["out"], non_blocking=True)
+
+        def pipelined_steps(i0, m):
+            # (issued with `stream` current; the copy streams fork from it and join it at the end)
+            fork = torch.cuda.Event()
+            fork.record(stream)
+            h2d.wait_event(fork)
+            d2h.wait_event(fork)
+            with torch.cuda.stream(h2d):
+                bufs[i0 % 2]["stage"].copy_(stage_h, non_blocking=True)
+                bufs[i0 % 2]["in_done"].record(h2d)
+            for i in range(i0, i0 + m):
+                bf, nb = bufs[i % 2], bufs[(i + 1) % 2]
+                if i + 1 < i0 + m:
+                    if i > i0:
+                        h2d.wait_event(nb["comp_done"])  # step i - 1's kernels have read that buffer
+                    with torch.cuda.stream(h2d):
+                        nb["stage"].copy_(stage_h, non_blocking=True)
+                        nb["in_done"].record(h2d)
+                stream.wait_event(bf["in_done"])
+                if i >= i0 + 2:
+                    stream.wait_event(bf["out_done"])  # step i - 2's result has left this buffer
+                compute(i, bf)
+                bf["comp_done"].record(stream)
+                d2h.wait_event(bf["comp_done"])
+                with torch.cuda.stream(d2h):
+                    bf["out_h"].copy_(bf["out"], non_blocking=True)
+                    bf["out_done"].record(d2h)
+            stream.wait_event(bufs[(i0 + m - 1) % 2]["out_done"])
+            if m > 1:
+                stream.wait_event(bufs[(i0 + m - 2) % 2]["out_done"])
+            stream.wait_event(bufs[(i0 + m - 1) % 2]["in_done"])
+
+        def e2e_graphs(fn):
+            with torch.cuda.stream(stream):
+                fn(0, 3)
+            torch.cuda.synchronize()
+            graphs = []
+            left, i0 = K, 0
+            while left > 0:
+                m = min(500, left)
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    fn(i0, m)
+                graphs.append(g)
+                left -= m
+                i0 += m
+            return graphs
+
+        graphs = e2e_graphs(pipelined_steps)
         e2e_ms, _ = timed(graphs)
         e2e_ms = max_over_ranks(e2e_ms, world)
         del graphs
-        # the same step as eager C-ABI calls (host launch overhead included)
+        last = bufs[(K - 1) % 2]
+        assert torch.equal(last["out_h"], last["out"].cpu())
+        graphs = e2e_graphs(serial_steps)
+        serial_ms, _ = timed(graphs)
+        serial_ms = max_over_ranks(serial_ms, world)
+        del graphs
+        # the pipelined steps as eager C-ABI calls (host launch overhead included)
         n_eager = min(K, 2000)
         with torch.cuda.stream(stream):
             a = torch.cuda.Event(enable_timing=True)
             z = torch.cuda.Event(enable_timing=True)
             barrier(world)
             a.record(stream)
-            for i in range(n_eager):
-                e2e_step(i)
+            pipelined_steps(0, n_eager)
             z.record(stream)
         torch.cuda.synchronize()
         barrier(world)
         eager_ms = max_over_ranks(a.elapsed_time(z), world)
-        assert torch.equal(out_h, out_d.cpu())
         e2e = {"value": round(e2e_ms * 1e3 / K, 3), "unit": UNIT,
                "h2d_bytes_per_step": int(stage_h.numel()),
-               "d2h_bytes_per_step": out_h.numel() * 2, "steps": K,
-               "launch": "CUDA graph replay of: one H2D copy of " +
+               "d2h_bytes_per_step": bufs[0]["out_h"].numel() * 2, "steps": K,
+               "launch": "CUDA graph replay of, per step: one H2D copy of " +
                          ("the new token's q/k/v rows" if layer_op else "q") +
                          " + block table + seq_lens from a pinned staging buffer, the C-ABI " +
                          ("new-token step and " if layer_op else "") +
-                         "decode calls, one D2H copy of out to pinned host memory",
+                         "decode calls, one D2H copy of out to pinned host memory; copies on two copy streams "
+                         "overlap the neighbouring steps' kernels (two device buffers each way)",
+               "serial_value": round(serial_ms * 1e3 / K, 3),
                "eager_value": round(eager_ms * 1e3 / n_eager, 3), "eager_steps": n_eager}
         step.check(stream)
 

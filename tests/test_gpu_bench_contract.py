@@ -36,7 +36,9 @@ def test_default_line_keeps_the_contract():
     c = d["cpu_baseline"]
     assert c["kind"] == "oracle" and c["cores"] >= 1 and c["value"] > 0 and c["sample"]
     e = d["e2e"]
-    assert e["value"] >= d["value"] and e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
+    # the copies overlap the neighbouring steps' kernels: e2e is at least about the kernels' time
+    assert e["value"] >= 0.97 * d["value"] and e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
+    assert e["serial_value"] >= 0.97 * e["value"]
     assert d["gpu_launches"] >= d["steps"]
     assert d["clocks"]["sm_mhz"] > 0 and isinstance(d["clocks"]["reasons"], list)
 
