@@ -112,7 +112,10 @@ typedef struct {
 /* Launch plan: a plain value filled by paged_decode_plan, copyable, reusable for
  * any call with the same layer, batch and no longer sequences than it was made
  * for. Callers read workspace_bytes and num_splits; the other fields are the
- * library's. */
+ * library's. Every launch call checks the fields against one another first (the
+ * grid against the pieces and batch, the workspace offsets and size against
+ * what the launches write) and returns PD_ERR_INVALID_ARG for a plan that no
+ * longer agrees with itself, before any CUDA call. */
 typedef struct {
   pd_layer_desc layer;
   int32_t batch;

@@ -387,8 +387,10 @@ bool plan_is_valid(const pd_plan* plan) {
   }
   if (ly.head_dim != v.head_dim || ly.kv_shared != v.kv_shared) return false;
   if ((ly.kv_dtype == PD_KV_FP8_E4M3) != (v.kv_fp8 == 1)) return false;
-  if (plan->num_splits < 1 || plan->chunk_tokens < 16 || plan->chunk_tokens % 16 != 0) return false;
-  if (plan->batch < 0 || plan->grid_x != plan->num_splits) return false;
+  if (plan->num_splits < 1 || plan->num_splits > kMaxSplits || plan->chunk_tokens < 16 || plan->chunk_tokens % 16 != 0)
+    return false;
+  if (plan->batch < 0 || plan->grid_x != plan->num_splits || plan->grid_z != plan->batch) return false;
+  if (plan->block_tokens != v.block_tokens) return false;
   if (plan->threads_per_cta != v.threads || plan->smem_bytes != v.smem_bytes) return false;
   if (plan->merge_mode < 0 || plan->merge_mode > 2) return false;
   if (plan->test_stall_bytes < 0 || plan->test_stall_bytes > (1 << 16) || plan->test_stall_bytes % 16 != 0)
@@ -399,6 +401,23 @@ bool plan_is_valid(const pd_plan* plan) {
                     : ((plan->num_splits == 1) != (plan->merge_mode == 0)))
     return false;
   if (plan->merge_mode == 2 && plan->num_splits > std::min(kMaxClusterSplits, v.max_cluster)) return false;
+  // The workspace the plan asks for must hold what its launches write: the
+  // error word, and in merge mode 1 the [rows][S] log-sum-exps and the
+  // [rows][S][d] fp32 partials at their offsets (a plan edited by hand to more
+  // pieces is refused here instead of writing past the caller's buffer).
+  if (plan->workspace_bytes < pd::kWorkspaceHeader) return false;
+  if (plan->merge_mode == 1) {
+    if (plan->lse_offset < pd::kWorkspaceHeader || plan->lse_offset % 256 != 0 || plan->opart_offset % 256 != 0)
+      return false;
+    uint64_t lse_bytes = 0, opart_bytes = 0, lse_end = 0, opart_end = 0;
+    const uint64_t rows = (uint64_t)plan->batch * (uint64_t)plan->query_tokens * (uint64_t)ly.num_q_heads;
+    if (__builtin_mul_overflow(rows, (uint64_t)plan->num_splits * 4ull, &lse_bytes) ||
+        __builtin_mul_overflow(lse_bytes, (uint64_t)ly.head_dim, &opart_bytes) ||
+        __builtin_add_overflow(plan->lse_offset, lse_bytes, &lse_end) ||
+        __builtin_add_overflow(plan->opart_offset, opart_bytes, &opart_end))
+      return false;
+    if (plan->opart_offset < lse_end || plan->workspace_bytes < opart_end) return false;
+  }
   return true;
 }
 

@@ -275,6 +275,47 @@ def test_early_kv_is_a_flag_the_caller_sets(lib):
     assert lib.paged_decode_merge(ctypes.byref(pl), fake, 1 << 20, fake, None) == b.PD_ERR_INVALID_ARG
 
 
+def test_plans_edited_past_their_workspace_are_refused(lib):
+    """A plan whose pieces, grid or workspace offsets were changed after
+    planning, so that its launches would write past the workspace it asks for,
+    is refused before any launch (here: no CUDA call, so INVALID_ARG rather
+    than PD_ERR_CUDA)."""
+    import copy
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a device is present")
+    fake = 1 << 20
+    pl = b.paged_decode_plan(b.layer_desc(16, 4, 512, 16, 8192, 4096), [65536, 65536], 152)
+    assert pl.merge_mode == 1 and pl.num_splits > 1
+
+    def launch(p, ws_bytes=None):
+        wb = p.workspace_bytes if ws_bytes is None else ws_bytes
+        return lib.paged_decode_global(ctypes.byref(p), fake, fake, fake + 4096, fake, fake, 0.05, fake, wb, fake,
+                                       None)
+
+    assert launch(pl) == b.PD_ERR_CUDA  # valid: reaches CUDA, absent here
+    edits = [
+        lambda p: (setattr(p, "num_splits", p.num_splits * 2), setattr(p, "grid_x", p.num_splits)),
+        lambda p: setattr(p, "opart_offset", p.lse_offset),
+        lambda p: setattr(p, "workspace_bytes", p.workspace_bytes - 4),
+        lambda p: setattr(p, "lse_offset", 0),
+        lambda p: setattr(p, "opart_offset", p.opart_offset + 4),
+        lambda p: setattr(p, "grid_z", p.batch + 1),
+        lambda p: setattr(p, "block_tokens", 32),
+        lambda p: (setattr(p, "num_splits", 2000), setattr(p, "grid_x", 2000)),
+    ]
+    for i, edit in enumerate(edits):
+        bad = copy.copy(pl)
+        edit(bad)
+        assert launch(bad, ws_bytes=1 << 40) == b.PD_ERR_INVALID_ARG, i
+        assert lib.paged_decode_merge(ctypes.byref(bad), fake, 1 << 40, fake, None) == b.PD_ERR_INVALID_ARG, i
+    # one-piece and cluster plans still need the error word
+    one = b.paged_decode_plan(b.layer_desc(16, 4, 512, 16, 64, 8), [100], 152)
+    assert one.merge_mode in (0, 2)
+    one.workspace_bytes = 4
+    assert launch(one, ws_bytes=1 << 20) == b.PD_ERR_INVALID_ARG
+
+
 def test_planner_invariants_on_random_shapes(lib):
     """300 seeded random layer shapes and batches, decode / multi-token / partial
     plans, bf16 and FP8: every plan covers every attended token, its grid and
