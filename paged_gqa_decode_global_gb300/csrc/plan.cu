@@ -84,76 +84,153 @@ int col_groups(const pd::VariantInfo& v, int query_tokens, int group) {
 
 uint64_t align_up(uint64_t x, uint64_t a) { return (x + a - 1) / a * a; }
 
-// Cost model of one launch, in microseconds: every CTA takes a fixed start-up
-// cost plus its tokens' bytes at one SM's share of HBM bandwidth; CTAs are
-// handed to `slots` resident positions in launch order (split index fastest),
-// each to the position that frees first. Pieces past a request's range exit
-// almost at once. A split count above one adds the merge launch and its traffic.
+// Cost model of one stage-1 launch, in microseconds. Units (a CTA, or a
+// thread-block cluster of S CTAs) go to `slots` resident positions in launch
+// order (split index fastest), each to the position that frees first. A CTA
+// spends cta_fixed_us before its first bytes arrive (empty_cta_us if its range
+// is empty), then streams its tokens. The n CTAs streaming at a moment share
+//   agg(n) = ((n * cap)^-4 + hbm^-4)^(-1/4)   tokens / us
+// equally: `cap` is what one CTA of the instance streams on its own (its ring
+// latency or its per-block arithmetic, whichever binds), `hbm` the memory's
+// rate; the smooth minimum fits the rates measured on a GB300 with 16, 32, 64,
+// 96, 144 and 152 CTAs to a few percent. A unit ends `tail_us` after its last
+// CTA. More than one piece adds the merge launch and its traffic (merge mode 1)
+// or the in-cluster merge (mode 2).
 struct CostModel {
-  double us_per_token;   // one KV head's token bytes / per-SM bandwidth
-  double cta_fixed_us;   // launch, pipeline fill, epilogue
+  double cap_tok_per_us;  // one CTA alone
+  double hbm_tok_per_us;  // all CTAs together
+  double cta_fixed_us;    // launch, first copies in flight, epilogue
   double empty_cta_us;
   double merge_fixed_us;
   double merge_us_per_byte;
   double cluster_merge_us;
-  int slots;
+  int slots;                          // resident CTAs (one per SM: shared memory bound)
+  std::vector<double> per_cta_rate;   // [n] = agg(n) / n, n = 0..slots
 };
 
-// GPCs the SMs are grouped in (GB300: 8). Only the cost model uses it.
-constexpr int kAssumedGpcs = 8;
 constexpr int kMaxClusterSplits = 8;
 
-double simulate(const std::vector<int>& n_tok, int hkv, int chunk, int splits, const CostModel& cm,
-                uint64_t merge_bytes) {
-  std::priority_queue<double, std::vector<double>, std::greater<double>> free_at;
-  for (int i = 0; i < cm.slots; ++i) free_at.push(0.0);
-  double makespan = 0.0;
-  for (size_t b = 0; b < n_tok.size(); ++b) {
-    for (int g = 0; g < hkv; ++g) {
-      for (int s = 0; s < splits; ++s) {
-        const long long lo = (long long)s * chunk;
-        long long len = (s == splits - 1) ? n_tok[b] - lo : std::min<long long>(chunk, n_tok[b] - lo);
-        const double dur = len > 0 ? cm.cta_fixed_us + len * cm.us_per_token : cm.empty_cta_us;
-        const double start = free_at.top();
-        free_at.pop();
-        const double end = start + dur;
-        free_at.push(end);
-        makespan = std::max(makespan, end);
-      }
+// Clusters of S CTAs (one CTA per SM, ~230 KB of shared memory each) resident
+// at once on a 152-SM GB300, as cudaOccupancyMaxActiveClusters reports: the
+// GPCs hold unequal numbers of SMs, so sizes 7 and 8 fit 15 clusters, not 16.
+// Other SM counts scale it. Only the cost model uses it.
+int cluster_slots(int splits, int sm_count) {
+  static const int kGb300[kMaxClusterSplits + 1] = {0, 152, 76, 46, 36, 28, 23, 15, 15};
+  if (splits < 1 || splits > kMaxClusterSplits) return 0;
+  return (int)((long long)kGb300[splits] * sm_count / 152);
+}
+
+// Tokens per microsecond one stage-1 CTA streams when few CTAs run (measured
+// on a GB300 with 16 CTAs over 2 x 65536 tokens, 4 KV heads): per (head_dim,
+// K=V, FP8) for CTAs of one 8-column tile (decode, or query tokens and heads
+// in one tile), and for bf16 CTAs of two tiles.
+double cta_tokens_per_us(const pd::VariantInfo& v) {
+  const bool kvs = v.kv_shared != 0;
+  if (v.tiles == 2) {
+    if (v.head_dim == 512) return kvs ? 48.5 : 47.2;
+    return 67.0;  // d256 (K=V not measured: the K != V figure)
+  }
+  if (v.kv_fp8) {
+    if (v.head_dim == 512) return kvs ? 85.1 : 49.4;
+    return kvs ? 76.8 : 98.0;
+  }
+  if (v.head_dim == 512) return kvs ? 61.7 : 55.4;
+  if (v.head_dim == 256) return kvs ? 90.5 : 74.6;
+  return kvs ? 165.5 : 74.7;
+}
+
+// Unit u's CTA i: its token count (<= 0: an empty range).
+using UnitTokens = std::function<long long(long long u, int i)>;
+
+double simulate_fluid(long long num_units, int ctas_per_unit, const UnitTokens& tokens, int slots, double tail_us,
+                      const CostModel& cm) {
+  struct Wall {
+    double t;
+    long long u;   // unit
+    long long tok; // > 0: a CTA's fixed phase ends and it starts streaming; 0: a CTA is done; -1: a slot frees
+    bool operator>(const Wall& o) const { return t > o.t; }
+  };
+  struct Stream {
+    double v_end;  // service level (tokens per streaming CTA) at which it is done
+    long long u;
+    bool operator>(const Stream& o) const { return v_end > o.v_end; }
+  };
+  std::priority_queue<Wall, std::vector<Wall>, std::greater<Wall>> wall;
+  std::priority_queue<Stream, std::vector<Stream>, std::greater<Stream>> streams;
+  std::vector<int> left;  // CTAs of each started unit still running
+  left.reserve((size_t)std::min<long long>(num_units, 1 << 20));
+  long long next = 0;
+  double t = 0.0, level = 0.0, makespan = 0.0;
+  auto start_unit = [&](double at) {
+    const long long u = next++;
+    left.push_back(ctas_per_unit);
+    for (int i = 0; i < ctas_per_unit; ++i) {
+      const long long n = tokens(u, i);
+      if (n > 0)
+        wall.push({at + cm.cta_fixed_us, u, n});
+      else
+        wall.push({at + cm.empty_cta_us, u, 0});
+    }
+  };
+  auto cta_done = [&](long long u) {
+    if (--left[(size_t)u] == 0) wall.push({t + tail_us, u, -1});
+  };
+  for (int s = 0; s < slots && next < num_units; ++s) start_unit(0.0);
+  while (!wall.empty() || !streams.empty()) {
+    const size_t n = streams.size();
+    const double rate = n ? cm.per_cta_rate[std::min(n, cm.per_cta_rate.size() - 1)] : 0.0;
+    const double t_stream = n ? t + (streams.top().v_end - level) / rate : 1e300;
+    const double t_wall = wall.empty() ? 1e300 : wall.top().t;
+    if (n && t_stream <= t_wall) {
+      t = std::max(t, t_stream);
+      level = streams.top().v_end;
+      const long long u = streams.top().u;
+      streams.pop();
+      cta_done(u);
+      continue;
+    }
+    const Wall e = wall.top();
+    wall.pop();
+    if (n) level += rate * (e.t - t);
+    t = std::max(t, e.t);
+    if (e.tok > 0) {
+      streams.push({level + (double)e.tok, e.u});
+    } else if (e.tok == 0) {
+      cta_done(e.u);
+    } else {
+      makespan = std::max(makespan, t);
+      if (next < num_units) start_unit(t);
     }
   }
+  return makespan;
+}
+
+// Tokens of piece s of a request whose block-aligned span is n tokens (the
+// last piece takes the remainder).
+long long piece_tokens(int n, int chunk, int splits, int s) {
+  const long long lo = (long long)s * chunk;
+  return (s == splits - 1) ? n - lo : std::min<long long>(chunk, n - lo);
+}
+
+// One launch with a CTA per (request, KV head CTA, piece), then the merge launch.
+double simulate(const std::vector<int>& n_tok, int hkv, int chunk, int splits, const CostModel& cm,
+                uint64_t merge_bytes) {
+  const long long units = (long long)n_tok.size() * hkv * splits;
+  auto tok = [&](long long u, int) { return piece_tokens(n_tok[(size_t)(u / ((long long)hkv * splits))], chunk, splits, (int)(u % splits)); };
+  double makespan = simulate_fluid(units, 1, tok, cm.slots, 0.0, cm);
   if (splits > 1) makespan += cm.merge_fixed_us + merge_bytes * cm.merge_us_per_byte;
   return makespan;
 }
 
 // The same launch with the S pieces of each (request, KV head) run as one
-// thread-block cluster (merged in the cluster, no merge launch): a cluster
-// needs S SMs of one GPC at once, so only floor(SMs per GPC / S) clusters fit
-// in a GPC; it lasts as long as its longest piece plus the in-cluster merge.
-double simulate_clusters(const std::vector<int>& n_tok, int hkv, int chunk, int splits, const CostModel& cm,
-                         int gpcs) {
-  const int per_gpc = cm.slots / gpcs;
-  const int cl_slots = gpcs * (per_gpc / splits);
+// thread-block cluster, merged in the cluster: only cluster_slots(S) clusters
+// are resident at a time.
+double simulate_clusters(const std::vector<int>& n_tok, int hkv, int chunk, int splits, const CostModel& cm) {
+  const int cl_slots = cluster_slots(splits, cm.slots);
   if (cl_slots <= 0) return 1e300;
-  std::priority_queue<double, std::vector<double>, std::greater<double>> free_at;
-  for (int i = 0; i < cl_slots; ++i) free_at.push(0.0);
-  double makespan = 0.0;
-  for (size_t b = 0; b < n_tok.size(); ++b) {
-    double dur = cm.empty_cta_us;
-    for (int s = 0; s < splits; ++s) {
-      const long long lo = (long long)s * chunk;
-      const long long len = (s == splits - 1) ? n_tok[b] - lo : std::min<long long>(chunk, n_tok[b] - lo);
-      if (len > 0) dur = std::max(dur, cm.cta_fixed_us + len * cm.us_per_token);
-    }
-    dur += cm.cluster_merge_us;
-    for (int g = 0; g < hkv; ++g) {
-      const double start = free_at.top();
-      free_at.pop();
-      free_at.push(start + dur);
-      makespan = std::max(makespan, start + dur);
-    }
-  }
-  return makespan;
+  const long long units = (long long)n_tok.size() * hkv;
+  auto tok = [&](long long u, int i) { return piece_tokens(n_tok[(size_t)(u / hkv)], chunk, splits, i); };
+  return simulate_fluid(units, splits, tok, cl_slots, cm.cluster_merge_us, cm);
 }
 
 }  // namespace
@@ -271,14 +348,20 @@ pd_status plan_impl(const pd_layer_desc* layer, int32_t batch, int32_t query_tok
   CostModel cm;
   const double kv_bytes_per_token =
       (double)ly.head_dim * (ly.kv_dtype == PD_KV_FP8_E4M3 ? 1.0 : 2.0) * (ly.kv_shared ? 1.0 : 2.0);
-  const double sm_bw_bytes_per_us = 7.0e12 / 1e6 / sm_count;  // ~7 TB/s shared by the SMs
-  cm.us_per_token = kv_bytes_per_token / sm_bw_bytes_per_us;
+  // ~7.3 TB/s of HBM on a 152-SM GB300, in proportion for other SM counts
+  cm.hbm_tok_per_us = 7.3e12 / 1e6 / kv_bytes_per_token * sm_count / 152.0;
+  cm.cap_tok_per_us = cta_tokens_per_us(*v);
   cm.cta_fixed_us = 2.0;
   cm.empty_cta_us = 0.2;
   cm.merge_fixed_us = 2.0;
   cm.merge_us_per_byte = 1.0 / 7.0e6;
   cm.cluster_merge_us = 0.5;
   cm.slots = sm_count;  // one resident CTA per SM (shared memory bound)
+  cm.per_cta_rate.assign((size_t)sm_count + 1, 0.0);
+  for (int n = 1; n <= sm_count; ++n) {
+    const double agg = std::pow(std::pow(n * cm.cap_tok_per_us, -4.0) + std::pow(cm.hbm_tok_per_us, -4.0), -0.25);
+    cm.per_cta_rate[(size_t)n] = agg / n;
+  }
 
   // pieces are whole stages where possible (a stage holds blocks_per_stage blocks)
   const uint64_t unit = 16ull * v->blocks_per_stage;
@@ -312,7 +395,7 @@ pd_status plan_impl(const pd_layer_desc* layer, int32_t batch, int32_t query_tok
       double cost = simulate(n_tok, hkv_ctas, c, s, cm, merge_bytes);
       bool cluster = false;
       if (!partial && s >= 2 && s <= std::min(kMaxClusterSplits, v->max_cluster)) {
-        const double cc = simulate_clusters(n_tok, hkv_ctas, c, s, cm, kAssumedGpcs);
+        const double cc = simulate_clusters(n_tok, hkv_ctas, c, s, cm);
         if (cc < cost) {
           cost = cc;
           cluster = true;

@@ -246,7 +246,7 @@ def test_noalloc_checks_every_argument_before_queueing_work(lib):
     assert call(bf, q=fake + 2) == b.PD_ERR_INVALID_ARG    # misaligned q
     assert call(bf, v=fake) == b.PD_ERR_INVALID_ARG        # V aliasing K on a K != V layer
     assert call(bf, scale=float("nan")) == b.PD_ERR_INVALID_ARG
-    big = b.paged_decode_plan(b.layer_desc(16, 4, 512, 16, 64 * 512 + 1, 512), [8192] * 64, 4000)
+    big = b.paged_decode_plan(b.layer_desc(16, 4, 512, 16, 4 * 8192 + 1, 8192), [131072] * 4, 4000)
     assert big.workspace_bytes > 8 << 20 and call(big) == b.PD_ERR_WORKSPACE_TOO_SMALL
     assert call(bf) == b.PD_ERR_CUDA                  # valid: gets as far as CUDA, which is absent here
 

@@ -311,7 +311,7 @@ def test_many_pieces_merge(sms):
     assert torch.equal(out, again)
 
 
-@pytest.mark.parametrize("lens,sms,mode", [([32], 152, 0), ([1000, 900], 152, 1), ([1000, 900], 20, 2)])
+@pytest.mark.parametrize("lens,sms,mode", [([32], 152, 0), ([4000, 3000], 152, 1), ([1000, 900], 20, 2)])
 def test_pipeline_wait_timeout_is_reported_and_context_survives(lens, sms, mode):
     """A stage that never completes (the copies deliver fewer bytes than the
     stage expects): every wait gives up after ~1 s, the kernel returns, the

@@ -100,10 +100,11 @@ def test_noalloc_matches_oracle_and_workspace_path_twice(lens, window, kvs, d, G
 
 
 def test_noalloc_rejects_plans_beyond_its_scratch():
-    # a plan for 64 requests x 16 heads x 31 pieces needs far more than 8 MiB of
-    # partials; the call must refuse it before touching any buffer
-    lens = [8192] * 64
-    plan = b.paged_decode_plan(b.layer_desc(16, 4, 512, 16, 64 * 512 + 1, 512), lens, 4000)
+    # a plan for 4 requests x 16 heads x ~150 pieces (planned for 4000 SMs) needs
+    # far more than 8 MiB of partials; the call must refuse it before touching
+    # any buffer
+    lens = [131072] * 4
+    plan = b.paged_decode_plan(b.layer_desc(16, 4, 512, 16, 4 * 8192 + 1, 8192), lens, 4000)
     li = synth.make_layer("small", [16], 16, 4, 512, pool_pages=2, seed=3, device="cuda")
     assert plan.workspace_bytes > 8 << 20
     out = torch.zeros_like(li.q)
