@@ -55,20 +55,21 @@ L2_BYTES = 129 * 1000 * 1000
 FALLBACK_HBM_GBS = 6800.0
 
 # DRAM bytes (read + write) per stage-1 launch from an ncu capture, keyed by the
-# hash of the kernel sources it was taken on; stale entries are ignored (the
-# captures and their commands are summarised under profiles/).
+# hash of the kernel and planner sources it was taken on (the plan sets the
+# pieces, hence the partials written); stale entries are ignored (the captures
+# and their commands are summarised under profiles/).
 NCU_TRAFFIC = {
-    "cf4afb6b93f92e43": {"w4a": 1073912832 + 3335168, "w2": 67298816 + 441088, "w3": 68275200 + 333568,
-                         "w4a-fp8": 537299968 + 3247616, "w5global": 1596612864 + 4693504,
-                         "w5global-fp8": 798941952 + 5015808, "w5sliding": 68171776 + 550144},
+    "13b1fc0b0cb7c7a4": {"w4a": 1073906176 + 2811392, "w2": 67307008 + 450048, "w3": 68280064 + 405504,
+                         "w4a-fp8": 537347072 + 2884864, "w5global": 1596588288 + 4382720,
+                         "w5global-fp8": 798939904 + 4985344, "w5sliding": 68175104 + 545792},
 }
 
 # the same for the fused QKV norm + RoPE + cache-write kernel (--op prepare)
 PREP_NCU_TRAFFIC = {
-    "fed05ad210b6d714": {"w2": 216832},
+    "78d6f35095226450": {"w2": 220928},
 }
 
-STAGE1_SOURCES = ("stage1.cu", "pd_common.cuh", "pd_variants.h", "pd_kernels.h")
+STAGE1_SOURCES = ("stage1.cu", "pd_common.cuh", "pd_variants.h", "pd_kernels.h", "plan.cu")
 
 
 PREP_SOURCES = ("prepare.cu", "pd_common.cuh", "pd_variants.h")
