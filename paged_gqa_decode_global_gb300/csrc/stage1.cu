@@ -96,12 +96,39 @@ __device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t& lo, uint32
 }
 
 // FP8 QK order of the head dims. In k-step ks = 8*sl + 4*hf + jj the MMA's
-// columns 2*(lane%4) + {0, 1} and + {8, 9} are the dims returned + {0, 1} and
-// + {2, 3}: four consecutive bytes of the 16-byte chunk 2*(lane%4) + hf of the
-// 128-dim slab sl, so one load of a token row feeds four k-steps. (A sum over
-// the dims may take them in any order, as long as q and K agree.)
-__device__ __forceinline__ int kv8_qk_dim(int ks, int lane) {
-  return (ks >> 3) * 128 + (2 * (lane & 3) + ((ks >> 2) & 1)) * 16 + 4 * (ks & 3);
+// columns 2*(lane%4) + {0, 1} and + {8, 9} are the dims d + {0, 1} and
+// d + {2, 3}, d = 128*sl + 16*(2*(lane%4) + hf) + 4*jj: four consecutive bytes
+// of the 16-byte chunk 2*(lane%4) + hf of the 128-dim slab sl, so one load of a
+// token row feeds four k-steps. (A sum over the dims may take them in any
+// order, as long as q and K agree.)
+
+// Lane r of each group of four lanes holds words v[0..3] of row r of a 4 x 4
+// matrix of 32-bit words; afterwards it holds column r (v[s] = row s's word r):
+// two butterfly rounds, each swapping the 2 x 2 blocks' off-diagonal halves.
+__device__ __forceinline__ void quad_transpose(uint4& v, int lane) {
+  const bool odd = (lane & 1) != 0;
+  uint32_t s0 = odd ? v.x : v.y, s1 = odd ? v.z : v.w;
+  s0 = __shfl_xor_sync(kFullMask, s0, 1);
+  s1 = __shfl_xor_sync(kFullMask, s1, 1);
+  if (odd) {
+    v.x = s0;
+    v.z = s1;
+  } else {
+    v.y = s0;
+    v.w = s1;
+  }
+  const bool hi = (lane & 2) != 0;
+  s0 = hi ? v.x : v.z;
+  s1 = hi ? v.y : v.w;
+  s0 = __shfl_xor_sync(kFullMask, s0, 2);
+  s1 = __shfl_xor_sync(kFullMask, s1, 2);
+  if (hi) {
+    v.x = s0;
+    v.y = s1;
+  } else {
+    v.z = s0;
+    v.w = s1;
+  }
 }
 
 // Transpose an 8x8 bf16 matrix held one row pair per lane (fragment layout).
@@ -284,26 +311,74 @@ __device__ __forceinline__ int stage1_cta(const Stage1Params& p, uint8_t* smem) 
   // B fragments of q (heads on N, dims on K): lane holds head lane/4, dims
   // 2*(lane%4) + {0,1} and + {8,9} of every 16-dim step; heads past G are zero.
   const int qh = lane >> 2;
-  const int qk = (lane & 3) * 2;
   uint32_t qb[C::KSTEPS][2];
   if (warp != C::NW) {
+    const bool qv = cm.valid(cb + qh);
+    const uint16_t* qrow = p.q + (qv ? cm.row(cb + qh) * C::D : 0);
+    if constexpr (C::KV8) {
+      // dims in the FP8 QK order (see the consumer loop): half hf of slab sl
+      // gives lane r the 16 dims of chunk 2r + hf, four per k-step; the
+      // products run in f16, so q rounds to f16 once here
 #pragma unroll
-    for (int ks = 0; ks < C::KSTEPS; ++ks) {
-      if (cm.valid(cb + qh)) {
-        if constexpr (C::KV8) {
-          // dims in the FP8 QK order (see the consumer loop); the products run
-          // in f16, so q rounds to f16 once here
-          const uint2 x = __ldg(reinterpret_cast<const uint2*>(p.q + cm.row(cb + qh) * C::D + kv8_qk_dim(ks, lane)));
-          qb[ks][0] = pack_f16x2(__uint_as_float(x.x << 16), __uint_as_float(x.x & 0xffff0000u));
-          qb[ks][1] = pack_f16x2(__uint_as_float(x.y << 16), __uint_as_float(x.y & 0xffff0000u));
-        } else {
-          const uint16_t* qrow = p.q + cm.row(cb + qh) * C::D + ks * 16 + qk;
-          qb[ks][0] = __ldg(reinterpret_cast<const unsigned int*>(qrow));
-          qb[ks][1] = __ldg(reinterpret_cast<const unsigned int*>(qrow + 8));
+      for (int sl = 0; sl < C::TMA_SLABS; ++sl) {
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          uint4 a = make_uint4(0u, 0u, 0u, 0u), c = a;
+          if (qv) {
+            const uint4* src = reinterpret_cast<const uint4*>(qrow + sl * 128 + (2 * (lane & 3) + hf) * 16);
+            a = __ldg(src);
+            c = __ldg(src + 1);
+          }
+          const uint32_t w[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            const int ks = sl * 8 + hf * 4 + jj;
+            qb[ks][0] = pack_f16x2(__uint_as_float(w[2 * jj] << 16), __uint_as_float(w[2 * jj] & 0xffff0000u));
+            qb[ks][1] =
+                pack_f16x2(__uint_as_float(w[2 * jj + 1] << 16), __uint_as_float(w[2 * jj + 1] & 0xffff0000u));
+          }
         }
-      } else {
-        qb[ks][0] = 0u;
-        qb[ks][1] = 0u;
+      }
+    } else if constexpr (!C::MQ) {
+      // decode: this lane's q dims 16 ks + 2r + {0, 1} and 16 ks + 8 + 2r +
+      // {0, 1} as 4-byte loads (issued together here; the vector form below
+      // measured slower for these instances)
+      const int qk = (lane & 3) * 2;
+#pragma unroll
+      for (int ks = 0; ks < C::KSTEPS; ++ks) {
+        if (qv) {
+          qb[ks][0] = __ldg(reinterpret_cast<const unsigned int*>(qrow + ks * 16 + qk));
+          qb[ks][1] = __ldg(reinterpret_cast<const unsigned int*>(qrow + ks * 16 + 8 + qk));
+        } else {
+          qb[ks][0] = 0u;
+          qb[ks][1] = 0u;
+        }
+      }
+    } else {
+      // column-tiled instances, whose 4-byte loads issued in several round
+      // trips (~2.5 us against ~0.7): lane r of a quad loads both 16-byte
+      // halves of k-steps 4i + r (the quad reads 128 contiguous bytes); a
+      // 4 x 4 transpose of 32-bit words across the quad then leaves with lane
+      // r word r of every half: q dims 16 ks + 2r + {0, 1} and 16 ks + 8 + 2r
+      // + {0, 1}
+#pragma unroll
+      for (int i = 0; i < C::KSTEPS / 4; ++i) {
+        const int ks = 4 * i + (lane & 3);
+        uint4 a = make_uint4(0u, 0u, 0u, 0u), c = a;
+        if (qv) {
+          a = __ldg(reinterpret_cast<const uint4*>(qrow + ks * 16));
+          c = __ldg(reinterpret_cast<const uint4*>(qrow + ks * 16 + 8));
+        }
+        quad_transpose(a, lane);
+        quad_transpose(c, lane);
+        qb[4 * i + 0][0] = a.x;
+        qb[4 * i + 1][0] = a.y;
+        qb[4 * i + 2][0] = a.z;
+        qb[4 * i + 3][0] = a.w;
+        qb[4 * i + 0][1] = c.x;
+        qb[4 * i + 1][1] = c.y;
+        qb[4 * i + 2][1] = c.z;
+        qb[4 * i + 3][1] = c.w;
       }
     }
   }
@@ -647,7 +722,7 @@ __device__ __forceinline__ int stage1_cta(const Stage1Params& p, uint8_t* smem) 
       if constexpr (C::KV8) {
         // A fragments straight from the e4m3 rows: one 16-byte chunk of token
         // rows lane/4 and lane/4 + 8 holds this lane's part of four k-steps
-        // (the dims are taken in the order kv8_qk_dim gives; q follows it)
+        // (the dims are taken in the FP8 QK order; q follows it)
         const uint8_t* kb = stg + u * C::KV_BYTES;
 #pragma unroll
         for (int sl = 0; sl < C::TMA_SLABS; ++sl) {
