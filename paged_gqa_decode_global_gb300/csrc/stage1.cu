@@ -237,77 +237,8 @@ __device__ __forceinline__ int stage1_cta(const Stage1Params& p, uint8_t* smem) 
   const int team = warp / C::WB;
   const int cb = team * C::G;  // first CTA column of this warp's team
 
-  // ---- attended range of this request and this piece -------------------------
-  const int cap = p.max_pages * p.page_size;
-  const int32_t* table = p.block_tables + (size_t)b * p.max_pages;
-  // On a global layer a piece starts at split * chunk whatever the length, so
-  // the producer fetches its first page ids while the length is in flight:
-  // with one lane per stage, lane st those of stage block st; with the batch
-  // walk, lane k that of block k.
-  constexpr bool kLanePerStage = C::LANE_PER_STAGE;
-  int page_spec[C::NSUB];
-#pragma unroll
-  for (int u = 0; u < C::NSUB; ++u) {
-    page_spec[u] = -1;
-    const int blk = kLanePerStage ? lane * C::NSUB + u : (u == 0 ? lane : -1);
-    if (warp == C::NW && p.window == 0 && blk >= 0 && (!kLanePerStage || lane < C::NST)) {
-      const long long t = (long long)split * p.chunk_tokens + (long long)blk * C::TB;
-      if (t < cap) page_spec[u] = __ldg(table + t / p.page_size);
-    }
-  }
-  int L = p.seq_lens[b];
-  if (L < 0 || L > cap || (C::MQ && cm.T > 1 && L < cm.T)) {
-    if (threadIdx.x == 0) atomicOr(p.err, kErrBadSeqLen);
-    L = L < 0 ? 0 : (L > cap ? cap : L);
-  }
-  // attended range [lo, hi) of this CTA's query rows: decode, the last W (or
-  // all) positions; multi-token, the union of its tokens' causal ranges, token
-  // j ending at its own position L - T + j (inclusive)
-  int hi = L, lo;
-  if constexpr (C::MQ) {
-    const int j_first = cm.token(0);
-    int j_last = cm.token(C::CC - 1);
-    if (j_last > cm.T - 1) j_last = cm.T - 1;
-    hi = L - cm.T + j_last + 1;
-    if (hi < 0) hi = 0;
-    const int first_hi = L - cm.T + j_first + 1;
-    lo = (p.window > 0 && first_hi > p.window) ? first_hi - p.window : 0;
-  } else {
-    lo = (p.window > 0 && L > p.window) ? L - p.window : 0;
-  }
-  const int base = (lo / C::TB) * C::TB;
-  const long long piece_lo = (long long)base + (long long)split * p.chunk_tokens;
-  const int tlo = (int)(piece_lo > lo ? piece_lo : lo);
-  // the last piece takes whatever remains, so a device length longer than the
-  // planned one is still attended in full
-  const long long piece_hi = (split == p.num_splits - 1) ? (long long)hi : piece_lo + p.chunk_tokens;
-  const int thi = (int)(piece_hi < hi ? piece_hi : hi);
-  const int blk_lo = (tlo / C::TB) * C::TB;
-  const int nblk = (thi > tlo) ? (thi - blk_lo + C::TB - 1) / C::TB : 0;
-  // stages of this piece: NSUB consecutive blocks each (the last may hold fewer)
-  const int nstg = (nblk + C::NSUB - 1) / C::NSUB;
-
-  if (nblk == 0) {
-    // nothing attended in this piece
-    if (early) grid_dependency_wait();
-    if (p.cluster_merge) {
-      if (threadIdx.x < C::CC) reinterpret_cast<float*>(smem + C::CTA_LSE_OFFSET)[threadIdx.x] = -INFINITY;
-    } else if (p.direct_out) {
-      for (int i = threadIdx.x; i < C::CC * C::D; i += C::THREADS)
-        if (cm.valid(i / C::D))
-          reinterpret_cast<__nv_bfloat16*>(p.out)[cm.row(i / C::D) * C::D + i % C::D] = __float2bfloat16_rn(0.f);
-    } else {
-      // weight 0 and a zero partial row, so the merge needs no special case
-      for (int i = threadIdx.x; i < C::CC * C::D; i += C::THREADS)
-        if (cm.valid(i / C::D)) p.o_part[(cm.row(i / C::D) * p.num_splits + split) * C::D + i % C::D] = 0.f;
-      if (threadIdx.x < C::CC && cm.valid(threadIdx.x))
-        p.lse_part[cm.row(threadIdx.x) * p.num_splits + split] = -INFINITY;
-    }
-    return kMergeNothing;
-  }
-
-  // The consumers start their q loads before the barrier set-up so their
-  // latency overlaps it.
+  // The consumers issue their q loads first, so that their latency overlaps
+  // the length's (q does not depend on it); an empty piece drops them.
   // B fragments of q (heads on N, dims on K): lane holds head lane/4, dims
   // 2*(lane%4) + {0,1} and + {8,9} of every 16-dim step; heads past G are zero.
   const int qh = lane >> 2;
@@ -381,6 +312,76 @@ __device__ __forceinline__ int stage1_cta(const Stage1Params& p, uint8_t* smem) 
         qb[4 * i + 3][1] = c.w;
       }
     }
+  }
+
+
+  // ---- attended range of this request and this piece -------------------------
+  const int cap = p.max_pages * p.page_size;
+  const int32_t* table = p.block_tables + (size_t)b * p.max_pages;
+  // On a global layer a piece starts at split * chunk whatever the length, so
+  // the producer fetches its first page ids while the length is in flight:
+  // with one lane per stage, lane st those of stage block st; with the batch
+  // walk, lane k that of block k.
+  constexpr bool kLanePerStage = C::LANE_PER_STAGE;
+  int page_spec[C::NSUB];
+#pragma unroll
+  for (int u = 0; u < C::NSUB; ++u) {
+    page_spec[u] = -1;
+    const int blk = kLanePerStage ? lane * C::NSUB + u : (u == 0 ? lane : -1);
+    if (warp == C::NW && p.window == 0 && blk >= 0 && (!kLanePerStage || lane < C::NST)) {
+      const long long t = (long long)split * p.chunk_tokens + (long long)blk * C::TB;
+      if (t < cap) page_spec[u] = __ldg(table + t / p.page_size);
+    }
+  }
+  int L = p.seq_lens[b];
+  if (L < 0 || L > cap || (C::MQ && cm.T > 1 && L < cm.T)) {
+    if (threadIdx.x == 0) atomicOr(p.err, kErrBadSeqLen);
+    L = L < 0 ? 0 : (L > cap ? cap : L);
+  }
+  // attended range [lo, hi) of this CTA's query rows: decode, the last W (or
+  // all) positions; multi-token, the union of its tokens' causal ranges, token
+  // j ending at its own position L - T + j (inclusive)
+  int hi = L, lo;
+  if constexpr (C::MQ) {
+    const int j_first = cm.token(0);
+    int j_last = cm.token(C::CC - 1);
+    if (j_last > cm.T - 1) j_last = cm.T - 1;
+    hi = L - cm.T + j_last + 1;
+    if (hi < 0) hi = 0;
+    const int first_hi = L - cm.T + j_first + 1;
+    lo = (p.window > 0 && first_hi > p.window) ? first_hi - p.window : 0;
+  } else {
+    lo = (p.window > 0 && L > p.window) ? L - p.window : 0;
+  }
+  const int base = (lo / C::TB) * C::TB;
+  const long long piece_lo = (long long)base + (long long)split * p.chunk_tokens;
+  const int tlo = (int)(piece_lo > lo ? piece_lo : lo);
+  // the last piece takes whatever remains, so a device length longer than the
+  // planned one is still attended in full
+  const long long piece_hi = (split == p.num_splits - 1) ? (long long)hi : piece_lo + p.chunk_tokens;
+  const int thi = (int)(piece_hi < hi ? piece_hi : hi);
+  const int blk_lo = (tlo / C::TB) * C::TB;
+  const int nblk = (thi > tlo) ? (thi - blk_lo + C::TB - 1) / C::TB : 0;
+  // stages of this piece: NSUB consecutive blocks each (the last may hold fewer)
+  const int nstg = (nblk + C::NSUB - 1) / C::NSUB;
+
+  if (nblk == 0) {
+    // nothing attended in this piece
+    if (early) grid_dependency_wait();
+    if (p.cluster_merge) {
+      if (threadIdx.x < C::CC) reinterpret_cast<float*>(smem + C::CTA_LSE_OFFSET)[threadIdx.x] = -INFINITY;
+    } else if (p.direct_out) {
+      for (int i = threadIdx.x; i < C::CC * C::D; i += C::THREADS)
+        if (cm.valid(i / C::D))
+          reinterpret_cast<__nv_bfloat16*>(p.out)[cm.row(i / C::D) * C::D + i % C::D] = __float2bfloat16_rn(0.f);
+    } else {
+      // weight 0 and a zero partial row, so the merge needs no special case
+      for (int i = threadIdx.x; i < C::CC * C::D; i += C::THREADS)
+        if (cm.valid(i / C::D)) p.o_part[(cm.row(i / C::D) * p.num_splits + split) * C::D + i % C::D] = 0.f;
+      if (threadIdx.x < C::CC && cm.valid(threadIdx.x))
+        p.lse_part[cm.row(threadIdx.x) * p.num_splits + split] = -INFINITY;
+    }
+    return kMergeNothing;
   }
 
   // The ring's barriers (set up by the producer's lane 0 at entry) are
