@@ -59,9 +59,9 @@ FALLBACK_HBM_GBS = 6800.0
 # pieces, hence the partials written); stale entries are ignored (the captures
 # and their commands are summarised under profiles/).
 NCU_TRAFFIC = {
-    "13b1fc0b0cb7c7a4": {"w4a": 1073906176 + 2811392, "w2": 67307008 + 450048, "w3": 68280064 + 405504,
-                         "w4a-fp8": 537347072 + 2884864, "w5global": 1596588288 + 4382720,
-                         "w5global-fp8": 798939904 + 4985344, "w5sliding": 68175104 + 545792},
+    "9ee344afd7342fa0": {"w4a": 1073913088 + 2816512, "w2": 67298816 + 530432, "w3": 68278016 + 413952,
+                         "w4a-fp8": 537301248 + 2789632, "w5global": 1596588544 + 4348928,
+                         "w5global-fp8": 798931456 + 4535808, "w5sliding": 68172032 + 553984},
 }
 
 # the same for the fused QKV norm + RoPE + cache-write kernel (--op prepare)

@@ -61,7 +61,9 @@ CASES = [
     # name, lens, Hq, Hkv, d, window, kv_shared, sm_count (sets the merge mode)
     ("global d512 one piece", [300, 17, 1, 64], 16, 4, 512, 0, False, 4),
     ("global d512 cluster", [1000, 977, 513, 64], 16, 4, 512, 0, False, 152),
-    ("global d512 K=V merge kernel", [1000, 977, 513, 64], 16, 2, 512, 0, True, 4000),
+    ("global d512 K=V cluster of 8", [1000, 977, 513, 64], 16, 2, 512, 0, True, 4000),
+    ("global d512 K=V merge kernel", [8000, 7000, 513, 64], 16, 2, 512, 0, True, 20),
+    ("global d512 K=V merge kernel, 125 pieces", [20000, 64], 16, 2, 512, 0, True, 1000),
     ("sliding d256", [4100, 4000, 1, 15], 16, 8, 256, 1024, False, 152),
     ("sliding d256 K=V", [700, 33, 129], 8, 4, 256, 100, True, 152),
 ]

@@ -294,16 +294,25 @@ def test_nan_in_unattended_rows_does_not_leak(kvs, window, d):
     compare(out, ref, li, "nan rows")
 
 
-@pytest.mark.parametrize("sms", [20, 152, 4000])
-def test_many_pieces_merge(sms):
-    """From a few pieces to one per 16-token page: the merge matches the oracle,
-    and a second call on the same workspace gives the same bits."""
-    lens = [1000, 977, 513, 64]
-    li = synth.make_layer("mm", lens, 16, 2, 512, pool_pages=200, seed=13, device="cuda")
+MERGE_CASES = [  # (lengths, SM count given to the planner, merge mode it picks)
+    ([1000, 977, 513, 64], 20, 2),      # 2 pieces merged in the cluster
+    ([1000, 977, 513, 64], 4000, 2),    # 8 pieces merged in the cluster
+    ([8000, 7000, 513, 64], 20, 1),     # 5 pieces, the merge launch
+    ([8000, 7000, 513, 64], 1000, 1),   # 63 pieces
+    ([9000], 1000, 1),                  # 141 pieces of one request
+]
+
+
+@pytest.mark.parametrize("lens,sms,mode", MERGE_CASES)
+def test_many_pieces_merge(lens, sms, mode):
+    """From a few pieces to one per 16-token page, in both merge modes: the
+    merge matches the oracle, and a second call on the same workspace gives the
+    same bits."""
+    li = synth.make_layer("mm", lens, 16, 2, 512, pool_pages=sum((L + 15) // 16 for L in lens) + 8, seed=13,
+                          device="cuda")
     ref = run_oracle(li)
     out, step = run_gpu(li, sm_count=sms)
-    assert step.plan.num_splits > 1
-    assert step.plan.merge_mode == (2 if step.plan.num_splits <= 8 else 1)
+    assert step.plan.num_splits > 1 and step.plan.merge_mode == mode
     compare(out, ref, li, f"S={step.plan.num_splits}")
     again = torch.empty_like(out)
     step.run(li, again)
@@ -407,3 +416,34 @@ def test_fp8_scales_reach_the_result():
     assert step.check() == 0
     assert torch.equal(out3, out4)  # products with 2 are exact in fp32
     assert not torch.equal(out3, out)
+
+
+def test_one_workspace_serves_changing_plans():
+    """Serving replans every step: one workspace, zeroed once, runs plans of
+    every merge mode and of different batches in turn, each call matching the
+    oracle and leaving the error word clear."""
+    shapes = [  # (lengths, SM count, merge mode)
+        ([4097, 1500, 77, 0, 3000], 152, 1),
+        ([9000], 1000, 1),
+        ([2000] * 8, 152, 2),
+        ([8000, 7000, 513, 64, 1, 4000, 300, 2500], 40, 1),
+        ([300, 17], 1, 0),
+        ([4097, 1500, 77, 0, 3000], 152, 1),
+    ]
+    layers, plans, need = [], [], 0
+    for i, (lens, sms, mode) in enumerate(shapes):
+        li = synth.make_layer(f"ws{i}", lens, 16, 4, 512, pool_pages=sum((L + 15) // 16 for L in lens) + 8,
+                              seed=40 + i, device="cuda")
+        step = b.LayerStep.for_inputs(li, sm_count=sms)
+        assert step.plan.merge_mode == mode, (lens, sms, step.plan.merge_mode)
+        layers.append(li)
+        plans.append(step.plan)
+        need = max(need, int(step.plan.workspace_bytes))
+    ws = torch.zeros((need + 255) // 256 * 256, dtype=torch.uint8, device="cuda")
+    for rep in range(2):
+        for li, plan in zip(layers, plans):
+            out = torch.full_like(li.q, float("nan"))
+            b.paged_decode_global(plan, li.q, li.k_pool, li.v_pool, li.block_tables, li.seq_lens, li.scale, ws, out)
+            b.paged_decode_merge(plan, ws, out)
+            assert b.paged_decode_check_device_error(plan, ws) == 0
+            compare(out, run_oracle(li), li, f"rep {rep} mode {plan.merge_mode} S={plan.num_splits}")
