@@ -130,8 +130,8 @@ struct Stage1Cfg {
 // one block a stage; d256 K!=V: two blocks), 16 KiB x 12 (d512 K=V: one block;
 // d256 K=V and d128 K!=V: two blocks), 8 KiB x 24 (d128 K=V: two blocks).
 // FP8: seven consumer warps (two per SM sub-partition hide the latency of
-// widening e4m3 fragments to f16), one block a stage (two for d256 K=V),
-// rings of 168-224 KiB.
+// widening e4m3 fragments to f16), one block a stage (two for the
+// column-tiled d256 K=V instance), rings of 112-224 KiB.
 // Column-tiled (ids 32-35): the group-8 geometry, any group up to 16 and any
 // number of query tokens at run time, one tile of 8 columns per CTA (ids
 // 44-47: the same over an FP8 cache); ids 48-51: two tiles per CTA, served by
@@ -166,10 +166,10 @@ struct Stage1Cfg {
   X(25, 256, 2, false, true, 7, 4, false, 1, 1)  \
   X(26, 256, 4, false, true, 7, 4, false, 1, 1)  \
   X(27, 256, 8, false, true, 7, 4, false, 1, 1)  \
-  X(28, 256, 1, true, true, 7, 3, false, 2, 1)   \
-  X(29, 256, 2, true, true, 7, 3, false, 2, 1)   \
-  X(30, 256, 4, true, true, 7, 3, false, 2, 1)   \
-  X(31, 256, 8, true, true, 7, 3, false, 2, 1)   \
+  X(28, 256, 1, true, true, 7, 4, false, 1, 1)   \
+  X(29, 256, 2, true, true, 7, 4, false, 1, 1)   \
+  X(30, 256, 4, true, true, 7, 4, false, 1, 1)   \
+  X(31, 256, 8, true, true, 7, 4, false, 1, 1)   \
   X(32, 512, 8, false, false, 3, 2, true, 1, 1)  \
   X(33, 512, 8, true, false, 3, 4, true, 1, 1)   \
   X(34, 256, 8, false, false, 3, 2, true, 2, 1)  \
@@ -185,7 +185,7 @@ struct Stage1Cfg {
   X(44, 512, 8, false, true, 7, 2, true, 1, 1)   \
   X(45, 512, 8, true, true, 7, 4, true, 1, 1)    \
   X(46, 256, 8, false, true, 7, 4, true, 1, 1)   \
-  X(47, 256, 8, true, true, 7, 3, true, 2, 1)    \
+  X(47, 256, 8, true, true, 7, 4, true, 2, 1)    \
   X(48, 512, 8, false, false, 6, 2, true, 1, 2)  \
   X(49, 512, 8, true, false, 6, 4, true, 1, 2)   \
   X(50, 256, 8, false, false, 6, 2, true, 2, 2)  \

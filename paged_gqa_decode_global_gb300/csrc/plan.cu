@@ -132,7 +132,7 @@ double cta_tokens_per_us(const pd::VariantInfo& v) {
   }
   if (v.kv_fp8) {
     if (v.head_dim == 512) return kvs ? 85.1 : 49.4;
-    return kvs ? 76.8 : 98.0;
+    return kvs ? 120.0 : 98.0;
   }
   if (v.head_dim == 512) return kvs ? 61.7 : 55.4;
   if (v.head_dim == 256) return kvs ? 90.5 : 74.6;
