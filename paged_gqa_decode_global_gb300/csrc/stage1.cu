@@ -1122,21 +1122,33 @@ __device__ __forceinline__ void cluster_merge(const Stage1Params& p, uint8_t* sm
   }
   __syncthreads();
   const ColMap<C> cm(p);
-#pragma unroll 2
+#pragma unroll 1
   for (int e = tid; e < C::CC * D4; e += C::THREADS) {
     const int h = e / D4;
     if (C::MQ && !cm.valid(h)) continue;
+    // all S pieces' weights and rows loaded before any is used; an empty
+    // piece pushed no row (its slot may hold anything) and weighs 0: selected
+    // out rather than multiplied
+    float w[C::MAX_CLUSTER];
+    float4 v[C::MAX_CLUSTER];
+#pragma unroll
+    for (int r = 0; r < C::MAX_CLUSTER; ++r) {
+      if (r < S) {
+        w[r] = wts[r * C::CC + h];
+        v[r] = r == 0 ? my_out[e] : push_out[(r - 1) * C::CC * D4 + e];
+      } else {
+        w[r] = 0.f;
+        v[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int r = 0; r < C::MAX_CLUSTER; ++r) {
-      if (r >= S) break;
-      const float w = wts[r * C::CC + h];
-      if (w == 0.f) continue;  // an empty piece pushed no result
-      const float4 v = r == 0 ? my_out[e] : push_out[(r - 1) * C::CC * D4 + e];
-      acc.x = fmaf(w, v.x, acc.x);
-      acc.y = fmaf(w, v.y, acc.y);
-      acc.z = fmaf(w, v.z, acc.z);
-      acc.w = fmaf(w, v.w, acc.w);
+      const bool use = w[r] != 0.f;
+      acc.x = use ? fmaf(w[r], v[r].x, acc.x) : acc.x;
+      acc.y = use ? fmaf(w[r], v[r].y, acc.y) : acc.y;
+      acc.z = use ? fmaf(w[r], v[r].z, acc.z) : acc.z;
+      acc.w = use ? fmaf(w[r], v[r].w, acc.w) : acc.w;
     }
     uint2 packed;
     packed.x = pack_bf16x2(acc.x, acc.y);
