@@ -15,9 +15,9 @@
 // as a programmatic dependent (it waits for stage 1 before reading). Every
 // warp reduces the row's S log-sum-exps itself; then lane 4c + g of warp w
 // sums float4 column 8w + c of the slice over pieces g, g + 4, g + 8, ...
-// (eight lanes of one piece group read 128 contiguous bytes of a piece, and
-// all of a lane's loads are in flight together), and two shuffles add the
-// four groups. The kernel holds no shared memory, so one of its CTAs fits
+// (eight lanes of one piece group read 128 contiguous bytes of a piece; a
+// lane's first four pieces' rows are loaded together with the log-sum-exps,
+// before the weights are known), and two shuffles add the four groups. The kernel holds no shared memory, so one of its CTAs fits
 // beside a stage-1 CTA of the next launch on the same SM.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -32,6 +32,7 @@ namespace {
 constexpr int kMergeMaxSplits = 1024;  // pieces of one row (the plan's cap, and the combine's rank limit)
 constexpr int kMergeThreads = 128;  // 32 float4 columns x 4 piece groups: 128 dims a CTA
 constexpr int kMergeGroups = 4;
+constexpr int kPrefetch = 4;  // pieces per lane whose rows load with the log-sum-exps (S <= 16 in one go)
 
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams p) {
   grid_dependency_wait();  // stage 1 (launched before this grid) has finished
@@ -42,6 +43,19 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int S = p.num_splits;
   const float* lse = p.lse_part + row * p.lse_row_stride;
+  const int g = lane % kMergeGroups;
+  const int d4 = blockIdx.y * (kMergeThreads / kMergeGroups) + warp * (32 / kMergeGroups) + lane / kMergeGroups;
+  const bool active = d4 < p.head_dim / 4;
+  const float* src = p.o_part + row * p.row_stride + (size_t)d4 * 4;
+  // the rows of this lane's first kPrefetch pieces do not depend on the
+  // weights: their loads go out with the log-sum-exps'
+  float4 pre[kPrefetch];
+#pragma unroll
+  for (int i = 0; i < kPrefetch; ++i) {
+    const int s = g + i * kMergeGroups;
+    pre[i] = (active && s < S) ? *reinterpret_cast<const float4*>(src + (size_t)s * p.piece_stride)
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
   float M = -INFINITY;
   for (int s = lane; s < S; s += 32) M = fmaxf(M, lse[s * p.lse_piece_stride]);
 #pragma unroll
@@ -53,18 +67,26 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
 #pragma unroll
   for (int m = 16; m >= 1; m >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, m);
   const float inv = sum > 0.f ? 1.f / sum : 0.f;
-  const int D4 = p.head_dim / 4;
   if (p.out_lse && blockIdx.y == 0 && threadIdx.x == 0) p.out_lse[row] = sum > 0.f ? M + __logf(sum) : -INFINITY;
-  const int g = lane % kMergeGroups;
-  const int d4 = blockIdx.y * (kMergeThreads / kMergeGroups) + warp * (32 / kMergeGroups) + lane / kMergeGroups;
-  const bool active = d4 < D4;
-  const float* src = p.o_part + row * p.row_stride + (size_t)d4 * 4;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   if (active && M != -INFINITY) {
-#pragma unroll 4
-    for (int s = g; s < S; s += kMergeGroups) {
+    // an empty piece weighs 0 and its row may never have been written:
+    // selected out, not multiplied
+#pragma unroll
+    for (int i = 0; i < kPrefetch; ++i) {
+      const int s = g + i * kMergeGroups;
+      if (s >= S) break;
       const float ws = exp2f((lse[s * p.lse_piece_stride] - M) * kLog2e) * inv;
-      if (ws == 0.f) continue;  // an empty piece (its row may never have been written)
+      const bool use = ws != 0.f;
+      acc.x = use ? fmaf(ws, pre[i].x, acc.x) : acc.x;
+      acc.y = use ? fmaf(ws, pre[i].y, acc.y) : acc.y;
+      acc.z = use ? fmaf(ws, pre[i].z, acc.z) : acc.z;
+      acc.w = use ? fmaf(ws, pre[i].w, acc.w) : acc.w;
+    }
+#pragma unroll 4
+    for (int s = g + kPrefetch * kMergeGroups; s < S; s += kMergeGroups) {
+      const float ws = exp2f((lse[s * p.lse_piece_stride] - M) * kLog2e) * inv;
+      if (ws == 0.f) continue;
       const float4 o = *reinterpret_cast<const float4*>(src + (size_t)s * p.piece_stride);
       acc.x = fmaf(ws, o.x, acc.x);
       acc.y = fmaf(ws, o.y, acc.y);
