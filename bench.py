@@ -59,14 +59,14 @@ FALLBACK_HBM_GBS = 6800.0
 # pieces, hence the partials written); stale entries are ignored (the captures
 # and their commands are summarised under profiles/).
 NCU_TRAFFIC = {
-    "9ee344afd7342fa0": {"w4a": 1073913088 + 2816512, "w2": 67298816 + 530432, "w3": 68278016 + 413952,
-                         "w4a-fp8": 537301248 + 2789632, "w5global": 1596588544 + 4348928,
-                         "w5global-fp8": 798931456 + 4535808, "w5sliding": 68172032 + 553984},
+    "d1cfd00d281ecb47": {"w4a": 1073899264 + 2771968, "w2": 67295488 + 527872, "w3": 68277248 + 321024,
+                         "w4a-fp8": 537290240 + 2711296, "w5global": 1596576000 + 4366592,
+                         "w5global-fp8": 798929920 + 4851968, "w5sliding": 68174080 + 544000},
 }
 
 # the same for the fused QKV norm + RoPE + cache-write kernel (--op prepare)
 PREP_NCU_TRAFFIC = {
-    "78d6f35095226450": {"w2": 220928},
+    "d2ddd8d8f8c32361": {"w2": 221184},
 }
 
 STAGE1_SOURCES = ("stage1.cu", "pd_common.cuh", "pd_variants.h", "pd_kernels.h", "plan.cu")
