@@ -9,7 +9,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstring>
-#include <functional>
+#include <deque>
 #include <queue>
 #include <vector>
 
@@ -139,23 +139,27 @@ double cta_tokens_per_us(const pd::VariantInfo& v) {
   return kvs ? 165.5 : 74.7;
 }
 
-// Unit u's CTA i: its token count (<= 0: an empty range).
-using UnitTokens = std::function<long long(long long u, int i)>;
-
+// `tokens(u, i)`: unit u's CTA i's token count (<= 0: an empty range). Units
+// start at non-decreasing times and every CTA's fixed phase (and an empty
+// CTA's) has the same length, so the fixed phases, the empty CTAs and the
+// slots freed each end in the order they began: three FIFO queues; only the
+// streaming CTAs need a heap. Returns 1e300 as soon as the clock passes
+// `limit` by more than rounding (a launch that long cannot be the one chosen).
+template <class UnitTokens>
 double simulate_fluid(long long num_units, int ctas_per_unit, const UnitTokens& tokens, int slots, double tail_us,
-                      const CostModel& cm) {
-  struct Wall {
+                      const CostModel& cm, double limit = 1e300) {
+  struct Ev {
     double t;
-    long long u;   // unit
-    long long tok; // > 0: a CTA's fixed phase ends and it starts streaming; 0: a CTA is done; -1: a slot frees
-    bool operator>(const Wall& o) const { return t > o.t; }
+    long long u;
+    long long tok;
   };
   struct Stream {
     double v_end;  // service level (tokens per streaming CTA) at which it is done
     long long u;
     bool operator>(const Stream& o) const { return v_end > o.v_end; }
   };
-  std::priority_queue<Wall, std::vector<Wall>, std::greater<Wall>> wall;
+  std::deque<Ev> fixed_q, empty_q;  // a CTA's fixed phase ends / an empty CTA ends
+  std::deque<double> free_q;        // a slot frees
   std::priority_queue<Stream, std::vector<Stream>, std::greater<Stream>> streams;
   std::vector<int> left;  // CTAs of each started unit still running
   left.reserve((size_t)std::min<long long>(num_units, 1 << 20));
@@ -167,20 +171,24 @@ double simulate_fluid(long long num_units, int ctas_per_unit, const UnitTokens& 
     for (int i = 0; i < ctas_per_unit; ++i) {
       const long long n = tokens(u, i);
       if (n > 0)
-        wall.push({at + cm.cta_fixed_us, u, n});
+        fixed_q.push_back({at + cm.cta_fixed_us, u, n});
       else
-        wall.push({at + cm.empty_cta_us, u, 0});
+        empty_q.push_back({at + cm.empty_cta_us, u, 0});
     }
   };
   auto cta_done = [&](long long u) {
-    if (--left[(size_t)u] == 0) wall.push({t + tail_us, u, -1});
+    if (--left[(size_t)u] == 0) free_q.push_back(t + tail_us);
   };
   for (int s = 0; s < slots && next < num_units; ++s) start_unit(0.0);
-  while (!wall.empty() || !streams.empty()) {
+  while (!fixed_q.empty() || !empty_q.empty() || !free_q.empty() || !streams.empty()) {
+    if (t > limit * (1.0 + 1e-6)) return 1e300;
     const size_t n = streams.size();
     const double rate = n ? cm.per_cta_rate[std::min(n, cm.per_cta_rate.size() - 1)] : 0.0;
     const double t_stream = n ? t + (streams.top().v_end - level) / rate : 1e300;
-    const double t_wall = wall.empty() ? 1e300 : wall.top().t;
+    const double t_fixed = fixed_q.empty() ? 1e300 : fixed_q.front().t;
+    const double t_empty = empty_q.empty() ? 1e300 : empty_q.front().t;
+    const double t_free = free_q.empty() ? 1e300 : free_q.front();
+    const double t_wall = std::min(t_fixed, std::min(t_empty, t_free));
     if (n && t_stream <= t_wall) {
       t = std::max(t, t_stream);
       level = streams.top().v_end;
@@ -189,15 +197,17 @@ double simulate_fluid(long long num_units, int ctas_per_unit, const UnitTokens& 
       cta_done(u);
       continue;
     }
-    const Wall e = wall.top();
-    wall.pop();
-    if (n) level += rate * (e.t - t);
-    t = std::max(t, e.t);
-    if (e.tok > 0) {
-      streams.push({level + (double)e.tok, e.u});
-    } else if (e.tok == 0) {
-      cta_done(e.u);
+    if (n) level += rate * (t_wall - t);
+    t = std::max(t, t_wall);
+    if (t_wall == t_fixed) {
+      streams.push({level + (double)fixed_q.front().tok, fixed_q.front().u});
+      fixed_q.pop_front();
+    } else if (t_wall == t_empty) {
+      const long long u = empty_q.front().u;
+      empty_q.pop_front();
+      cta_done(u);
     } else {
+      free_q.pop_front();
       makespan = std::max(makespan, t);
       if (next < num_units) start_unit(t);
     }
@@ -214,23 +224,26 @@ long long piece_tokens(int n, int chunk, int splits, int s) {
 
 // One launch with a CTA per (request, KV head CTA, piece), then the merge launch.
 double simulate(const std::vector<int>& n_tok, int hkv, int chunk, int splits, const CostModel& cm,
-                uint64_t merge_bytes) {
+                uint64_t merge_bytes, double limit = 1e300) {
   const long long units = (long long)n_tok.size() * hkv * splits;
-  auto tok = [&](long long u, int) { return piece_tokens(n_tok[(size_t)(u / ((long long)hkv * splits))], chunk, splits, (int)(u % splits)); };
-  double makespan = simulate_fluid(units, 1, tok, cm.slots, 0.0, cm);
-  if (splits > 1) makespan += cm.merge_fixed_us + merge_bytes * cm.merge_us_per_byte;
-  return makespan;
+  auto tok = [&](long long u, int) {
+    return piece_tokens(n_tok[(size_t)(u / ((long long)hkv * splits))], chunk, splits, (int)(u % splits));
+  };
+  const double merge_us = splits > 1 ? cm.merge_fixed_us + merge_bytes * cm.merge_us_per_byte : 0.0;
+  const double makespan = simulate_fluid(units, 1, tok, cm.slots, 0.0, cm, limit - merge_us);
+  return makespan >= 1e300 ? 1e300 : makespan + merge_us;
 }
 
 // The same launch with the S pieces of each (request, KV head) run as one
 // thread-block cluster, merged in the cluster: only cluster_slots(S) clusters
 // are resident at a time.
-double simulate_clusters(const std::vector<int>& n_tok, int hkv, int chunk, int splits, const CostModel& cm) {
+double simulate_clusters(const std::vector<int>& n_tok, int hkv, int chunk, int splits, const CostModel& cm,
+                         double limit = 1e300) {
   const int cl_slots = cluster_slots(splits, cm.slots);
   if (cl_slots <= 0) return 1e300;
   const long long units = (long long)n_tok.size() * hkv;
   auto tok = [&](long long u, int i) { return piece_tokens(n_tok[(size_t)(u / hkv)], chunk, splits, i); };
-  return simulate_fluid(units, splits, tok, cl_slots, cm.cluster_merge_us, cm);
+  return simulate_fluid(units, splits, tok, cl_slots, cm.cluster_merge_us, cm, limit);
 }
 
 }  // namespace
@@ -386,16 +399,65 @@ pd_status plan_impl(const pd_layer_desc* layer, int32_t batch, int32_t query_tok
     cands.push_back(c_max);
     std::sort(cands.begin(), cands.end());
     cands.erase(std::unique(cands.begin(), cands.end()), cands.end());
+    // A launch lasts at least as long as all its tokens take at the memory's
+    // rate, and as its longest piece takes at one CTA's rate after the fixed
+    // start (the model's shared rate is below both); a candidate whose bound
+    // exceeds the best cost so far cannot be chosen, so it is not simulated.
+    // The "exactly w waves" sizes, usually near the best, seed that cost.
+    const double total_tok = (double)total * hkv_ctas;
+    auto merge_bytes_of = [&](int s) {
+      return (uint64_t)batch * T * ly.num_q_heads * s * (ly.head_dim + 1) * 4ull * 2ull;
+    };
+    auto stream_bound = [&](int c) {
+      return std::max(total_tok / cm.hbm_tok_per_us, cm.cta_fixed_us + std::min(c, max_n) / cm.cap_tok_per_us);
+    };
+    // and, each CTA holding its slot for at least its fixed start plus its
+    // tokens at one CTA's rate, at least the sum of those over the slots (a
+    // cluster: its longest piece, and its merge)
+    auto slot_bound = [&](int c, int s) {
+      double direct = 0.0, clustered = 0.0;
+      for (int b = 0; b < batch; ++b) {
+        const int busy = n_tok[b] > 0 ? std::min(s, (n_tok[b] + c - 1) / c) : 0;
+        direct += busy * cm.cta_fixed_us + (s - busy) * cm.empty_cta_us;
+        clustered += (n_tok[b] > 0 ? cm.cta_fixed_us + std::min(c, n_tok[b]) / cm.cap_tok_per_us : cm.empty_cta_us) +
+                     cm.cluster_merge_us;
+      }
+      direct = (direct * hkv_ctas + total_tok / cm.cap_tok_per_us) / cm.slots;
+      const int cl_slots = cluster_slots(s, cm.slots);
+      clustered = cl_slots > 0 ? clustered * hkv_ctas / cl_slots : 1e300;
+      return std::make_pair(direct, clustered);
+    };
+    auto may_cluster = [&](int s) { return !partial && s >= 2 && s <= std::min(kMaxClusterSplits, v->max_cluster); };
     double best = 1e300;
+    for (int w = 1; w <= 2; ++w) {
+      const long long pairs = (long long)batch * hkv_ctas;
+      const long long sw = std::max<long long>(1, (long long)w * cm.slots / std::max<long long>(1, pairs));
+      const int c = (int)align_up((uint64_t)((max_n + sw - 1) / sw), unit);
+      const int s = (max_n + c - 1) / c;
+      if (c < 16 || s > kMaxSplits) continue;
+      best = std::min(best, simulate(n_tok, hkv_ctas, c, s, cm, merge_bytes_of(s)));
+      if (may_cluster(s)) best = std::min(best, simulate_clusters(n_tok, hkv_ctas, c, s, cm));
+    }
+    const double seed = best;
+    best = 1e300;
     for (int c : cands) {
       if (c < 16) continue;
       const int s = (max_n + c - 1) / c;
       if (s > kMaxSplits) continue;
-      const uint64_t merge_bytes = (uint64_t)batch * T * ly.num_q_heads * s * (ly.head_dim + 1) * 4ull * 2ull;
-      double cost = simulate(n_tok, hkv_ctas, c, s, cm, merge_bytes);
+      const uint64_t merge_bytes = merge_bytes_of(s);
+      const auto slots_b = slot_bound(c, s);
+      const double merge_us = s > 1 ? cm.merge_fixed_us + merge_bytes * cm.merge_us_per_byte : 0.0;
+      const double bound_direct = std::max(stream_bound(c), slots_b.first) + merge_us;
+      const double bound_cluster = std::max(stream_bound(c) + cm.cluster_merge_us, slots_b.second);
+      // (the margin keeps rounding from dropping a candidate that ties the best)
+      const double limit = std::min(best, seed);
+      const double prune_at = limit * (1.0 + 1e-6);
+      const bool try_cluster = may_cluster(s) && bound_cluster <= prune_at;
+      if (bound_direct > prune_at && !try_cluster) continue;
+      double cost = bound_direct > prune_at ? 1e300 : simulate(n_tok, hkv_ctas, c, s, cm, merge_bytes, limit);
       bool cluster = false;
-      if (!partial && s >= 2 && s <= std::min(kMaxClusterSplits, v->max_cluster)) {
-        const double cc = simulate_clusters(n_tok, hkv_ctas, c, s, cm);
+      if (try_cluster) {
+        const double cc = simulate_clusters(n_tok, hkv_ctas, c, s, cm, limit);
         if (cc < cost) {
           cost = cc;
           cluster = true;
