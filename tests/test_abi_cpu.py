@@ -316,6 +316,20 @@ def test_plans_edited_past_their_workspace_are_refused(lib):
     assert launch(one, ws_bytes=1 << 20) == b.PD_ERR_INVALID_ARG
 
 
+@pytest.mark.parametrize("lens,Hq,Hkv,d,window,want", [
+    ([32768] * 4, 16, 4, 512, 0, (9, 3648, 1)),     # one wave of 144 CTAs, then the merge kernel
+    ([65536] * 2, 16, 4, 512, 0, (19, 3456, 1)),    # one wave of 152
+    ([131072], 16, 4, 512, 0, (38, 3456, 1)),
+    ([1024] * 8, 16, 4, 512, 0, (4, 256, 2)),       # clusters of 4 (36 fit at once: all 32 run together)
+    ([256], 8, 2, 512, 0, (4, 64, 2)),
+    ([4100] * 8, 16, 8, 256, 1024, (2, 544, 2)),    # pieces of whole two-block stages
+])
+def test_planner_choices_on_the_measured_workloads(lib, lens, Hq, Hkv, d, window, want):
+    """The plans the measured steps ran (152 SMs): pieces, piece size, merge mode."""
+    pl = _plan(lens, Hq=Hq, Hkv=Hkv, d=d, window=window, pages=10 ** 6, sms=152)
+    assert (pl.num_splits, pl.chunk_tokens, pl.merge_mode) == want
+
+
 def test_planner_invariants_on_random_shapes(lib):
     """300 seeded random layer shapes and batches, decode / multi-token / partial
     plans, bf16 and FP8: every plan covers every attended token, its grid and
