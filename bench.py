@@ -55,13 +55,20 @@ L2_BYTES = 129 * 1000 * 1000
 FALLBACK_HBM_GBS = 6800.0
 
 # DRAM bytes (read + write) per stage-1 launch from an ncu capture, keyed by the
-# hash of the kernel and planner sources it was taken on (the plan sets the
-# pieces, hence the partials written); stale entries are ignored (the captures
+# hash of the kernel sources it was taken on, each with the plan that launch ran
+# (pieces, tokens per piece, merge mode: they set the partials written); an
+# entry whose sources or plan differ from the run's is not used (the captures
 # and their commands are summarised under profiles/).
 NCU_TRAFFIC = {
-    "d1cfd00d281ecb47": {"w4a": 1073899264 + 2771968, "w2": 67295488 + 527872, "w3": 68277248 + 321024,
-                         "w4a-fp8": 537290240 + 2711296, "w5global": 1596576000 + 4366592,
-                         "w5global-fp8": 798929920 + 4851968, "w5sliding": 68174080 + 544000},
+    "6551688c2f7560a0": {
+        "w4a": (1073899264 + 2771968, (9, 3648, 1)),
+        "w2": (67295488 + 527872, (4, 256, 2)),
+        "w3": (68277248 + 321024, (2, 544, 2)),
+        "w4a-fp8": (537290240 + 2711296, (9, 3648, 1)),
+        "w5global": (1596576000 + 4366592, (19, 5456, 1)),
+        "w5global-fp8": (798929920 + 4851968, (19, 5456, 1)),
+        "w5sliding": (68174080 + 544000, (2, 544, 2)),
+    },
 }
 
 # the same for the fused QKV norm + RoPE + cache-write kernel (--op prepare)
@@ -69,7 +76,7 @@ PREP_NCU_TRAFFIC = {
     "d2ddd8d8f8c32361": {"w2": 221184},
 }
 
-STAGE1_SOURCES = ("stage1.cu", "pd_common.cuh", "pd_variants.h", "pd_kernels.h", "plan.cu")
+STAGE1_SOURCES = ("stage1.cu", "pd_common.cuh", "pd_variants.h", "pd_kernels.h")
 
 
 PREP_SOURCES = ("prepare.cu", "pd_common.cuh", "pd_variants.h")
@@ -431,8 +438,10 @@ def run_ours(args, world, rank, local):
     achieved = alg_bytes / (s1_us * 1e-6) / 1e9
     kv_gbs = touched / (us_per_step * 1e-6) / 1e9
     src_hash = kernel_source_hash()
-    traffic = NCU_TRAFFIC.get(src_hash, {}).get(
+    captured = NCU_TRAFFIC.get(src_hash, {}).get(
         f"w{args.workload}{args.part or ''}{'-fp8' if fp8 else ''}{f'-t{T}' if T > 1 else ''}")
+    run_plan = (int(plan.num_splits), int(plan.chunk_tokens), int(plan.merge_mode))
+    traffic = captured[0] if captured is not None and tuple(captured[1]) == run_plan else None
 
 
     # end to end: every step copies its inputs (q, block table, seq_lens) from
