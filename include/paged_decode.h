@@ -167,10 +167,11 @@ typedef struct {
  *                 later call whose lengths do not exceed max(seq_lens_host)
  *   sm_count      streaming multiprocessors of the target GPU (> 0)
  *   plan          output
- * Groups (Hq / Hkv) of 1..16 are served: up to 8 by one CTA per (request, KV
- * head, piece) that reads each KV byte once for all query heads; 9..16 by
- * CTAs of 8 query heads each (two per KV head, each reading the KV head's
- * pages; head_dim 256 or 512).
+ * Groups (Hq / Hkv) of 1..16 are served: 1, 2, 4 and 8 by one CTA per
+ * (request, KV head, piece) that reads each KV byte once for all query heads;
+ * the others by CTAs of 8-column tiles of query heads (3, 5, 6, 7: one tile;
+ * 9..16: two, a CTA each over short contexts, one CTA for both over long ones;
+ * head_dim 256 or 512 -- at head_dim 128 only 1, 2, 4 and 8).
  * Returns PD_ERR_INVALID_ARG for a malformed shape or length, PD_ERR_UNSUPPORTED
  * for a head_dim or group size this build has no kernel for (group > 16).
  */

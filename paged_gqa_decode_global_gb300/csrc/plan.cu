@@ -54,11 +54,11 @@ constexpr int kMaxQueryTokens = 256;
 // Largest GQA group (query heads per KV head) a plan accepts.
 constexpr int kMaxGroup = 16;
 
-// Decode (one query token) with a group of at most 8: the instance of exactly
-// this group. Several query tokens, or a group of 9..16: the column-tiled
-// instance (CTAs of 8 columns of (token, head) pairs), which serves any group
-// up to kMaxGroup.
-bool tiled(int query_tokens, int group) { return query_tokens > 1 || group > 8; }
+// Decode (one query token) with a group of 1, 2, 4 or 8: the instance of
+// exactly this group. Several query tokens, or any other group up to
+// kMaxGroup (3, 5..7, 9..16): the column-tiled instance (CTAs of 8 columns of
+// (token, head) pairs), which takes the group at run time.
+bool tiled(int query_tokens, int group) { return query_tokens > 1 || group > 8 || (group & (group - 1)) != 0; }
 
 // Column-tiled plans with more than one 8-column tile use, over a bf16 cache,
 // the instances whose CTA serves two tiles from one ring (one copy of every

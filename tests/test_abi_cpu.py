@@ -330,6 +330,20 @@ def test_planner_choices_on_the_measured_workloads(lib, lens, Hq, Hkv, d, window
     assert (pl.num_splits, pl.chunk_tokens, pl.merge_mode) == want
 
 
+@pytest.mark.parametrize("G", [3, 5, 6, 7])
+def test_groups_between_the_decode_instances_are_served(lib, G):
+    """Groups without an instance of their own (3, 5, 6, 7) go to the column-
+    tiled instances at one query token as well: one CTA of 8 columns per KV
+    head; head_dim 128 has no such instance."""
+    for d, window, kvs, fp8 in [(512, 0, False, False), (256, 1024, True, False), (512, 37, False, True)]:
+        desc = b.layer_desc(4 * G, 4, d, 16, 10 ** 5, 2000, window, kvs, b.PD_KV_FP8_E4M3 if fp8 else b.PD_KV_BF16)
+        pl = b.paged_decode_plan(desc, [3000, 40, 0], 152)
+        assert pl.grid_y == 4 and pl.query_tokens == 1
+    with pytest.raises(b.PagedDecodeError) as e:
+        b.paged_decode_plan(b.layer_desc(4 * G, 4, 128, 16, 10 ** 5, 2000), [3000], 152)
+    assert e.value.status == b.PD_ERR_UNSUPPORTED
+
+
 def test_planner_invariants_on_random_shapes(lib):
     """300 seeded random layer shapes and batches, decode / multi-token / partial
     plans, bf16 and FP8: every plan covers every attended token, its grid and
@@ -341,7 +355,7 @@ def test_planner_invariants_on_random_shapes(lib):
     for _ in range(300):
         d, window = shapes[rng.integers(len(shapes))]
         Hkv = int(rng.choice([1, 2, 4, 8]))
-        G = int(rng.choice([1, 2, 4, 8, 12, 16] if d != 128 else [1, 2, 4, 8]))
+        G = int(rng.choice([1, 2, 3, 4, 6, 8, 12, 16] if d != 128 else [1, 2, 4, 8]))
         kvs = bool(rng.integers(2))
         fp8 = d != 128 and bool(rng.integers(2))
         T = 1 if d == 128 or rng.random() < 0.6 else int(rng.integers(2, 9))

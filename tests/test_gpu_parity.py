@@ -131,6 +131,39 @@ def test_groups_above_8_ragged(d, G, kvs, window, long):
         assert 0 in modes and len(modes) >= 2, modes
 
 
+@pytest.mark.parametrize("d,G,kvs", [(512, 3, False), (512, 6, True), (256, 5, False), (256, 7, True)])
+@pytest.mark.parametrize("window", [0, 37, 1000])
+def test_groups_between_the_decode_instances_ragged(d, G, kvs, window):
+    """Groups of 3, 5, 6 and 7 query heads per KV head (no decode instance of
+    their own: one 8-column tile per KV head): ragged lengths with an empty
+    request, windows, one piece / cluster merge / merge kernel."""
+    Hkv = 2
+    lens = [1, 17, 300, 0, 1000, 33, 3000]
+    li = synth.make_layer("gm", lens, Hkv * G, Hkv, d, window=window, kv_shared=kvs,
+                          pool_pages=sum((L + 15) // 16 for L in lens) + 5, seed=11 * d + G + 100 * kvs + window,
+                          device="cuda")
+    ref = run_oracle(li)
+    modes = set()
+    for sms in (1, 3, 40, 152, 1000):
+        out, step = run_gpu(li, sm_count=sms)
+        assert step.plan.grid_y == Hkv
+        modes.add(int(step.plan.merge_mode))
+        compare(out, ref, li, f"d{d} G{G} kvs{kvs} W{window} sms{sms} S{step.plan.num_splits}")
+    if window == 1000:
+        assert modes == {0, 1, 2}, modes
+
+
+@pytest.mark.parametrize("G", [3, 6])
+def test_groups_between_the_decode_instances_over_fp8(G):
+    li = synth.make_layer("gm8", [1, 17, 300, 1000, 33], 2 * G, 2, 512, window=37,
+                          pool_pages=100, seed=90 + G, device="cuda")
+    f = synth.quantize_kv_fp8(li)
+    ref = run_oracle_fp8(f)
+    for sms in (3, 152):
+        out, step = run_gpu(f, sm_count=sms)
+        compare(out, ref, f, f"fp8 G{G} sms{sms} S{step.plan.num_splits}")
+
+
 def test_group_16_single_token_is_bit_exact():
     li = synth.make_layer("one16", [1, 1], 32, 2, 512, pool_pages=5, seed=13, device="cuda")
     out, _ = run_gpu(li)
