@@ -51,6 +51,17 @@ def _cases(n=120, seed=20261203):
 CASES = _cases()
 
 
+def _cases_pages(n=80, seed=20261204):
+    """The same draws plus the page size (16..64 tokens: pages of one to four
+    16-token blocks, an e4m3 scale per page) and the plan's early_kv flag."""
+    rng = np.random.default_rng(seed)
+    base = _cases(n, seed)
+    return [c + (int(rng.choice([16, 32, 48, 64])), bool(rng.integers(2))) for c in base]
+
+
+CASES_PAGES = _cases_pages()
+
+
 def _compare(got, ref, empty_rows, tag):
     got = got.float().cpu().numpy().astype(np.float64)
     assert np.isfinite(got).all(), f"{tag}: non-finite output"
@@ -71,16 +82,26 @@ def _case_id(c):
 
 @pytest.mark.parametrize("case", CASES, ids=[_case_id(c) for c in CASES])
 def test_random_shape_matches_oracle(case):
-    d, G, Hkv, kvs, fp8, T, window, lens, sms = case
+    _run_case(*case)
+
+
+@pytest.mark.parametrize("case", CASES_PAGES,
+                         ids=[_case_id(c[:9]) + f"-P{c[9]}-early{int(c[10])}" for c in CASES_PAGES])
+def test_random_shape_with_page_size_and_early_kv_matches_oracle(case):
+    _run_case(*case)
+
+
+def _run_case(d, G, Hkv, kvs, fp8, T, window, lens, sms, P=16, early=False):
     Hq = G * Hkv
     li = synth.make_layer("rnd", lens, Hq, Hkv, d, window=window, kv_shared=kvs,
-                          pool_pages=sum((L + 15) // 16 for L in lens) + 3,
+                          pool_pages=sum((L + P - 1) // P for L in lens) + 3, page_size=P,
                           seed=d + 7 * G + 31 * T + window + len(lens), device="cuda")
     g = torch.Generator(device="cuda").manual_seed(sms + T)
     q = li.q if T == 1 else (torch.randn(len(lens), T, Hq, d, generator=g, device="cuda")).to(torch.bfloat16)
     kv_dtype = b.PD_KV_FP8_E4M3 if fp8 else b.PD_KV_BF16
     desc = b.layer_desc(Hq, Hkv, d, li.page_size, li.num_pages, li.block_tables.shape[1], window, kvs, kv_dtype)
     plan = b.paged_decode_plan_multi(desc, T, lens, sms) if T > 1 else b.paged_decode_plan(desc, lens, sms)
+    plan.early_kv = int(early)
     ws = torch.zeros(max(256, int(plan.workspace_bytes)), dtype=torch.uint8, device="cuda")
     out = torch.full_like(q, float("nan"))
     if fp8:
@@ -94,7 +115,7 @@ def test_random_shape_matches_oracle(case):
         fn(*args, *((window,) if window > 0 else ()), li.scale, ws, out)
     b.paged_decode_merge(plan, ws, out)
     assert b.paged_decode_check_device_error(plan, ws) == 0
-    tag = f"S={plan.num_splits} mode={plan.merge_mode}"
+    tag = f"S={plan.num_splits} mode={plan.merge_mode} P={P}"
 
     tables, seq = li.block_tables.cpu().numpy(), li.seq_lens.cpu().numpy()
     if fp8:
