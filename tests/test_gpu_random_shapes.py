@@ -141,3 +141,60 @@ def _run_case(d, G, Hkv, kvs, fp8, T, window, lens, sms, P=16, early=False):
     if T == 1:
         empty[np.array(lens) == 0] = True
     _compare(out, ref, empty, tag)
+
+
+def _cases_sharded(n=40, seed=20261205):
+    """Sequence-sharded decode: R virtual ranks each run the partial decode over
+    their shard of the cache; the kernel combines the stacked partials."""
+    from paged_gqa_decode_global_gb300 import dcp
+    rng = np.random.default_rng(seed)
+    out = []
+    while len(out) < n:
+        d = int(rng.choice([256, 512]))
+        G = int(rng.choice([1, 2, 3, 4, 8, 12, 16]))
+        Hkv = int(rng.choice([1, 2, 4]))
+        kvs = bool(rng.random() < 0.4)
+        B = int(rng.integers(1, 6))
+        lens = [int(x) for x in np.exp(rng.uniform(0.0, np.log(8000), B))]
+        if rng.random() < 0.3:
+            lens[int(rng.integers(B))] = 0
+        R = int(rng.integers(1, 5))
+        mode = str(rng.choice(dcp.MODES))
+        sms = int(rng.choice([3, 40, 152, 1000]))
+        if B * G * Hkv * max(lens) > 3_000_000:
+            continue
+        out.append((d, G, Hkv, kvs, lens, R, mode, sms))
+    return out
+
+
+CASES_SHARDED = _cases_sharded()
+
+
+def _sharded_id(c):
+    d, G, Hkv, kvs, lens, R, mode, sms = c
+    return f"d{d}-G{G}-Hkv{Hkv}-{'kvs' if kvs else 'kv'}-B{len(lens)}-R{R}-{mode}-sm{sms}"
+
+
+@pytest.mark.parametrize("case", CASES_SHARDED, ids=[_sharded_id(c) for c in CASES_SHARDED])
+def test_random_sharded_decode_matches_oracle(case):
+    from paged_gqa_decode_global_gb300 import dcp
+    d, G, Hkv, kvs, lens, R, mode, sms = case
+    li = synth.make_layer("rsh", lens, G * Hkv, Hkv, d, kv_shared=kvs,
+                          pool_pages=sum((L + 15) // 16 for L in lens) + 3,
+                          seed=d + G + 13 * R + len(lens), device="cuda")
+    os_, lses = [], []
+    for r in range(R):
+        k, v, table, shard_lens = dcp.shard_cache(li.k_pool, li.v_pool, li.block_tables, lens, R, r, mode)
+        desc = b.layer_desc(li.num_q_heads, Hkv, d, li.page_size, k.shape[0], table.shape[1], 0, kvs)
+        step = dcp.PartialStep(desc, shard_lens.tolist(), sms, "cuda")
+        o, lse = step(li.q, k, v, table, shard_lens, li.scale)
+        os_.append(o)
+        lses.append(lse)
+    out = dcp.combine(torch.stack(os_), torch.stack(lses))
+    torch.cuda.synchronize()
+    ref = oracle.decode(synth.bits_u16(li.q), synth.bits_u16(li.k_pool),
+                        None if li.v_pool is None else synth.bits_u16(li.v_pool), li.block_tables.cpu().numpy(),
+                        li.seq_lens.cpu().numpy(), li.scale, 0)
+    empty = np.zeros(tuple(li.q.shape[:-1]), dtype=bool)
+    empty[np.array(lens) == 0] = True
+    _compare(out, ref, empty, f"R={R} {mode}")
