@@ -106,8 +106,44 @@ def test_rope_table_matches_oracle(rot, theta, n_pos):
     assert np.abs(got - exp).max() <= 2.0 ** -24 + 1e-10
 
 
+def _random_layers(n=30, seed=20261206):
+    """Seeded random shapes of the step before decode: head_dim, groups 1..16,
+    K=V, page sizes of 16..64 tokens, rotary dims from none to the whole head,
+    windows, ragged lengths."""
+    rng = np.random.default_rng(seed)
+    out = []
+    while len(out) < n:
+        d = int(rng.choice([256, 512]))
+        Hkv = int(rng.choice([1, 2, 4, 8]))
+        G = int(rng.choice([1, 2, 3, 4, 8, 16]))
+        kvs = bool(rng.random() < 0.4)
+        P = int(rng.choice([16, 32, 48, 64]))
+        rot = int(rng.choice([0, 2, 64, d // 4, d // 2, d]))
+        theta = float(rng.choice([100.0, 1e4, 1e6]))
+        window = int(rng.choice([0, 1024]))
+        B = int(rng.integers(1, 7))
+        lens = [max(1, int(x)) for x in np.exp(rng.uniform(0.0, np.log(5000), B))]
+        if B * max(lens) * Hkv * d > 40_000_000:  # keeps the host-side pools small
+            continue
+        name = f"rnd{len(out)} d{d} G{G} Hkv{Hkv} kvs{int(kvs)} P{P} rot{rot} W{window}"
+        out.append((name, lens, G * Hkv, Hkv, d, window, kvs, P, rot, theta))
+    return out
+
+
+RANDOM_LAYERS = _random_layers()
+
+
 @pytest.mark.parametrize("case", LAYERS, ids=[c[0] for c in LAYERS])
 def test_prepare_matches_oracle(case):
+    _check_prepare(case)
+
+
+@pytest.mark.parametrize("case", RANDOM_LAYERS, ids=[c[0] for c in RANDOM_LAYERS])
+def test_prepare_random_shapes_match_oracle(case):
+    _check_prepare(case)
+
+
+def _check_prepare(case):
     pi = _make(*case)
     li = pi.layer
     g = GpuPrepare(pi)
