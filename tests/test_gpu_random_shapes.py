@@ -75,6 +75,31 @@ def _compare(got, ref, empty_rows, tag):
     assert cos > MIN_COS, f"{tag}: cosine {cos:.7f}"
 
 
+def _cases_big_batch(n=20, seed=20261207):
+    """Batches of 16..256 short requests: many (request, KV head) pairs, the
+    planner's few-pieces end, a launch grid deep in its third dimension."""
+    rng = np.random.default_rng(seed)
+    out = []
+    while len(out) < n:
+        d = int(rng.choice([256, 512]))
+        fp8 = rng.random() < 0.3
+        T = 1 if rng.random() < 0.6 else int(rng.choice([2, 4]))
+        G = int(rng.choice([1, 2, 4, 8, 16]))
+        Hkv = int(rng.choice([1, 2, 4]))
+        kvs = bool(rng.random() < 0.4)
+        window = int(rng.choice([0, 0, 256]))
+        B = int(rng.integers(16, 257))
+        lens = [max(T, int(x)) for x in np.exp(rng.uniform(0.0, np.log(2000), B))]
+        sms = int(rng.choice([40, 152, 1000]))
+        if B * T * G * Hkv * max(lens) > 6_000_000:
+            continue
+        out.append((d, G, Hkv, kvs, fp8, T, window, lens, sms))
+    return out
+
+
+CASES_BIG_BATCH = _cases_big_batch()
+
+
 def _case_id(c):
     d, G, Hkv, kvs, fp8, T, window, lens, sms = c
     return f"d{d}-G{G}-Hkv{Hkv}-{'kvs' if kvs else 'kv'}-{'fp8' if fp8 else 'bf16'}-T{T}-W{window}-B{len(lens)}-sm{sms}"
@@ -88,6 +113,11 @@ def test_random_shape_matches_oracle(case):
 @pytest.mark.parametrize("case", CASES_PAGES,
                          ids=[_case_id(c[:9]) + f"-P{c[9]}-early{int(c[10])}" for c in CASES_PAGES])
 def test_random_shape_with_page_size_and_early_kv_matches_oracle(case):
+    _run_case(*case)
+
+
+@pytest.mark.parametrize("case", CASES_BIG_BATCH, ids=[_case_id(c) for c in CASES_BIG_BATCH])
+def test_random_big_batch_matches_oracle(case):
     _run_case(*case)
 
 
