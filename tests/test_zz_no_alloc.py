@@ -113,3 +113,64 @@ def test_noalloc_rejects_plans_beyond_its_scratch():
     assert e.value.status == b.PD_ERR_WORKSPACE_TOO_SMALL
     torch.cuda.synchronize()
     assert (out == 0).all()
+
+
+def _random_cases(n=20, seed=20261208):
+    """Seeded random bf16 shapes (head_dim, group 1..16, K=V, 1..4 query
+    tokens, windows, ragged requests, the SM count the plan is sized for)
+    whose plans fit the 8 MiB scratch array."""
+    rng = np.random.default_rng(seed)
+    out = []
+    while len(out) < n:
+        d = int(rng.choice([256, 512]))
+        G = int(rng.choice([1, 2, 3, 4, 8, 12, 16]))
+        Hkv = int(rng.choice([1, 2, 4]))
+        kvs = bool(rng.random() < 0.4)
+        T = 1 if rng.random() < 0.6 else int(rng.choice([2, 4]))
+        window = int(rng.choice([0, 0, 37, 1024]))
+        B = int(rng.integers(1, 7))
+        lens = [max(T, int(x)) for x in np.exp(rng.uniform(0.0, np.log(6000), B))]
+        sms = int(rng.choice([3, 40, 152, 1000]))
+        if B * T * G * Hkv * max(lens) > 3_000_000:
+            continue
+        desc = b.layer_desc(G * Hkv, Hkv, d, 16, sum((L + 15) // 16 for L in lens) + 3,
+                            max((L + 15) // 16 for L in lens), window, kvs)
+        plan = b.paged_decode_plan_multi(desc, T, lens, sms) if T > 1 else b.paged_decode_plan(desc, lens, sms)
+        if plan.workspace_bytes > 8 << 20:
+            continue
+        out.append((d, G, Hkv, kvs, T, window, lens, sms))
+    return out
+
+
+def _random_id(c):
+    d, G, Hkv, kvs, T, window, lens, sms = c
+    return f"d{d}-G{G}-Hkv{Hkv}-kvs{int(kvs)}-T{T}-W{window}-B{len(lens)}-sm{sms}"
+
+
+@pytest.mark.parametrize("case", _random_cases(), ids=_random_id)
+def test_noalloc_random_shapes_match_oracle_twice(case):
+    d, G, Hkv, kvs, T, window, lens, sms = case
+    li = synth.make_layer("nar", lens, G * Hkv, Hkv, d, window=window, kv_shared=kvs,
+                          pool_pages=sum((L + 15) // 16 for L in lens) + 3, seed=d + G + T + len(lens),
+                          device="cuda")
+    desc = b.layer_desc(G * Hkv, Hkv, d, 16, li.num_pages, li.block_tables.shape[1], window, kvs)
+    plan = b.paged_decode_plan_multi(desc, T, lens, sms) if T > 1 else b.paged_decode_plan(desc, lens, sms)
+    gen = torch.Generator(device="cuda").manual_seed(5 + sms)
+    flags = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    kp = synth.bits_u16(li.k_pool)
+    vp = None if li.v_pool is None else synth.bits_u16(li.v_pool)
+    tables, seq = li.block_tables.cpu().numpy(), li.seq_lens.cpu().numpy()
+    for call in range(2):
+        q = (torch.randn((len(lens), T, G * Hkv, d) if T > 1 else tuple(li.q.shape), generator=gen,
+                         device="cuda")).to(torch.bfloat16)
+        out = torch.full_like(q, float("nan"))
+        b.paged_decode_noalloc(plan, q, li.k_pool, li.v_pool, li.block_tables, li.seq_lens, window, li.scale, out,
+                               device_flags=flags)
+        torch.cuda.synchronize()
+        assert int(flags.item()) == 0, f"call {call}: device flags {int(flags.item()):#x}"
+        if T == 1:
+            ref = oracle.decode(synth.bits_u16(q), kp, vp, tables, seq, li.scale, window)
+        else:
+            ref = oracle.decode_multi(synth.bits_u16(q.cpu()), kp, vp, tables, seq, li.scale, window)
+        _close(out.float().cpu().numpy().astype(np.float64), ref, f"call {call}, S={plan.num_splits} "
+               f"mode={plan.merge_mode}")
