@@ -480,3 +480,60 @@ def test_one_workspace_serves_changing_plans():
             b.paged_decode_merge(plan, ws, out)
             assert b.paged_decode_check_device_error(plan, ws) == 0
             compare(out, run_oracle(li), li, f"rep {rep} mode {plan.merge_mode} S={plan.num_splits}")
+
+
+@pytest.mark.parametrize("d,G,kvs,window,T,fp8", [(512, 4, False, 0, 1, False), (512, 4, True, 0, 1, False),
+                                                  (256, 2, False, 1024, 1, False), (512, 4, False, 0, 3, False),
+                                                  (256, 8, False, 37, 2, False), (512, 4, False, 0, 1, True),
+                                                  (256, 2, True, 1024, 1, True)])
+@pytest.mark.parametrize("sms", [3, 40, 152, 1000])
+def test_plan_made_for_longer_lengths_serves_shorter_ones(d, G, kvs, window, T, fp8, sms):
+    """A plan stays valid for any later step whose lengths do not exceed the
+    ones it was made for: planned with headroom (lengths + 2000), run on the
+    actual lengths (a request one token long, an empty one when decoding one
+    token), against the oracle at the actual lengths."""
+    Hkv = 2
+    lens = [max(T, L) for L in [4100, 1, 777, 0, 3000]] if T > 1 else [4100, 1, 777, 0, 3000]
+    plan_lens = [L + 2000 for L in lens]
+    li = synth.make_layer("hr", lens, Hkv * G, Hkv, d, window=window, kv_shared=kvs,
+                          pool_pages=sum((L + 15) // 16 for L in lens) + 3, seed=d + G + window + T + 7 * fp8,
+                          device="cuda")
+    desc = b.layer_desc(Hkv * G, Hkv, d, 16, li.num_pages, (max(plan_lens) + 15) // 16, window, kvs,
+                        b.PD_KV_FP8_E4M3 if fp8 else b.PD_KV_BF16)
+    plan = b.paged_decode_plan_multi(desc, T, plan_lens, sms) if T > 1 else b.paged_decode_plan(desc, plan_lens, sms)
+    # the block table is as wide as the plan's layer says: pad the rows
+    table = torch.zeros(len(lens), desc.max_pages_per_seq, dtype=torch.int32, device="cuda")
+    table[:, :li.block_tables.shape[1]] = li.block_tables
+    g = torch.Generator(device="cuda").manual_seed(3 + sms)
+    q = li.q if T == 1 else torch.randn(len(lens), T, Hkv * G, d, generator=g, device="cuda").to(torch.bfloat16)
+    ws = torch.zeros(max(256, int(plan.workspace_bytes)), dtype=torch.uint8, device="cuda")
+    out = torch.full_like(q, float("nan"))
+    if fp8:
+        f8 = synth.quantize_kv_fp8(li)
+        args = (plan, q, f8.k8, f8.v8, f8.k_scale, f8.v_scale, table, li.seq_lens)
+        if window > 0:
+            b.paged_decode_window_fp8(*args, window, li.scale, ws, out)
+        else:
+            b.paged_decode_global_fp8(*args, li.scale, ws, out)
+    else:
+        args = (plan, q, li.k_pool, li.v_pool, table, li.seq_lens)
+        if window > 0:
+            b.paged_decode_window(*args, window, li.scale, ws, out)
+        else:
+            b.paged_decode_global(*args, li.scale, ws, out)
+    b.paged_decode_merge(plan, ws, out)
+    assert b.paged_decode_check_device_error(plan, ws) == 0
+    tables, seq = li.block_tables.cpu().numpy(), li.seq_lens.cpu().numpy()
+    if fp8:
+        k8, v8 = f8.k8.cpu().numpy(), None if f8.v8 is None else f8.v8.cpu().numpy()
+        ks, vs = f8.k_scale.cpu().numpy(), None if f8.v_scale is None else f8.v_scale.cpu().numpy()
+        ref = oracle.decode_fp8(synth.bits_u16(q), k8, v8, ks, vs, tables, seq, li.scale, window)
+        compare(out, ref, f8, f"fp8 S={plan.num_splits} mode={plan.merge_mode}")
+    elif T == 1:
+        compare(out, run_oracle(li), li, f"S={plan.num_splits} mode={plan.merge_mode}")
+    else:
+        ref = oracle.decode_multi(synth.bits_u16(q.cpu()), synth.bits_u16(li.k_pool),
+                                  None if li.v_pool is None else synth.bits_u16(li.v_pool), tables, seq, li.scale,
+                                  window)
+        got = out.float().cpu().numpy().astype(np.float64)
+        assert np.isfinite(got).all() and np.abs(got - ref).max() <= MAX_ABS
