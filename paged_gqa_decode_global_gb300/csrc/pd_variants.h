@@ -137,6 +137,10 @@ struct Stage1Cfg {
 // 44-47: the same over an FP8 cache); ids 48-51: two tiles per CTA, served by
 // two teams of three consumer warps from one ring (bf16, more than 8 columns).
 // head_dim 128: ids 36-43 (bf16, one query token).
+// ids 52-59: the FP8 K!=V decode geometries with six consumer warps, whose
+// smaller ring (192 KiB) leaves room beside it for the cluster's pushed
+// results (one cluster barrier); for spans under 4096 tokens, where the
+// launch's fixed costs weigh more than the seventh warp's arithmetic.
 #define PD_FOR_EACH_VARIANT(X) \
   X(0, 512, 1, false, false, 3, 2, false, 1, 1)  \
   X(1, 512, 2, false, false, 3, 2, false, 1, 1)  \
@@ -189,7 +193,15 @@ struct Stage1Cfg {
   X(48, 512, 8, false, false, 6, 2, true, 1, 2)  \
   X(49, 512, 8, true, false, 6, 4, true, 1, 2)   \
   X(50, 256, 8, false, false, 6, 2, true, 2, 2)  \
-  X(51, 256, 8, true, false, 6, 4, true, 2, 2)
+  X(51, 256, 8, true, false, 6, 4, true, 2, 2)  \
+  X(52, 512, 1, false, true, 6, 2, false, 1, 1) \
+  X(53, 512, 2, false, true, 6, 2, false, 1, 1) \
+  X(54, 512, 4, false, true, 6, 2, false, 1, 1) \
+  X(55, 512, 8, false, true, 6, 2, false, 1, 1) \
+  X(56, 256, 1, false, true, 6, 4, false, 1, 1) \
+  X(57, 256, 2, false, true, 6, 4, false, 1, 1) \
+  X(58, 256, 4, false, true, 6, 4, false, 1, 1) \
+  X(59, 256, 8, false, true, 6, 4, false, 1, 1)
 
 struct VariantInfo {
   int id, head_dim, group, kv_shared, kv_fp8, nw, spw, block_tokens, threads, smem_bytes, max_cluster, multi,

@@ -63,12 +63,16 @@ bool tiled(int query_tokens, int group) { return query_tokens > 1 || group > 8 |
 // Column-tiled plans with more than one 8-column tile use, over a bf16 cache,
 // the instances whose CTA serves two tiles from one ring (one copy of every
 // block for both); other plans those with one tile per CTA.
-const pd::VariantInfo* find_variant(int head_dim, int group, int kv_shared, int kv_fp8, int multi, int tiles) {
+// Where two instances serve the same shape (the FP8 K != V decode ones, with
+// seven and with six consumer warps), `nw` > 0 asks for that many warps; 0
+// takes the first in the table.
+const pd::VariantInfo* find_variant(int head_dim, int group, int kv_shared, int kv_fp8, int multi, int tiles,
+                                    int nw = 0) {
   if (group < 1 || group > kMaxGroup) return nullptr;
   for (int i = 0; i < pd::kNumVariants; ++i) {
     const pd::VariantInfo& v = pd::kVariants[i];
     if (v.head_dim != head_dim || v.kv_shared != kv_shared || v.kv_fp8 != kv_fp8 || v.multi != multi) continue;
-    if (v.tiles != tiles) continue;
+    if (v.tiles != tiles || (nw > 0 && v.nw != nw)) continue;
     if (multi || v.group == group) return &v;
   }
   return nullptr;
@@ -131,8 +135,10 @@ double cta_tokens_per_us(const pd::VariantInfo& v) {
     return 67.0;  // d256 (K=V not measured: the K != V figure)
   }
   if (v.kv_fp8) {
-    if (v.head_dim == 512) return kvs ? 85.1 : 49.4;
-    return kvs ? 120.0 : 98.0;
+    // (the six-warp K != V instances: the seven-warp figure scaled by 6 / 7)
+    const double warps = v.nw == 6 ? 6.0 / 7.0 : 1.0;
+    if (v.head_dim == 512) return kvs ? 85.1 : 49.4 * warps;
+    return kvs ? 120.0 : 98.0 * warps;
   }
   if (v.head_dim == 512) return kvs ? 61.7 : 55.4;
   if (v.head_dim == 256) return kvs ? 90.5 : 74.6;
@@ -335,7 +341,13 @@ pd_status plan_impl(const pd_layer_desc* layer, int32_t batch, int32_t query_tok
   }
   const int tiles_needed = multi ? col_tiles(T, group) : 1;
   const int want_tiles = (multi && !fp8 && (tiles_needed >= 3 || (tiles_needed == 2 && longest_span >= 4096))) ? 2 : 1;
-  const pd::VariantInfo* v = find_variant(ly.head_dim, group, ly.kv_shared, fp8, multi, want_tiles);
+  // FP8 K != V decode over spans under 4096 tokens: the six-warp instance,
+  // whose cluster merges need one barrier (same-box: 64 MiB 11.13 -> 10.39
+  // us, windows of 1024 -1.6%); longer spans keep the seventh warp's
+  // arithmetic (1 GiB: 84.1 us against 86.0 with six).
+  const int want_nw = (fp8 && !ly.kv_shared && !multi && longest_span < 4096) ? 6 : 0;
+  const pd::VariantInfo* v = find_variant(ly.head_dim, group, ly.kv_shared, fp8, multi, want_tiles, want_nw);
+  if (!v && want_nw > 0) v = find_variant(ly.head_dim, group, ly.kv_shared, fp8, multi, want_tiles);
   if (!v && want_tiles > 1) v = find_variant(ly.head_dim, group, ly.kv_shared, fp8, multi, 1);
   if (!v) return PD_ERR_UNSUPPORTED;
   const int TB = v->block_tokens;

@@ -344,6 +344,21 @@ def test_groups_between_the_decode_instances_are_served(lib, G):
     assert e.value.status == b.PD_ERR_UNSUPPORTED
 
 
+def test_fp8_kneqv_decode_instance_follows_the_span(lib):
+    """FP8 K != V decode: six consumer warps (224 threads) for spans under 4096
+    tokens, seven (256) for longer ones; K = V and the column-tiled instances
+    have one form."""
+    for d in (256, 512):
+        for G in (1, 2, 4, 8):
+            fp8 = b.layer_desc(2 * G, 2, d, 16, 10 ** 5, 2000, 0, False, b.PD_KV_FP8_E4M3)
+            assert b.paged_decode_plan(fp8, [4095, 12], 152).threads_per_cta == 224
+            assert b.paged_decode_plan(fp8, [4096, 12], 152).threads_per_cta == 256
+            win = b.layer_desc(2 * G, 2, d, 16, 10 ** 5, 2000, 1024, False, b.PD_KV_FP8_E4M3)
+            assert b.paged_decode_plan(win, [30000], 152).threads_per_cta == 224  # the window bounds the span
+            kvs = b.layer_desc(2 * G, 2, d, 16, 10 ** 5, 2000, 0, True, b.PD_KV_FP8_E4M3)
+            assert b.paged_decode_plan(kvs, [100], 152).threads_per_cta == 256
+
+
 def test_planner_invariants_on_random_shapes(lib):
     """300 seeded random layer shapes and batches, decode / multi-token / partial
     plans, bf16 and FP8: every plan covers every attended token, its grid and

@@ -385,16 +385,21 @@ def run_oracle_fp8(f):
 
 @pytest.mark.parametrize("d,G,kvs", FP8_VARIANTS + [(512, 16, True), (256, 12, False)])
 @pytest.mark.parametrize("window", [0, 37])
-def test_fp8_variants_ragged(d, G, kvs, window):
+@pytest.mark.parametrize("long", [False, True])
+def test_fp8_variants_ragged(d, G, kvs, window, long):
+    """Every FP8 instance on a ragged batch; K != V spans under 4096 tokens run
+    on the six-warp instances, longer ones on the seven-warp ones."""
     Hkv = 2
-    lens = [1, 17, 300, 0, 1000, 33]
+    lens = [1, 17, 300, 0, 1000, 33] + ([5000] if long else [])
     li = synth.make_layer("f8", lens, Hkv * G, Hkv, d, window=window, kv_shared=kvs,
                           pool_pages=sum((L + 15) // 16 for L in lens) + 5, seed=500 + d + G + 100 * kvs + window,
                           device="cuda")
     f = synth.quantize_kv_fp8(li)
     ref = run_oracle_fp8(f)
+    span = max(min(L, window) if window else L for L in lens)
     for sms in (3, 152):
         out, step = run_gpu(f, sm_count=sms)
+        assert step.plan.threads_per_cta == (224 if not kvs and G <= 8 and span < 4096 else 256)
         compare(out, ref, f, f"fp8 d{d} G{G} kvs{kvs} W{window} sms{sms} S{step.plan.num_splits}")
 
 
