@@ -60,14 +60,14 @@ FALLBACK_HBM_GBS = 6800.0
 # entry whose sources or plan differ from the run's is not used (the captures
 # and their commands are summarised under profiles/).
 NCU_TRAFFIC = {
-    "6551688c2f7560a0": {
-        "w4a": (1073899264 + 2771968, (9, 3648, 1)),
-        "w2": (67295488 + 527872, (4, 256, 2)),
-        "w3": (68277248 + 321024, (2, 544, 2)),
-        "w4a-fp8": (537290240 + 2711296, (9, 3648, 1)),
-        "w5global": (1596576000 + 4366592, (19, 5456, 1)),
-        "w5global-fp8": (798929920 + 4851968, (19, 5456, 1)),
-        "w5sliding": (68174080 + 544000, (2, 544, 2)),
+    "ab3edbe6d252c5e4": {
+        "w4a": (1073899776 + 2798080, (9, 3648, 1)),
+        "w2": (67297280 + 514560, (4, 256, 2)),
+        "w3": (68277504 + 376064, (2, 544, 2)),
+        "w4a-fp8": (537291264 + 2669824, (9, 3648, 1)),
+        "w5global": (1596573952 + 4372480, (19, 5456, 1)),
+        "w5global-fp8": (798929920 + 4911360, (19, 5456, 1)),
+        "w5sliding": (68173568 + 622080, (2, 544, 2)),
     },
 }
 
