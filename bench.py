@@ -73,7 +73,7 @@ NCU_TRAFFIC = {
 
 # the same for the fused QKV norm + RoPE + cache-write kernel (--op prepare)
 PREP_NCU_TRAFFIC = {
-    "d2ddd8d8f8c32361": {"w2": 221184},
+    "bddd86ff645abd50": {"w2": 221184},
 }
 
 STAGE1_SOURCES = ("stage1.cu", "pd_common.cuh", "pd_variants.h", "pd_kernels.h")
