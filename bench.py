@@ -453,10 +453,13 @@ def run_ours(args, world, rank, local):
         # Every step copies its inputs (q -- or the new token's raw rows --,
         # block table, seq_lens) from one pinned host staging buffer and its
         # result back to pinned host memory. The decode loop a caller writes
-        # pipelines this: two device copies of the staging buffer and of out,
-        # the input copy of step i + 1 and the result copy of step i on copy
-        # streams of their own while step i's kernels run, each step's kernels
-        # waiting for its inputs and each result buffer for its copy-out.
+        # pipelines this with one step of look-ahead and keeps the chain of
+        # programmatic dependent launches unbroken: after step i's kernels one
+        # paged_decode_stage_copy kernel copies step i + 1's inputs into the
+        # other device staging buffer and step i - 1's result out, then waits
+        # for step i; a last one (waiting first) copies the final result out.
+        # Two device buffers each way. The decodes run with early_kv cleared:
+        # the copy in front of a stage 1 writes the block table it reads.
         if layer_op:  # the new token's raw q / k / v rows instead of q
             parts = [pi.q_in, pi.k_in] + ([] if pi.v_in is None else [pi.v_in]) + [li.block_tables, li.seq_lens]
         else:
@@ -475,11 +478,9 @@ def run_ours(args, world, rank, local):
             vd = [sd[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape) for t, o in zip(parts, offs)]
             bufs.append({"stage": sd, "views": vd, "q": torch.empty_like(q_rows) if layer_op else vd[0],
                          "out": torch.empty_like(q_rows),
-                         "out_h": torch.empty(q_rows.shape, dtype=q_rows.dtype, pin_memory=True),
-                         "in_done": torch.cuda.Event(), "comp_done": torch.cuda.Event(),
-                         "out_done": torch.cuda.Event()})
-        h2d = torch.cuda.Stream(device=dev)
-        d2h = torch.cuda.Stream(device=dev)
+                         "out_h": torch.empty(q_rows.shape, dtype=q_rows.dtype, pin_memory=True)})
+        for bf in bufs:
+            bf["stage"].copy_(stage_h)
 
         def compute(i, bf):
             k, v = pools[i % replicas]
@@ -497,35 +498,16 @@ def run_ours(args, world, rank, local):
                 bf["out_h"].copy_(bf["out"], non_blocking=True)
 
         def pipelined_steps(i0, m):
-            # (issued with `stream` current; the copy streams fork from it and join it at the end)
-            fork = torch.cuda.Event()
-            fork.record(stream)
-            h2d.wait_event(fork)
-            d2h.wait_event(fork)
-            with torch.cuda.stream(h2d):
-                bufs[i0 % 2]["stage"].copy_(stage_h, non_blocking=True)
-                bufs[i0 % 2]["in_done"].record(h2d)
+            stage_copy = pdb.paged_decode_stage_copy
+            stage_copy(bufs[i0 % 2]["stage"], stage_h, None, None, 0, stream)
             for i in range(i0, i0 + m):
-                bf, nb = bufs[i % 2], bufs[(i + 1) % 2]
-                if i + 1 < i0 + m:
-                    if i > i0:
-                        h2d.wait_event(nb["comp_done"])  # step i - 1's kernels have read that buffer
-                    with torch.cuda.stream(h2d):
-                        nb["stage"].copy_(stage_h, non_blocking=True)
-                        nb["in_done"].record(h2d)
-                stream.wait_event(bf["in_done"])
-                if i >= i0 + 2:
-                    stream.wait_event(bf["out_done"])  # step i - 2's result has left this buffer
+                bf, other = bufs[i % 2], bufs[(i + 1) % 2]
                 compute(i, bf)
-                bf["comp_done"].record(stream)
-                d2h.wait_event(bf["comp_done"])
-                with torch.cuda.stream(d2h):
-                    bf["out_h"].copy_(bf["out"], non_blocking=True)
-                    bf["out_done"].record(d2h)
-            stream.wait_event(bufs[(i0 + m - 1) % 2]["out_done"])
-            if m > 1:
-                stream.wait_event(bufs[(i0 + m - 2) % 2]["out_done"])
-            stream.wait_event(bufs[(i0 + m - 1) % 2]["in_done"])
+                more, prev = i + 1 < i0 + m, i > i0  # a next step to feed, a previous result to fetch
+                stage_copy(other["stage"] if more else None, stage_h if more else None,
+                           other["out_h"] if prev else None, other["out"] if prev else None, 0, stream)
+            last = bufs[(i0 + m - 1) % 2]
+            stage_copy(None, None, last["out_h"], last["out"], 1, stream)
 
         def e2e_graphs(fn):
             with torch.cuda.stream(stream):
@@ -543,12 +525,14 @@ def run_ours(args, world, rank, local):
                 i0 += m
             return graphs
 
+        early_kv = int(plan.early_kv)
+        plan.early_kv = 0
         graphs = e2e_graphs(pipelined_steps)
         e2e_ms, _ = timed(graphs)
         e2e_ms = max_over_ranks(e2e_ms, world)
         del graphs
-        last = bufs[(K - 1) % 2]
-        assert torch.equal(last["out_h"], last["out"].cpu())
+        for bf in bufs:  # the last two steps' results reached the host
+            assert torch.equal(bf["out_h"], bf["out"].cpu())
         graphs = e2e_graphs(serial_steps)
         serial_ms, _ = timed(graphs)
         serial_ms = max_over_ranks(serial_ms, world)
@@ -565,15 +549,17 @@ def run_ours(args, world, rank, local):
         torch.cuda.synchronize()
         barrier(world)
         eager_ms = max_over_ranks(a.elapsed_time(z), world)
+        plan.early_kv = early_kv
         e2e = {"value": round(e2e_ms * 1e3 / K, 3), "unit": UNIT,
                "h2d_bytes_per_step": int(stage_h.numel()),
                "d2h_bytes_per_step": bufs[0]["out_h"].numel() * 2, "steps": K,
-               "launch": "CUDA graph replay of, per step: one H2D copy of " +
-                         ("the new token's q/k/v rows" if layer_op else "q") +
-                         " + block table + seq_lens from a pinned staging buffer, the C-ABI " +
+               "launch": "CUDA graph replay of, per step: the C-ABI " +
                          ("new-token step and " if layer_op else "") +
-                         "decode calls, one D2H copy of out to pinned host memory; copies on two copy streams "
-                         "overlap the neighbouring steps' kernels (two device buffers each way)",
+                         "decode calls, then one paged_decode_stage_copy kernel copying the next step's " +
+                         ("new q/k/v rows" if layer_op else "q") +
+                         " + block table + seq_lens in from a pinned staging buffer and the previous step's out "
+                         "to pinned host memory (the last out by a final copy); one stream, one chain of "
+                         "programmatic dependent launches, early_kv cleared, two device buffers each way",
                "serial_value": round(serial_ms * 1e3 / K, 3),
                "eager_value": round(eager_ms * 1e3 / n_eager, 3), "eager_steps": n_eager}
         step.check(stream)

@@ -433,6 +433,40 @@ pd_status paged_decode_qkv_norm_rope_write(const pd_layer_desc* layer, int32_t b
                                            const int32_t* block_tables, const int32_t* seq_lens, void* q_out,
                                            void* k_pool, void* v_pool, uint32_t* device_flags, void* stream);
 
+/* ---- Host-in/host-out decode loops ---------------------------------------------
+ *
+ * Not an operation of the decode method: plumbing for a caller whose inputs
+ * (q, block table, lengths) come from, and whose results go to, page-locked
+ * host memory every step. A step issued as memcpy + decode + memcpy, or with
+ * its copies on other streams joined by event waits, ends the chain of
+ * programmatic dependent launches at every copy, so the next stage 1 cannot
+ * start while the step in front drains. This call copies as one kernel that
+ * lets the launch behind it start at once.
+ *
+ * Two copies, in_bytes from in_src to in_dst and out_bytes from out_src to
+ * out_dst (names only; either may go either way):
+ *   after_wait 0  both copies run, then the kernel waits for the launch in front
+ *                 of it (griddepcontrol.wait), so it completes after that launch:
+ *                 for data nothing in flight writes or reads -- the next step's
+ *                 inputs into a buffer the steps in flight do not read, the result
+ *                 of the step before the one in front
+ *   after_wait 1  the kernel waits first: for the result of the launch in front
+ *   stream        cudaStream_t as void*
+ * A decode loop: copy(step 0's inputs in, nothing out, 0); then per step i:
+ * decode(i) [+ merge(i)], copy(step i+1's inputs into the other input buffer,
+ * step i-1's result out, 0); at the end copy(nothing in, the last result out,
+ * 1). Two input buffers and two result buffers, used alternately.
+ * Every pointer of a non-empty copy is device memory of the current device or
+ * page-locked host memory (cudaHostAlloc / cudaHostRegister, reached through its
+ * device address), 16-byte aligned; sizes are multiples of 16; a copy's source
+ * and destination do not overlap. A copy of 0 bytes is skipped (its pointers
+ * may be NULL); the kernel is launched even when both are empty.
+ * Returns PD_ERR_INVALID_ARG without launching (pageable or foreign memory,
+ * misalignment, overlap, after_wait not 0 or 1), PD_ERR_CUDA if the launch fails.
+ */
+pd_status paged_decode_stage_copy(void* in_dst, const void* in_src, size_t in_bytes, void* out_dst,
+                                  const void* out_src, size_t out_bytes, int32_t after_wait, void* stream);
+
 /* Static, human-readable name of a status. */
 const char* paged_decode_status_string(pd_status status);
 

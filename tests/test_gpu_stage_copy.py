@@ -1,0 +1,164 @@
+"""paged_decode_stage_copy: copies between page-locked host memory and device
+memory as one kernel in the stream's chain of programmatic dependent launches,
+and the host-in/host-out decode loop built on it (one step of look-ahead: after
+step i's kernels one copy brings step i + 1's inputs in and takes step i - 1's
+result out; a last copy, waiting first, takes the final result out).
+
+The loop's steps each get their own q and lengths, so a copy that landed late
+or a result taken before its step finished shows up as a wrong step; every
+host result is compared bit for bit with the same decode run on its own
+(itself held to the oracle by the parity tests). Eager calls and a CUDA graph
+of the loop, merge in a cluster and through the merge kernel, K=V and K!=V,
+a window layer, FP8.
+"""
+import numpy as np
+import pytest
+import torch
+
+from paged_gqa_decode_global_gb300 import binding as b
+from paged_gqa_decode_global_gb300 import inputs as synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("nbytes", [16, 4096 + 16, 3 << 20])
+@pytest.mark.parametrize("after_wait", [0, 1])
+def test_round_trip_through_the_device(nbytes, after_wait):
+    g = torch.Generator().manual_seed(nbytes + after_wait)
+    src = torch.randint(0, 256, (nbytes,), dtype=torch.uint8, generator=g).pin_memory()
+    dev = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    back = torch.zeros(nbytes, dtype=torch.uint8).pin_memory()
+    b.paged_decode_stage_copy(dev, src, None, None, after_wait)
+    b.paged_decode_stage_copy(None, None, back, dev, 1)  # waits for the copy in front
+    torch.cuda.synchronize()
+    assert torch.equal(back, src)
+    assert torch.equal(dev.cpu(), src)
+
+
+def test_both_copies_of_one_launch():
+    g = torch.Generator().manual_seed(7)
+    a = torch.randint(0, 256, (1 << 16,), dtype=torch.uint8, generator=g).pin_memory()
+    c = torch.randint(0, 256, (3 * 1024,), dtype=torch.uint8, generator=g).cuda()
+    a_dev = torch.empty_like(a, device="cuda")
+    c_host = torch.zeros(c.shape, dtype=torch.uint8).pin_memory()
+    b.paged_decode_stage_copy(a_dev, a, c_host, c, 0)
+    torch.cuda.synchronize()
+    assert torch.equal(a_dev.cpu(), a)
+    assert torch.equal(c_host, c.cpu())
+
+
+def test_refused_without_launching():
+    dev = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    pinned = torch.zeros(256, dtype=torch.uint8).pin_memory()
+    pageable = torch.zeros(256, dtype=torch.uint8)
+    cases = [
+        (dev, pageable, 0),               # pageable host memory
+        (dev[8:24], pinned[:16], 0),      # misaligned destination
+        (dev[:8], pinned[:8], 0),         # not a multiple of 16 bytes
+        (dev[16:48], dev[0:32], 0),       # source and destination overlap
+        (dev[:16], pinned[:16], 2),       # after_wait neither 0 nor 1
+    ]
+    for dst, src, wait in cases:
+        with pytest.raises(b.PagedDecodeError) as e:
+            b.paged_decode_stage_copy(dst, src, None, None, wait)
+        assert e.value.status == b.PD_ERR_INVALID_ARG
+    with pytest.raises(ValueError):
+        b.paged_decode_stage_copy(dev, None)
+    torch.cuda.synchronize()
+    assert int(dev.count_nonzero()) == 0
+
+
+LOOP_CASES = [
+    # (head_dim, group, kv heads, K=V, window, lengths, SM count the plan is made for, fp8)
+    (512, 4, 4, False, 0, [1024] * 8, 152, False),        # clusters of 4 (64 MiB layer's shape)
+    (512, 4, 4, False, 0, [3000, 777, 4096, 1], 400, False),  # many pieces: the merge kernel
+    (256, 2, 8, False, 1024, [1500, 4000, 300], 152, False),  # window layer
+    (512, 4, 2, True, 0, [2048, 513], 152, False),            # K=V
+    (512, 4, 4, False, 0, [2000, 1024, 64], 152, True),       # FP8 cache
+]
+
+
+def _layer(case, seed):
+    d, G, Hkv, kvs, window, lens, sms, fp8 = case
+    li = synth.make_layer("loop", lens, G * Hkv, Hkv, d, window=window, kv_shared=kvs,
+                          pool_pages=sum((L + 15) // 16 for L in lens) + 4, seed=seed, device="cuda")
+    return (synth.quantize_kv_fp8(li) if fp8 else li), sms
+
+
+@pytest.mark.parametrize("graph", [False, True], ids=["eager", "graph"])
+@pytest.mark.parametrize("case", LOOP_CASES, ids=[f"d{c[0]}-G{c[1]}-kvs{int(c[3])}-W{c[4]}-sm{c[6]}-fp8{int(c[7])}"
+                                                  for c in LOOP_CASES])
+def test_host_in_host_out_loop(case, graph):
+    li, sms = _layer(case, seed=11)
+    step = b.LayerStep.for_inputs(li, sm_count=sms)  # early_kv 0: the copy in front writes the block table
+    fp8 = hasattr(li, "k8")
+    k, v = (li.k8, li.v8) if fp8 else (li.k_pool, li.v_pool)
+    ks, vs = (li.k_scale, li.v_scale) if fp8 else (None, None)
+    n_steps = 7
+    gen = torch.Generator(device="cuda").manual_seed(3)
+    lens0 = li.seq_lens.cpu()
+    # each step its own q and lengths (a request shrinking by j tokens, never below 1 if it had any)
+    qs = [(torch.randn(li.q.shape, generator=gen, device="cuda")).to(torch.bfloat16) for _ in range(n_steps)]
+    lens = [torch.where(lens0 > 0, torch.clamp(lens0 - 5 * j, min=1), lens0).to(torch.int32) for j in range(n_steps)]
+
+    # what each step gives run on its own
+    expect = []
+    for j in range(n_steps):
+        out = torch.empty_like(li.q)
+        step(qs[j], k, v, li.block_tables, lens[j].cuda(), li.scale, out, k_scale=ks, v_scale=vs)
+        expect.append(out.cpu())
+    torch.cuda.synchronize()
+    assert step.check() == 0
+
+    # one pinned staging buffer per step: q | block table | lengths, each 256-byte aligned
+    parts = [li.q, li.block_tables, li.seq_lens]
+    offs, total = [], 0
+    for t in parts:
+        offs.append(total)
+        total += (t.numel() * t.element_size() + 255) // 256 * 256
+    stage_h = []
+    for j in range(n_steps):
+        h = torch.zeros(total, dtype=torch.uint8).pin_memory()
+        for t, o in zip([qs[j].cpu(), li.block_tables.cpu(), lens[j]], offs):
+            n = t.numel() * t.element_size()
+            h[o:o + n].view(t.dtype).view(t.shape).copy_(t)
+        stage_h.append(h)
+    dev_stage = [torch.zeros(total, dtype=torch.uint8, device="cuda") for _ in range(2)]
+    views = [[s[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape) for t, o in zip(parts, offs)]
+             for s in dev_stage]
+    dev_out = [torch.empty_like(li.q) for _ in range(2)]
+    host_out = [torch.zeros(li.q.shape, dtype=torch.bfloat16).pin_memory() for _ in range(n_steps)]
+    stream = torch.cuda.Stream()
+
+    def loop():
+        b.paged_decode_stage_copy(dev_stage[0], stage_h[0], None, None, 0, stream)
+        for j in range(n_steps):
+            cur, other = j % 2, (j + 1) % 2
+            q, bt, sl = views[cur]
+            step(q, k, v, bt, sl, li.scale, dev_out[cur], stream, k_scale=ks, v_scale=vs)
+            more, prev = j + 1 < n_steps, j > 0
+            b.paged_decode_stage_copy(dev_stage[other] if more else None, stage_h[j + 1] if more else None,
+                                      host_out[j - 1] if prev else None, dev_out[other] if prev else None, 0,
+                                      stream)
+        b.paged_decode_stage_copy(None, None, host_out[n_steps - 1], dev_out[(n_steps - 1) % 2], 1, stream)
+
+    if graph:
+        with torch.cuda.stream(stream):
+            loop()  # warm-up outside the capture
+        torch.cuda.synchronize()
+        for h in host_out:
+            h.zero_()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            loop()
+        for h in host_out:
+            h.zero_()
+        for _ in range(2):
+            g.replay()
+    else:
+        with torch.cuda.stream(stream):
+            loop()
+    torch.cuda.synchronize()
+    assert step.check() == 0
+    for j in range(n_steps):
+        assert torch.equal(host_out[j], expect[j]), f"step {j}"
