@@ -447,15 +447,25 @@ pd_status paged_decode_qkv_norm_rope_write(const pd_layer_desc* layer, int32_t b
  * out_dst (names only; either may go either way):
  *   after_wait 0  both copies run, then the kernel waits for the launch in front
  *                 of it (griddepcontrol.wait), so it completes after that launch:
- *                 for data nothing in flight writes or reads -- the next step's
- *                 inputs into a buffer the steps in flight do not read, the result
- *                 of the step before the one in front
- *   after_wait 1  the kernel waits first: for the result of the launch in front
+ *                 for data that nothing possibly still running writes or reads.
+ *                 Possibly still running as it starts: the launch in front and,
+ *                 if that one lets its dependents start before its own wait, the
+ *                 one before it, and so on. This library's decode and merge
+ *                 kernels let them start after their wait (with pd_plan.early_kv
+ *                 0); paged_decode_qkv_norm_rope_write and this copy before.
+ *   after_wait 1  the kernel waits first: for data the launch in front writes
+ *                 or, behind a launch that lets its dependents start before its
+ *                 own wait, for anything that launch's predecessors touch
  *   stream        cudaStream_t as void*
- * A decode loop: copy(step 0's inputs in, nothing out, 0); then per step i:
- * decode(i) [+ merge(i)], copy(step i+1's inputs into the other input buffer,
- * step i-1's result out, 0); at the end copy(nothing in, the last result out,
- * 1). Two input buffers and two result buffers, used alternately.
+ * A decode loop with one step of look-ahead, two input buffers and two result
+ * buffers used alternately: copy(step 0's inputs in, nothing out, 0); per step
+ * i: decode(i) [+ merge(i)], then copy(step i+1's inputs into the other input
+ * buffer, step i-1's result out, 0); at the end copy(nothing in, the last result
+ * out, 1). Its decodes need pd_plan.early_kv 0: with the flag stage 1 reads its
+ * block table before its wait, while the copy in front may still write it. A
+ * loop whose last kernel of a step lets its dependents start before its own wait
+ * (paged_decode_qkv_norm_rope_write alone) copies after it with after_wait 1:
+ * the next step's inputs in and that step's own result out.
  * Every pointer of a non-empty copy is device memory of the current device or
  * page-locked host memory (cudaHostAlloc / cudaHostRegister, reached through its
  * device address), 16-byte aligned; sizes are multiples of 16; a copy's source
