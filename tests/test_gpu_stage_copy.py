@@ -162,3 +162,85 @@ def test_host_in_host_out_loop(case, graph):
     assert step.check() == 0
     for j in range(n_steps):
         assert torch.equal(host_out[j], expect[j]), f"step {j}"
+
+
+@pytest.mark.parametrize("graph", [False, True], ids=["eager", "graph"])
+def test_new_token_step_loop_copies_after_waiting(graph):
+    """Behind paged_decode_qkv_norm_rope_write, which lets its dependents start
+    before its own wait, the loop copies with after_wait 1: the next step's new
+    rows in and that step's q out. Seven steps, each with its own rows; every
+    host q equals the step run on its own."""
+    lens = [1000, 17, 4096, 1]
+    li = synth.make_layer("newtok", lens, 16, 4, 512, pool_pages=sum((L + 15) // 16 for L in lens) + 4, seed=5,
+                          device="cuda")
+    pi = synth.make_prepare(li, rot=128, theta=1e6, seed=5)
+    desc = b.layer_desc(li.num_q_heads, li.num_kv_heads, li.head_dim, li.page_size, li.num_pages,
+                        li.block_tables.shape[1], 0, False)
+    cos_sin = torch.empty(pi.max_positions, pi.rot, dtype=torch.float32, device="cuda")
+    b.paged_decode_rope_table(pi.theta, pi.rot, pi.max_positions, cos_sin)
+    k_pool, v_pool = li.k_pool.clone(), li.v_pool.clone()
+    flags = torch.zeros(1, dtype=torch.int32, device="cuda")
+    n_steps = 7
+    gen = torch.Generator(device="cuda").manual_seed(9)
+    rows = [[(3.0 * torch.randn(t.shape, generator=gen, device="cuda")).to(torch.bfloat16)
+             for t in (pi.q_in, pi.k_in, pi.v_in)] for _ in range(n_steps)]
+
+    def prep(q_in, k_in, v_in, seq, q_out, stream=None):
+        b.paged_decode_qkv_norm_rope_write(desc, pi.rot, pi.max_positions, pi.eps, q_in, k_in, v_in, pi.q_w,
+                                           pi.k_w, pi.v_w, cos_sin, li.block_tables, seq, q_out, k_pool, v_pool,
+                                           flags, stream)
+
+    expect = []
+    for j in range(n_steps):
+        q_out = torch.empty_like(pi.q_in)
+        prep(*rows[j], li.seq_lens, q_out)
+        expect.append(q_out.cpu())
+    torch.cuda.synchronize()
+    assert int(flags.item()) == 0
+
+    parts = [pi.q_in, pi.k_in, pi.v_in, li.seq_lens]
+    offs, total = [], 0
+    for t in parts:
+        offs.append(total)
+        total += (t.numel() * t.element_size() + 255) // 256 * 256
+    stage_h = []
+    for j in range(n_steps):
+        h = torch.zeros(total, dtype=torch.uint8).pin_memory()
+        for t, o in zip(rows[j] + [li.seq_lens], offs):
+            n = t.numel() * t.element_size()
+            h[o:o + n].view(t.dtype).view(t.shape).copy_(t.cpu())
+        stage_h.append(h)
+    dev_stage = [torch.zeros(total, dtype=torch.uint8, device="cuda") for _ in range(2)]
+    views = [[s[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape) for t, o in zip(parts, offs)]
+             for s in dev_stage]
+    dev_q = [torch.empty_like(pi.q_in) for _ in range(2)]
+    host_q = [torch.zeros(pi.q_in.shape, dtype=torch.bfloat16).pin_memory() for _ in range(n_steps)]
+    stream = torch.cuda.Stream()
+
+    def loop():
+        b.paged_decode_stage_copy(dev_stage[0], stage_h[0], None, None, 0, stream)
+        for j in range(n_steps):
+            cur, other = j % 2, (j + 1) % 2
+            q, k, v, sl = views[cur]
+            prep(q, k, v, sl, dev_q[cur], stream)
+            more = j + 1 < n_steps
+            b.paged_decode_stage_copy(dev_stage[other] if more else None, stage_h[j + 1] if more else None,
+                                      host_q[j], dev_q[cur], 1, stream)
+
+    if graph:
+        with torch.cuda.stream(stream):
+            loop()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            loop()
+        for h in host_q:
+            h.zero_()
+        g.replay()
+    else:
+        with torch.cuda.stream(stream):
+            loop()
+    torch.cuda.synchronize()
+    assert int(flags.item()) == 0
+    for j in range(n_steps):
+        assert torch.equal(host_q[j], expect[j]), f"step {j}"
