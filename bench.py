@@ -451,63 +451,80 @@ def run_ours(args, world, rank, local):
     e2e = None
     if not args.no_e2e:
         # Every step copies its inputs (q -- or the new token's raw rows --,
-        # block table, seq_lens) from one pinned host staging buffer and its
-        # result back to pinned host memory. The decode loop a caller writes
-        # pipelines this with one step of look-ahead and keeps the chain of
-        # programmatic dependent launches unbroken: after step i's kernels one
-        # paged_decode_stage_copy kernel copies step i + 1's inputs into the
-        # other device staging buffer and step i - 1's result out, then waits
+        # block table, seq_lens) from pinned host memory and its result back to
+        # pinned host memory. The decode loop a caller writes pipelines this and
+        # keeps the chain of programmatic dependent launches unbroken: after
+        # step i's kernels one paged_decode_stage_copy kernel copies step i + 1's
+        # q (or rows) into the other q buffer, the block table and lengths of
+        # the step `ahead` steps on, and step i - 1's result out, then waits
         # for step i; a last one (waiting first) copies the final result out.
-        # Two device buffers each way. The decodes run with early_kv cleared:
-        # the copy in front of a stage 1 writes the block table it reads.
-        if layer_op:  # the new token's raw q / k / v rows instead of q
-            parts = [pi.q_in, pi.k_in] + ([] if pi.v_in is None else [pi.v_in]) + [li.block_tables, li.seq_lens]
-        else:
-            parts = [q_rows, li.block_tables, li.seq_lens]
-        offs, total = [], 0
-        for t in parts:
-            offs.append(total)
-            total += (t.numel() * t.element_size() + 255) // 256 * 256
-        stage_h = torch.zeros(total, dtype=torch.uint8, pin_memory=True)
-        for t, o in zip(parts, offs):
-            n = t.numel() * t.element_size()
-            stage_h[o:o + n].view(t.dtype).view(t.shape).copy_(t.cpu())
-        bufs = []
-        for _ in range(2):
-            sd = torch.empty(total, dtype=torch.uint8, device=dev)
-            vd = [sd[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape) for t, o in zip(parts, offs)]
-            bufs.append({"stage": sd, "views": vd, "q": torch.empty_like(q_rows) if layer_op else vd[0],
-                         "out": torch.empty_like(q_rows),
-                         "out_h": torch.empty(q_rows.shape, dtype=q_rows.dtype, pin_memory=True)})
-        for bf in bufs:
-            bf["stage"].copy_(stage_h)
+        # With early_kv stage 1 reads its block table and lengths before its
+        # wait, so those go two steps ahead (never written by the copy in front
+        # of the stage 1 that reads them), else one. Two q / result buffers,
+        # three for the table and lengths; before the loop, ordinary copies of
+        # the first step's inputs (and, two steps ahead, the second's table).
+        q_parts = ([pi.q_in, pi.k_in] + ([] if pi.v_in is None else [pi.v_in])) if layer_op else [q_rows]
+        meta_parts = [li.block_tables, li.seq_lens]
 
-        def compute(i, bf):
+        def staged(parts, n_dev):
+            offs, total = [], 0
+            for t in parts:
+                offs.append(total)
+                total += (t.numel() * t.element_size() + 255) // 256 * 256
+            host = torch.zeros(total, dtype=torch.uint8, pin_memory=True)
+            for t, o in zip(parts, offs):
+                n = t.numel() * t.element_size()
+                host[o:o + n].view(t.dtype).view(t.shape).copy_(t.cpu())
+            devs = []
+            for _ in range(n_dev):
+                sd = torch.empty(total, dtype=torch.uint8, device=dev)
+                sd.copy_(host)
+                devs.append({"stage": sd, "views": [sd[o:o + t.numel() * t.element_size()].view(t.dtype)
+                                                    .view(t.shape) for t, o in zip(parts, offs)]})
+            return host, devs
+
+        q_h, qbufs = staged(q_parts, 2)
+        meta_h, mbufs = staged(meta_parts, 3)
+        for qb in qbufs:
+            qb["q"] = torch.empty_like(q_rows) if layer_op else qb["views"][0]
+            qb["out"] = torch.empty_like(q_rows)
+            qb["out_h"] = torch.empty(q_rows.shape, dtype=q_rows.dtype, pin_memory=True)
+        ahead = 2 if plan.early_kv else 1
+
+        def compute(i, qb, mb):
             k, v = pools[i % replicas]
-            vd = bf["views"]
+            qv, (bt, sl) = qb["views"], mb["views"]
             if layer_op:
-                prep(k, v, q_in=vd[0], k_in=vd[1], v_in=None if pi.v_in is None else vd[2],
-                     bt=vd[-2], sl=vd[-1], q_out=bf["q"])
-            step(bf["q"], k, v, vd[-2], vd[-1], li.scale, bf["out"], stream, k_scale=k_sc, v_scale=v_sc)
+                prep(k, v, q_in=qv[0], k_in=qv[1], v_in=None if pi.v_in is None else qv[2], bt=bt, sl=sl,
+                     q_out=qb["q"])
+            step(qb["q"], k, v, bt, sl, li.scale, qb["out"], stream, k_scale=k_sc, v_scale=v_sc)
 
         def serial_steps(i0, m):
-            bf = bufs[0]
+            qb, mb = qbufs[0], mbufs[0]
             for i in range(i0, i0 + m):
-                bf["stage"].copy_(stage_h, non_blocking=True)
-                compute(i, bf)
-                bf["out_h"].copy_(bf["out"], non_blocking=True)
+                qb["stage"].copy_(q_h, non_blocking=True)
+                mb["stage"].copy_(meta_h, non_blocking=True)
+                compute(i, qb, mb)
+                qb["out_h"].copy_(qb["out"], non_blocking=True)
 
         def pipelined_steps(i0, m):
             stage_copy = pdb.paged_decode_stage_copy
-            stage_copy(bufs[i0 % 2]["stage"], stage_h, None, None, 0, stream)
+            qbufs[i0 % 2]["stage"].copy_(q_h, non_blocking=True)
+            for j in range(i0, min(i0 + ahead, i0 + m)):
+                mbufs[j % 3]["stage"].copy_(meta_h, non_blocking=True)
             for i in range(i0, i0 + m):
-                bf, other = bufs[i % 2], bufs[(i + 1) % 2]
-                compute(i, bf)
-                more, prev = i + 1 < i0 + m, i > i0  # a next step to feed, a previous result to fetch
-                stage_copy(other["stage"] if more else None, stage_h if more else None,
-                           other["out_h"] if prev else None, other["out"] if prev else None, 0, stream)
-            last = bufs[(i0 + m - 1) % 2]
-            stage_copy(None, None, last["out_h"], last["out"], 1, stream)
+                compute(i, qbufs[i % 2], mbufs[i % 3])
+                other = qbufs[(i + 1) % 2]  # step i + 1's q buffer, step i - 1's result
+                pairs = []
+                if i + 1 < i0 + m:
+                    pairs.append((other["stage"], q_h))
+                if i + ahead < i0 + m:
+                    pairs.append((mbufs[(i + ahead) % 3]["stage"], meta_h))
+                if i > i0:
+                    pairs.append((other["out_h"], other["out"]))
+                stage_copy(pairs, 0, stream)
+            last = qbufs[(i0 + m - 1) % 2]
+            stage_copy([(last["out_h"], last["out"])], 1, stream)
 
         def e2e_graphs(fn):
             with torch.cuda.stream(stream):
@@ -525,14 +542,12 @@ def run_ours(args, world, rank, local):
                 i0 += m
             return graphs
 
-        early_kv = int(plan.early_kv)
-        plan.early_kv = 0
         graphs = e2e_graphs(pipelined_steps)
         e2e_ms, _ = timed(graphs)
         e2e_ms = max_over_ranks(e2e_ms, world)
         del graphs
-        for bf in bufs:  # the last two steps' results reached the host
-            assert torch.equal(bf["out_h"], bf["out"].cpu())
+        for qb in qbufs:  # the last two steps' results reached the host
+            assert torch.equal(qb["out_h"], qb["out"].cpu())
         graphs = e2e_graphs(serial_steps)
         serial_ms, _ = timed(graphs)
         serial_ms = max_over_ranks(serial_ms, world)
@@ -549,17 +564,16 @@ def run_ours(args, world, rank, local):
         torch.cuda.synchronize()
         barrier(world)
         eager_ms = max_over_ranks(a.elapsed_time(z), world)
-        plan.early_kv = early_kv
         e2e = {"value": round(e2e_ms * 1e3 / K, 3), "unit": UNIT,
-               "h2d_bytes_per_step": int(stage_h.numel()),
-               "d2h_bytes_per_step": bufs[0]["out_h"].numel() * 2, "steps": K,
+               "h2d_bytes_per_step": int(q_h.numel() + meta_h.numel()),
+               "d2h_bytes_per_step": qbufs[0]["out_h"].numel() * 2, "steps": K,
                "launch": "CUDA graph replay of, per step: the C-ABI " +
                          ("new-token step and " if layer_op else "") +
                          "decode calls, then one paged_decode_stage_copy kernel copying the next step's " +
                          ("new q/k/v rows" if layer_op else "q") +
-                         " + block table + seq_lens in from a pinned staging buffer and the previous step's out "
+                         f" in, the block table + seq_lens of the step {ahead} on, and the previous step's out "
                          "to pinned host memory (the last out by a final copy); one stream, one chain of "
-                         "programmatic dependent launches, early_kv cleared, two device buffers each way",
+                         "programmatic dependent launches" + (", early_kv set" if ahead == 2 else ""),
                "serial_value": round(serial_ms * 1e3 / K, 3),
                "eager_value": round(eager_ms * 1e3 / n_eager, 3), "eager_steps": n_eager}
         step.check(stream)
@@ -803,14 +817,14 @@ def run_prepare(args, world, rank, local):
                          "qo_h": torch.empty(pi.q_in.shape, dtype=torch.bfloat16, pin_memory=True)})
 
         def chain(i0, m):
-            pdb.paged_decode_stage_copy(bufs[i0 % 2]["stage"], stage_h, None, None, 0, stream)
+            pdb.paged_decode_stage_copy([(bufs[i0 % 2]["stage"], stage_h)], 0, stream)
             for i in range(i0, i0 + m):
                 bf, other = bufs[i % 2], bufs[(i + 1) % 2]
                 vw = bf["views"]
                 one(i, qi=vw[0], ki=vw[1], vi=vw[2] if pi.v_in is not None else None, qo=bf["qo"], seq=vw[-1])
                 more = i + 1 < i0 + m
-                pdb.paged_decode_stage_copy(other["stage"] if more else None, stage_h if more else None,
-                                            bf["qo_h"], bf["qo"], 1, stream)
+                pdb.paged_decode_stage_copy([(other["stage"], stage_h) if more else (None, None),
+                                             (bf["qo_h"], bf["qo"])], 1, stream)
 
         with torch.cuda.stream(stream):
             chain(0, 3)

@@ -442,40 +442,52 @@ pd_status paged_decode_qkv_norm_rope_write(const pd_layer_desc* layer, int32_t b
  * programmatic dependent launches at every copy, so the next stage 1 cannot
  * start while the step in front drains. This call copies as one kernel that
  * lets the launch behind it start at once.
- *
- * Two copies, in_bytes from in_src to in_dst and out_bytes from out_src to
- * out_dst (names only; either may go either way):
- *   after_wait 0  both copies run, then the kernel waits for the launch in front
+ */
+#define PD_MAX_STAGE_COPIES 4
+
+typedef struct {
+  void* dst;
+  const void* src;
+  size_t bytes;   /* a multiple of 16; 0: the entry is skipped (its pointers may be NULL) */
+} pd_copy;
+
+/*
+ * Copies copies[0 .. num_copies) (num_copies 0..PD_MAX_STAGE_COPIES; the kernel
+ * is launched even when nothing is copied):
+ *   after_wait 0  the copies run, then the kernel waits for the launch in front
  *                 of it (griddepcontrol.wait), so it completes after that launch:
  *                 for data that nothing possibly still running writes or reads.
  *                 Possibly still running as it starts: the launch in front and,
  *                 if that one lets its dependents start before its own wait, the
  *                 one before it, and so on. This library's decode and merge
- *                 kernels let them start after their wait (with pd_plan.early_kv
- *                 0); paged_decode_qkv_norm_rope_write and this copy before.
+ *                 kernels let them start after their wait;
+ *                 paged_decode_qkv_norm_rope_write and this copy before.
  *   after_wait 1  the kernel waits first: for data the launch in front writes
  *                 or, behind a launch that lets its dependents start before its
  *                 own wait, for anything that launch's predecessors touch
  *   stream        cudaStream_t as void*
- * A decode loop with one step of look-ahead, two input buffers and two result
- * buffers used alternately: copy(step 0's inputs in, nothing out, 0); per step
- * i: decode(i) [+ merge(i)], then copy(step i+1's inputs into the other input
- * buffer, step i-1's result out, 0); at the end copy(nothing in, the last result
- * out, 1). Its decodes need pd_plan.early_kv 0: with the flag stage 1 reads its
- * block table before its wait, while the copy in front may still write it. A
- * loop whose last kernel of a step lets its dependents start before its own wait
- * (paged_decode_qkv_norm_rope_write alone) copies after it with after_wait 1:
- * the next step's inputs in and that step's own result out.
  * Every pointer of a non-empty copy is device memory of the current device or
  * page-locked host memory (cudaHostAlloc / cudaHostRegister, reached through its
- * device address), 16-byte aligned; sizes are multiples of 16; a copy's source
- * and destination do not overlap. A copy of 0 bytes is skipped (its pointers
- * may be NULL); the kernel is launched even when both are empty.
+ * device address), 16-byte aligned; a copy's source and destination do not
+ * overlap, nor do the copies of one call.
+ *
+ * A decode loop with one step of look-ahead for q: two q buffers and two result
+ * buffers used alternately. Without pd_plan.early_kv: copy(step 0's inputs in,
+ * 0); per step i: decode(i) [+ merge(i)], then copy(step i+1's inputs in, step
+ * i-1's result out, 0); at the end copy(the last result out, 1). With
+ * pd_plan.early_kv stage 1 reads its block table and lengths before its wait,
+ * so the copy in front of it must not write them: the block table and lengths
+ * go two steps ahead (three buffers), copied for steps 0 and 1 with an ordinary
+ * copy before the loop and for step i+2 by step i's copy. A loop whose last
+ * kernel of a step lets its dependents start before its own wait
+ * (paged_decode_qkv_norm_rope_write alone) copies after it with after_wait 1:
+ * the next step's inputs in and that step's own result out.
+ *
  * Returns PD_ERR_INVALID_ARG without launching (pageable or foreign memory,
- * misalignment, overlap, after_wait not 0 or 1), PD_ERR_CUDA if the launch fails.
+ * misalignment, a size off 16, overlap, more than PD_MAX_STAGE_COPIES copies,
+ * after_wait not 0 or 1), PD_ERR_CUDA if the launch fails.
  */
-pd_status paged_decode_stage_copy(void* in_dst, const void* in_src, size_t in_bytes, void* out_dst,
-                                  const void* out_src, size_t out_bytes, int32_t after_wait, void* stream);
+pd_status paged_decode_stage_copy(const pd_copy* copies, int32_t num_copies, int32_t after_wait, void* stream);
 
 /* Static, human-readable name of a status. */
 const char* paged_decode_status_string(pd_status status);

@@ -154,7 +154,7 @@ def load_library(path: Optional[str] = None):
         lib.paged_decode_global_partial.restype = ctypes.c_int
         lib.paged_decode_combine.argtypes = [i32, i32, i32, vp, vp, vp, vp]
         lib.paged_decode_combine.restype = ctypes.c_int
-        lib.paged_decode_stage_copy.argtypes = [vp, vp, u64, vp, vp, u64, i32, vp]
+        lib.paged_decode_stage_copy.argtypes = [ctypes.c_void_p, i32, i32, vp]
         lib.paged_decode_stage_copy.restype = ctypes.c_int
         lib.paged_decode_rope_table.argtypes = [ctypes.c_double, i32, i32, vp, vp]
         lib.paged_decode_rope_table.restype = ctypes.c_int
@@ -423,25 +423,31 @@ def paged_decode_global_partial(plan: Plan, q, k_pool, v_pool, block_tables, seq
     _check(st, "paged_decode_global_partial")
 
 
-def paged_decode_stage_copy(in_dst=None, in_src=None, out_dst=None, out_src=None, after_wait: int = 0,
-                            stream=None) -> None:
-    """Copy in_src -> in_dst and out_src -> out_dst (tensors of equal byte size,
-    device or page-locked host memory; a pair left None is skipped) as one kernel
-    in the stream's chain of programmatic dependent launches; after_wait 1 waits
-    for the launch in front first."""
-    def nbytes(dst, src):
+MAX_STAGE_COPIES = 4  # PD_MAX_STAGE_COPIES
+
+
+class Copy(ctypes.Structure):
+    _fields_ = [("dst", ctypes.c_void_p), ("src", ctypes.c_void_p), ("bytes", ctypes.c_size_t)]
+
+
+def paged_decode_stage_copy(pairs, after_wait: int = 0, stream=None) -> None:
+    """Copy each (dst, src) pair of tensors (equal byte sizes; device or
+    page-locked host memory; a pair of Nones is skipped) as one kernel in the
+    stream's chain of programmatic dependent launches; after_wait 1 waits for
+    the launch in front first."""
+    entries = []
+    for dst, src in pairs:
         if dst is None and src is None:
-            return 0
+            continue
         if dst is None or src is None:
             raise ValueError("a copy needs both its source and its destination")
         n = dst.numel() * dst.element_size()
         if src.numel() * src.element_size() != n:
             raise ValueError(f"copy of {src.numel() * src.element_size()} bytes into {n} bytes")
-        return n
-
-    n_in, n_out = nbytes(in_dst, in_src), nbytes(out_dst, out_src)
-    st = load_library().paged_decode_stage_copy(_ptr(in_dst), _ptr(in_src), n_in, _ptr(out_dst), _ptr(out_src),
-                                                n_out, int(after_wait), _stream_ptr(stream))
+        entries.append(Copy(_ptr(dst), _ptr(src), n))
+    arr = (Copy * max(1, len(entries)))(*entries)
+    st = load_library().paged_decode_stage_copy(ctypes.cast(arr, ctypes.c_void_p), len(entries), int(after_wait),
+                                                _stream_ptr(stream))
     _check(st, "paged_decode_stage_copy")
 
 

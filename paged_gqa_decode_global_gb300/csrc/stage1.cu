@@ -392,8 +392,11 @@ __device__ __forceinline__ int stage1_cta(const Stage1Params& p, uint8_t* smem) 
     named_bar_arrive(2, C::THREADS);
   else
     named_bar_sync(2, C::THREADS);
-  // a merge launched behind this kernel may start its (waiting) CTAs now
-  grid_launch_dependents();
+  // a merge launched behind this kernel may start its (waiting) CTAs now.
+  // Every thread that signals has waited for the launch in front: a producer
+  // lane with early_kv signals once it has (below), so that a launch behind
+  // this one can rely on everything in front of this one being complete.
+  if (!early) grid_launch_dependents();
 
   // ---- producer ------------------------------------------------------------------
   if (warp == C::NW) {
@@ -456,6 +459,7 @@ __device__ __forceinline__ int stage1_cta(const Stage1Params& p, uint8_t* smem) 
         fetch(jb + C::NST, pg_next, sc_next);
         if (!waited && (jb >= C::NST || blk_lo + (jb + 1) * C::NSUB * C::TB > fresh_from)) {
           grid_dependency_wait();
+          grid_launch_dependents();
           waited = true;
         }
         const int round = jb / C::NST;
@@ -511,7 +515,10 @@ __device__ __forceinline__ int stage1_cta(const Stage1Params& p, uint8_t* smem) 
         }
       }
     }
-    if (!waited) grid_dependency_wait();
+    if (!waited) {
+      grid_dependency_wait();
+      grid_launch_dependents();
+    }
     // no copy may still be landing in shared memory when the CTA exits: each
     // lane waits for its stage's last copies
     if (last_jb >= 0 && !mbar_wait(&full_bar[lane], (last_jb / C::NST) & 1)) err_bits |= kErrTimeout;
@@ -569,6 +576,7 @@ __device__ __forceinline__ int stage1_cta(const Stage1Params& p, uint8_t* smem) 
           const int jb = (j0 + k) / C::NSUB;  // stage block
           if (!waited && (jb >= C::NST || blk_lo + (j0 + k + C::NSUB) * C::TB > fresh_from)) {
             grid_dependency_wait();
+            grid_launch_dependents();
             waited = true;
           }
           const int st = jb % C::NST;
@@ -622,7 +630,10 @@ __device__ __forceinline__ int stage1_cta(const Stage1Params& p, uint8_t* smem) 
       // lane 0 is done with this batch's entries before they are rewritten
       stop = __shfl_sync(kFullMask, stop, 0);
     }
-    if (early && !(lane == 0 && waited)) grid_dependency_wait();
+    if (early && !(lane == 0 && waited)) {
+      grid_dependency_wait();
+      grid_launch_dependents();
+    }
     // no copy may still be landing in shared memory when the CTA exits (one
     // deadline for all stages)
     if (lane == 0) {

@@ -10,7 +10,7 @@
 // stream its older KV rows while the step in front drains. Here each copy is a
 // kernel that lets the launch behind it start at once.
 //
-// Order: with after_wait = 0 both copies run, then the kernel waits for the
+// Order: with after_wait = 0 the copies run, then the kernel waits for the
 // launch in front of it (griddepcontrol.wait), so it completes only after that
 // launch -- the chain's order of completions is kept, and a launch behind it
 // that waits sees everything in front complete. With after_wait = 1 it waits
@@ -43,13 +43,17 @@ __device__ __forceinline__ void copy_span(const uint4* __restrict__ src, uint4* 
   for (; i < n; i += stride) dst[i] = src[i];
 }
 
-__global__ void __launch_bounds__(kCopyThreads) stage_copy_kernel(const uint4* a_src, uint4* a_dst, size_t n_a,
-                                                                  const uint4* b_src, uint4* b_dst, size_t n_b,
-                                                                  int after_wait) {
+struct CopyList {
+  const uint4* src[PD_MAX_STAGE_COPIES];
+  uint4* dst[PD_MAX_STAGE_COPIES];
+  size_t n[PD_MAX_STAGE_COPIES];  // 16-byte units; 0 for an unused slot
+};
+
+__global__ void __launch_bounds__(kCopyThreads) stage_copy_kernel(const CopyList list, int after_wait) {
   asm volatile("griddepcontrol.launch_dependents;");
   if (after_wait) asm volatile("griddepcontrol.wait;" ::: "memory");
-  copy_span(a_src, a_dst, n_a);
-  copy_span(b_src, b_dst, n_b);
+#pragma unroll
+  for (int c = 0; c < PD_MAX_STAGE_COPIES; ++c) copy_span(list.src[c], list.dst[c], list.n[c]);
   if (!after_wait) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
@@ -86,26 +90,28 @@ bool overlap(const void* a, const void* b, size_t n) {
 }  // namespace
 }  // namespace pd
 
-extern "C" pd_status paged_decode_stage_copy(void* in_dst, const void* in_src, size_t in_bytes, void* out_dst,
-                                             const void* out_src, size_t out_bytes, int32_t after_wait,
+extern "C" pd_status paged_decode_stage_copy(const pd_copy* copies, int32_t num_copies, int32_t after_wait,
                                              void* stream) {
   using namespace pd;
   if (after_wait != 0 && after_wait != 1) return PD_ERR_INVALID_ARG;
-  if ((in_bytes | out_bytes) & 15u) return PD_ERR_INVALID_ARG;
-  const void* ends[2][2] = {{in_src, in_dst}, {out_src, out_dst}};
-  const size_t bytes[2] = {in_bytes, out_bytes};
-  const void* dev[2][2] = {{nullptr, nullptr}, {nullptr, nullptr}};
-  for (int c = 0; c < 2; ++c) {
-    if (bytes[c] == 0) continue;
-    for (int e = 0; e < 2; ++e) {
-      if (!ends[c][e] || !aligned16(ends[c][e])) return PD_ERR_INVALID_ARG;
-      dev[c][e] = device_address(ends[c][e]);
-      if (!dev[c][e] || !aligned16(dev[c][e])) return PD_ERR_INVALID_ARG;
-    }
-    if (overlap(ends[c][0], ends[c][1], bytes[c])) return PD_ERR_INVALID_ARG;
+  if (num_copies < 0 || num_copies > PD_MAX_STAGE_COPIES || (num_copies > 0 && !copies)) return PD_ERR_INVALID_ARG;
+  CopyList list{};
+  size_t longest = 0;
+  for (int c = 0; c < num_copies; ++c) {
+    const pd_copy& cp = copies[c];
+    if (cp.bytes == 0) continue;
+    if (cp.bytes & 15u) return PD_ERR_INVALID_ARG;
+    if (!cp.dst || !cp.src || !aligned16(cp.dst) || !aligned16(cp.src)) return PD_ERR_INVALID_ARG;
+    if (overlap(cp.dst, cp.src, cp.bytes)) return PD_ERR_INVALID_ARG;
+    const void* s = device_address(cp.src);
+    const void* d = device_address(cp.dst);
+    if (!s || !d || !aligned16(s) || !aligned16(d)) return PD_ERR_INVALID_ARG;
+    list.src[c] = static_cast<const uint4*>(s);
+    list.dst[c] = static_cast<uint4*>(const_cast<void*>(d));
+    list.n[c] = cp.bytes / 16;
+    if (list.n[c] > longest) longest = list.n[c];
   }
-  const size_t n = (in_bytes > out_bytes ? in_bytes : out_bytes) / 16;
-  size_t blocks = (n + kCopyThreads - 1) / kCopyThreads;
+  size_t blocks = (longest + kCopyThreads - 1) / kCopyThreads;
   if (blocks > (size_t)kMaxCopyBlocks) blocks = kMaxCopyBlocks;
   if (blocks < 1) blocks = 1;
   cudaLaunchConfig_t cfg{};
@@ -117,11 +123,7 @@ extern "C" pd_status paged_decode_stage_copy(void* in_dst, const void* in_src, s
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const cudaError_t e =
-      cudaLaunchKernelEx(&cfg, stage_copy_kernel, static_cast<const uint4*>(dev[0][0]),
-                         static_cast<uint4*>(const_cast<void*>(dev[0][1])), in_bytes / 16,
-                         static_cast<const uint4*>(dev[1][0]), static_cast<uint4*>(const_cast<void*>(dev[1][1])),
-                         out_bytes / 16, (int)after_wait);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, stage_copy_kernel, list, (int)after_wait);
   if (e != cudaSuccess) {
     (void)cudaGetLastError();
     return PD_ERR_CUDA;

@@ -1,15 +1,17 @@
 """paged_decode_stage_copy: copies between page-locked host memory and device
 memory as one kernel in the stream's chain of programmatic dependent launches,
-and the host-in/host-out decode loop built on it (one step of look-ahead: after
-step i's kernels one copy brings step i + 1's inputs in and takes step i - 1's
-result out; a last copy, waiting first, takes the final result out).
+and the host-in/host-out decode loop built on it (after step i's kernels one
+copy brings step i + 1's q in, the block table and lengths of the step one
+on -- two on with pd_plan.early_kv, whose stage 1 reads them before its wait --
+and takes step i - 1's result out; a last copy, waiting first, takes the final
+result out).
 
 The loop's steps each get their own q and lengths, so a copy that landed late
 or a result taken before its step finished shows up as a wrong step; every
 host result is compared bit for bit with the same decode run on its own
 (itself held to the oracle by the parity tests). Eager calls and a CUDA graph
-of the loop, merge in a cluster and through the merge kernel, K=V and K!=V,
-a window layer, FP8.
+of the loop, with and without early_kv, merge in a cluster and through the
+merge kernel, K=V and K!=V, a window layer, FP8.
 """
 import numpy as np
 import pytest
@@ -28,23 +30,28 @@ def test_round_trip_through_the_device(nbytes, after_wait):
     src = torch.randint(0, 256, (nbytes,), dtype=torch.uint8, generator=g).pin_memory()
     dev = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
     back = torch.zeros(nbytes, dtype=torch.uint8).pin_memory()
-    b.paged_decode_stage_copy(dev, src, None, None, after_wait)
-    b.paged_decode_stage_copy(None, None, back, dev, 1)  # waits for the copy in front
+    b.paged_decode_stage_copy([(dev, src)], after_wait)
+    b.paged_decode_stage_copy([(back, dev)], 1)  # waits for the copy in front
     torch.cuda.synchronize()
     assert torch.equal(back, src)
     assert torch.equal(dev.cpu(), src)
 
 
-def test_both_copies_of_one_launch():
+def test_four_copies_of_one_launch():
     g = torch.Generator().manual_seed(7)
     a = torch.randint(0, 256, (1 << 16,), dtype=torch.uint8, generator=g).pin_memory()
     c = torch.randint(0, 256, (3 * 1024,), dtype=torch.uint8, generator=g).cuda()
-    a_dev = torch.empty_like(a, device="cuda")
+    e = torch.randint(0, 256, (48,), dtype=torch.uint8, generator=g).pin_memory()
+    f = torch.randint(0, 256, (5 << 20,), dtype=torch.uint8, generator=g).cuda()
+    a_dev, e_dev = torch.empty_like(a, device="cuda"), torch.empty_like(e, device="cuda")
     c_host = torch.zeros(c.shape, dtype=torch.uint8).pin_memory()
-    b.paged_decode_stage_copy(a_dev, a, c_host, c, 0)
+    f_dev = torch.zeros_like(f)
+    b.paged_decode_stage_copy([(a_dev, a), (c_host, c), (e_dev, e), (f_dev, f)], 0)
     torch.cuda.synchronize()
     assert torch.equal(a_dev.cpu(), a)
     assert torch.equal(c_host, c.cpu())
+    assert torch.equal(e_dev.cpu(), e)
+    assert torch.equal(f_dev, f)
 
 
 def test_refused_without_launching():
@@ -60,10 +67,13 @@ def test_refused_without_launching():
     ]
     for dst, src, wait in cases:
         with pytest.raises(b.PagedDecodeError) as e:
-            b.paged_decode_stage_copy(dst, src, None, None, wait)
+            b.paged_decode_stage_copy([(dst, src)], wait)
         assert e.value.status == b.PD_ERR_INVALID_ARG
+    with pytest.raises(b.PagedDecodeError) as e:  # more than PD_MAX_STAGE_COPIES
+        b.paged_decode_stage_copy([(dev[16 * i:16 * i + 16], pinned[16 * i:16 * i + 16]) for i in range(5)])
+    assert e.value.status == b.PD_ERR_INVALID_ARG
     with pytest.raises(ValueError):
-        b.paged_decode_stage_copy(dev, None)
+        b.paged_decode_stage_copy([(dev, None)])
     torch.cuda.synchronize()
     assert int(dev.count_nonzero()) == 0
 
@@ -85,19 +95,45 @@ def _layer(case, seed):
     return (synth.quantize_kv_fp8(li) if fp8 else li), sms
 
 
+def _staged(tensors_per_step, parts):
+    """One pinned host buffer per step holding its tensors (each 256-byte
+    aligned) and the layout (offsets, total bytes) of `parts`."""
+    offs, total = [], 0
+    for t in parts:
+        offs.append(total)
+        total += (t.numel() * t.element_size() + 255) // 256 * 256
+    hosts = []
+    for tensors in tensors_per_step:
+        h = torch.zeros(total, dtype=torch.uint8).pin_memory()
+        for t, o in zip(tensors, offs):
+            n = t.numel() * t.element_size()
+            h[o:o + n].view(t.dtype).view(t.shape).copy_(t.cpu())
+        hosts.append(h)
+    return hosts, offs, total
+
+
+def _device_buffers(parts, offs, total, n):
+    bufs = [torch.zeros(total, dtype=torch.uint8, device="cuda") for _ in range(n)]
+    views = [[s[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape) for t, o in zip(parts, offs)]
+             for s in bufs]
+    return bufs, views
+
+
 @pytest.mark.parametrize("graph", [False, True], ids=["eager", "graph"])
+@pytest.mark.parametrize("early_kv", [0, 1], ids=["table-1-ahead", "early_kv-table-2-ahead"])
 @pytest.mark.parametrize("case", LOOP_CASES, ids=[f"d{c[0]}-G{c[1]}-kvs{int(c[3])}-W{c[4]}-sm{c[6]}-fp8{int(c[7])}"
                                                   for c in LOOP_CASES])
-def test_host_in_host_out_loop(case, graph):
+def test_host_in_host_out_loop(case, early_kv, graph):
     li, sms = _layer(case, seed=11)
-    step = b.LayerStep.for_inputs(li, sm_count=sms)  # early_kv 0: the copy in front writes the block table
+    step = b.LayerStep.for_inputs(li, sm_count=sms, early_kv=bool(early_kv))
+    ahead = 2 if early_kv else 1  # steps the block table and lengths go ahead of their decode
     fp8 = hasattr(li, "k8")
     k, v = (li.k8, li.v8) if fp8 else (li.k_pool, li.v_pool)
     ks, vs = (li.k_scale, li.v_scale) if fp8 else (None, None)
     n_steps = 7
     gen = torch.Generator(device="cuda").manual_seed(3)
     lens0 = li.seq_lens.cpu()
-    # each step its own q and lengths (a request shrinking by j tokens, never below 1 if it had any)
+    # each step its own q and lengths (a request shrinking by 5 tokens a step, never below 1 if it had any)
     qs = [(torch.randn(li.q.shape, generator=gen, device="cuda")).to(torch.bfloat16) for _ in range(n_steps)]
     lens = [torch.where(lens0 > 0, torch.clamp(lens0 - 5 * j, min=1), lens0).to(torch.int32) for j in range(n_steps)]
 
@@ -110,44 +146,38 @@ def test_host_in_host_out_loop(case, graph):
     torch.cuda.synchronize()
     assert step.check() == 0
 
-    # one pinned staging buffer per step: q | block table | lengths, each 256-byte aligned
-    parts = [li.q, li.block_tables, li.seq_lens]
-    offs, total = [], 0
-    for t in parts:
-        offs.append(total)
-        total += (t.numel() * t.element_size() + 255) // 256 * 256
-    stage_h = []
-    for j in range(n_steps):
-        h = torch.zeros(total, dtype=torch.uint8).pin_memory()
-        for t, o in zip([qs[j].cpu(), li.block_tables.cpu(), lens[j]], offs):
-            n = t.numel() * t.element_size()
-            h[o:o + n].view(t.dtype).view(t.shape).copy_(t)
-        stage_h.append(h)
-    dev_stage = [torch.zeros(total, dtype=torch.uint8, device="cuda") for _ in range(2)]
-    views = [[s[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape) for t, o in zip(parts, offs)]
-             for s in dev_stage]
+    q_h, q_offs, q_total = _staged([[qs[j]] for j in range(n_steps)], [li.q])
+    meta_parts = [li.block_tables, li.seq_lens]
+    meta_h, m_offs, m_total = _staged([[li.block_tables, lens[j]] for j in range(n_steps)], meta_parts)
+    q_dev, q_views = _device_buffers([li.q], q_offs, q_total, 2)
+    m_dev, m_views = _device_buffers(meta_parts, m_offs, m_total, 3)
     dev_out = [torch.empty_like(li.q) for _ in range(2)]
     host_out = [torch.zeros(li.q.shape, dtype=torch.bfloat16).pin_memory() for _ in range(n_steps)]
     stream = torch.cuda.Stream()
 
     def loop():
-        b.paged_decode_stage_copy(dev_stage[0], stage_h[0], None, None, 0, stream)
+        # ordinary copies before the loop: step 0's q, the tables of the first `ahead` steps
+        q_dev[0].copy_(q_h[0], non_blocking=True)
+        for j in range(ahead):
+            m_dev[j % 3].copy_(meta_h[j], non_blocking=True)
         for j in range(n_steps):
-            cur, other = j % 2, (j + 1) % 2
-            q, bt, sl = views[cur]
-            step(q, k, v, bt, sl, li.scale, dev_out[cur], stream, k_scale=ks, v_scale=vs)
-            more, prev = j + 1 < n_steps, j > 0
-            b.paged_decode_stage_copy(dev_stage[other] if more else None, stage_h[j + 1] if more else None,
-                                      host_out[j - 1] if prev else None, dev_out[other] if prev else None, 0,
-                                      stream)
-        b.paged_decode_stage_copy(None, None, host_out[n_steps - 1], dev_out[(n_steps - 1) % 2], 1, stream)
+            (q,), (bt, sl) = q_views[j % 2], m_views[j % 3]
+            step(q, k, v, bt, sl, li.scale, dev_out[j % 2], stream, k_scale=ks, v_scale=vs)
+            other = (j + 1) % 2
+            pairs = []
+            if j + 1 < n_steps:
+                pairs.append((q_dev[other], q_h[j + 1]))
+            if j + ahead < n_steps:
+                pairs.append((m_dev[(j + ahead) % 3], meta_h[j + ahead]))
+            if j > 0:
+                pairs.append((host_out[j - 1], dev_out[other]))
+            b.paged_decode_stage_copy(pairs, 0, stream)
+        b.paged_decode_stage_copy([(host_out[n_steps - 1], dev_out[(n_steps - 1) % 2])], 1, stream)
 
     if graph:
         with torch.cuda.stream(stream):
             loop()  # warm-up outside the capture
         torch.cuda.synchronize()
-        for h in host_out:
-            h.zero_()
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             loop()
@@ -218,14 +248,14 @@ def test_new_token_step_loop_copies_after_waiting(graph):
     stream = torch.cuda.Stream()
 
     def loop():
-        b.paged_decode_stage_copy(dev_stage[0], stage_h[0], None, None, 0, stream)
+        b.paged_decode_stage_copy([(dev_stage[0], stage_h[0])], 0, stream)
         for j in range(n_steps):
             cur, other = j % 2, (j + 1) % 2
             q, k, v, sl = views[cur]
             prep(q, k, v, sl, dev_q[cur], stream)
             more = j + 1 < n_steps
-            b.paged_decode_stage_copy(dev_stage[other] if more else None, stage_h[j + 1] if more else None,
-                                      host_q[j], dev_q[cur], 1, stream)
+            b.paged_decode_stage_copy([(dev_stage[other], stage_h[j + 1]) if more else (None, None),
+                                       (host_q[j], dev_q[cur])], 1, stream)
 
     if graph:
         with torch.cuda.stream(stream):
