@@ -60,14 +60,14 @@ FALLBACK_HBM_GBS = 6800.0
 # entry whose sources or plan differ from the run's is not used (the captures
 # and their commands are summarised under profiles/).
 NCU_TRAFFIC = {
-    "ab3edbe6d252c5e4": {
-        "w4a": (1073899776 + 2798080, (9, 3648, 1)),
-        "w2": (67297280 + 514560, (4, 256, 2)),
-        "w3": (68277504 + 376064, (2, 544, 2)),
-        "w4a-fp8": (537291264 + 2669824, (9, 3648, 1)),
-        "w5global": (1596573952 + 4372480, (19, 5456, 1)),
-        "w5global-fp8": (798929920 + 4911360, (19, 5456, 1)),
-        "w5sliding": (68173568 + 622080, (2, 544, 2)),
+    "e0d402f4fe9a104a": {
+        "w4a": (1074000640 + 2827264, (9, 3648, 1)),
+        "w2": (67294720 + 435456, (4, 256, 2)),
+        "w3": (68276736 + 323328, (2, 544, 2)),
+        "w4a-fp8": (537289472 + 2491648, (9, 3648, 1)),
+        "w5global": (1596588288 + 4432896, (19, 5456, 1)),
+        "w5global-fp8": (798931456 + 4816896, (19, 5456, 1)),
+        "w5sliding": (68172800 + 510464, (2, 544, 2)),
     },
 }
 
