@@ -3,9 +3,11 @@
 #include <atomic>
 #include <cmath>
 #include <cstring>
+#include <mutex>
 
 #include <cuda_runtime.h>
 
+#include "host_ctx.h"
 #include "paged_decode.h"
 #include "pd_kernels.h"
 
@@ -16,10 +18,20 @@ bool plan_is_valid(const pd_plan* plan);
 namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kMaxDevices = 64;
+constexpr int kMaxContexts = 64;
 
-// Per device, one bit per variant whose dynamic shared-memory limit is raised.
-std::atomic<uint64_t> g_smem_ready[kMaxDevices];
+// Per CUDA context, one bit per variant whose dynamic shared-memory limit has
+// been raised there (a function attribute belongs to the context it was set in).
+struct SmemReady {
+  unsigned long long ctx_id;
+  uint64_t bits;
+};
+#define PD_VARIANT_ID_FITS_A_BIT(ID, ...) static_assert((ID) >= 0 && (ID) < 64, "one bit per variant id");
+PD_FOR_EACH_VARIANT(PD_VARIANT_ID_FITS_A_BIT)
+#undef PD_VARIANT_ID_FITS_A_BIT
+std::mutex g_smem_mu;
+SmemReady g_smem_ready[kMaxContexts] = {};
+int g_smem_contexts = 0;
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
@@ -98,13 +110,34 @@ pd_status encode_pool_maps(pd::Stage1Params& p, const void* k_pool, const void* 
 }
 
 pd_status ensure_smem_attr(int variant, const void* fn, int smem_bytes) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return PD_ERR_CUDA;
+  const pd::CtxFns* f = pd::ctx_fns();
+  const unsigned long long id = f ? pd::current_ctx_id(*f) : 0;
   const uint64_t bit = 1ull << variant;
-  if (dev >= 0 && dev < kMaxDevices && (g_smem_ready[dev].load(std::memory_order_acquire) & bit)) return PD_OK;
-  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes) != cudaSuccess)
+  std::lock_guard<std::mutex> lock(g_smem_mu);
+  SmemReady* e = nullptr;
+  if (id != 0) {
+    for (int i = 0; i < g_smem_contexts; ++i)
+      if (g_smem_ready[i].ctx_id == id) e = &g_smem_ready[i];
+    if (e && (e->bits & bit)) return PD_OK;
+  }
+  // the first launch of this instance in this context (or no context id to
+  // key on: set it every time)
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes) != cudaSuccess) {
+    (void)cudaGetLastError();
     return PD_ERR_CUDA;
-  if (dev >= 0 && dev < kMaxDevices) g_smem_ready[dev].fetch_or(bit, std::memory_order_acq_rel);
+  }
+  const unsigned long long now = f ? pd::current_ctx_id(*f) : 0;  // the runtime call may have made one current
+  if (now == 0) return PD_OK;
+  if (!e || now != id) {
+    e = nullptr;
+    for (int i = 0; i < g_smem_contexts; ++i)
+      if (g_smem_ready[i].ctx_id == now) e = &g_smem_ready[i];
+    if (!e && g_smem_contexts < kMaxContexts) {
+      e = &g_smem_ready[g_smem_contexts++];
+      *e = SmemReady{now, 0};
+    }
+  }
+  if (e) e->bits |= bit;
   return PD_OK;
 }
 

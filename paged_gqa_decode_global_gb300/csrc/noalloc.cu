@@ -26,6 +26,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "host_ctx.h"
 #include "paged_decode.h"
 
 namespace pd {
@@ -40,46 +41,6 @@ constexpr int kMaxContexts = 64;
 // Partials, log-sum-exps and the device error word of the calls below.
 static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 
-// Driver entry points for the current context and its process-unique id,
-// fetched once through the runtime (the library does not link libcuda).
-using CtxGetCurrentFn = CUresult (*)(CUcontext*);
-using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
-
-struct CtxFns {
-  CtxGetCurrentFn get_current = nullptr;
-  CtxGetIdFn get_id = nullptr;
-};
-
-void* driver_fn(const char* name) {
-  void* sym = nullptr;
-  cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
-  if (cudaGetDriverEntryPointByVersion(name, &sym, 12000, cudaEnableDefault, &q) != cudaSuccess ||
-      q != cudaDriverEntryPointSuccess) {
-    (void)cudaGetLastError();
-    return nullptr;
-  }
-  return sym;
-}
-
-const CtxFns* ctx_fns() {
-  static CtxFns fns;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    fns.get_current = reinterpret_cast<CtxGetCurrentFn>(driver_fn("cuCtxGetCurrent"));
-    fns.get_id = reinterpret_cast<CtxGetIdFn>(driver_fn("cuCtxGetId"));
-  });
-  return (fns.get_current && fns.get_id) ? &fns : nullptr;
-}
-
-// The id of the context current on this thread, or 0 if there is none yet.
-unsigned long long current_ctx_id(const CtxFns& f) {
-  CUcontext ctx = nullptr;
-  unsigned long long id = 0;
-  if (f.get_current(&ctx) != CUDA_SUCCESS || !ctx) return 0;
-  if (f.get_id(ctx, &id) != CUDA_SUCCESS) return 0;
-  return id;
-}
-
 std::mutex g_mu;
 struct Entry {
   unsigned long long ctx_id;
@@ -90,9 +51,9 @@ int g_cached = 0;
 
 // Device address of g_scratch in the current context.
 pd_status scratch_for_current_context(void** out) {
-  const CtxFns* f = ctx_fns();
+  const pd::CtxFns* f = pd::ctx_fns();
   if (!f) return PD_ERR_CUDA;
-  unsigned long long id = current_ctx_id(*f);
+  unsigned long long id = pd::current_ctx_id(*f);
   std::lock_guard<std::mutex> lock(g_mu);
   if (id != 0) {
     for (int i = 0; i < g_cached; ++i)
@@ -108,7 +69,7 @@ pd_status scratch_for_current_context(void** out) {
     (void)cudaGetLastError();
     return PD_ERR_CUDA;
   }
-  if (id == 0) id = current_ctx_id(*f);
+  if (id == 0) id = pd::current_ctx_id(*f);
   if (id != 0 && g_cached < kMaxContexts) g_cache[g_cached++] = Entry{id, p};
   *out = p;
   return PD_OK;
