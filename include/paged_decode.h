@@ -173,7 +173,7 @@ typedef struct {
  * 9..16: two, a CTA each over short contexts, one CTA for both over long ones;
  * head_dim 256 or 512 -- at head_dim 128 only 1, 2, 4 and 8).
  * Returns PD_ERR_INVALID_ARG for a malformed shape or length, PD_ERR_UNSUPPORTED
- * for a head_dim or group size this build has no kernel for (group > 16).
+ * for a head_dim or group size no kernel instance of the library serves (group > 16).
  */
 pd_status paged_decode_plan(const pd_layer_desc* layer, int32_t batch, const int32_t* seq_lens_host,
                             int32_t sm_count, pd_plan* plan);
