@@ -880,6 +880,8 @@ __device__ __forceinline__ int stage1_cta(const Stage1Params& p, uint8_t* smem) 
         const bool ok1 = ok && t_a + 1 >= tlo && t_a + 1 < thi;
         const bool ok2 = ok && t_a + 8 >= tlo && t_a + 8 < thi;
         const bool ok3 = ok && t_a + 9 >= tlo && t_a + 9 < thi;
+        // a block every row of which is attended (all but the edge blocks) needs no zeroing
+        const bool edge_u = __any_sync(kFullMask, !(ok0 && ok1 && ok2 && ok3));
         const uint8_t* vstg = (C::KVS ? stg : stg + C::V_OFFSET) + u * C::KV_BYTES;
 #pragma unroll
         for (int sl = 0; sl < C::TMA_SLABS; ++sl) {
@@ -890,10 +892,12 @@ __device__ __forceinline__ int stage1_cta(const Stage1Params& p, uint8_t* smem) 
           uint4 r1 = *reinterpret_cast<const uint4*>(vp + (tv + 1) * 128 + ((qh ^ (tv + 1)) << 4));
           uint4 r2 = *reinterpret_cast<const uint4*>(vp + (tv + 8) * 128 + ((qh ^ tv) << 4));
           uint4 r3 = *reinterpret_cast<const uint4*>(vp + (tv + 9) * 128 + ((qh ^ (tv + 1)) << 4));
-          if (!ok0) r0 = zero;
-          if (!ok1) r1 = zero;
-          if (!ok2) r2 = zero;
-          if (!ok3) r3 = zero;
+          if (edge_u) {
+            if (!ok0) r0 = zero;
+            if (!ok1) r1 = zero;
+            if (!ok2) r2 = zero;
+            if (!ok3) r3 = zero;
+          }
           const uint32_t x0[4] = {r0.x, r0.y, r0.z, r0.w}, x1[4] = {r1.x, r1.y, r1.z, r1.w};
           const uint32_t x2[4] = {r2.x, r2.y, r2.z, r2.w}, x3[4] = {r3.x, r3.y, r3.z, r3.w};
 #pragma unroll
