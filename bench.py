@@ -60,14 +60,14 @@ FALLBACK_HBM_GBS = 6800.0
 # entry whose sources or plan differ from the run's is not used (the captures
 # and their commands are summarised under profiles/).
 NCU_TRAFFIC = {
-    "e0d402f4fe9a104a": {
-        "w4a": (1074000640 + 2827264, (9, 3648, 1)),
-        "w2": (67294720 + 435456, (4, 256, 2)),
-        "w3": (68276736 + 323328, (2, 544, 2)),
-        "w4a-fp8": (537289472 + 2491648, (9, 3648, 1)),
-        "w5global": (1596588288 + 4432896, (19, 5456, 1)),
-        "w5global-fp8": (798931456 + 4816896, (19, 5456, 1)),
-        "w5sliding": (68172800 + 510464, (2, 544, 2)),
+    "390644f8bf77bb67": {
+        "w4a": (1073983488 + 2760704, (9, 3648, 1)),
+        "w2": (67294976 + 501504, (4, 256, 2)),
+        "w3": (68276992 + 407808, (2, 544, 2)),
+        "w4a-fp8": (537289728 + 2464768, (9, 3648, 1)),
+        "w5global": (1596576512 + 4325632, (19, 5456, 1)),
+        "w5global-fp8": (798929920 + 4875776, (19, 5456, 1)),
+        "w5sliding": (68173312 + 504320, (2, 544, 2)),
     },
 }
 
