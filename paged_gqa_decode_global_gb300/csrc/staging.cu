@@ -95,14 +95,19 @@ extern "C" pd_status paged_decode_stage_copy(const pd_copy* copies, int32_t num_
   using namespace pd;
   if (after_wait != 0 && after_wait != 1) return PD_ERR_INVALID_ARG;
   if (num_copies < 0 || num_copies > PD_MAX_STAGE_COPIES || (num_copies > 0 && !copies)) return PD_ERR_INVALID_ARG;
-  CopyList list{};
-  size_t longest = 0;
+  // every check that needs no CUDA call first, over the whole list
   for (int c = 0; c < num_copies; ++c) {
     const pd_copy& cp = copies[c];
     if (cp.bytes == 0) continue;
     if (cp.bytes & 15u) return PD_ERR_INVALID_ARG;
     if (!cp.dst || !cp.src || !aligned16(cp.dst) || !aligned16(cp.src)) return PD_ERR_INVALID_ARG;
     if (overlap(cp.dst, cp.src, cp.bytes)) return PD_ERR_INVALID_ARG;
+  }
+  CopyList list{};
+  size_t longest = 0;
+  for (int c = 0; c < num_copies; ++c) {
+    const pd_copy& cp = copies[c];
+    if (cp.bytes == 0) continue;
     const void* s = device_address(cp.src);
     const void* d = device_address(cp.dst);
     if (!s || !d || !aligned16(s) || !aligned16(d)) return PD_ERR_INVALID_ARG;

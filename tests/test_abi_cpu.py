@@ -7,6 +7,7 @@ import os
 import re
 
 import pytest
+import torch
 
 from paged_gqa_decode_global_gb300 import binding as b
 from paged_gqa_decode_global_gb300 import build
@@ -219,6 +220,36 @@ def test_groups_above_8_are_served_by_column_tiles(lib, G, d, window, kvs):
     f8 = b.paged_decode_plan(b.layer_desc(4 * G, 4, d, 16, 10 ** 5, 2000, window, kvs, b.PD_KV_FP8_E4M3),
                              [3000, 40], 152)
     assert f8.grid_y == 4 * tiles
+
+
+def test_stage_copy_rejects_bad_arguments_before_any_cuda_call(lib):
+    """Refusals that need no pointer lookup come first, so they answer here,
+    with no GPU: a copy count off 0..4, a missing list, a bad wait flag, a size
+    off 16 bytes, a NULL or misaligned pointer, overlapping ends."""
+    fake = 1 << 20
+
+    def copies(*entries):
+        arr = (b.Copy * max(1, len(entries)))(*[b.Copy(d, s_, n) for d, s_, n in entries])
+        return ctypes.cast(arr, ctypes.c_void_p), len(entries)
+
+    call = lib.paged_decode_stage_copy
+    assert b.MAX_STAGE_COPIES == 4
+    arr, _ = copies(*[(fake + 64 * i, 2 * fake + 64 * i, 16) for i in range(5)])
+    assert call(arr, 5, 0, None) == b.PD_ERR_INVALID_ARG
+    assert call(arr, -1, 0, None) == b.PD_ERR_INVALID_ARG
+    assert call(None, 1, 0, None) == b.PD_ERR_INVALID_ARG
+    assert call(*copies((fake, 2 * fake, 16)), 2, None) == b.PD_ERR_INVALID_ARG
+    assert call(*copies((fake, 2 * fake, 24)), 0, None) == b.PD_ERR_INVALID_ARG
+    assert call(*copies((None, 2 * fake, 16)), 0, None) == b.PD_ERR_INVALID_ARG
+    assert call(*copies((fake + 8, 2 * fake, 16)), 1, None) == b.PD_ERR_INVALID_ARG
+    assert call(*copies((fake, fake + 16, 32)), 0, None) == b.PD_ERR_INVALID_ARG
+    # a refused copy anywhere in the list refuses the call
+    assert call(*copies((None, None, 0), (fake, 2 * fake, 16), (fake, 2 * fake, 8)), 0, None) == b.PD_ERR_INVALID_ARG
+    # the binding checks the pairs before calling
+    with pytest.raises(ValueError):
+        b.paged_decode_stage_copy([(torch.zeros(16, dtype=torch.uint8), None)])
+    with pytest.raises(ValueError):
+        b.paged_decode_stage_copy([(torch.zeros(16, dtype=torch.uint8), torch.zeros(32, dtype=torch.uint8))])
 
 
 def test_noalloc_checks_every_argument_before_queueing_work(lib):
