@@ -43,6 +43,7 @@ import torch
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
+from paged_gqa_decode_global_gb300 import host_loop  # noqa: E402
 from paged_gqa_decode_global_gb300 import binding as pdb  # noqa: E402
 from paged_gqa_decode_global_gb300 import build as pd_build  # noqa: E402
 from paged_gqa_decode_global_gb300 import inputs as synth  # noqa: E402
@@ -463,6 +464,7 @@ def run_ours(args, world, rank, local):
         # of the stage 1 that reads them), else one. Two q / result buffers,
         # three for the table and lengths; before the loop, ordinary copies of
         # the first step's inputs (and, two steps ahead, the second's table).
+        # The schedule of these copies is host_loop.schedule.
         q_parts = ([pi.q_in, pi.k_in] + ([] if pi.v_in is None else [pi.v_in])) if layer_op else [q_rows]
         meta_parts = [li.block_tables, li.seq_lens]
 
@@ -489,7 +491,7 @@ def run_ours(args, world, rank, local):
             qb["q"] = torch.empty_like(q_rows) if layer_op else qb["views"][0]
             qb["out"] = torch.empty_like(q_rows)
             qb["out_h"] = torch.empty(q_rows.shape, dtype=q_rows.dtype, pin_memory=True)
-        ahead = 2 if plan.early_kv else 1
+        ahead = host_loop.schedule(1, early_kv=bool(plan.early_kv)).ahead
 
         def compute(i, qb, mb):
             k, v = pools[i % replicas]
@@ -508,23 +510,22 @@ def run_ours(args, world, rank, local):
                 qb["out_h"].copy_(qb["out"], non_blocking=True)
 
         def pipelined_steps(i0, m):
-            stage_copy = pdb.paged_decode_stage_copy
-            qbufs[i0 % 2]["stage"].copy_(q_h, non_blocking=True)
-            for j in range(i0, min(i0 + ahead, i0 + m)):
-                mbufs[j % 3]["stage"].copy_(meta_h, non_blocking=True)
-            for i in range(i0, i0 + m):
-                compute(i, qbufs[i % 2], mbufs[i % 3])
-                other = qbufs[(i + 1) % 2]  # step i + 1's q buffer, step i - 1's result
-                pairs = []
-                if i + 1 < i0 + m:
-                    pairs.append((other["stage"], q_h))
-                if i + ahead < i0 + m:
-                    pairs.append((mbufs[(i + ahead) % 3]["stage"], meta_h))
-                if i > i0:
-                    pairs.append((other["out_h"], other["out"]))
-                stage_copy(pairs, 0, stream)
-            last = qbufs[(i0 + m - 1) % 2]
-            stage_copy([(last["out_h"], last["out"])], 1, stream)
+            # the copies of an m-step loop (buffers indexed from the loop's first step)
+            sch = host_loop.schedule(m, early_kv=bool(plan.early_kv))
+
+            def dst(c):
+                return (qbufs[c.buffer]["stage"] if c.kind == "q" else mbufs[c.buffer]["stage"] if c.kind == "meta"
+                        else qbufs[c.buffer]["out_h"])
+
+            def src(c):
+                return q_h if c.kind == "q" else meta_h if c.kind == "meta" else qbufs[c.buffer]["out"]
+
+            for c in sch.before:
+                dst(c).copy_(src(c), non_blocking=True)
+            for j in range(m):
+                compute(i0 + j, qbufs[host_loop.q_buffer(j)], mbufs[host_loop.meta_buffer(j)])
+                pdb.paged_decode_stage_copy([(dst(c), src(c)) for c in sch.after_step[j]], 0, stream)
+            pdb.paged_decode_stage_copy([(dst(c), src(c)) for c in sch.final], 1, stream)
 
         def e2e_graphs(fn):
             with torch.cuda.stream(stream):

@@ -18,6 +18,7 @@ import pytest
 import torch
 
 from paged_gqa_decode_global_gb300 import binding as b
+from paged_gqa_decode_global_gb300 import host_loop
 from paged_gqa_decode_global_gb300 import inputs as synth
 
 pytestmark = pytest.mark.gpu
@@ -155,24 +156,23 @@ def test_host_in_host_out_loop(case, early_kv, graph):
     host_out = [torch.zeros(li.q.shape, dtype=torch.bfloat16).pin_memory() for _ in range(n_steps)]
     stream = torch.cuda.Stream()
 
+    sch = host_loop.schedule(n_steps, early_kv=bool(early_kv))
+    assert sch.ahead == ahead
+
+    def dst(c):
+        return q_dev[c.buffer] if c.kind == "q" else m_dev[c.buffer] if c.kind == "meta" else host_out[c.step]
+
+    def src(c):
+        return q_h[c.step] if c.kind == "q" else meta_h[c.step] if c.kind == "meta" else dev_out[c.buffer]
+
     def loop():
-        # ordinary copies before the loop: step 0's q, the tables of the first `ahead` steps
-        q_dev[0].copy_(q_h[0], non_blocking=True)
-        for j in range(ahead):
-            m_dev[j % 3].copy_(meta_h[j], non_blocking=True)
+        for c in sch.before:  # ordinary copies before the loop
+            dst(c).copy_(src(c), non_blocking=True)
         for j in range(n_steps):
-            (q,), (bt, sl) = q_views[j % 2], m_views[j % 3]
-            step(q, k, v, bt, sl, li.scale, dev_out[j % 2], stream, k_scale=ks, v_scale=vs)
-            other = (j + 1) % 2
-            pairs = []
-            if j + 1 < n_steps:
-                pairs.append((q_dev[other], q_h[j + 1]))
-            if j + ahead < n_steps:
-                pairs.append((m_dev[(j + ahead) % 3], meta_h[j + ahead]))
-            if j > 0:
-                pairs.append((host_out[j - 1], dev_out[other]))
-            b.paged_decode_stage_copy(pairs, 0, stream)
-        b.paged_decode_stage_copy([(host_out[n_steps - 1], dev_out[(n_steps - 1) % 2])], 1, stream)
+            (q,), (bt, sl) = q_views[host_loop.q_buffer(j)], m_views[host_loop.meta_buffer(j)]
+            step(q, k, v, bt, sl, li.scale, dev_out[host_loop.out_buffer(j)], stream, k_scale=ks, v_scale=vs)
+            b.paged_decode_stage_copy([(dst(c), src(c)) for c in sch.after_step[j]], 0, stream)
+        b.paged_decode_stage_copy([(dst(c), src(c)) for c in sch.final], 1, stream)
 
     if graph:
         with torch.cuda.stream(stream):
